@@ -1,0 +1,253 @@
+"""Pins for the CPU oracle: brute force, hand-worked cases, library routines,
+invariants, special cases and the two-level identity. CPU only.
+
+The oracle is the reference every GPU parity test compares against, so each of
+its functions is checked here against something other than itself.
+"""
+import itertools
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads
+from _checks import (brute_blocked_row, brute_topk_row, check_invariants, equal_outputs,
+                     lexsort_topk_row)
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _f(v):
+    return float(v)  # accepts "inf", "-inf", "nan", "-0.0" as strings
+
+
+def _arr(vals):
+    return np.array([_f(v) for v in vals], dtype=np.float32)
+
+
+# ---------------------------------------------------------------- hand-worked cases
+
+def _load(name):
+    with open(os.path.join(GOLDEN, name)) as fh:
+        return [json.loads(line) for line in fh if line.strip()]
+
+
+@pytest.mark.parametrize("case", _load("topk_hand_cases.jsonl"), ids=lambda c: c["name"])
+def test_hand_cases_topk(case):
+    s = _arr(case["scores"])
+    idx, val = oracle.topk(s[None, :], np.array([case["L"]], np.int32), case["k"], nthreads=1)
+    assert idx[0].tolist() == case["idx"]
+    want = _arr(case["val"])
+    # bit-exact, including the sign of zero
+    assert np.array_equal(np.where(np.isnan(val[0]), 0, val[0].view(np.uint32)),
+                          np.where(np.isnan(want), 0, want.view(np.uint32)))
+    assert np.array_equal(np.isnan(val[0]), np.isnan(want))
+
+
+@pytest.mark.parametrize("case", _load("blocked_hand_cases.jsonl"), ids=lambda c: c["name"])
+def test_hand_cases_blocked(case):
+    s = _arr(case["scores"])
+    idx, val, blk = oracle.topk_blocked(s[None, :], np.array([case["L"]], np.int32), case["block"],
+                                        case["k_blocks"], case["k"], nthreads=1)
+    assert idx[0].tolist() == case["idx"]
+    assert blk[0].tolist() == case["blocks"]
+    want = _arr(case["val"])
+    assert np.array_equal(val[0], want)
+
+
+# ---------------------------------------------------------------- brute force
+
+ALPHABET = [0.0, 1.0, 2.0]
+
+
+def test_exhaustive_small_alphabet():
+    """Every row over {0,1,2} with n <= 7, every k in 1..n+1, against Python sorted."""
+    rows = []
+    for n in range(0, 8):
+        for combo in itertools.product(ALPHABET, repeat=n):
+            rows.append(list(combo) + [9.0] * (7 - n))  # 9.0 sits beyond L (poison)
+    lens = []
+    for n in range(0, 8):
+        lens += [n] * (len(ALPHABET) ** n)
+    S = np.array(rows, dtype=np.float32)
+    Lv = np.array(lens, dtype=np.int32)
+    for k in range(1, 9):
+        idx, _ = oracle.topk(S, Lv, k)
+        for r in range(S.shape[0]):
+            assert idx[r].tolist() == brute_topk_row(S[r], int(Lv[r]), k), (r, k)
+
+
+SPECIALS = [float("inf"), float("-inf"), 0.0, -0.0, float("nan"), 1.0, -1.0, 1e-45]
+
+
+def test_random_specials_against_two_brute_forces():
+    rng = np.random.default_rng(1)
+    for trial in range(400):
+        n = int(rng.integers(0, 13))
+        s = np.array(rng.choice(SPECIALS, size=12), dtype=np.float32)
+        k = int(rng.integers(1, 15))
+        idx, val = oracle.topk(s[None, :], np.array([n], np.int32), k, nthreads=1)
+        assert idx[0].tolist() == brute_topk_row(s, n, k), (s, n, k)
+        assert idx[0].tolist() == lexsort_topk_row(s, n, k), (s, n, k)
+
+
+def test_lexsort_on_seeded_tie_heavy_rows():
+    S, _ = workloads.random_rows(6, 3000, seed=5, dist="coarse")
+    S = S.numpy()
+    idx, _ = oracle.topk(S, None, 700)
+    for r in range(S.shape[0]):
+        assert idx[r].tolist() == lexsort_topk_row(S[r], S.shape[1], 700)
+
+
+# ---------------------------------------------------------------- library cross-checks
+
+def test_values_match_library_sorts():
+    """The multiset of top-k values does not depend on the tie rule."""
+    S, _ = workloads.random_rows(8, 5000, seed=7, dist="bf16")
+    S = S.numpy()
+    k = 512
+    _, val = oracle.topk(S, None, k)
+    tv = torch.topk(torch.from_numpy(S), k, dim=1, sorted=True).values.numpy()
+    ns = -np.sort(-S, axis=1)[:, :k]
+    assert np.array_equal(val, tv)
+    assert np.array_equal(val, ns)
+
+
+def test_k1_is_first_argmax():
+    S, _ = workloads.random_rows(16, 777, seed=11, dist="coarse")
+    S = S.numpy()
+    idx, _ = oracle.topk(S, None, 1)
+    assert np.array_equal(idx[:, 0], np.argmax(S, axis=1))
+
+
+def test_k_ge_L_is_stable_argsort():
+    S, _ = workloads.random_rows(4, 300, seed=12, dist="coarse")
+    S = S.numpy()
+    idx, _ = oracle.topk(S, None, 300)
+    assert np.array_equal(idx, np.argsort(-S, axis=1, kind="stable"))
+
+
+def test_all_equal_and_monotone_rows():
+    S, _ = workloads.random_rows(2, 1000, seed=0, dist="equal")
+    idx, _ = oracle.topk(S.numpy(), None, 64)
+    assert np.array_equal(idx, np.tile(np.arange(64), (2, 1)))
+    S, _ = workloads.random_rows(2, 1000, seed=0, dist="asc")
+    idx, _ = oracle.topk(S.numpy(), None, 64)
+    assert np.array_equal(idx, np.tile(np.arange(999, 999 - 64, -1), (2, 1)))
+    S, _ = workloads.random_rows(2, 1000, seed=0, dist="desc")
+    idx, _ = oracle.topk(S.numpy(), None, 64)
+    assert np.array_equal(idx, np.tile(np.arange(64), (2, 1)))
+
+
+# ---------------------------------------------------------------- invariants on the workloads
+
+@pytest.mark.parametrize("name", ["c1_single_4096", "c2_decode_262144", "c3_ragged_64"])
+def test_invariants_on_workloads(name):
+    S, L, w = workloads.make(name)
+    S = S.numpy()
+    Ln = None if L is None else L.numpy()
+    idx, val = oracle.topk(S, Ln, w.k)
+    assert check_invariants(S, Ln, w.k, idx, val) == []
+
+
+def test_invariants_on_prefill_rows_subset():
+    S, L, w = workloads.make("c4_prefill_4096")
+    sel = [0, 1, 2047, 4095]
+    Ssub = S[sel].numpy()
+    Lsub = L[sel].numpy()
+    idx, val = oracle.topk(Ssub, Lsub, w.k)
+    assert check_invariants(Ssub, Lsub, w.k, idx, val) == []
+
+
+def test_seed0_config1_threshold_has_ties():
+    """Config 1 really exercises the tie fill: 509 above the threshold, 5 equal."""
+    S, _, w = workloads.make("c1_single_4096")
+    S = S.numpy()[0]
+    idx, val = oracle.topk(S[None], None, 512)
+    t = val[0, -1]
+    assert (S > t).sum() == 509 and (S == t).sum() == 5
+    ties = np.nonzero(S == t)[0]
+    assert idx[0, 509:].tolist() == ties[:3].tolist()
+
+
+# ---------------------------------------------------------------- two-level
+
+def test_blocked_against_brute_force_small():
+    rng = np.random.default_rng(3)
+    for trial in range(300):
+        B = int(rng.choice([1, 2, 3, 4, 8]))
+        n = int(rng.integers(0, 40))
+        s = np.array(rng.choice([0.0, 1.0, 2.0, -1.0, float("nan"), -0.0], size=40), dtype=np.float32)
+        kb = int(rng.integers(1, 8))
+        k = int(rng.integers(1, 20))
+        idx, val, blk = oracle.topk_blocked(s[None], np.array([n], np.int32), B, kb, k, nthreads=1)
+        bi, bb = brute_blocked_row(s, n, B, kb, k)
+        assert idx[0].tolist() == bi, (s, n, B, kb, k)
+        assert blk[0].tolist() == bb, (s, n, B, kb, k)
+
+
+@pytest.mark.parametrize("dist", ["normal", "coarse", "bf16", "special"])
+def test_blocked_equals_plain_when_kblocks_ge_k(dist):
+    """With k_blocks >= k every block holding a plain top-k position is kept (the
+    blocks ranked above it each hold a distinct, higher-ranked position), so the
+    two-level result equals the plain top-k, ties included."""
+    S, L = workloads.random_rows(8, 4096, seed=21, dist=dist, lengths="ragged")
+    S = S.numpy()
+    L = L.numpy()
+    for kb, k in [(64, 64), (128, 64), (512, 100)]:
+        i1, v1, _ = oracle.topk_blocked(S, L, 8, kb, k)
+        i2, v2 = oracle.topk(S, L, k)
+        assert equal_outputs(i1, v1, i2, v2)
+
+
+def test_blocked_workload_rows_invariants():
+    S, L, w = workloads.make("c5_blocked_16")
+    S = S[:2].numpy()
+    idx, val, blk = oracle.topk_blocked(S, None, w.block, w.k_blocks, w.k)
+    assert check_invariants(S, None, w.k, idx, val) == []
+    for r in range(2):
+        b = blk[r]
+        assert np.all(np.diff(b) > 0) and b.size == w.k_blocks
+        # every output position lies in a kept block
+        assert np.isin(idx[r] // w.block, b).all()
+
+
+# ---------------------------------------------------------------- the pins have teeth
+
+def test_checkers_reject_planted_mistakes():
+    """Corrupt a correct oracle output in the ways a buggy oracle would and check that
+    the invariant checker or the brute force notices each one."""
+    S, _, w = workloads.make("c1_single_4096")
+    S = S.numpy()
+    idx, val = oracle.topk(S, None, 512)
+    assert check_invariants(S, None, 512, idx, val) == []
+    # (a) tie broken by highest index instead of lowest
+    t = val[0, -1]
+    ties = np.nonzero(S[0] == t)[0]
+    bad = idx.copy()
+    bad[0, 509:] = ties[-3:][::-1]
+    assert check_invariants(S, None, 512, bad, val) != []
+    # (b) one element dropped (replaced by the 513th)
+    order = np.lexsort((np.arange(S.shape[1]), -S[0].astype(np.float64)))
+    bad = idx.copy()
+    badv = val.copy()
+    bad[0, 100] = order[512]
+    badv[0, 100] = S[0, order[512]]
+    assert check_invariants(S, None, 512, bad, badv) != []
+    # (c) ascending instead of descending
+    assert check_invariants(S, None, 512, idx[:, ::-1].copy(), val[:, ::-1].copy()) != []
+    # (d) value bits not copied (-0 written as +0)
+    z = np.array([[-0.0, 1.0]], dtype=np.float32)
+    zi, zv = oracle.topk(z, None, 2)
+    zv2 = zv.copy()
+    zv2[0, 1] = 0.0
+    assert check_invariants(z, None, 2, zi, zv) == []
+    assert check_invariants(z, None, 2, zi, zv2) != []
+    # (e) NaN ranked on top instead of at the bottom
+    s = np.array([1.0, float("nan"), 2.0], dtype=np.float32)
+    assert brute_topk_row(s, 3, 3) == [2, 0, 1]
+    assert lexsort_topk_row(s, 3, 3) == [2, 0, 1]
