@@ -1,0 +1,428 @@
+#!/usr/bin/env python3
+"""Benchmark of the indexer top-k (Lightning TopK) on one GB300.
+
+Headline (the metric the pages quote): top-k latency per row at batch size 1,
+n = 262144 compressed positions (a 1M-token context at 4:1), k = 512, in
+microseconds per row. One step = one lt_topk call on one row. Inputs rotate
+over copies whose total exceeds twice the L2 size, so every step reads its row
+from HBM.
+
+Also reported on the same line: the batched workloads (64 ragged rows, the
+4096-row prefill chunk, the 16-row two-level selection) as rows/s and HBM GB/s
+against the measured copy bandwidth, the dominant kernel's roofline, the CPU
+oracle timed on this host, torch.topk on the same row, an end-to-end number
+through the public API with host buffers, and SM clocks sampled while timing.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+With --gpus N > 1 (torchrun, one process per GPU) every rank runs its own
+replica of the step (rows are independent; there is no collective on the
+data path) and rank 0 prints the aggregate.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import workloads  # noqa: E402
+
+HEADLINE = "c2_decode_262144"
+METRIC = "top-k µs/row (n=262144,k=512,BS=1); batched rows/s and HBM GB/s vs roofline"
+PUBLISHED_US = 15.0  # the pages' Lightning TopK figure at 1M context, BS=1 (hardware not stated)
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-batched", action="store_true", help="headline only")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    return ap.parse_args()
+
+
+# ------------------------------------------------------------------ distributed (replicas)
+
+def dist_setup(n_gpus):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(0)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ------------------------------------------------------------------ clocks
+
+class Clocks:
+    """nvidia-smi sampling of SM clocks and throttle reasons while the GPU works."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except FileNotFoundError:
+            self.proc = None
+        time.sleep(0.2)
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            time.sleep(0.1)
+            self.proc.terminate()
+            self.proc.wait(timeout=10)
+
+    def summary(self):
+        if self.proc is None or not self.path:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        sms, mx, reasons, power = [], [], set(), []
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sms.append(float(parts[0]))
+                mx.append(float(parts[1]))
+                power.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[4:8]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        os.unlink(self.path)
+        if not sms:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        busy = [s for s, p in zip(sms, power) if p > 1.2 * min(power)] or sms
+        return {"sm_mhz": statistics.median(busy), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sms)}
+
+
+# ------------------------------------------------------------------ timing helpers
+
+def timed_launches(launch, steps: int, warmup: int, world: int):
+    """Run warmup untimed steps, then exactly `steps` steps with an event pair
+    around each launch. A sleep kernel queued first keeps the GPU busy while
+    the host enqueues the steps, so the events see GPU time only.
+    Returns (total_ms from first start to last end, [per-launch ms])."""
+    for i in range(warmup):
+        launch(i)
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    barrier(world)
+    torch.cuda.synchronize()
+    torch.cuda._sleep(int(2e6 + steps * 1e5))  # covers the host-side enqueue of all steps
+    for i in range(steps):
+        ev[i][0].record()
+        launch(warmup + i)
+        ev[i][1].record()
+    torch.cuda.synchronize()
+    barrier(world)
+    per = [a.elapsed_time(b) for a, b in ev]
+    total = ev[0][0].elapsed_time(ev[-1][1])
+    return total, per
+
+
+def l2_bytes():
+    try:
+        return int(torch.cuda.get_device_properties(torch.cuda.current_device()).L2_cache_size)
+    except Exception:
+        return 128 << 20
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as fh:
+            d = json.load(fh)
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def profile_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from a committed ncu summary, if it matches the current source."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    try:
+        with open(path) as fh:
+            d = json.load(fh)
+        e = d.get(f"{kernel}:{workload}")
+        if not e:
+            return None
+        from sparse_attention_indexer_lt_gb300 import build as b
+        if e.get("source_hash") != b.source_hash():
+            return None
+        return float(e["dram_bytes_per_launch"])
+    except Exception:
+        return None
+
+
+# ------------------------------------------------------------------ our arm
+
+def bench_ours(args, world, rank):
+    import sparse_attention_indexer_lt_gb300 as lt
+    from sparse_attention_indexer_lt_gb300 import build as ltb
+    ltb.build()
+    dev = torch.device("cuda", torch.cuda.current_device())
+    peak, peak_kind = measured_peaks()
+    L2 = l2_bytes()
+    result = {}
+
+    # ---- headline: BS=1, n=262144, k=512
+    S, _, w = workloads.make(HEADLINE)
+    row_bytes = 4 * w.row_stride
+    ncopies = workloads.l2_rotation_copies(row_bytes, L2)
+    base = S.to(dev)
+    copies = [base.clone() for _ in range(ncopies)]
+    oi = torch.empty(w.rows, w.k, dtype=torch.int32, device=dev)
+    ov = torch.empty(w.rows, w.k, dtype=torch.float32, device=dev)
+
+    def step(i):
+        lt.topk(copies[i % ncopies], None, w.k, out_idx=oi, out_val=ov)
+
+    with Clocks(dev.index) as clk:
+        total_ms, per = timed_launches(step, args.steps, args.warmup, world)
+        # warm-L2 latency (the indexer that produced the row has just written it)
+        warm_total, warm_per = timed_launches(lambda i: lt.topk(base, None, w.k, out_idx=oi, out_val=ov),
+                                              args.steps, args.warmup, world)
+        batched = [] if args.no_batched else bench_batched(lt, dev, args, world, peak, L2)
+        ttk = bench_torch_topk(base, w.k, args, world)
+    clocks = clk.summary()
+    total_ms = max_over_ranks(total_ms, world)
+    us_per_row = total_ms * 1000.0 / (args.steps * w.rows * world)
+    kern_ms = statistics.mean(per)
+    achieved = (4 * w.row_stride * w.rows) / (kern_ms * 1e-3) / 1e9
+    traffic = profile_traffic("topk_kernel", HEADLINE)
+    plan = lt.plan(w.rows, w.row_stride, w.k)
+
+    # ---- end to end through the public API: pinned host row -> device, top-k, results -> host
+    e2e = bench_e2e(lt, S, w, dev, args, world)
+
+    line = {
+        "metric": METRIC,
+        "value": round(us_per_row, 3),
+        "unit": "µs/row",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(total_ms / args.steps, 6),
+        "higher_is_better": False,
+        "scaling": "weak",
+        "vs_baseline": round(us_per_row / PUBLISHED_US, 4),
+        "dtype": "u32",
+        "data": "synthetic (seeded N(0,1)->bf16 + U(2,6) tail on 1%, no dataset)",
+        "config": {"workload": HEADLINE, "rows": w.rows, "n": w.row_stride, "k": w.k,
+                   "l2": f"rotating {ncopies} input copies ({ncopies * row_bytes >> 20} MiB > 2x L2)",
+                   "plan": plan, "parallelism": "replicas" if world > 1 else "single GPU",
+                   "warm_l2_us_per_row": round(statistics.median(warm_per) * 1000.0, 3),
+                   "kernel_us_median": round(statistics.median(per) * 1000.0, 3)},
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 5), "traffic": traffic,
+                     "peak_kind": f"{peak_kind} copy bandwidth (burst)",
+                     "kernel": "lt::topk_kernel", "algorithmic_bytes_per_launch": 4 * w.row_stride * w.rows},
+        "e2e": e2e,
+        "gpu_launches": args.steps,
+        "clocks": clocks,
+        "torch_topk_us": ttk,
+        "batched": batched,
+        "published_context": {"lightning_topk_us": PUBLISHED_US, "plain_pytorch_us": 100.0,
+                              "hardware": "not stated on the pages"},
+    }
+    if rank == 0 and world == 1 and not args.no_cpu:
+        line["cpu_baseline"] = cpu_baseline(S, w, args.cpu_seconds)
+    return line
+
+
+def bench_batched(lt, dev, args, world, peak, L2):
+    out = []
+    steps = max(3, min(args.steps, 50))
+    for name in ("c3_ragged_64", "c4_prefill_4096", "c5_blocked_16"):
+        S, L, w = workloads.make(name)
+        nbytes = workloads.read_bytes(L, w.rows, w.row_stride)
+        ncopies = workloads.l2_rotation_copies(nbytes, L2) if nbytes < 4 * L2 else 1
+        base = S.to(dev)
+        copies = [base] + [base.clone() for _ in range(ncopies - 1)]
+        ld = None if L is None else L.to(dev)
+        oi = torch.empty(w.rows, w.k, dtype=torch.int32, device=dev)
+        ov = torch.empty(w.rows, w.k, dtype=torch.float32, device=dev)
+        ob = torch.empty(w.rows, w.k_blocks, dtype=torch.int32, device=dev) if w.blocked else None
+        if w.blocked:
+            def step(i, c=copies, n=ncopies):
+                lt.topk_blocked(c[i % n], ld, w.block, w.k_blocks, w.k, out_idx=oi, out_val=ov, out_blocks=ob)
+        else:
+            def step(i, c=copies, n=ncopies):
+                lt.topk(c[i % n], ld, w.k, out_idx=oi, out_val=ov)
+        total_ms, per = timed_launches(step, steps, max(3, args.warmup), world)
+        total_ms = max_over_ranks(total_ms, world)
+        step_ms = total_ms / steps
+        kern_ms = statistics.mean(per)
+        gbs = nbytes / (kern_ms * 1e-3) / 1e9
+        out.append({
+            "workload": name, "rows": w.rows, "read_bytes": nbytes,
+            "rows_per_s": round(w.rows * world / (step_ms * 1e-3), 1),
+            "us_per_row": round(step_ms * 1000.0 / w.rows, 4),
+            "kernel_us": round(kern_ms * 1000.0, 2),
+            "hbm_gbs": round(gbs, 1), "frac_of_peak": round(gbs / peak, 4),
+            "l2": f"{ncopies} rotating copies" if ncopies > 1 else "input larger than 4x L2",
+            "plan": lt.plan(w.rows, w.row_stride, w.k, blocked=w.blocked, k_blocks=w.k_blocks),
+        })
+        del copies, base
+        torch.cuda.empty_cache()
+    return out
+
+
+def bench_torch_topk(x, k, args, world):
+    steps = max(3, min(args.steps, 50))
+    _, per = timed_launches(lambda i: torch.topk(x, k, dim=1, sorted=True), steps, 3, world)
+    return round(statistics.median(per) * 1000.0, 3)
+
+
+def bench_e2e(lt, S, w, dev, args, world):
+    host = S.pin_memory()
+    dev_in = torch.empty_like(S, device=dev)
+    oi = torch.empty(w.rows, w.k, dtype=torch.int32, device=dev)
+    ov = torch.empty(w.rows, w.k, dtype=torch.float32, device=dev)
+    hi = torch.empty(w.rows, w.k, dtype=torch.int32).pin_memory()
+    hv = torch.empty(w.rows, w.k, dtype=torch.float32).pin_memory()
+
+    def step(_):
+        dev_in.copy_(host, non_blocking=True)
+        lt.topk(dev_in, None, w.k, out_idx=oi, out_val=ov)
+        hi.copy_(oi, non_blocking=True)
+        hv.copy_(ov, non_blocking=True)
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    barrier(world)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for i in range(args.steps):
+        step(i)
+    b.record()
+    torch.cuda.synchronize()
+    barrier(world)
+    ms = max_over_ranks(a.elapsed_time(b), world)
+    return {"value": round(ms * 1000.0 / (args.steps * w.rows * world), 3), "unit": "µs/row",
+            "h2d_bytes_per_step": host.numel() * 4, "d2h_bytes_per_step": 8 * w.rows * w.k,
+            "note": "pinned host row -> device, lt.topk, indices and values -> pinned host; "
+                    "host launch overhead included"}
+
+
+def cpu_baseline(S, w, seconds):
+    import oracle
+    oracle.build()
+    x = S.numpy()
+    oracle.topk(x, None, w.k, nthreads=1)
+    n, t0 = 0, time.perf_counter()
+    while time.perf_counter() - t0 < seconds:
+        oracle.topk(x, None, w.k, nthreads=1)
+        n += 1
+    dt = time.perf_counter() - t0
+    return {"value": round(dt / (n * w.rows) * 1e6, 1), "unit": "µs/row", "cores": 1, "kind": "oracle",
+            "sample": f"{n} repetitions of the {HEADLINE} row (std::stable_sort, one thread: batch size 1)",
+            "cpu": cpu_name()}
+
+
+def cpu_name():
+    try:
+        for line in open("/proc/cpuinfo"):
+            if line.lower().startswith(("model name", "cpu part", "hardware")):
+                return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    import platform
+    return platform.machine()
+
+
+# ------------------------------------------------------------------ reference arm (the CPU oracle)
+
+def bench_reference(args, world, rank):
+    import oracle
+    oracle.build()
+    S, _, w = workloads.make(HEADLINE)
+    x = S.numpy()
+    for _ in range(args.warmup):
+        oracle.topk(x, None, w.k, nthreads=1)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.topk(x, None, w.k, nthreads=1)
+    dt = time.perf_counter() - t0
+    v = round(dt / (args.steps * w.rows) * 1e6, 1)
+    return {
+        "impl": "reference", "metric": METRIC, "value": v, "unit": "µs/row", "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt * 1000.0 / args.steps, 4),
+        "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic (seeded)", "config": {"workload": HEADLINE, "rows": w.rows, "n": w.row_stride, "k": w.k},
+        "cpu_baseline": {"value": v, "unit": "µs/row", "cores": 1, "kind": "oracle",
+                         "sample": f"{args.steps} timed steps of the {HEADLINE} row, one thread",
+                         "cpu": cpu_name()},
+        "e2e": {"value": v, "unit": "µs/row", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        # the reference arm is the CPU oracle: rank 0 runs it, other ranks exit without work
+        if int(os.environ.get("RANK", "0")) == 0:
+            print(json.dumps(bench_reference(args, 1, 0)), flush=True)
+        return
+    world, rank, local = dist_setup(args.gpus)
+    line = bench_ours(args, world, rank)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,146 @@
+/*
+ * lt_topk.h -- C ABI of the GB300 (sm_103a) indexer top-k library.
+ *
+ * The operation. Compressed sparse attention scores every compressed KV
+ * position of a query row with an indexer and keeps only the k best positions
+ * ("CSA: 4:1 compression + TopK selection", AICon 2026 Shenzhen speaker page,
+ * abstract and outline section 1.1). At a million tokens that is a top-512 over
+ * 262,144 positions, run in every layer; the pages name the kernel that does it
+ * Lightning TopK: the row is split over the CTAs of one thread-block cluster,
+ * each CTA builds a local histogram and the partial results are combined over
+ * the SM-to-SM network instead of HBM (AICon page, outline section 3.2; SGLang
+ * DeepSeek-V4 inference talk notes, section 3.2 "LightningTopK"). The two-level
+ * variant restricts the top-512 to the positions of up to 2048 eight-position
+ * candidate blocks chosen by block score (SGLang and Miles day-0 support for
+ * DeepSeek-V4.1, Q&A on cross-layer sharing).
+ *
+ * The pages fix neither a tie rule nor an output order; this library fixes
+ * both so that every row has exactly one correct answer:
+ *   - positions are ranked by score descending, ties by index ascending;
+ *   - -0.0 and +0.0 are equal; NaN ranks below -inf (NaNs tie, index decides);
+ *   - the k outputs of a row are written in that rank order.
+ *
+ * Memory. Every pointer argument is DEVICE memory owned by the caller. The
+ * library allocates nothing, keeps no per-call state and never synchronises
+ * the stream. Layouts are row-major:
+ *   scores      float  [rows][row_stride]; row r is read on [0, L_r) only
+ *   lengths     int32  [rows] or NULL; L_r = clamp(lengths[r], 0, row_stride),
+ *                      NULL means L_r = row_stride for every row
+ *   out_idx     int32  [rows][k]; row-relative, 0-based positions
+ *   out_val     float  [rows][k] or NULL; bit copies of scores[r][out_idx]
+ *   out_blocks  int32  [rows][k_blocks] or NULL (two-level only)
+ * A row with L_r < k fills slots [L_r, k) with index -1 and value -inf.
+ * Rows whose start is 16-byte aligned (scores 16-byte aligned and row_stride a
+ * multiple of 4) use 128-bit loads; any other alignment takes scalar loads.
+ *
+ * Errors. Argument errors return LT_ERR_INVALID_ARG or LT_ERR_UNSUPPORTED
+ * synchronously and launch nothing. A failed launch returns LT_ERR_CUDA
+ * (the CUDA error is left for cudaGetLastError). The kernels contain no
+ * unbounded waits and no device-side traps.
+ */
+#ifndef LT_TOPK_H
+#define LT_TOPK_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum lt_status {
+  LT_OK = 0,
+  LT_ERR_INVALID_ARG = 1,  /* null pointer, k < 1, rows < 0, ... */
+  LT_ERR_UNSUPPORTED = 2,  /* valid but outside this build's limits */
+  LT_ERR_CUDA = 3          /* a CUDA runtime call failed */
+} lt_status;
+
+/* Largest k and k_blocks accepted. */
+#define LT_MAX_K 2048
+/* Largest row_stride accepted (positions must fit a signed 32-bit index). */
+#define LT_MAX_ROW_STRIDE 1073741824LL
+
+/*
+ * lt_topk -- per-row top-k of the indexer scores.
+ *
+ * For every row r in [0, rows): order the positions i in [0, L_r) by
+ * (scores[r][i] descending, i ascending) and write the first min(k, L_r) to
+ * out_idx[r][*] (and the copied scores to out_val[r][*]); pad the remaining
+ * slots with (-1, -inf).
+ *
+ *   scores, lengths, rows, row_stride  as described above (rows >= 0,
+ *                                      1 <= row_stride <= LT_MAX_ROW_STRIDE)
+ *   k        1 <= k <= LT_MAX_K
+ *   stream   a cudaStream_t (passed as void*); 0 is the legacy default stream
+ *
+ * rows == 0 returns LT_OK and launches nothing.
+ */
+lt_status lt_topk(const float* scores, const int32_t* lengths, int32_t rows, int64_t row_stride,
+                  int32_t k, int32_t* out_idx, float* out_val, void* stream);
+
+/*
+ * lt_topk_blocked -- two-level, candidate-restricted top-k.
+ *
+ * Per row (L = L_r, nblocks = ceil(L / block)):
+ *   stage A: block score of block j = max of scores[r][i] over its valid
+ *            positions i in [j*block, min(L, (j+1)*block)); keep the first
+ *            min(k_blocks, nblocks) blocks by (block score desc, block id asc);
+ *   stage B: among the valid positions of the kept blocks, keep the first
+ *            min(k, ncand) by (score desc, position asc).
+ * out_idx / out_val are written as for lt_topk; out_blocks[r][*] (if not NULL)
+ * receives the kept block ids in ascending order, padded with -1.
+ *
+ *   block     1 <= block <= 64 and a power of two (the pages use 8)
+ *   k_blocks  1 <= k_blocks <= LT_MAX_K
+ *   k         1 <= k <= LT_MAX_K
+ */
+lt_status lt_topk_blocked(const float* scores, const int32_t* lengths, int32_t rows,
+                          int64_t row_stride, int32_t block, int32_t k_blocks, int32_t k,
+                          int32_t* out_idx, float* out_val, int32_t* out_blocks, void* stream);
+
+/*
+ * Launch-plan control, for tests and measurement (not needed for normal use).
+ *
+ *   force_cluster  0 lets the planner choose; 1, 2, 4, 8 or 16 forces the
+ *                  number of CTAs that share one row (16 needs a device that
+ *                  can schedule a 16-CTA cluster, else LT_ERR_UNSUPPORTED)
+ *   force_exact    nonzero skips the sampled-threshold fast path and runs the
+ *                  streaming radix select on every row (same results)
+ *   counters       NULL, or device int32[LT_NUM_COUNTERS] that the kernel
+ *                  increments atomically, once per row: [0] rows finished on
+ *                  the fast path, [1] rows finished on the streaming radix
+ *                  select, [2] rows whose candidate set overflowed, [3] rows
+ *                  whose sampled threshold kept fewer than k candidates.
+ *                  For the two-level call, each row counts once per stage.
+ */
+#define LT_NUM_COUNTERS 4
+lt_status lt_topk_ex(const float* scores, const int32_t* lengths, int32_t rows,
+                     int64_t row_stride, int32_t k, int32_t* out_idx, float* out_val,
+                     int32_t force_cluster, int32_t force_exact, int32_t* counters,
+                     void* stream);
+lt_status lt_topk_blocked_ex(const float* scores, const int32_t* lengths, int32_t rows,
+                             int64_t row_stride, int32_t block, int32_t k_blocks, int32_t k,
+                             int32_t* out_idx, float* out_val, int32_t* out_blocks,
+                             int32_t force_cluster, int32_t force_exact, int32_t* counters,
+                             void* stream);
+
+/*
+ * lt_topk_plan -- the launch the planner would make, without launching.
+ * blocked selects the two-level kernel (k_blocks is ignored otherwise).
+ * Writes the CTAs per row (cluster size), threads per CTA and dynamic shared
+ * memory bytes per CTA to the non-NULL host pointers.
+ */
+lt_status lt_topk_plan(int32_t rows, int64_t row_stride, int32_t k, int32_t blocked,
+                       int32_t k_blocks, int32_t force_cluster, int32_t* cluster_size,
+                       int32_t* threads_per_cta, int32_t* smem_bytes);
+
+/* Static description of a status code. */
+const char* lt_status_string(lt_status status);
+
+/* Library version, major*10000 + minor*100 + patch. */
+int32_t lt_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LT_TOPK_H */

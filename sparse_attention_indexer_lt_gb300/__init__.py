@@ -1,0 +1,184 @@
+"""GB300-native indexer top-k (Lightning TopK) -- Python binding.
+
+Thin ``ctypes`` binding of ``liblt_topk.so`` (see ``include/lt_topk.h``). It
+only checks and marshals arguments: device pointers, sizes and the current
+CUDA stream go to the C ABI, and every step of the selection runs in the
+library's sm_103a kernels. There is no CPU path: if the library is missing or
+the tensors are not on a CUDA device, the call raises.
+
+    idx, val = topk(scores, lengths, k=512)
+    idx, val, blocks = topk_blocked(scores, lengths, block=8, k_blocks=2048, k=512)
+"""
+from __future__ import annotations
+
+import ctypes
+from pathlib import Path
+
+import torch
+
+__all__ = ["topk", "topk_blocked", "plan", "load", "library_path", "LtError", "NUM_COUNTERS",
+           "status_string", "version"]
+
+_LIB_PATH = Path(__file__).resolve().parent / "liblt_topk.so"
+_lib = None
+NUM_COUNTERS = 4
+
+
+class LtError(RuntimeError):
+    """A non-zero lt_status from the library."""
+
+    def __init__(self, fn: str, status: int):
+        super().__init__(f"{fn} failed: {status_string(status)} (status {status})")
+        self.status = status
+
+
+def library_path() -> Path:
+    return _LIB_PATH
+
+
+def load() -> ctypes.CDLL:
+    """Load liblt_topk.so (built in-tree by ``build.build()``); raise if it is missing."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not _LIB_PATH.exists():
+        raise RuntimeError(
+            f"{_LIB_PATH} is not built; run `python -m sparse_attention_indexer_lt_gb300.build` "
+            "(needs nvcc) -- there is no fallback implementation")
+    lib = ctypes.CDLL(str(_LIB_PATH))
+    i32, i64, vp = ctypes.c_int32, ctypes.c_int64, ctypes.c_void_p
+    lib.lt_topk.argtypes = [vp, vp, i32, i64, i32, vp, vp, vp]
+    lib.lt_topk.restype = ctypes.c_int
+    lib.lt_topk_ex.argtypes = [vp, vp, i32, i64, i32, vp, vp, i32, i32, vp, vp]
+    lib.lt_topk_ex.restype = ctypes.c_int
+    lib.lt_topk_blocked.argtypes = [vp, vp, i32, i64, i32, i32, i32, vp, vp, vp, vp]
+    lib.lt_topk_blocked.restype = ctypes.c_int
+    lib.lt_topk_blocked_ex.argtypes = [vp, vp, i32, i64, i32, i32, i32, vp, vp, vp, i32, i32, vp, vp]
+    lib.lt_topk_blocked_ex.restype = ctypes.c_int
+    lib.lt_topk_plan.argtypes = [i32, i64, i32, i32, i32, i32, vp, vp, vp]
+    lib.lt_topk_plan.restype = ctypes.c_int
+    lib.lt_status_string.argtypes = [ctypes.c_int]
+    lib.lt_status_string.restype = ctypes.c_char_p
+    lib.lt_version.argtypes = []
+    lib.lt_version.restype = i32
+    _lib = lib
+    return lib
+
+
+def status_string(status: int) -> str:
+    return load().lt_status_string(int(status)).decode()
+
+
+def version() -> int:
+    return int(load().lt_version())
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _check_scores(scores: torch.Tensor):
+    if not isinstance(scores, torch.Tensor) or not scores.is_cuda:
+        raise TypeError("scores must be a CUDA tensor")
+    if scores.dtype != torch.float32:
+        raise TypeError("scores must be float32")
+    if scores.dim() != 2:
+        raise ValueError("scores must be 2-D [rows, positions]")
+    rows, n = scores.shape
+    if n < 1:
+        raise ValueError("scores must have at least one position per row")
+    if rows > 0 and scores.stride(1) != 1:
+        raise ValueError("scores rows must be contiguous (stride(1) == 1)")
+    if rows > 1 and scores.stride(0) != n:
+        raise ValueError("scores must have contiguous rows (stride(0) == number of positions)")
+    return rows, n
+
+
+def _check_lengths(lengths, rows, device):
+    if lengths is None:
+        return None
+    if not isinstance(lengths, torch.Tensor) or lengths.device != device:
+        raise TypeError("lengths must be a tensor on the same device as scores")
+    if lengths.dtype != torch.int32 or lengths.numel() != rows or not lengths.is_contiguous():
+        raise ValueError("lengths must be a contiguous int32 tensor with one entry per row")
+    return lengths
+
+
+def _out(t, shape, dtype, device, name):
+    if t is None:
+        return torch.empty(shape, dtype=dtype, device=device)
+    if t.dtype != dtype or tuple(t.shape) != tuple(shape) or t.device != device or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous {dtype} tensor of shape {tuple(shape)} on {device}")
+    return t
+
+
+def _counters(c, device):
+    if c is None:
+        return None
+    if c.dtype != torch.int32 or c.numel() < NUM_COUNTERS or c.device != device:
+        raise ValueError(f"counters must be an int32 tensor with >= {NUM_COUNTERS} entries on {device}")
+    return c
+
+
+def topk(scores: torch.Tensor, lengths: torch.Tensor | None = None, k: int = 512, *,
+         out_idx: torch.Tensor | None = None, out_val: torch.Tensor | None = None,
+         with_values: bool = True, force_cluster: int = 0, force_exact: bool = False,
+         counters: torch.Tensor | None = None, stream: torch.cuda.Stream | None = None):
+    """Per-row top-k by (score desc, index asc); returns (idx int32 [rows, k], val float32 [rows, k] or None)."""
+    lib = load()
+    rows, n = _check_scores(scores)
+    dev = scores.device
+    lengths = _check_lengths(lengths, rows, dev)
+    out_idx = _out(out_idx, (rows, k), torch.int32, dev, "out_idx")
+    if with_values:
+        out_val = _out(out_val, (rows, k), torch.float32, dev, "out_val")
+    else:
+        out_val = None
+    counters = _counters(counters, dev)
+    with torch.cuda.device(dev):
+        s = (stream or torch.cuda.current_stream(dev)).cuda_stream
+        st = lib.lt_topk_ex(_ptr(scores), _ptr(lengths), rows, max(n, 1), int(k), _ptr(out_idx),
+                            _ptr(out_val), int(force_cluster), int(bool(force_exact)),
+                            _ptr(counters), ctypes.c_void_p(s))
+    if st != 0:
+        raise LtError("lt_topk", st)
+    return out_idx, out_val
+
+
+def topk_blocked(scores: torch.Tensor, lengths: torch.Tensor | None = None, block: int = 8,
+                 k_blocks: int = 2048, k: int = 512, *, out_idx: torch.Tensor | None = None,
+                 out_val: torch.Tensor | None = None, out_blocks: torch.Tensor | None = None,
+                 with_values: bool = True, with_blocks: bool = True, force_cluster: int = 0,
+                 force_exact: bool = False, counters: torch.Tensor | None = None,
+                 stream: torch.cuda.Stream | None = None):
+    """Two-level top-k; returns (idx [rows, k], val [rows, k] or None, blocks [rows, k_blocks] or None)."""
+    lib = load()
+    rows, n = _check_scores(scores)
+    dev = scores.device
+    lengths = _check_lengths(lengths, rows, dev)
+    out_idx = _out(out_idx, (rows, k), torch.int32, dev, "out_idx")
+    out_val = _out(out_val, (rows, k), torch.float32, dev, "out_val") if with_values else None
+    out_blocks = _out(out_blocks, (rows, k_blocks), torch.int32, dev, "out_blocks") if with_blocks else None
+    counters = _counters(counters, dev)
+    with torch.cuda.device(dev):
+        s = (stream or torch.cuda.current_stream(dev)).cuda_stream
+        st = lib.lt_topk_blocked_ex(_ptr(scores), _ptr(lengths), rows, max(n, 1), int(block),
+                                    int(k_blocks), int(k), _ptr(out_idx), _ptr(out_val),
+                                    _ptr(out_blocks), int(force_cluster), int(bool(force_exact)),
+                                    _ptr(counters), ctypes.c_void_p(s))
+    if st != 0:
+        raise LtError("lt_topk_blocked", st)
+    return out_idx, out_val, out_blocks
+
+
+def plan(rows: int, row_stride: int, k: int, *, blocked: bool = False, k_blocks: int = 2048,
+         force_cluster: int = 0, device: int | None = None) -> dict:
+    """The launch the planner would make: {'cluster', 'threads', 'smem'}."""
+    lib = load()
+    c, t, s = ctypes.c_int32(), ctypes.c_int32(), ctypes.c_int32()
+    with torch.cuda.device(device if device is not None else torch.cuda.current_device()):
+        st = lib.lt_topk_plan(int(rows), int(row_stride), int(k), int(bool(blocked)), int(k_blocks),
+                              int(force_cluster), ctypes.byref(c), ctypes.byref(t), ctypes.byref(s))
+    if st != 0:
+        raise LtError("lt_topk_plan", st)
+    return {"cluster": c.value, "threads": t.value, "smem": s.value}

@@ -1,0 +1,294 @@
+// lt_api.cu -- the C ABI: argument checks, launch planning and launches.
+//
+// Planning. One cluster of C CTAs owns one row. C is 1 when the batch alone
+// fills the GPU; otherwise it doubles (up to 16, the largest cluster an
+// sm_103a GPC can host) while rows * C stays below two CTAs per SM and each
+// CTA still gets at least one round of the row (8192 positions). A 16-CTA
+// cluster is non-portable: the plan asks the occupancy calculator whether one
+// can be scheduled with the chosen shared memory and halves C if not.
+
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <cstdlib>
+#include <mutex>
+
+#include "../../include/lt_topk.h"
+#include "lt_device.cuh"
+#include "lt_launch.h"
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+constexpr int kPositionsPerRound = lt::kThreads * lt::kVecPerRound * 4;  // 8192
+
+struct DeviceInfo {
+  bool ready = false;
+  int sms = 0;
+  int smem_optin = 0;
+};
+
+std::mutex g_mu;
+DeviceInfo g_dev[kMaxDevices];
+int g_smem_set[kMaxDevices][8];  // largest dynamic smem already granted per kernel slot
+bool g_nonportable_set[kMaxDevices][8];
+
+int kernel_slot(bool blocked, int block) {
+  if (!blocked) return 0;
+  switch (block) {
+    case 4: return 1;
+    case 8: return 2;
+    case 16: return 3;
+    case 32: return 4;
+    default: return -1;
+  }
+}
+
+uint32_t next_pow2(uint32_t x) {
+  uint32_t p = 1;
+  while (p < x) p <<= 1;
+  return p;
+}
+
+struct Plan {
+  int cluster = 1;
+  int threads = lt::kThreads;
+  uint32_t cap = 0;
+  uint32_t sel_cap = 0;
+  uint32_t smem = 0;
+  const void* func = nullptr;
+};
+
+lt_status device_info(DeviceInfo** out, int* dev_out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return LT_ERR_CUDA;
+  if (dev < 0 || dev >= kMaxDevices) return LT_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lk(g_mu);
+  DeviceInfo& d = g_dev[dev];
+  if (!d.ready) {
+    if (cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return LT_ERR_CUDA;
+    if (cudaDeviceGetAttribute(&d.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
+      return LT_ERR_CUDA;
+    d.ready = true;
+  }
+  *out = &d;
+  *dev_out = dev;
+  return LT_OK;
+}
+
+// Grant the kernel the shared memory and cluster size it needs (once per device).
+lt_status prepare_kernel(int dev, int slot, const void* func, uint32_t smem, int cluster) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  if ((int)smem > g_smem_set[dev][slot]) {
+    if (cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+      return LT_ERR_CUDA;
+    g_smem_set[dev][slot] = (int)smem;
+  }
+  if (cluster > 8 && !g_nonportable_set[dev][slot]) {
+    if (cudaFuncSetAttribute(func, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess)
+      return LT_ERR_UNSUPPORTED;
+    g_nonportable_set[dev][slot] = true;
+  }
+  return LT_OK;
+}
+
+bool cluster_fits(const void* func, int cluster, uint32_t smem) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)cluster);
+  cfg.blockDim = dim3(lt::kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cudaLaunchAttribute attr;
+  attr.id = cudaLaunchAttributeClusterDimension;
+  attr.val.clusterDim.x = (unsigned)cluster;
+  attr.val.clusterDim.y = 1;
+  attr.val.clusterDim.z = 1;
+  cfg.attrs = &attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, func, &cfg) != cudaSuccess) {
+    (void)cudaGetLastError();  // clear the error this query may leave behind
+    return false;
+  }
+  return n > 0;
+}
+
+lt_status make_plan(int32_t rows, int64_t row_stride, int32_t k, bool blocked, int32_t block,
+                    int32_t k_blocks, int32_t force_cluster, Plan* plan, int* dev_out) {
+  DeviceInfo* di = nullptr;
+  int dev = 0;
+  lt_status st = device_info(&di, &dev);
+  if (st != LT_OK) return st;
+  const int slot = kernel_slot(blocked, block);
+  if (slot < 0) return LT_ERR_UNSUPPORTED;
+  plan->func = blocked ? lt::blocked_kernel_ptr(block) : lt::topk_kernel_ptr();
+  if (!plan->func) return LT_ERR_UNSUPPORTED;
+
+  const uint32_t kmax = (uint32_t)(blocked ? (k > k_blocks ? k : k_blocks) : k);
+  uint32_t cap = next_pow2(4 * kmax);
+  cap = cap < 2048u ? 2048u : (cap > 4096u ? 4096u : cap);
+  plan->cap = cap;
+  plan->sel_cap = next_pow2(kmax < 32u ? 32u : kmax);
+
+  int c = 1;
+  if (force_cluster > 0) {
+    c = force_cluster;
+  } else {
+    const int64_t useful = (row_stride + kPositionsPerRound - 1) / kPositionsPerRound;
+    while (c < 16 && c < useful && (int64_t)rows * c < 2LL * di->sms) c *= 2;
+  }
+  for (;;) {
+    const uint32_t smem = lt::make_layout(c > 1, plan->cap, plan->sel_cap).total;
+    if ((int)smem > di->smem_optin) return LT_ERR_UNSUPPORTED;
+    st = prepare_kernel(dev, slot, plan->func, smem, c);
+    if (st != LT_OK && !(st == LT_ERR_UNSUPPORTED && force_cluster == 0 && c > 8)) return st;
+    if (st == LT_OK && (c == 1 || cluster_fits(plan->func, c, smem))) {
+      plan->cluster = c;
+      plan->smem = smem;
+      break;
+    }
+    if (force_cluster > 0 || c == 1) return LT_ERR_UNSUPPORTED;
+    c /= 2;
+  }
+  if ((int64_t)rows * plan->cluster > 0x7fffffffLL) return LT_ERR_UNSUPPORTED;
+  *dev_out = dev;
+  return LT_OK;
+}
+
+lt_status check_common(const float* scores, int32_t rows, int64_t row_stride, int32_t k,
+                       const int32_t* out_idx, int32_t force_cluster) {
+  if (rows < 0 || row_stride < 1 || k < 1) return LT_ERR_INVALID_ARG;
+  if (rows > 0 && (scores == nullptr || out_idx == nullptr)) return LT_ERR_INVALID_ARG;
+  if (!(force_cluster == 0 || force_cluster == 1 || force_cluster == 2 || force_cluster == 4 ||
+        force_cluster == 8 || force_cluster == 16))
+    return LT_ERR_INVALID_ARG;
+  if (k > LT_MAX_K || row_stride > LT_MAX_ROW_STRIDE) return LT_ERR_UNSUPPORTED;
+  return LT_OK;
+}
+
+lt_status launch(const Plan& plan, const lt::Params& prm, int32_t rows, void* stream) {
+  lt::Params p = prm;
+  p.cap = (int32_t)plan.cap;
+  p.sel_cap = (int32_t)plan.sel_cap;
+  p.clustered = plan.cluster > 1 ? 1 : 0;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)((int64_t)rows * plan.cluster));
+  cfg.blockDim = dim3(lt::kThreads);
+  cfg.dynamicSmemBytes = plan.smem;
+  cfg.stream = static_cast<cudaStream_t>(stream);
+  cudaLaunchAttribute attr;
+  attr.id = cudaLaunchAttributeClusterDimension;
+  attr.val.clusterDim.x = (unsigned)plan.cluster;
+  attr.val.clusterDim.y = 1;
+  attr.val.clusterDim.z = 1;
+  cfg.attrs = &attr;
+  cfg.numAttrs = plan.cluster > 1 ? 1 : 0;
+  void* args[] = {&p};
+  return cudaLaunchKernelExC(&cfg, plan.func, args) == cudaSuccess ? LT_OK : LT_ERR_CUDA;
+}
+
+bool aligned16(const void* p, int64_t row_stride) {
+  return (reinterpret_cast<uintptr_t>(p) % 16u) == 0 && (row_stride % 4) == 0;
+}
+
+}  // namespace
+
+extern "C" {
+
+lt_status lt_topk_ex(const float* scores, const int32_t* lengths, int32_t rows, int64_t row_stride,
+                     int32_t k, int32_t* out_idx, float* out_val, int32_t force_cluster,
+                     int32_t force_exact, int32_t* counters, void* stream) {
+  lt_status st = check_common(scores, rows, row_stride, k, out_idx, force_cluster);
+  if (st != LT_OK) return st;
+  if (rows == 0) return LT_OK;
+  Plan plan;
+  int dev = 0;
+  st = make_plan(rows, row_stride, k, false, 4, 1, force_cluster, &plan, &dev);
+  if (st != LT_OK) return st;
+  lt::Params p = {};
+  p.scores = scores;
+  p.lengths = lengths;
+  p.row_stride = row_stride;
+  p.out_idx = out_idx;
+  p.out_val = out_val;
+  p.out_blocks = nullptr;
+  p.counters = counters;
+  p.rows = rows;
+  p.k = k;
+  p.k_blocks = 1;
+  p.force_exact = force_exact ? 1 : 0;
+  p.vec_ok = aligned16(scores, row_stride) ? 1 : 0;
+  return launch(plan, p, rows, stream);
+}
+
+lt_status lt_topk(const float* scores, const int32_t* lengths, int32_t rows, int64_t row_stride,
+                  int32_t k, int32_t* out_idx, float* out_val, void* stream) {
+  return lt_topk_ex(scores, lengths, rows, row_stride, k, out_idx, out_val, 0, 0, nullptr, stream);
+}
+
+lt_status lt_topk_blocked_ex(const float* scores, const int32_t* lengths, int32_t rows,
+                             int64_t row_stride, int32_t block, int32_t k_blocks, int32_t k,
+                             int32_t* out_idx, float* out_val, int32_t* out_blocks,
+                             int32_t force_cluster, int32_t force_exact, int32_t* counters,
+                             void* stream) {
+  lt_status st = check_common(scores, rows, row_stride, k, out_idx, force_cluster);
+  if (st != LT_OK) return st;
+  if (block < 1 || k_blocks < 1) return LT_ERR_INVALID_ARG;
+  if (k_blocks > LT_MAX_K || kernel_slot(true, block) < 0) return LT_ERR_UNSUPPORTED;
+  if (rows == 0) return LT_OK;
+  Plan plan;
+  int dev = 0;
+  st = make_plan(rows, row_stride, k, true, block, k_blocks, force_cluster, &plan, &dev);
+  if (st != LT_OK) return st;
+  lt::Params p = {};
+  p.scores = scores;
+  p.lengths = lengths;
+  p.row_stride = row_stride;
+  p.out_idx = out_idx;
+  p.out_val = out_val;
+  p.out_blocks = out_blocks;
+  p.counters = counters;
+  p.rows = rows;
+  p.k = k;
+  p.k_blocks = k_blocks;
+  p.force_exact = force_exact ? 1 : 0;
+  p.vec_ok = aligned16(scores, row_stride) ? 1 : 0;
+  return launch(plan, p, rows, stream);
+}
+
+lt_status lt_topk_blocked(const float* scores, const int32_t* lengths, int32_t rows,
+                          int64_t row_stride, int32_t block, int32_t k_blocks, int32_t k,
+                          int32_t* out_idx, float* out_val, int32_t* out_blocks, void* stream) {
+  return lt_topk_blocked_ex(scores, lengths, rows, row_stride, block, k_blocks, k, out_idx, out_val,
+                            out_blocks, 0, 0, nullptr, stream);
+}
+
+lt_status lt_topk_plan(int32_t rows, int64_t row_stride, int32_t k, int32_t blocked, int32_t k_blocks,
+                       int32_t force_cluster, int32_t* cluster_size, int32_t* threads_per_cta,
+                       int32_t* smem_bytes) {
+  if (rows < 1 || row_stride < 1 || k < 1) return LT_ERR_INVALID_ARG;
+  if (k > LT_MAX_K || row_stride > LT_MAX_ROW_STRIDE) return LT_ERR_UNSUPPORTED;
+  if (blocked && (k_blocks < 1 || k_blocks > LT_MAX_K)) return LT_ERR_INVALID_ARG;
+  Plan plan;
+  int dev = 0;
+  lt_status st = make_plan(rows, row_stride, k, blocked != 0, 8, blocked ? k_blocks : 1, force_cluster,
+                           &plan, &dev);
+  if (st != LT_OK) return st;
+  if (cluster_size) *cluster_size = plan.cluster;
+  if (threads_per_cta) *threads_per_cta = plan.threads;
+  if (smem_bytes) *smem_bytes = (int32_t)plan.smem;
+  return LT_OK;
+}
+
+const char* lt_status_string(lt_status status) {
+  switch (status) {
+    case LT_OK: return "ok";
+    case LT_ERR_INVALID_ARG: return "invalid argument";
+    case LT_ERR_UNSUPPORTED: return "unsupported by this build (size, block or cluster limit)";
+    case LT_ERR_CUDA: return "CUDA runtime error";
+    default: return "unknown status";
+  }
+}
+
+int32_t lt_version(void) { return 100; }
+
+}  // extern "C"

@@ -1,0 +1,97 @@
+// lt_blocked_kernels.cu -- the two-level (candidate-restricted) top-k kernel.
+#include "lt_kernels.cuh"
+#include "lt_launch.h"
+
+namespace lt {
+
+// Stage A selects the top k_blocks blocks of W positions by block key (the
+// key of the block's best score), ties by lowest block id; stage B selects the
+// top k positions inside the kept blocks, ties by lowest position. The kept
+// block ids are also written in ascending order.
+template <int W>
+__global__ void __launch_bounds__(kThreads, 2) blocked_kernel(Params p) {
+  extern __shared__ __align__(128) unsigned char smem[];
+  Row R;
+  setup_row<W>(R, p, smem);
+  Misc* m = R.m;
+  float4 va[kVecPerRound], vb[kVecPerRound];
+  int na[Geo<W>::kSlots], nb[Geo<W>::kSlots];
+  const int64_t nblocks = (R.L + W - 1) / W;
+  const uint32_t KA = (uint32_t)(nblocks < (int64_t)p.k_blocks ? nblocks : (int64_t)p.k_blocks);
+
+  // ---- stage A: the top k_blocks blocks by (block key desc, block id asc)
+  bool intact;
+  const uint64_t TA =
+      select_stage<W, true>(R, p, va, na, vb, nb, false, KA, nblocks, nblocks, KeepAll{}, &intact, true);
+
+  // ---- kept block ids in ascending order: this CTA's own kept blocks,
+  // sorted, placed after the kept blocks of the lower-ranked slices.
+  const uint64_t* selA = reinterpret_cast<const uint64_t*>(R.sel);
+  const int64_t b0 = R.begin / W, b1 = (R.end + W - 1) / W;
+  uint32_t before = 0, ncand_part = 0;
+  for (uint32_t i = threadIdx.x; i < KA; i += kThreads) {
+    const uint32_t bid = ~(uint32_t)selA[i];
+    before += ((int64_t)bid < b0) ? 1u : 0u;
+    const int64_t lo = (int64_t)bid * W;
+    const int64_t hi = lo + W < R.L ? lo + W : R.L;
+    ncand_part += (uint32_t)(hi - lo);
+  }
+  const uint32_t n_before = block_sum(before, m);
+  const uint32_t ncand = block_sum(ncand_part, m);
+  uint32_t* ids = R.hist;  // own kept ids, stored as ~id so a descending sort is ascending
+  if (threadIdx.x == 0) m->own_count = 0;
+  __syncthreads();
+  for (uint32_t base = 0; base < KA; base += kThreads) {
+    const uint32_t i = base + threadIdx.x;
+    uint32_t bid = 0;
+    bool mine = false;
+    if (i < KA) {
+      bid = ~(uint32_t)selA[i];
+      mine = (int64_t)bid >= b0 && (int64_t)bid < b1;
+    }
+    const unsigned msk = __ballot_sync(kFull, mine);
+    if (msk) {
+      const int lane = threadIdx.x & 31, leader = __ffs(msk) - 1;
+      uint32_t bb = 0;
+      if (lane == leader) bb = atomicAdd(&m->own_count, (uint32_t)__popc(msk));
+      bb = __shfl_sync(kFull, bb, leader);
+      const uint32_t pos = bb + __popc(msk & ((1u << lane) - 1u));
+      if (mine && pos < (uint32_t)kBins) ids[pos] = ~bid;
+    }
+  }
+  __syncthreads();
+  const uint32_t n_own = m->own_count < (uint32_t)kBins ? m->own_count : (uint32_t)kBins;
+  if (p.out_blocks) {
+    uint32_t P = 2;
+    while (P < n_own) P <<= 1;
+    for (uint32_t i = n_own + threadIdx.x; i < P; i += kThreads) ids[i] = 0u;
+    __syncthreads();
+    bitonic_sort_desc(ids, P);
+    int32_t* ob = p.out_blocks + R.row * (int64_t)p.k_blocks;
+    for (uint32_t i = threadIdx.x; i < n_own; i += kThreads) ob[n_before + i] = (int32_t)(~ids[i]);
+    if (R.rank == 0) {
+      for (uint32_t j = KA + threadIdx.x; j < (uint32_t)p.k_blocks; j += kThreads) ob[j] = -1;
+    }
+  }
+  __syncthreads();
+
+  // ---- stage B: the top k among the positions of the kept blocks
+  const uint32_t KB = ncand < (uint32_t)p.k ? ncand : (uint32_t)p.k;
+  bool intact_b;
+  select_stage<W, false>(R, p, va, na, vb, nb, intact, KB, (int64_t)ncand, p.row_stride,
+                         KeepBlocks<W>{TA}, &intact_b, false);
+  write_ordered(R, p, KB, (uint32_t)p.k, [&R](uint32_t idx) { return in_slice(R, idx); });
+  finish_row(R);
+}
+
+const void* blocked_kernel_ptr(int block) {
+  switch (block) {
+    case 4: return reinterpret_cast<const void*>(&blocked_kernel<4>);
+    case 8: return reinterpret_cast<const void*>(&blocked_kernel<8>);
+    case 16: return reinterpret_cast<const void*>(&blocked_kernel<16>);
+    case 32: return reinterpret_cast<const void*>(&blocked_kernel<32>);
+    default: return nullptr;
+  }
+}
+
+}  // namespace lt

@@ -1,0 +1,80 @@
+"""C-ABI checks that need no GPU: the library loads, exports every function the
+header declares, and rejects bad arguments before touching CUDA."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "lt_topk.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from sparse_attention_indexer_lt_gb300 import build, load
+    build.build()
+    return load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(lt_[a-z_]+)\s*\(", text)))
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for n in ["lt_topk", "lt_topk_blocked", "lt_topk_ex", "lt_topk_blocked_ex", "lt_topk_plan",
+              "lt_status_string", "lt_version"]:
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for n in declared_functions():
+        assert hasattr(lib, n), n
+
+
+def test_status_strings_and_version(lib):
+    assert lib.lt_status_string(0) == b"ok"
+    assert b"invalid" in lib.lt_status_string(1)
+    assert lib.lt_status_string(99) == b"unknown status"
+    assert lib.lt_version() >= 100
+
+
+P = ctypes.c_void_p
+
+
+def _topk(lib, scores, lengths, rows, stride, k, oi, ov, fc=0):
+    return lib.lt_topk_ex(scores, lengths, rows, stride, k, oi, ov, fc, 0, None, None)
+
+
+def test_invalid_arguments_rejected_without_launch(lib):
+    fake = P(0x1000)  # never dereferenced: validation fails first
+    assert _topk(lib, None, None, 1, 16, 4, fake, None) == 1  # scores NULL
+    assert _topk(lib, fake, None, 1, 16, 4, None, None) == 1  # out_idx NULL
+    assert _topk(lib, fake, None, -1, 16, 4, fake, None) == 1  # rows < 0
+    assert _topk(lib, fake, None, 1, 0, 4, fake, None) == 1   # row_stride < 1
+    assert _topk(lib, fake, None, 1, 16, 0, fake, None) == 1  # k < 1
+    assert _topk(lib, fake, None, 1, 16, 4, fake, None, fc=3) == 1  # cluster not a power of two
+    assert _topk(lib, fake, None, 1, 16, 4096, fake, None) == 2  # k > LT_MAX_K
+    assert _topk(lib, fake, None, 1, (1 << 30) + 1, 4, fake, None) == 2  # row too long
+    # rows == 0 is a valid no-op
+    assert _topk(lib, None, None, 0, 16, 4, None, None) == 0
+
+
+def test_blocked_invalid_arguments(lib):
+    fake = P(0x1000)
+    f = lib.lt_topk_blocked_ex
+    assert f(fake, None, 1, 64, 0, 4, 4, fake, None, None, 0, 0, None, None) == 1   # block < 1
+    assert f(fake, None, 1, 64, 8, 0, 4, fake, None, None, 0, 0, None, None) == 1   # k_blocks < 1
+    assert f(fake, None, 1, 64, 6, 4, 4, fake, None, None, 0, 0, None, None) == 2   # block unsupported
+    assert f(fake, None, 1, 64, 8, 5000, 4, fake, None, None, 0, 0, None, None) == 2
+    assert f(None, None, 0, 64, 8, 4, 4, None, None, None, 0, 0, None, None) == 0
+
+
+def test_binding_refuses_cpu_tensors():
+    import torch
+    import sparse_attention_indexer_lt_gb300 as lt
+    with pytest.raises(TypeError):
+        lt.topk(torch.zeros(2, 8), None, 2)

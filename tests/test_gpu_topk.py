@@ -1,0 +1,129 @@
+"""GPU parity of lt_topk against the CPU oracle (bit-exact indices and value bits)."""
+import numpy as np
+import pytest
+import torch
+
+import workloads
+from _gpu import counters, gpu_topk, parity_topk
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from sparse_attention_indexer_lt_gb300 import build
+    build.build()
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+
+
+@pytest.mark.parametrize("name", ["c1_single_4096", "c2_decode_262144", "c3_ragged_64", "c4_prefill_4096"])
+def test_workload_parity_and_fast_path(name):
+    S, L, w = workloads.make(name)
+    c = counters()
+    parity_topk(S.numpy(), None if L is None else L.numpy(), w.k, what=name, counters=c)
+    cnt = c.cpu().numpy()
+    assert cnt[0] + cnt[1] == w.rows
+    # the seeded workloads never need the streaming radix select
+    assert cnt[1] == 0, cnt
+
+
+@pytest.mark.parametrize("name", ["c1_single_4096", "c2_decode_262144", "c3_ragged_64"])
+def test_workload_parity_exact_path(name):
+    S, L, w = workloads.make(name)
+    c = counters()
+    parity_topk(S.numpy(), None if L is None else L.numpy(), w.k, what=name + "/exact",
+                force_exact=True, counters=c)
+    assert c.cpu().numpy()[1] == w.rows
+
+
+def test_prefill_rows_exact_path_subset():
+    S, L, w = workloads.make("c4_prefill_4096")
+    sel = list(range(0, 4096, 97))
+    parity_topk(S[sel].numpy(), L[sel].numpy(), w.k, what="c4 subset/exact", force_exact=True)
+
+
+DISTS = ["normal", "bf16", "coarse", "equal", "asc", "desc", "special", "tail"]
+
+
+@pytest.mark.parametrize("dist", DISTS)
+@pytest.mark.parametrize("shape", [(3, 1000), (2, 5000), (2, 40000), (1, 300000)])
+def test_small_distributions(dist, shape):
+    rows, stride = shape
+    S, L = workloads.random_rows(rows, stride, seed=hash((dist, stride)) % 1000, dist=dist,
+                                 lengths="ragged", min_len=0)
+    for k in (1, 64, 512):
+        parity_topk(S.numpy(), L.numpy(), k, what=f"{dist}{shape} k={k}")
+
+
+@pytest.mark.parametrize("k", [1, 512, 2048])
+def test_edge_lengths_and_poisoned_padding(k):
+    stride = 20000
+    lens = [0, 1, 2, 3, 4, 5, 7, 8, 9, k - 1, k, k + 1, 1023, 1024, 1025, 8191, 8192, 8193,
+            16383, 16384, 16385, stride - 1, stride]
+    lens = [max(0, min(stride, x)) for x in lens]
+    S, _ = workloads.random_rows(len(lens), stride, seed=3, dist="bf16")
+    S = S.numpy().copy()
+    for r, l in enumerate(lens):
+        S[r, l:] = np.inf  # never read: positions >= L must not be selected
+    parity_topk(S, np.array(lens, np.int32), k, what=f"edges k={k}")
+
+
+@pytest.mark.parametrize("fc", [1, 2, 4, 8, 16])
+def test_forced_cluster_sizes_agree(fc):
+    S, L = workloads.random_rows(4, 100000, seed=9, dist="bf16", lengths="ragged", min_len=1)
+    parity_topk(S.numpy(), L.numpy(), 512, what=f"cluster {fc}", force_cluster=fc)
+    S2, L2 = workloads.random_rows(3, 70001, seed=10, dist="special", lengths="ragged")
+    parity_topk(S2.numpy(), L2.numpy(), 300, what=f"cluster {fc} special", force_cluster=fc)
+    parity_topk(S2.numpy(), L2.numpy(), 300, what=f"cluster {fc} special exact", force_cluster=fc,
+                force_exact=True)
+
+
+def test_unaligned_rows_take_the_scalar_path():
+    S, L = workloads.random_rows(5, 30001, seed=4, dist="bf16", lengths="ragged")
+    parity_topk(S.numpy(), L.numpy(), 512, what="stride 30001")
+    # a row starting 4 bytes past a 16-byte boundary
+    big = torch.randn(1, 50001, generator=torch.Generator().manual_seed(5))
+    s = big.cuda()[:, 1:]
+    import oracle
+    import sparse_attention_indexer_lt_gb300 as lt
+    idx, val = lt.topk(s, None, 512)
+    oi, ov = oracle.topk(big[:, 1:].contiguous().numpy(), None, 512)
+    assert np.array_equal(idx.cpu().numpy(), oi)
+    assert np.array_equal(val.cpu().numpy().view(np.uint32), ov.view(np.uint32))
+
+
+@pytest.mark.parametrize("k", [1000, 2048])
+def test_large_k(k):
+    S, L = workloads.random_rows(3, 262144, seed=12, dist="bf16", lengths="ragged", min_len=1000)
+    parity_topk(S.numpy(), L.numpy(), k, what=f"k={k}")
+
+
+def test_rows_longer_than_one_register_pass():
+    S, L = workloads.random_rows(2, 1048576, seed=13, dist="normal")
+    parity_topk(S.numpy(), None, 512, what="1M positions")
+    S, L = workloads.random_rows(2, 600000, seed=14, dist="tail", lengths="ragged")
+    parity_topk(S.numpy(), L.numpy(), 512, what="600K ragged", force_cluster=4)
+
+
+def test_determinism_repeated_runs():
+    S, L, w = workloads.make("c3_ragged_64")
+    s, l = S.cuda(), L.cuda()
+    import sparse_attention_indexer_lt_gb300 as lt
+    i0, v0 = lt.topk(s, l, 512)
+    for _ in range(50):
+        i1, v1 = lt.topk(s, l, 512)
+        assert torch.equal(i0, i1) and torch.equal(v0.view(torch.int32), v1.view(torch.int32))
+
+
+def test_values_optional_and_side_stream():
+    import oracle
+    import sparse_attention_indexer_lt_gb300 as lt
+    S, _ = workloads.random_rows(8, 9000, seed=15, dist="normal")
+    s = S.cuda()
+    st = torch.cuda.Stream()
+    with torch.cuda.stream(st):
+        idx, val = lt.topk(s, None, 128, with_values=False)
+    st.synchronize()
+    assert val is None
+    oi, _ = oracle.topk(S.numpy(), None, 128)
+    assert np.array_equal(idx.cpu().numpy(), oi)
