@@ -52,6 +52,8 @@ def parse():
     ap.add_argument("--no-batched", action="store_true", help="headline only")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--only", choices=sorted(workloads.CONFIGS), default=None,
+                    help="time one workload's kernel alone (for profilers); prints a short JSON line")
     return ap.parse_args()
 
 
@@ -318,6 +320,38 @@ def bench_batched(lt, dev, args, world, peak, L2):
     return out
 
 
+def bench_only(args, world):
+    """One workload, one kernel: warmup + steps launches on rotating copies."""
+    import sparse_attention_indexer_lt_gb300 as lt
+    from sparse_attention_indexer_lt_gb300 import build as ltb
+    ltb.build()
+    dev = torch.device("cuda", torch.cuda.current_device())
+    S, L, w = workloads.make(args.only)
+    nbytes = workloads.read_bytes(L, w.rows, w.row_stride)
+    L2 = l2_bytes()
+    ncopies = workloads.l2_rotation_copies(nbytes, L2) if nbytes < 4 * L2 else 1
+    base = S.to(dev)
+    copies = [base] + [base.clone() for _ in range(ncopies - 1)]
+    ld = None if L is None else L.to(dev)
+    oi = torch.empty(w.rows, w.k, dtype=torch.int32, device=dev)
+    ov = torch.empty(w.rows, w.k, dtype=torch.float32, device=dev)
+    ob = torch.empty(w.rows, w.k_blocks, dtype=torch.int32, device=dev) if w.blocked else None
+
+    def step(i):
+        c = copies[i % ncopies]
+        if w.blocked:
+            lt.topk_blocked(c, ld, w.block, w.k_blocks, w.k, out_idx=oi, out_val=ov, out_blocks=ob)
+        else:
+            lt.topk(c, ld, w.k, out_idx=oi, out_val=ov)
+
+    total_ms, per = timed_launches(step, args.steps, args.warmup, world)
+    kern = statistics.mean(per)
+    return {"workload": args.only, "steps": args.steps, "kernel_us_mean": round(kern * 1000, 3),
+            "step_us": round(total_ms * 1000 / args.steps, 3), "read_bytes": nbytes,
+            "hbm_gbs": round(nbytes / (kern * 1e-3) / 1e9, 1), "copies": ncopies,
+            "plan": lt.plan(w.rows, w.row_stride, w.k, blocked=w.blocked, k_blocks=w.k_blocks)}
+
+
 def bench_torch_topk(x, k, args, world):
     steps = max(3, min(args.steps, 50))
     _, per = timed_launches(lambda i: torch.topk(x, k, dim=1, sorted=True), steps, 3, world)
@@ -416,6 +450,11 @@ def main():
             print(json.dumps(bench_reference(args, 1, 0)), flush=True)
         return
     world, rank, local = dist_setup(args.gpus)
+    if args.only:
+        line = bench_only(args, world)
+        if rank == 0:
+            print(json.dumps(line), flush=True)
+        return
     line = bench_ours(args, world, rank)
     if rank == 0:
         print(json.dumps(line), flush=True)
