@@ -89,7 +89,7 @@ lt_status lt_topk(const float* scores, const int32_t* lengths, int32_t rows, int
  * out_idx / out_val are written as for lt_topk; out_blocks[r][*] (if not NULL)
  * receives the kept block ids in ascending order, padded with -1.
  *
- *   block     1 <= block <= 64 and a power of two (the pages use 8)
+ *   block     4, 8, 16 or 32 (the pages use 8)
  *   k_blocks  1 <= k_blocks <= LT_MAX_K
  *   k         1 <= k <= LT_MAX_K
  */
@@ -103,6 +103,8 @@ lt_status lt_topk_blocked(const float* scores, const int32_t* lengths, int32_t r
  *   force_cluster  0 lets the planner choose; 1, 2, 4, 8 or 16 forces the
  *                  number of CTAs that share one row (16 needs a device that
  *                  can schedule a 16-CTA cluster, else LT_ERR_UNSUPPORTED)
+ *   force_threads  0 lets the planner choose; 256 (several CTAs per SM, for
+ *                  large batches) or 1024 (one CTA per SM, for few rows)
  *   force_exact    nonzero skips the sampled-threshold fast path and runs the
  *                  streaming radix select on every row (same results)
  *   counters       NULL, or device int32[LT_NUM_COUNTERS] that the kernel
@@ -115,23 +117,24 @@ lt_status lt_topk_blocked(const float* scores, const int32_t* lengths, int32_t r
 #define LT_NUM_COUNTERS 4
 lt_status lt_topk_ex(const float* scores, const int32_t* lengths, int32_t rows,
                      int64_t row_stride, int32_t k, int32_t* out_idx, float* out_val,
-                     int32_t force_cluster, int32_t force_exact, int32_t* counters,
-                     void* stream);
+                     int32_t force_cluster, int32_t force_threads, int32_t force_exact,
+                     int32_t* counters, void* stream);
 lt_status lt_topk_blocked_ex(const float* scores, const int32_t* lengths, int32_t rows,
                              int64_t row_stride, int32_t block, int32_t k_blocks, int32_t k,
                              int32_t* out_idx, float* out_val, int32_t* out_blocks,
-                             int32_t force_cluster, int32_t force_exact, int32_t* counters,
-                             void* stream);
+                             int32_t force_cluster, int32_t force_threads, int32_t force_exact,
+                             int32_t* counters, void* stream);
 
 /*
  * lt_topk_plan -- the launch the planner would make, without launching.
- * blocked selects the two-level kernel (k_blocks is ignored otherwise).
- * Writes the CTAs per row (cluster size), threads per CTA and dynamic shared
- * memory bytes per CTA to the non-NULL host pointers.
+ * blocked selects the two-level kernel (block and k_blocks are ignored
+ * otherwise). Writes the CTAs per row (cluster size), threads per CTA and
+ * dynamic shared memory bytes per CTA to the non-NULL host pointers.
  */
 lt_status lt_topk_plan(int32_t rows, int64_t row_stride, int32_t k, int32_t blocked,
-                       int32_t k_blocks, int32_t force_cluster, int32_t* cluster_size,
-                       int32_t* threads_per_cta, int32_t* smem_bytes);
+                       int32_t block, int32_t k_blocks, int32_t force_cluster,
+                       int32_t force_threads, int32_t* cluster_size, int32_t* threads_per_cta,
+                       int32_t* smem_bytes);
 
 /* Static description of a status code. */
 const char* lt_status_string(lt_status status);

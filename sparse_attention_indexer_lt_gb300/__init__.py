@@ -49,13 +49,13 @@ def load() -> ctypes.CDLL:
     i32, i64, vp = ctypes.c_int32, ctypes.c_int64, ctypes.c_void_p
     lib.lt_topk.argtypes = [vp, vp, i32, i64, i32, vp, vp, vp]
     lib.lt_topk.restype = ctypes.c_int
-    lib.lt_topk_ex.argtypes = [vp, vp, i32, i64, i32, vp, vp, i32, i32, vp, vp]
+    lib.lt_topk_ex.argtypes = [vp, vp, i32, i64, i32, vp, vp, i32, i32, i32, vp, vp]
     lib.lt_topk_ex.restype = ctypes.c_int
     lib.lt_topk_blocked.argtypes = [vp, vp, i32, i64, i32, i32, i32, vp, vp, vp, vp]
     lib.lt_topk_blocked.restype = ctypes.c_int
-    lib.lt_topk_blocked_ex.argtypes = [vp, vp, i32, i64, i32, i32, i32, vp, vp, vp, i32, i32, vp, vp]
+    lib.lt_topk_blocked_ex.argtypes = [vp, vp, i32, i64, i32, i32, i32, vp, vp, vp, i32, i32, i32, vp, vp]
     lib.lt_topk_blocked_ex.restype = ctypes.c_int
-    lib.lt_topk_plan.argtypes = [i32, i64, i32, i32, i32, i32, vp, vp, vp]
+    lib.lt_topk_plan.argtypes = [i32, i64, i32, i32, i32, i32, i32, i32, vp, vp, vp]
     lib.lt_topk_plan.restype = ctypes.c_int
     lib.lt_status_string.argtypes = [ctypes.c_int]
     lib.lt_status_string.restype = ctypes.c_char_p
@@ -122,8 +122,9 @@ def _counters(c, device):
 
 def topk(scores: torch.Tensor, lengths: torch.Tensor | None = None, k: int = 512, *,
          out_idx: torch.Tensor | None = None, out_val: torch.Tensor | None = None,
-         with_values: bool = True, force_cluster: int = 0, force_exact: bool = False,
-         counters: torch.Tensor | None = None, stream: torch.cuda.Stream | None = None):
+         with_values: bool = True, force_cluster: int = 0, force_threads: int = 0,
+         force_exact: bool = False, counters: torch.Tensor | None = None,
+         stream: torch.cuda.Stream | None = None):
     """Per-row top-k by (score desc, index asc); returns (idx int32 [rows, k], val float32 [rows, k] or None)."""
     lib = load()
     rows, n = _check_scores(scores)
@@ -138,8 +139,8 @@ def topk(scores: torch.Tensor, lengths: torch.Tensor | None = None, k: int = 512
     with torch.cuda.device(dev):
         s = (stream or torch.cuda.current_stream(dev)).cuda_stream
         st = lib.lt_topk_ex(_ptr(scores), _ptr(lengths), rows, max(n, 1), int(k), _ptr(out_idx),
-                            _ptr(out_val), int(force_cluster), int(bool(force_exact)),
-                            _ptr(counters), ctypes.c_void_p(s))
+                            _ptr(out_val), int(force_cluster), int(force_threads),
+                            int(bool(force_exact)), _ptr(counters), ctypes.c_void_p(s))
     if st != 0:
         raise LtError("lt_topk", st)
     return out_idx, out_val
@@ -149,7 +150,8 @@ def topk_blocked(scores: torch.Tensor, lengths: torch.Tensor | None = None, bloc
                  k_blocks: int = 2048, k: int = 512, *, out_idx: torch.Tensor | None = None,
                  out_val: torch.Tensor | None = None, out_blocks: torch.Tensor | None = None,
                  with_values: bool = True, with_blocks: bool = True, force_cluster: int = 0,
-                 force_exact: bool = False, counters: torch.Tensor | None = None,
+                 force_threads: int = 0, force_exact: bool = False,
+                 counters: torch.Tensor | None = None,
                  stream: torch.cuda.Stream | None = None):
     """Two-level top-k; returns (idx [rows, k], val [rows, k] or None, blocks [rows, k_blocks] or None)."""
     lib = load()
@@ -164,21 +166,23 @@ def topk_blocked(scores: torch.Tensor, lengths: torch.Tensor | None = None, bloc
         s = (stream or torch.cuda.current_stream(dev)).cuda_stream
         st = lib.lt_topk_blocked_ex(_ptr(scores), _ptr(lengths), rows, max(n, 1), int(block),
                                     int(k_blocks), int(k), _ptr(out_idx), _ptr(out_val),
-                                    _ptr(out_blocks), int(force_cluster), int(bool(force_exact)),
-                                    _ptr(counters), ctypes.c_void_p(s))
+                                    _ptr(out_blocks), int(force_cluster), int(force_threads),
+                                    int(bool(force_exact)), _ptr(counters), ctypes.c_void_p(s))
     if st != 0:
         raise LtError("lt_topk_blocked", st)
     return out_idx, out_val, out_blocks
 
 
-def plan(rows: int, row_stride: int, k: int, *, blocked: bool = False, k_blocks: int = 2048,
-         force_cluster: int = 0, device: int | None = None) -> dict:
+def plan(rows: int, row_stride: int, k: int, *, blocked: bool = False, block: int = 8,
+         k_blocks: int = 2048, force_cluster: int = 0, force_threads: int = 0,
+         device: int | None = None) -> dict:
     """The launch the planner would make: {'cluster', 'threads', 'smem'}."""
     lib = load()
     c, t, s = ctypes.c_int32(), ctypes.c_int32(), ctypes.c_int32()
     with torch.cuda.device(device if device is not None else torch.cuda.current_device()):
-        st = lib.lt_topk_plan(int(rows), int(row_stride), int(k), int(bool(blocked)), int(k_blocks),
-                              int(force_cluster), ctypes.byref(c), ctypes.byref(t), ctypes.byref(s))
+        st = lib.lt_topk_plan(int(rows), int(row_stride), int(k), int(bool(blocked)), int(block),
+                              int(k_blocks), int(force_cluster), int(force_threads), ctypes.byref(c),
+                              ctypes.byref(t), ctypes.byref(s))
     if st != 0:
         raise LtError("lt_topk_plan", st)
     return {"cluster": c.value, "threads": t.value, "smem": s.value}

@@ -1,11 +1,14 @@
 // lt_api.cu -- the C ABI: argument checks, launch planning and launches.
 //
-// Planning. One cluster of C CTAs owns one row. C is 1 when the batch alone
-// fills the GPU; otherwise it doubles (up to 16, the largest cluster an
-// sm_103a GPC can host) while rows * C stays below two CTAs per SM and each
-// CTA still gets at least one round of the row (8192 positions). A 16-CTA
-// cluster is non-portable: the plan asks the occupancy calculator whether one
-// can be scheduled with the chosen shared memory and halves C if not.
+// Planning. One cluster of C CTAs owns one row. Two CTA shapes exist:
+//   narrow: 256 threads, several CTAs per SM -- used when the batch alone has
+//           at least one row per SM (C = 1: no cluster traffic at all);
+//   wide:   1024 threads, one CTA per SM -- used for few rows. C doubles (up
+//           to 16, the largest cluster a GPC can host) while the whole grid
+//           still fits on the SMs and each CTA still gets at least one round
+//           (16384 positions) of the row.
+// A 16-CTA cluster is non-portable: the plan asks the occupancy calculator
+// whether one can be scheduled with the chosen shared memory, halving C if not.
 
 #include <cuda_runtime.h>
 
@@ -20,7 +23,10 @@
 namespace {
 
 constexpr int kMaxDevices = 64;
-constexpr int kPositionsPerRound = lt::kThreads * lt::kVecPerRound * 4;  // 8192
+constexpr int kWideThreads = 1024;
+constexpr int kNarrowThreads = 256;
+constexpr int64_t kWideRound = 1024 * 4 * 4;  // positions per CTA per round (wide)
+constexpr int kSlots = 10;                    // kernel variants
 
 struct DeviceInfo {
   bool ready = false;
@@ -30,18 +36,24 @@ struct DeviceInfo {
 
 std::mutex g_mu;
 DeviceInfo g_dev[kMaxDevices];
-int g_smem_set[kMaxDevices][8];  // largest dynamic smem already granted per kernel slot
-bool g_nonportable_set[kMaxDevices][8];
+int g_smem_set[kMaxDevices][kSlots];  // largest dynamic smem already granted per kernel
+bool g_nonportable_set[kMaxDevices][kSlots];
 
-int kernel_slot(bool blocked, int block) {
-  if (!blocked) return 0;
+int block_index(int block) {
   switch (block) {
-    case 4: return 1;
-    case 8: return 2;
-    case 16: return 3;
-    case 32: return 4;
+    case 4: return 0;
+    case 8: return 1;
+    case 16: return 2;
+    case 32: return 3;
     default: return -1;
   }
+}
+
+int kernel_slot(bool blocked, int block, int threads) {
+  const int wide = threads == kWideThreads ? 1 : 0;
+  if (!blocked) return wide;
+  const int b = block_index(block);
+  return b < 0 ? -1 : 2 + 2 * b + wide;
 }
 
 uint32_t next_pow2(uint32_t x) {
@@ -52,7 +64,7 @@ uint32_t next_pow2(uint32_t x) {
 
 struct Plan {
   int cluster = 1;
-  int threads = lt::kThreads;
+  int threads = kNarrowThreads;
   uint32_t cap = 0;
   uint32_t sel_cap = 0;
   uint32_t smem = 0;
@@ -92,10 +104,10 @@ lt_status prepare_kernel(int dev, int slot, const void* func, uint32_t smem, int
   return LT_OK;
 }
 
-bool cluster_fits(const void* func, int cluster, uint32_t smem) {
+bool cluster_fits(const void* func, int cluster, int threads, uint32_t smem) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)cluster);
-  cfg.blockDim = dim3(lt::kThreads);
+  cfg.blockDim = dim3((unsigned)threads);
   cfg.dynamicSmemBytes = smem;
   cudaLaunchAttribute attr;
   attr.id = cudaLaunchAttributeClusterDimension;
@@ -113,14 +125,19 @@ bool cluster_fits(const void* func, int cluster, uint32_t smem) {
 }
 
 lt_status make_plan(int32_t rows, int64_t row_stride, int32_t k, bool blocked, int32_t block,
-                    int32_t k_blocks, int32_t force_cluster, Plan* plan, int* dev_out) {
+                    int32_t k_blocks, int32_t force_cluster, int32_t force_threads, Plan* plan,
+                    int* dev_out) {
   DeviceInfo* di = nullptr;
   int dev = 0;
   lt_status st = device_info(&di, &dev);
   if (st != LT_OK) return st;
-  const int slot = kernel_slot(blocked, block);
+
+  int threads = force_threads;
+  if (threads == 0) threads = (int64_t)rows >= di->sms ? kNarrowThreads : kWideThreads;
+  const int slot = kernel_slot(blocked, block, threads);
   if (slot < 0) return LT_ERR_UNSUPPORTED;
-  plan->func = blocked ? lt::blocked_kernel_ptr(block) : lt::topk_kernel_ptr();
+  plan->threads = threads;
+  plan->func = blocked ? lt::blocked_kernel_ptr(threads, block) : lt::topk_kernel_ptr(threads);
   if (!plan->func) return LT_ERR_UNSUPPORTED;
 
   const uint32_t kmax = (uint32_t)(blocked ? (k > k_blocks ? k : k_blocks) : k);
@@ -132,16 +149,15 @@ lt_status make_plan(int32_t rows, int64_t row_stride, int32_t k, bool blocked, i
   int c = 1;
   if (force_cluster > 0) {
     c = force_cluster;
-  } else {
-    const int64_t useful = (row_stride + kPositionsPerRound - 1) / kPositionsPerRound;
-    while (c < 16 && c < useful && (int64_t)rows * c < 2LL * di->sms) c *= 2;
+  } else if (threads == kWideThreads) {
+    while (c < 16 && (int64_t)rows * 2 * c <= di->sms && (int64_t)c * kWideRound < row_stride) c *= 2;
   }
   for (;;) {
     const uint32_t smem = lt::make_layout(c > 1, plan->cap, plan->sel_cap).total;
     if ((int)smem > di->smem_optin) return LT_ERR_UNSUPPORTED;
     st = prepare_kernel(dev, slot, plan->func, smem, c);
     if (st != LT_OK && !(st == LT_ERR_UNSUPPORTED && force_cluster == 0 && c > 8)) return st;
-    if (st == LT_OK && (c == 1 || cluster_fits(plan->func, c, smem))) {
+    if (st == LT_OK && (c == 1 || cluster_fits(plan->func, c, threads, smem))) {
       plan->cluster = c;
       plan->smem = smem;
       break;
@@ -155,8 +171,10 @@ lt_status make_plan(int32_t rows, int64_t row_stride, int32_t k, bool blocked, i
 }
 
 lt_status check_common(const float* scores, int32_t rows, int64_t row_stride, int32_t k,
-                       const int32_t* out_idx, int32_t force_cluster) {
+                       const int32_t* out_idx, int32_t force_cluster, int32_t force_threads) {
   if (rows < 0 || row_stride < 1 || k < 1) return LT_ERR_INVALID_ARG;
+  if (!(force_threads == 0 || force_threads == kNarrowThreads || force_threads == kWideThreads))
+    return LT_ERR_INVALID_ARG;
   if (rows > 0 && (scores == nullptr || out_idx == nullptr)) return LT_ERR_INVALID_ARG;
   if (!(force_cluster == 0 || force_cluster == 1 || force_cluster == 2 || force_cluster == 4 ||
         force_cluster == 8 || force_cluster == 16))
@@ -172,7 +190,7 @@ lt_status launch(const Plan& plan, const lt::Params& prm, int32_t rows, void* st
   p.clustered = plan.cluster > 1 ? 1 : 0;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)((int64_t)rows * plan.cluster));
-  cfg.blockDim = dim3(lt::kThreads);
+  cfg.blockDim = dim3((unsigned)plan.threads);
   cfg.dynamicSmemBytes = plan.smem;
   cfg.stream = static_cast<cudaStream_t>(stream);
   cudaLaunchAttribute attr;
@@ -196,13 +214,13 @@ extern "C" {
 
 lt_status lt_topk_ex(const float* scores, const int32_t* lengths, int32_t rows, int64_t row_stride,
                      int32_t k, int32_t* out_idx, float* out_val, int32_t force_cluster,
-                     int32_t force_exact, int32_t* counters, void* stream) {
-  lt_status st = check_common(scores, rows, row_stride, k, out_idx, force_cluster);
+                     int32_t force_threads, int32_t force_exact, int32_t* counters, void* stream) {
+  lt_status st = check_common(scores, rows, row_stride, k, out_idx, force_cluster, force_threads);
   if (st != LT_OK) return st;
   if (rows == 0) return LT_OK;
   Plan plan;
   int dev = 0;
-  st = make_plan(rows, row_stride, k, false, 4, 1, force_cluster, &plan, &dev);
+  st = make_plan(rows, row_stride, k, false, 4, 1, force_cluster, force_threads, &plan, &dev);
   if (st != LT_OK) return st;
   lt::Params p = {};
   p.scores = scores;
@@ -222,22 +240,22 @@ lt_status lt_topk_ex(const float* scores, const int32_t* lengths, int32_t rows, 
 
 lt_status lt_topk(const float* scores, const int32_t* lengths, int32_t rows, int64_t row_stride,
                   int32_t k, int32_t* out_idx, float* out_val, void* stream) {
-  return lt_topk_ex(scores, lengths, rows, row_stride, k, out_idx, out_val, 0, 0, nullptr, stream);
+  return lt_topk_ex(scores, lengths, rows, row_stride, k, out_idx, out_val, 0, 0, 0, nullptr, stream);
 }
 
 lt_status lt_topk_blocked_ex(const float* scores, const int32_t* lengths, int32_t rows,
                              int64_t row_stride, int32_t block, int32_t k_blocks, int32_t k,
                              int32_t* out_idx, float* out_val, int32_t* out_blocks,
-                             int32_t force_cluster, int32_t force_exact, int32_t* counters,
-                             void* stream) {
-  lt_status st = check_common(scores, rows, row_stride, k, out_idx, force_cluster);
+                             int32_t force_cluster, int32_t force_threads, int32_t force_exact,
+                             int32_t* counters, void* stream) {
+  lt_status st = check_common(scores, rows, row_stride, k, out_idx, force_cluster, force_threads);
   if (st != LT_OK) return st;
   if (block < 1 || k_blocks < 1) return LT_ERR_INVALID_ARG;
-  if (k_blocks > LT_MAX_K || kernel_slot(true, block) < 0) return LT_ERR_UNSUPPORTED;
+  if (k_blocks > LT_MAX_K || block_index(block) < 0) return LT_ERR_UNSUPPORTED;
   if (rows == 0) return LT_OK;
   Plan plan;
   int dev = 0;
-  st = make_plan(rows, row_stride, k, true, block, k_blocks, force_cluster, &plan, &dev);
+  st = make_plan(rows, row_stride, k, true, block, k_blocks, force_cluster, force_threads, &plan, &dev);
   if (st != LT_OK) return st;
   lt::Params p = {};
   p.scores = scores;
@@ -259,19 +277,22 @@ lt_status lt_topk_blocked(const float* scores, const int32_t* lengths, int32_t r
                           int64_t row_stride, int32_t block, int32_t k_blocks, int32_t k,
                           int32_t* out_idx, float* out_val, int32_t* out_blocks, void* stream) {
   return lt_topk_blocked_ex(scores, lengths, rows, row_stride, block, k_blocks, k, out_idx, out_val,
-                            out_blocks, 0, 0, nullptr, stream);
+                            out_blocks, 0, 0, 0, nullptr, stream);
 }
 
-lt_status lt_topk_plan(int32_t rows, int64_t row_stride, int32_t k, int32_t blocked, int32_t k_blocks,
-                       int32_t force_cluster, int32_t* cluster_size, int32_t* threads_per_cta,
-                       int32_t* smem_bytes) {
+lt_status lt_topk_plan(int32_t rows, int64_t row_stride, int32_t k, int32_t blocked, int32_t block,
+                       int32_t k_blocks, int32_t force_cluster, int32_t force_threads,
+                       int32_t* cluster_size, int32_t* threads_per_cta, int32_t* smem_bytes) {
   if (rows < 1 || row_stride < 1 || k < 1) return LT_ERR_INVALID_ARG;
+  if (!(force_threads == 0 || force_threads == kNarrowThreads || force_threads == kWideThreads))
+    return LT_ERR_INVALID_ARG;
+  if (blocked && block_index(block) < 0) return LT_ERR_UNSUPPORTED;
   if (k > LT_MAX_K || row_stride > LT_MAX_ROW_STRIDE) return LT_ERR_UNSUPPORTED;
   if (blocked && (k_blocks < 1 || k_blocks > LT_MAX_K)) return LT_ERR_INVALID_ARG;
   Plan plan;
   int dev = 0;
-  lt_status st = make_plan(rows, row_stride, k, blocked != 0, 8, blocked ? k_blocks : 1, force_cluster,
-                           &plan, &dev);
+  lt_status st = make_plan(rows, row_stride, k, blocked != 0, blocked ? block : 4, blocked ? k_blocks : 1,
+                           force_cluster, force_threads, &plan, &dev);
   if (st != LT_OK) return st;
   if (cluster_size) *cluster_size = plan.cluster;
   if (threads_per_cta) *threads_per_cta = plan.threads;
@@ -289,6 +310,6 @@ const char* lt_status_string(lt_status status) {
   }
 }
 
-int32_t lt_version(void) { return 100; }
+int32_t lt_version(void) { return 200; }
 
 }  // extern "C"

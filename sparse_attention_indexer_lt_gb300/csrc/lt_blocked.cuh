@@ -1,0 +1,112 @@
+// lt_blocked.cuh -- the two-level (candidate-restricted) top-k kernel.
+#pragma once
+
+#include "lt_kernels.cuh"
+
+namespace lt {
+
+// Stage A selects the top k_blocks blocks of W positions by block key (the
+// key of the block's best score), ties by lowest block id; stage B selects the
+// top k positions inside the kept blocks, ties by lowest position. The kept
+// block ids are also written in ascending order.
+template <int T, int W>
+__global__ void __launch_bounds__(T, (T <= 256 ? 3 : 1)) blocked_kernel(Params p) {
+  constexpr int U = (W / 4 > 4) ? W / 4 : 4;
+  using G = Geo<T, U, W>;
+  extern __shared__ __align__(128) unsigned char smem[];
+  Row R;
+  setup_row<T, U, W>(R, p, smem);
+  Misc* m = R.m;
+  float4 va[U], vb[U];
+  int na[G::kSlots], nb[G::kSlots];
+  const int64_t nblocks = (R.L + W - 1) / W;
+  const uint32_t KA = (uint32_t)(nblocks < (int64_t)p.k_blocks ? nblocks : (int64_t)p.k_blocks);
+  const uint32_t cap = (uint32_t)p.cap;
+
+  // ---- stage A: the top k_blocks blocks by (block key desc, block id asc)
+  bool intact;
+  uint64_t TcA;
+  const bool exactA = select_stage<T, U, W, true>(R, p, va, na, vb, nb, false, KA, nblocks, nblocks,
+                                                  KeepAll{}, true, &intact, &TcA);
+  uint64_t TA = 0;
+  if (KA > 0) {
+    const uint32_t NA = exactA ? KA : (m->cand_count < cap ? m->cand_count : cap);
+    TA = exactA ? TcA : select_local<T>(R, NA, KA, nblocks);
+    compact_selected<T>(R, NA, TA);  // stage[0, KA) = kept block composites
+  }
+
+  // ---- kept block ids in ascending order: this CTA's own kept blocks,
+  // sorted, placed after the kept blocks of the lower-ranked slices.
+  const int64_t b0 = R.begin / W, b1 = (R.end + W - 1) / W;
+  uint32_t before = 0, ncand_part = 0;
+  for (uint32_t i = threadIdx.x; i < KA; i += T) {
+    const uint32_t bid = ~(uint32_t)R.stage[i];
+    before += ((int64_t)bid < b0) ? 1u : 0u;
+    const int64_t lo = (int64_t)bid * W;
+    const int64_t hi = lo + W < R.L ? lo + W : R.L;
+    ncand_part += (uint32_t)(hi - lo);
+  }
+  const uint32_t n_before = block_sum<T>(before, m);
+  const uint32_t ncand = block_sum<T>(ncand_part, m);
+  if (p.out_blocks) {
+    uint32_t* ids = R.hist;  // own kept ids as ~id, so a descending sort is ascending
+    if (threadIdx.x == 0) m->own_count = 0;
+    __syncthreads();
+    for (uint32_t base = 0; base < KA; base += T) {
+      const uint32_t i = base + threadIdx.x;
+      uint32_t bid = 0;
+      bool mine = false;
+      if (i < KA) {
+        bid = ~(uint32_t)R.stage[i];
+        mine = (int64_t)bid >= b0 && (int64_t)bid < b1;
+      }
+      const unsigned msk = __ballot_sync(kFull, mine);
+      if (msk) {
+        const uint32_t lane = lane_id();
+        const int leader = __ffs(msk) - 1;
+        uint32_t bb = 0;
+        if ((int)lane == leader) bb = atomicAdd(&m->own_count, (uint32_t)__popc(msk));
+        bb = __shfl_sync(kFull, bb, leader);
+        const uint32_t pos = bb + (uint32_t)__popc(msk & ((1u << lane) - 1u));
+        if (mine && pos < (uint32_t)kBins) ids[pos] = ~bid;
+      }
+    }
+    __syncthreads();
+    const uint32_t n_own = m->own_count < (uint32_t)kBins ? m->own_count : (uint32_t)kBins;
+    uint32_t P = 2;
+    while (P < n_own) P <<= 1;
+    for (uint32_t i = n_own + threadIdx.x; i < P; i += T) ids[i] = 0u;
+    __syncthreads();
+    bitonic_sort_desc<T>(ids, P);
+    int32_t* ob = p.out_blocks + R.row * (int64_t)p.k_blocks;
+    for (uint32_t i = threadIdx.x; i < n_own; i += T) ob[n_before + i] = (int32_t)(~ids[i]);
+    if (R.rank == 0) {
+      for (uint32_t j = KA + threadIdx.x; j < (uint32_t)p.k_blocks; j += T) ob[j] = -1;
+    }
+  }
+  __syncthreads();
+
+  // ---- stage B: the top k among the positions of the kept blocks
+  const uint32_t KB = ncand < (uint32_t)p.k ? ncand : (uint32_t)p.k;
+  bool intact_b;
+  uint64_t TcB;
+  const bool exactB = select_stage<T, U, W, false>(R, p, va, na, vb, nb, intact, KB, (int64_t)ncand,
+                                                   p.row_stride, KeepBlocks<T, U, W>{TA}, false,
+                                                   &intact_b, &TcB);
+  output_positions<T>(R, p, exactB, TcB, KB, p.row_stride,
+                      [&R](uint32_t idx) { return R.nclus == 1 || in_slice(R, idx); });
+  finish_row(R);
+}
+
+template <int T>
+inline const void* blocked_ptr(int block) {
+  switch (block) {
+    case 4: return reinterpret_cast<const void*>(&blocked_kernel<T, 4>);
+    case 8: return reinterpret_cast<const void*>(&blocked_kernel<T, 8>);
+    case 16: return reinterpret_cast<const void*>(&blocked_kernel<T, 16>);
+    case 32: return reinterpret_cast<const void*>(&blocked_kernel<T, 32>);
+    default: return nullptr;
+  }
+}
+
+}  // namespace lt

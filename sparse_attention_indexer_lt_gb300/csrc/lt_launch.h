@@ -2,7 +2,10 @@
 #pragma once
 
 namespace lt {
-struct Params;
-const void* topk_kernel_ptr();
-const void* blocked_kernel_ptr(int block);  // nullptr for an unsupported block size
+// threads is 256 (batched rows, several CTAs per SM) or 1024 (few rows, one CTA per SM).
+const void* topk_kernel_ptr(int threads);
+// nullptr for an unsupported block size.
+const void* blocked_kernel_ptr(int threads, int block);
+const void* blocked_kernel_ptr_narrow(int block);
+const void* blocked_kernel_ptr_wide(int block);
 }  // namespace lt

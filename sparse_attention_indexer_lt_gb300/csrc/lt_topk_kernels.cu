@@ -6,19 +6,28 @@ namespace lt {
 
 // One CTA (or one cluster of CTAs) per row: select the top K = min(k, L)
 // positions and write them ordered by (score desc, index asc).
-__global__ void __launch_bounds__(kThreads, 2) topk_kernel(Params p) {
+template <int T, int U>
+__global__ void __launch_bounds__(T, (T <= 256 ? 3 : 1)) topk_kernel(Params p) {
   extern __shared__ __align__(128) unsigned char smem[];
+  using G = Geo<T, U, 4>;
   Row R;
-  setup_row<4>(R, p, smem);
-  float4 va[kVecPerRound], vb[kVecPerRound];
-  int na[Geo<4>::kSlots], nb[Geo<4>::kSlots];
+  setup_row<T, U, 4>(R, p, smem);
+  float4 va[U], vb[U];
+  int na[G::kSlots], nb[G::kSlots];
   const uint32_t K = (uint32_t)(R.L < (int64_t)p.k ? R.L : (int64_t)p.k);
   bool intact;
-  select_stage<4, false>(R, p, va, na, vb, nb, false, K, R.L, p.row_stride, KeepAll{}, &intact, true);
-  write_ordered(R, p, K, (uint32_t)p.k, [&R](uint32_t idx) { return in_slice(R, idx); });
+  uint64_t Tc;
+  const bool exact = select_stage<T, U, 4, false>(R, p, va, na, vb, nb, false, K, R.L, p.row_stride,
+                                                  KeepAll{}, true, &intact, &Tc);
+  output_positions<T>(R, p, exact, Tc, K, p.row_stride,
+                      [&R](uint32_t idx) { return R.nclus == 1 || in_slice(R, idx); });
   finish_row(R);
 }
 
-const void* topk_kernel_ptr() { return reinterpret_cast<const void*>(&topk_kernel); }
+const void* topk_kernel_ptr(int threads) {
+  if (threads == 256) return reinterpret_cast<const void*>(&topk_kernel<256, 4>);
+  if (threads == 1024) return reinterpret_cast<const void*>(&topk_kernel<1024, 4>);
+  return nullptr;
+}
 
 }  // namespace lt
