@@ -29,19 +29,30 @@ def test_blocked_workload_exact_path():
     parity_blocked(S[:4].numpy(), None, w.block, w.k_blocks, w.k, what="c5/exact", force_exact=True)
 
 
+@pytest.mark.parametrize("ft", [256, 1024])
 @pytest.mark.parametrize("block", [4, 8, 16, 32])
 @pytest.mark.parametrize("dist", ["normal", "coarse", "special", "equal", "asc"])
-def test_blocked_small(block, dist):
+def test_blocked_small(block, dist, ft):
     S, L = workloads.random_rows(3, 30000, seed=block * 7 + len(dist), dist=dist, lengths="ragged")
     for kb, k in [(16, 512), (300, 100), (2048, 512), (64, 64)]:
-        parity_blocked(S.numpy(), L.numpy(), block, kb, k, what=f"{dist} B={block} kb={kb} k={k}")
+        parity_blocked(S.numpy(), L.numpy(), block, kb, k, what=f"{dist} B={block} kb={kb} k={k} t={ft}",
+                       force_threads=ft)
 
 
+@pytest.mark.parametrize("ft", [256, 1024])
 @pytest.mark.parametrize("fc", [1, 2, 4, 8, 16])
-def test_blocked_forced_clusters(fc):
+def test_blocked_forced_plans(fc, ft):
     S, L = workloads.random_rows(2, 262144, seed=31, dist="bf16", lengths="ragged", min_len=1)
-    parity_blocked(S.numpy(), L.numpy(), 8, 2048, 512, what=f"cluster {fc}", force_cluster=fc)
-    parity_blocked(S.numpy(), L.numpy(), 8, 200, 512, what=f"cluster {fc} kb<k", force_cluster=fc)
+    parity_blocked(S.numpy(), L.numpy(), 8, 2048, 512, what=f"cluster {fc}x{ft}", force_cluster=fc,
+                   force_threads=ft)
+    parity_blocked(S.numpy(), L.numpy(), 8, 200, 512, what=f"cluster {fc}x{ft} kb<k", force_cluster=fc,
+                   force_threads=ft)
+
+
+@pytest.mark.parametrize("ft", [256, 1024])
+def test_blocked_workload_both_cta_shapes(ft):
+    S, L, w = workloads.make("c5_blocked_16")
+    parity_blocked(S.numpy(), None, w.block, w.k_blocks, w.k, what=f"c5/{ft}", force_threads=ft)
 
 
 def test_blocked_edge_lengths():

@@ -68,14 +68,26 @@ def test_edge_lengths_and_poisoned_padding(k):
     parity_topk(S, np.array(lens, np.int32), k, what=f"edges k={k}")
 
 
+@pytest.mark.parametrize("ft", [256, 1024])
 @pytest.mark.parametrize("fc", [1, 2, 4, 8, 16])
-def test_forced_cluster_sizes_agree(fc):
+def test_forced_plans_agree(fc, ft):
     S, L = workloads.random_rows(4, 100000, seed=9, dist="bf16", lengths="ragged", min_len=1)
-    parity_topk(S.numpy(), L.numpy(), 512, what=f"cluster {fc}", force_cluster=fc)
+    parity_topk(S.numpy(), L.numpy(), 512, what=f"cluster {fc}x{ft}", force_cluster=fc, force_threads=ft)
     S2, L2 = workloads.random_rows(3, 70001, seed=10, dist="special", lengths="ragged")
-    parity_topk(S2.numpy(), L2.numpy(), 300, what=f"cluster {fc} special", force_cluster=fc)
-    parity_topk(S2.numpy(), L2.numpy(), 300, what=f"cluster {fc} special exact", force_cluster=fc,
-                force_exact=True)
+    parity_topk(S2.numpy(), L2.numpy(), 300, what=f"cluster {fc}x{ft} special", force_cluster=fc,
+                force_threads=ft)
+    parity_topk(S2.numpy(), L2.numpy(), 300, what=f"cluster {fc}x{ft} special exact", force_cluster=fc,
+                force_threads=ft, force_exact=True)
+    S3, L3 = workloads.random_rows(5, 9000, seed=11, dist="coarse", lengths="ragged")
+    parity_topk(S3.numpy(), L3.numpy(), 700, what=f"cluster {fc}x{ft} coarse", force_cluster=fc,
+                force_threads=ft)
+
+
+@pytest.mark.parametrize("ft", [256, 1024])
+@pytest.mark.parametrize("name", ["c1_single_4096", "c2_decode_262144", "c3_ragged_64"])
+def test_workloads_both_cta_shapes(name, ft):
+    S, L, w = workloads.make(name)
+    parity_topk(S.numpy(), None if L is None else L.numpy(), w.k, what=f"{name}/{ft}", force_threads=ft)
 
 
 def test_unaligned_rows_take_the_scalar_path():
