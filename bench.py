@@ -52,6 +52,10 @@ def parse():
     ap.add_argument("--no-batched", action="store_true", help="headline only")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--trace", choices=sorted(workloads.CONFIGS), default=None,
+                    help="print per-phase kernel timestamps (thread 0 of each CTA) for one workload")
+    ap.add_argument("--force-threads", type=int, default=0)
+    ap.add_argument("--force-cluster", type=int, default=0)
     ap.add_argument("--only", choices=sorted(workloads.CONFIGS), default=None,
                     help="time one workload's kernel alone (for profilers); prints a short JSON line")
     return ap.parse_args()
@@ -352,6 +356,51 @@ def bench_only(args, world):
             "plan": lt.plan(w.rows, w.row_stride, w.k, blocked=w.blocked, k_blocks=w.k_blocks)}
 
 
+TRACE_NAMES = ["start", "hist", "merge", "estimate", "filter", "exchange", "exact", "output",
+               "B.start", "B.hist", "B.merge", "B.estimate", "B.filter", "B.exchange", "B.exact", "B.unused"]
+
+
+def bench_trace(args):
+    """Phase timestamps of one launch: per phase, the median and max over CTAs of
+    the time since that CTA started, and the median time since the first CTA started."""
+    import sparse_attention_indexer_lt_gb300 as lt
+    from sparse_attention_indexer_lt_gb300 import build as ltb
+    ltb.build()
+    dev = torch.device("cuda", torch.cuda.current_device())
+    S, L, w = workloads.make(args.trace)
+    base = S.to(dev)
+    copies = [base] + [base.clone() for _ in range(3)]
+    ld = None if L is None else L.to(dev)
+    pl = lt.plan(w.rows, w.row_stride, w.k, blocked=w.blocked, k_blocks=w.k_blocks,
+                 force_cluster=args.force_cluster, force_threads=args.force_threads)
+    ctas = w.rows * pl["cluster"]
+    tr = torch.full((ctas, 16), -1, dtype=torch.int64, device=dev)
+    kw = dict(force_cluster=args.force_cluster, force_threads=args.force_threads)
+    for i in range(max(3, args.warmup) + 1):
+        tr.fill_(-1)
+        c = copies[i % len(copies)]
+        if w.blocked:
+            lt.topk_blocked(c, ld, w.block, w.k_blocks, w.k, trace=tr, **kw)
+        else:
+            lt.topk(c, ld, w.k, trace=tr, **kw)
+        torch.cuda.synchronize()
+    t = tr.cpu()
+    start = t[:, 0]
+    t0 = int(start.min())
+    out = {"workload": args.trace, "plan": pl, "ctas": ctas, "phases_us": {}}
+    for i, name in enumerate(TRACE_NAMES):
+        col = t[:, i]
+        ok = col >= 0
+        if i == 0 or int(ok.sum()) == 0:
+            continue
+        rel = (col[ok] - start[ok]).double() / 1000.0
+        glob = (col[ok] - t0).double() / 1000.0
+        out["phases_us"][name] = {"median": round(float(rel.median()), 3), "max": round(float(rel.max()), 3),
+                                  "since_first_start_median": round(float(glob.median()), 3)}
+    out["start_spread_us"] = round(float((start - t0).double().max()) / 1000.0, 3)
+    return out
+
+
 def bench_torch_topk(x, k, args, world):
     steps = max(3, min(args.steps, 50))
     _, per = timed_launches(lambda i: torch.topk(x, k, dim=1, sorted=True), steps, 3, world)
@@ -450,6 +499,11 @@ def main():
             print(json.dumps(bench_reference(args, 1, 0)), flush=True)
         return
     world, rank, local = dist_setup(args.gpus)
+    if args.trace:
+        line = bench_trace(args)
+        if rank == 0:
+            print(json.dumps(line), flush=True)
+        return
     if args.only:
         line = bench_only(args, world)
         if rank == 0:

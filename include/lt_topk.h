@@ -113,17 +113,23 @@ lt_status lt_topk_blocked(const float* scores, const int32_t* lengths, int32_t r
  *                  select, [2] rows whose candidate set overflowed, [3] rows
  *                  whose sampled threshold kept fewer than k candidates.
  *                  For the two-level call, each row counts once per stage.
+ *   trace          NULL, or device int64[grid CTAs * 16] receiving, from
+ *                  thread 0 of each CTA, global-timer nanoseconds at phase
+ *                  boundaries (entry, sample histogram, first cluster merge,
+ *                  threshold, filter, candidate exchange, exact select,
+ *                  output; the two-level kernel's second stage uses slots
+ *                  9..14). CTA b of the grid is row b / cluster_size.
  */
 #define LT_NUM_COUNTERS 4
 lt_status lt_topk_ex(const float* scores, const int32_t* lengths, int32_t rows,
                      int64_t row_stride, int32_t k, int32_t* out_idx, float* out_val,
                      int32_t force_cluster, int32_t force_threads, int32_t force_exact,
-                     int32_t* counters, void* stream);
+                     int32_t* counters, int64_t* trace, void* stream);
 lt_status lt_topk_blocked_ex(const float* scores, const int32_t* lengths, int32_t rows,
                              int64_t row_stride, int32_t block, int32_t k_blocks, int32_t k,
                              int32_t* out_idx, float* out_val, int32_t* out_blocks,
                              int32_t force_cluster, int32_t force_threads, int32_t force_exact,
-                             int32_t* counters, void* stream);
+                             int32_t* counters, int64_t* trace, void* stream);
 
 /*
  * lt_topk_plan -- the launch the planner would make, without launching.

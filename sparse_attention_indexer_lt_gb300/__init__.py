@@ -49,11 +49,12 @@ def load() -> ctypes.CDLL:
     i32, i64, vp = ctypes.c_int32, ctypes.c_int64, ctypes.c_void_p
     lib.lt_topk.argtypes = [vp, vp, i32, i64, i32, vp, vp, vp]
     lib.lt_topk.restype = ctypes.c_int
-    lib.lt_topk_ex.argtypes = [vp, vp, i32, i64, i32, vp, vp, i32, i32, i32, vp, vp]
+    lib.lt_topk_ex.argtypes = [vp, vp, i32, i64, i32, vp, vp, i32, i32, i32, vp, vp, vp]
     lib.lt_topk_ex.restype = ctypes.c_int
     lib.lt_topk_blocked.argtypes = [vp, vp, i32, i64, i32, i32, i32, vp, vp, vp, vp]
     lib.lt_topk_blocked.restype = ctypes.c_int
-    lib.lt_topk_blocked_ex.argtypes = [vp, vp, i32, i64, i32, i32, i32, vp, vp, vp, i32, i32, i32, vp, vp]
+    lib.lt_topk_blocked_ex.argtypes = [vp, vp, i32, i64, i32, i32, i32, vp, vp, vp, i32, i32, i32, vp, vp,
+                                       vp]
     lib.lt_topk_blocked_ex.restype = ctypes.c_int
     lib.lt_topk_plan.argtypes = [i32, i64, i32, i32, i32, i32, i32, i32, vp, vp, vp]
     lib.lt_topk_plan.restype = ctypes.c_int
@@ -124,7 +125,7 @@ def topk(scores: torch.Tensor, lengths: torch.Tensor | None = None, k: int = 512
          out_idx: torch.Tensor | None = None, out_val: torch.Tensor | None = None,
          with_values: bool = True, force_cluster: int = 0, force_threads: int = 0,
          force_exact: bool = False, counters: torch.Tensor | None = None,
-         stream: torch.cuda.Stream | None = None):
+         trace: torch.Tensor | None = None, stream: torch.cuda.Stream | None = None):
     """Per-row top-k by (score desc, index asc); returns (idx int32 [rows, k], val float32 [rows, k] or None)."""
     lib = load()
     rows, n = _check_scores(scores)
@@ -140,7 +141,7 @@ def topk(scores: torch.Tensor, lengths: torch.Tensor | None = None, k: int = 512
         s = (stream or torch.cuda.current_stream(dev)).cuda_stream
         st = lib.lt_topk_ex(_ptr(scores), _ptr(lengths), rows, max(n, 1), int(k), _ptr(out_idx),
                             _ptr(out_val), int(force_cluster), int(force_threads),
-                            int(bool(force_exact)), _ptr(counters), ctypes.c_void_p(s))
+                            int(bool(force_exact)), _ptr(counters), _ptr(trace), ctypes.c_void_p(s))
     if st != 0:
         raise LtError("lt_topk", st)
     return out_idx, out_val
@@ -151,7 +152,7 @@ def topk_blocked(scores: torch.Tensor, lengths: torch.Tensor | None = None, bloc
                  out_val: torch.Tensor | None = None, out_blocks: torch.Tensor | None = None,
                  with_values: bool = True, with_blocks: bool = True, force_cluster: int = 0,
                  force_threads: int = 0, force_exact: bool = False,
-                 counters: torch.Tensor | None = None,
+                 counters: torch.Tensor | None = None, trace: torch.Tensor | None = None,
                  stream: torch.cuda.Stream | None = None):
     """Two-level top-k; returns (idx [rows, k], val [rows, k] or None, blocks [rows, k_blocks] or None)."""
     lib = load()
@@ -167,7 +168,7 @@ def topk_blocked(scores: torch.Tensor, lengths: torch.Tensor | None = None, bloc
         st = lib.lt_topk_blocked_ex(_ptr(scores), _ptr(lengths), rows, max(n, 1), int(block),
                                     int(k_blocks), int(k), _ptr(out_idx), _ptr(out_val),
                                     _ptr(out_blocks), int(force_cluster), int(force_threads),
-                                    int(bool(force_exact)), _ptr(counters), ctypes.c_void_p(s))
+                                    int(bool(force_exact)), _ptr(counters), _ptr(trace), ctypes.c_void_p(s))
     if st != 0:
         raise LtError("lt_topk_blocked", st)
     return out_idx, out_val, out_blocks

@@ -214,7 +214,8 @@ extern "C" {
 
 lt_status lt_topk_ex(const float* scores, const int32_t* lengths, int32_t rows, int64_t row_stride,
                      int32_t k, int32_t* out_idx, float* out_val, int32_t force_cluster,
-                     int32_t force_threads, int32_t force_exact, int32_t* counters, void* stream) {
+                     int32_t force_threads, int32_t force_exact, int32_t* counters, int64_t* trace,
+                     void* stream) {
   lt_status st = check_common(scores, rows, row_stride, k, out_idx, force_cluster, force_threads);
   if (st != LT_OK) return st;
   if (rows == 0) return LT_OK;
@@ -230,6 +231,7 @@ lt_status lt_topk_ex(const float* scores, const int32_t* lengths, int32_t rows, 
   p.out_val = out_val;
   p.out_blocks = nullptr;
   p.counters = counters;
+  p.trace = trace;
   p.rows = rows;
   p.k = k;
   p.k_blocks = 1;
@@ -240,14 +242,14 @@ lt_status lt_topk_ex(const float* scores, const int32_t* lengths, int32_t rows, 
 
 lt_status lt_topk(const float* scores, const int32_t* lengths, int32_t rows, int64_t row_stride,
                   int32_t k, int32_t* out_idx, float* out_val, void* stream) {
-  return lt_topk_ex(scores, lengths, rows, row_stride, k, out_idx, out_val, 0, 0, 0, nullptr, stream);
+  return lt_topk_ex(scores, lengths, rows, row_stride, k, out_idx, out_val, 0, 0, 0, nullptr, nullptr, stream);
 }
 
 lt_status lt_topk_blocked_ex(const float* scores, const int32_t* lengths, int32_t rows,
                              int64_t row_stride, int32_t block, int32_t k_blocks, int32_t k,
                              int32_t* out_idx, float* out_val, int32_t* out_blocks,
                              int32_t force_cluster, int32_t force_threads, int32_t force_exact,
-                             int32_t* counters, void* stream) {
+                             int32_t* counters, int64_t* trace, void* stream) {
   lt_status st = check_common(scores, rows, row_stride, k, out_idx, force_cluster, force_threads);
   if (st != LT_OK) return st;
   if (block < 1 || k_blocks < 1) return LT_ERR_INVALID_ARG;
@@ -265,6 +267,7 @@ lt_status lt_topk_blocked_ex(const float* scores, const int32_t* lengths, int32_
   p.out_val = out_val;
   p.out_blocks = out_blocks;
   p.counters = counters;
+  p.trace = trace;
   p.rows = rows;
   p.k = k;
   p.k_blocks = k_blocks;
@@ -277,7 +280,7 @@ lt_status lt_topk_blocked(const float* scores, const int32_t* lengths, int32_t r
                           int64_t row_stride, int32_t block, int32_t k_blocks, int32_t k,
                           int32_t* out_idx, float* out_val, int32_t* out_blocks, void* stream) {
   return lt_topk_blocked_ex(scores, lengths, rows, row_stride, block, k_blocks, k, out_idx, out_val,
-                            out_blocks, 0, 0, 0, nullptr, stream);
+                            out_blocks, 0, 0, 0, nullptr, nullptr, stream);
 }
 
 lt_status lt_topk_plan(int32_t rows, int64_t row_stride, int32_t k, int32_t blocked, int32_t block,

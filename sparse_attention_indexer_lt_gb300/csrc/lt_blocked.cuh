@@ -15,6 +15,7 @@ __global__ void __launch_bounds__(T, (T <= 256 ? 3 : 1)) blocked_kernel(Params p
   using G = Geo<T, U, W>;
   extern __shared__ __align__(128) unsigned char smem[];
   Row R;
+  stamp(p, kTrStart);
   setup_row<T, U, W>(R, p, smem);
   Misc* m = R.m;
   float4 va[U], vb[U];
@@ -27,7 +28,7 @@ __global__ void __launch_bounds__(T, (T <= 256 ? 3 : 1)) blocked_kernel(Params p
   bool intact;
   uint64_t TcA;
   const bool exactA = select_stage<T, U, W, true>(R, p, va, na, vb, nb, false, KA, nblocks, nblocks,
-                                                  KeepAll{}, true, &intact, &TcA);
+                                                  KeepAll{}, true, &intact, &TcA, 0);
   uint64_t TA = 0;
   if (KA > 0) {
     const uint32_t NA = exactA ? KA : (m->cand_count < cap ? m->cand_count : cap);
@@ -92,7 +93,7 @@ __global__ void __launch_bounds__(T, (T <= 256 ? 3 : 1)) blocked_kernel(Params p
   uint64_t TcB;
   const bool exactB = select_stage<T, U, W, false>(R, p, va, na, vb, nb, intact, KB, (int64_t)ncand,
                                                    p.row_stride, KeepBlocks<T, U, W>{TA}, false,
-                                                   &intact_b, &TcB);
+                                                   &intact_b, &TcB, kTrStageB);
   output_positions<T>(R, p, exactB, TcB, KB, p.row_stride,
                       [&R](uint32_t idx) { return R.nclus == 1 || in_slice(R, idx); });
   finish_row(R);

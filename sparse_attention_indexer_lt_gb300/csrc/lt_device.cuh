@@ -59,6 +59,21 @@ constexpr unsigned kFull = 0xffffffffu;
 
 enum Counter { kCntFast = 0, kCntExact = 1, kCntOverflow = 2, kCntShort = 3 };
 
+// Phase timestamps (nanoseconds of the global timer) written by thread 0 of
+// each CTA when a trace buffer is given: slot i of CTA b at trace[b * 16 + i].
+constexpr int kTraceSlots = 16;
+enum TracePoint {
+  kTrStart = 0,     // kernel entry
+  kTrHist = 1,      // sample histogram built (rounds 0/1 have arrived)
+  kTrMerge = 2,     // first cluster merge done
+  kTrEstimate = 3,  // threshold known
+  kTrFilter = 4,    // every round filtered
+  kTrExchange = 5,  // candidates replicated
+  kTrExact = 6,     // streaming radix select done (equal to kTrExchange when not taken)
+  kTrOutput = 7,    // outputs written
+  kTrStageB = 8     // offset of the second stage of the two-level kernel
+};
+
 struct Params {
   const float* scores;
   const int32_t* lengths;
@@ -67,6 +82,7 @@ struct Params {
   float* out_val;
   int32_t* out_blocks;
   int32_t* counters;
+  int64_t* trace;       // nullable: per-CTA phase timestamps (kTraceSlots per CTA)
   int32_t rows;
   int32_t k;
   int32_t k_blocks;
@@ -160,6 +176,14 @@ __device__ __forceinline__ uint32_t dsmem_atom_add(uint32_t addr, uint32_t v) {
 }
 __device__ __forceinline__ void dsmem_st_v2(uint32_t addr, uint2 v) {
   asm volatile("st.shared::cluster.v2.u32 [%0], {%1, %2};" :: "r"(addr), "r"(v.x), "r"(v.y) : "memory");
+}
+
+__device__ __forceinline__ void stamp(const Params& p, int slot) {
+  if (p.trace != nullptr && threadIdx.x == 0) {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    p.trace[(int64_t)blockIdx.x * kTraceSlots + slot] = (int64_t)t;
+  }
 }
 
 __device__ __forceinline__ float4 ldg4(const float* p) {

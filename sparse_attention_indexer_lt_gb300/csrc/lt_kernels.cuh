@@ -674,7 +674,7 @@ __device__ __forceinline__ bool select_stage(Row& R, const Params& p, float4 (&v
                                              int (&na)[Geo<T, U, W>::kSlots], float4 (&vb)[U],
                                              int (&nb)[Geo<T, U, W>::kSlots], bool loaded, uint32_t K,
                                              int64_t items, int64_t idx_limit, Keep keep, bool first,
-                                             bool* regs_intact, uint64_t* Tc) {
+                                             bool* regs_intact, uint64_t* Tc, int tr) {
   Misc* m = R.m;
   const bool vec = p.vec_ok != 0;
   const uint32_t cap = (uint32_t)p.cap;
@@ -712,7 +712,9 @@ __device__ __forceinline__ bool select_stage(Row& R, const Params& p, float4 (&v
         hist_round<T, U, W>(R, 0, va, na, 1, 0, keep);
         if (full) hist_round<T, U, W>(R, 1, vb, nb, 1, 0, keep);
       }
+      stamp(p, tr + kTrHist);
       const uint32_t* bins = merge_hist<T>(R, 0);
+      stamp(p, tr + kTrMerge);
       const uint32_t ns = full ? (uint32_t)items : bins_total<T>(bins, m);
       if (ns > 0) {
         const uint32_t r = sample_target(K, ns, items, full);
@@ -741,6 +743,7 @@ __device__ __forceinline__ bool select_stage(Row& R, const Params& p, float4 (&v
         release_merged<T>(R, 0);
       }
     }
+    stamp(p, tr + kTrEstimate);
     // ---- filter every round against the threshold
     const bool all = (t == 0u);
     const float g = threshold_float(all ? 1u : t);
@@ -754,7 +757,9 @@ __device__ __forceinline__ bool select_stage(Row& R, const Params& p, float4 (&v
         if (r + 3 < R.rounds) load_round<T, U, W>(R, vec, r + 3, vb, nb);
       }
     }
+    stamp(p, tr + kTrFilter);
     exchange<T>(R, cap);
+    stamp(p, tr + kTrExchange);
     const uint32_t N = m->cand_count;
     const bool overflow = (m->flags & 1u) || N > cap;
     if (overflow || N < K) {
@@ -803,9 +808,11 @@ __device__ __forceinline__ bool select_stage(Row& R, const Params& p, float4 (&v
       else capture_round<T, U, W>(R, r, va, na, tval, counter, list, cap, keep);
     }
     exchange<T>(R, cap);
+    stamp(p, tr + kTrExact);
     bump(p, R, kCntExact);
     return true;
   }
+  stamp(p, tr + kTrExact);
   if (K > 0) bump(p, R, kCntFast);
   return false;
 }
@@ -823,10 +830,12 @@ __device__ __forceinline__ void output_positions(Row& R, const Params& p, bool e
   }
   const uint32_t cap = (uint32_t)p.cap;
   const uint32_t N = exact ? K : (R.m->cand_count < cap ? R.m->cand_count : cap);
-  if (bucket_select_sort<T>(R, N, K, kout, oi, ov, owner)) return;
-  const uint64_t T64 = exact ? Tc : select_local<T>(R, N, K, idx_limit);
-  compact_selected<T>(R, N, T64);
-  write_sorted_fallback<T>(R, K, kout, oi, ov, owner);
+  if (!bucket_select_sort<T>(R, N, K, kout, oi, ov, owner)) {
+    const uint64_t T64 = exact ? Tc : select_local<T>(R, N, K, idx_limit);
+    compact_selected<T>(R, N, T64);
+    write_sorted_fallback<T>(R, K, kout, oi, ov, owner);
+  }
+  stamp(p, kTrOutput);
 }
 
 __device__ __forceinline__ bool in_slice(const Row& R, uint32_t idx) {

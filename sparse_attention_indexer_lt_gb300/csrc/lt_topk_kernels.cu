@@ -11,6 +11,7 @@ __global__ void __launch_bounds__(T, (T <= 256 ? 3 : 1)) topk_kernel(Params p) {
   extern __shared__ __align__(128) unsigned char smem[];
   using G = Geo<T, U, 4>;
   Row R;
+  stamp(p, kTrStart);
   setup_row<T, U, 4>(R, p, smem);
   float4 va[U], vb[U];
   int na[G::kSlots], nb[G::kSlots];
@@ -18,7 +19,7 @@ __global__ void __launch_bounds__(T, (T <= 256 ? 3 : 1)) topk_kernel(Params p) {
   bool intact;
   uint64_t Tc;
   const bool exact = select_stage<T, U, 4, false>(R, p, va, na, vb, nb, false, K, R.L, p.row_stride,
-                                                  KeepAll{}, true, &intact, &Tc);
+                                                  KeepAll{}, true, &intact, &Tc, 0);
   output_positions<T>(R, p, exact, Tc, K, p.row_stride,
                       [&R](uint32_t idx) { return R.nclus == 1 || in_slice(R, idx); });
   finish_row(R);

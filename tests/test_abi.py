@@ -46,7 +46,7 @@ P = ctypes.c_void_p
 
 
 def _topk(lib, scores, lengths, rows, stride, k, oi, ov, fc=0):
-    return lib.lt_topk_ex(scores, lengths, rows, stride, k, oi, ov, fc, 0, 0, None, None)
+    return lib.lt_topk_ex(scores, lengths, rows, stride, k, oi, ov, fc, 0, 0, None, None, None)
 
 
 def test_invalid_arguments_rejected_without_launch(lib):
@@ -59,7 +59,7 @@ def test_invalid_arguments_rejected_without_launch(lib):
     assert _topk(lib, fake, None, 1, 16, 4, fake, None, fc=3) == 1  # cluster not a power of two
     assert _topk(lib, fake, None, 1, 16, 4096, fake, None) == 2  # k > LT_MAX_K
     assert _topk(lib, fake, None, 1, (1 << 30) + 1, 4, fake, None) == 2  # row too long
-    assert lib.lt_topk_ex(fake, None, 1, 16, 4, fake, None, 0, 512, 0, None, None) == 1  # bad thread count
+    assert lib.lt_topk_ex(fake, None, 1, 16, 4, fake, None, 0, 512, 0, None, None, None) == 1  # bad thread count
     # rows == 0 is a valid no-op
     assert _topk(lib, None, None, 0, 16, 4, None, None) == 0
 
@@ -67,11 +67,11 @@ def test_invalid_arguments_rejected_without_launch(lib):
 def test_blocked_invalid_arguments(lib):
     fake = P(0x1000)
     f = lib.lt_topk_blocked_ex
-    assert f(fake, None, 1, 64, 0, 4, 4, fake, None, None, 0, 0, 0, None, None) == 1   # block < 1
-    assert f(fake, None, 1, 64, 8, 0, 4, fake, None, None, 0, 0, 0, None, None) == 1   # k_blocks < 1
-    assert f(fake, None, 1, 64, 6, 4, 4, fake, None, None, 0, 0, 0, None, None) == 2   # block unsupported
-    assert f(fake, None, 1, 64, 8, 5000, 4, fake, None, None, 0, 0, 0, None, None) == 2
-    assert f(None, None, 0, 64, 8, 4, 4, None, None, None, 0, 0, 0, None, None) == 0
+    assert f(fake, None, 1, 64, 0, 4, 4, fake, None, None, 0, 0, 0, None, None, None) == 1   # block < 1
+    assert f(fake, None, 1, 64, 8, 0, 4, fake, None, None, 0, 0, 0, None, None, None) == 1   # k_blocks < 1
+    assert f(fake, None, 1, 64, 6, 4, 4, fake, None, None, 0, 0, 0, None, None, None) == 2   # block unsupported
+    assert f(fake, None, 1, 64, 8, 5000, 4, fake, None, None, 0, 0, 0, None, None, None) == 2
+    assert f(None, None, 0, 64, 8, 4, 4, None, None, None, 0, 0, 0, None, None, None) == 0
 
 
 def test_binding_refuses_cpu_tensors():
