@@ -22,7 +22,6 @@ __global__ void __launch_bounds__(T, (T <= 256 ? 3 : 1)) blocked_kernel(Params p
   int na[G::kSlots], nb[G::kSlots];
   const int64_t nblocks = (R.L + W - 1) / W;
   const uint32_t KA = (uint32_t)(nblocks < (int64_t)p.k_blocks ? nblocks : (int64_t)p.k_blocks);
-  const uint32_t cap = (uint32_t)p.cap;
 
   // ---- stage A: the top k_blocks blocks by (block key desc, block id asc)
   bool intact;
@@ -31,9 +30,8 @@ __global__ void __launch_bounds__(T, (T <= 256 ? 3 : 1)) blocked_kernel(Params p
                                                   KeepAll{}, true, &intact, &TcA, 0);
   uint64_t TA = 0;
   if (KA > 0) {
-    const uint32_t NA = exactA ? KA : (m->cand_count < cap ? m->cand_count : cap);
-    TA = exactA ? TcA : select_local<T>(R, NA, KA, nblocks);
-    compact_selected<T>(R, NA, TA);  // stage[0, KA) = kept block composites
+    TA = exactA ? TcA : select_local<T>(R, KA, nblocks);
+    compact_selected<T>(R, TA);  // stage[0, KA) = kept block composites
   }
 
   // ---- kept block ids in ascending order: this CTA's own kept blocks,
@@ -94,9 +92,8 @@ __global__ void __launch_bounds__(T, (T <= 256 ? 3 : 1)) blocked_kernel(Params p
   const bool exactB = select_stage<T, U, W, false>(R, p, va, na, vb, nb, intact, KB, (int64_t)ncand,
                                                    p.row_stride, KeepBlocks<T, U, W>{TA}, false,
                                                    &intact_b, &TcB, kTrStageB);
-  output_positions<T>(R, p, exactB, TcB, KB, p.row_stride,
-                      [&R](uint32_t idx) { return R.nclus == 1 || in_slice(R, idx); });
-  finish_row(R);
+  output_positions<T>(R, p, exactB, TcB, KB, p.row_stride);
+  wait_init(R);
 }
 
 template <int T>

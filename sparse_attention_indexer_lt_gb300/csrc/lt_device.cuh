@@ -16,10 +16,11 @@
 //      scan gives the digit of the k-th key; a second 11-bit level runs when
 //      that bucket is still wide. The result is a key threshold t no larger
 //      than the k-th key (exact when the sample is the whole slice).
-//   3. filter + candidate exchange. Every key >= t is appended to a per-CTA
-//      list (one warp scan and one shared atomic per warp and round); the
-//      lists are pushed into every CTA of the cluster, so each CTA holds the
-//      same candidate multiset.
+//   3. filter + candidate exchange. Every key >= t is appended to this CTA's
+//      segment of its candidate array (one warp scan and one shared atomic
+//      per warp and round); each CTA then stores its segment and its count
+//      into the same segment of every peer over DSMEM, so after one cluster
+//      barrier every CTA holds the same candidate multiset.
 //   4. select + order. The candidates are spread over 2048 buckets that are
 //      linear in the key between the smallest and largest candidate key; a
 //      suffix scan of the bucket counts finds the bucket of the k-th item and
@@ -86,7 +87,8 @@ struct Params {
   int32_t rows;
   int32_t k;
   int32_t k_blocks;
-  int32_t cap;          // candidate capacity (entries)
+  int32_t cap;          // candidate slots: clusters * (1 << seg_shift)
+  int32_t seg_shift;    // log2 of the candidate slots one CTA may fill
   int32_t sel_cap;      // power of two >= max(k, k_blocks)
   int32_t force_exact;
   int32_t vec_ok;       // every row start is 16-byte aligned
@@ -96,11 +98,14 @@ struct Params {
 // ------------------------------------------------------------------ smem layout
 
 struct Misc {
-  uint32_t cand_count;   // entries in cand[] (receives peers' reservations)
-  uint32_t local_count;  // entries in local[]
-  uint32_t flags;        // bit 0: some CTA's list overflowed
+  uint32_t cand_count;   // flat candidate count (streaming exact select)
+  uint32_t local_count;  // candidates this CTA appended to its own segment
+  uint32_t flags;
   uint32_t own_count;
   uint32_t res_digit, res_above, res_cnt, res_max;
+  uint32_t kmin, kmax;   // candidate key range (bucket select)
+  uint32_t nseg, shift;  // current candidate layout: nseg segments of 1 << shift slots
+  uint32_t seg_cnt[kMaxCluster];  // entries in each segment (may exceed the segment: overflow)
   uint32_t peer_base[kMaxCluster];
   uint32_t warp_a[kMaxWarps];
   uint32_t warp_b[kMaxWarps];
@@ -108,7 +113,7 @@ struct Misc {
 };
 
 struct Layout {
-  uint32_t misc, hist, aux, merged0, merged1, cand, local, stage, total;
+  uint32_t misc, hist, aux, merged0, merged1, cand, stage, total;
 };
 
 __host__ __device__ inline uint32_t align_up_u32(uint32_t x, uint32_t a) { return (x + a - 1) / a * a; }
@@ -127,7 +132,6 @@ __host__ __device__ inline Layout make_layout(bool clustered, uint32_t cap, uint
     l.merged0 = l.merged1 = l.hist;
   }
   l.cand = o;    o += cap * 8;
-  if (clustered) { l.local = o; o += cap * 8; } else { l.local = l.cand; }
   l.stage = o;   o += (sel_cap + kMaxBucket) * 8;
   l.total = align_up_u32(o, 128);
   return l;
@@ -258,6 +262,8 @@ __device__ __forceinline__ void warp_append(bool pred, uint32_t key, uint32_t id
   }
 }
 
+// Block-wide sum: warp sums land in smem, warp 0 adds them, everyone reads
+// the result. Ends with __syncthreads.
 template <int T>
 __device__ __forceinline__ uint32_t block_sum(uint32_t x, Misc* m) {
   constexpr int NW = T / 32;
@@ -265,32 +271,13 @@ __device__ __forceinline__ uint32_t block_sum(uint32_t x, Misc* m) {
   __syncthreads();
   if (lane_id() == 0) m->warp_a[threadIdx.x >> 5] = x;
   __syncthreads();
-  uint32_t s = 0;
-#pragma unroll
-  for (int w = 0; w < NW; ++w) s += m->warp_a[w];
-  __syncthreads();
-  return s;
-}
-
-template <int T>
-__device__ __forceinline__ void block_minmax(uint32_t& lo, uint32_t& hi, Misc* m) {
-  constexpr int NW = T / 32;
-  lo = __reduce_min_sync(kFull, lo);
-  hi = __reduce_max_sync(kFull, hi);
-  __syncthreads();
-  if (lane_id() == 0) {
-    m->warp_a[threadIdx.x >> 5] = lo;
-    m->warp_b[threadIdx.x >> 5] = hi;
+  if (threadIdx.x < 32) {
+    uint32_t y = threadIdx.x < NW ? m->warp_a[threadIdx.x] : 0u;
+    y = __reduce_add_sync(kFull, y);
+    if (threadIdx.x == 0) m->warp_b[0] = y;
   }
   __syncthreads();
-  lo = 0xffffffffu;
-  hi = 0u;
-#pragma unroll
-  for (int w = 0; w < NW; ++w) {
-    lo = min(lo, m->warp_a[w]);
-    hi = max(hi, m->warp_b[w]);
-  }
-  __syncthreads();
+  return m->warp_b[0];
 }
 
 // Each thread owns BPT = kBins / T consecutive bins. Loads them into v[].
@@ -314,8 +301,9 @@ __device__ __forceinline__ void load_bins(const uint32_t* bins, uint32_t (&v)[kB
 }
 
 // Exclusive suffix sum over threads of per-thread totals (the keys in bins
-// owned by threads with a larger index). Contains one __syncthreads; the
-// caller must __syncthreads before warp_a is written again.
+// owned by threads with a larger index). Warp 0 scans the warp totals.
+// Contains two __syncthreads; the caller must __syncthreads before warp_a or
+// warp_b is written again.
 template <int T>
 __device__ __forceinline__ uint32_t block_suffix_excl(uint32_t tot, Misc* m) {
   constexpr int NW = T / 32;
@@ -328,11 +316,19 @@ __device__ __forceinline__ uint32_t block_suffix_excl(uint32_t tot, Misc* m) {
   }
   if (lane == 0) m->warp_a[warp] = incl;
   __syncthreads();
-  uint32_t after = 0;
+  if (threadIdx.x < 32) {
+    const uint32_t w = threadIdx.x;
+    const uint32_t own = w < (uint32_t)NW ? m->warp_a[w] : 0u;
+    uint32_t suf = own;  // sum over warps >= w
 #pragma unroll
-  for (int w = 0; w < NW; ++w)
-    if (w > (int)warp) after += m->warp_a[w];
-  return after + (incl - tot);
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t n = __shfl_down_sync(kFull, suf, o);
+      if (w + o < 32) suf += n;
+    }
+    if (w < (uint32_t)NW) m->warp_b[w] = suf - own;  // sum over warps > w
+  }
+  __syncthreads();
+  return m->warp_b[warp] + (incl - tot);
 }
 
 // Find digit d with suffix(d + 1) < r <= suffix(d), suffix(d) = sum of bins[b >= d].

@@ -4,10 +4,15 @@
 // T * W positions (one W-wide slot per thread per tile, W/4 float4 loads). A
 // "round" is U float4 per thread. Round r, slot s covers tile r + rounds * s,
 // so round 0 is spread over the whole slice and serves as a representative
-// sample. Rounds 0 and 1 are loaded up front and kept in registers; later
-// rounds stream through the same two register sets. For the top-k kernel
-// W = 4 (items are positions); for the two-level kernel W = block (stage A
-// items are blocks, stage B items are the positions of the kept blocks).
+// sample. Two register buffers hold the current and the next round; rounds
+// stream through them. For the top-k kernel W = 4 (items are positions); for
+// the two-level kernel W = block (stage A items are blocks, stage B items are
+// the positions of the kept blocks).
+//
+// Code layout: everything a normal row executes is inlined once; the paths
+// only adversarial rows take (the streaming exact select, the radix-select +
+// bitonic fallback of the output, scalar loads of ragged slot ends) are
+// separate functions, so the hot code stays small enough to fetch quickly.
 
 #pragma once
 
@@ -29,8 +34,7 @@ struct Row {
   uint32_t* aux;
   uint32_t* merged0;     // cluster merge targets (== hist with one CTA)
   uint32_t* merged1;
-  uint2* cand;
-  uint2* local;
+  uint2* cand;           // nclus segments of (1 << seg_shift) slots
   uint64_t* stage;
   const float* rowp;
   int64_t row;
@@ -39,10 +43,21 @@ struct Row {
   int64_t tbase;         // begin + threadIdx.x * W
   uint32_t rank, nclus;
   uint32_t stage_cap;
+  uint32_t seg_shift;
   int rounds;            // rounds of this CTA's slice
   int rounds_max;        // cluster-wide maximum
   bool init_pending;     // the start-up cluster barrier has not been waited on
 };
+
+// Items of this CTA's own slice (ranks in the output are written by their owner).
+struct OwnSlice {
+  int64_t b, e;
+  bool all;
+  __device__ __forceinline__ bool operator()(uint32_t idx) const {
+    return all || ((int64_t)idx >= b && (int64_t)idx < e);
+  }
+};
+__device__ __forceinline__ OwnSlice own_slice(const Row& R) { return OwnSlice{R.begin, R.end, R.nclus == 1}; }
 
 __device__ __forceinline__ float nan_f() { return __int_as_float(0x7fffffff); }
 
@@ -51,8 +66,16 @@ __device__ __forceinline__ int64_t slot_pos(const Row& R, int r, int s) {
   return R.tbase + (int64_t)(r + R.rounds * s) * Geo<T, U, W>::kTile;
 }
 
+// Scalar load of a ragged or unaligned group of four positions: [0, nv) are
+// read, the rest are NaN (no threshold compare accepts NaN).
+__device__ __forceinline__ float4 load4_scalar(const float* p, int nv) {
+  float e[4];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) e[q] = (q < nv) ? __ldg(p + q) : nan_f();
+  return make_float4(e[0], e[1], e[2], e[3]);
+}
+
 // Load round r; n[s] = valid positions of slot s (a prefix of the slot).
-// Invalid positions read as NaN, which no threshold compare accepts.
 template <int T, int U, int W>
 __device__ __forceinline__ void load_round(const Row& R, bool vec, int r, float4 (&v)[U],
                                            int (&n)[Geo<T, U, W>::kSlots]) {
@@ -69,13 +92,8 @@ __device__ __forceinline__ void load_round(const Row& R, bool vec, int r, float4
     } else {
 #pragma unroll
       for (int j = 0; j < G::kVS; ++j) {
-        float e[4];
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const int o = 4 * j + q;
-          e[q] = (o < nv) ? __ldg(R.rowp + pos + o) : nan_f();
-        }
-        v[s * G::kVS + j] = make_float4(e[0], e[1], e[2], e[3]);
+        const int64_t left = nv - 4 * j;
+        v[s * G::kVS + j] = load4_scalar(R.rowp + pos + 4 * j, left < 0 ? 0 : (left > 4 ? 4 : (int)left));
       }
     }
   }
@@ -133,9 +151,9 @@ __device__ __forceinline__ void setup_row(Row& R, const Params& p, unsigned char
   R.merged0 = reinterpret_cast<uint32_t*>(smem + lay.merged0);
   R.merged1 = reinterpret_cast<uint32_t*>(smem + lay.merged1);
   R.cand = reinterpret_cast<uint2*>(smem + lay.cand);
-  R.local = reinterpret_cast<uint2*>(smem + lay.local);
   R.stage = reinterpret_cast<uint64_t*>(smem + lay.stage);
   R.stage_cap = (uint32_t)p.sel_cap + kMaxBucket;
+  R.seg_shift = (uint32_t)p.seg_shift;
   int64_t L = p.row_stride;
   if (p.lengths) {
     L = (int64_t)p.lengths[R.row];
@@ -177,7 +195,7 @@ __device__ __forceinline__ void setup_row(Row& R, const Params& p, unsigned char
   }
 }
 
-__device__ __forceinline__ void finish_row(Row& R) {
+__device__ __forceinline__ void wait_init(Row& R) {
   if (R.init_pending) {
     cluster_wait();
     R.init_pending = false;
@@ -195,16 +213,44 @@ __device__ __forceinline__ void bump(const Params& p, const Row& R, int which) {
   if (p.counters && R.rank == 0 && threadIdx.x == 0) atomicAdd(&p.counters[which], 1);
 }
 
+__device__ __forceinline__ void dsmem_st_u32(uint32_t addr, uint32_t v) {
+  asm volatile("st.shared::cluster.u32 [%0], %1;" :: "r"(addr), "r"(v) : "memory");
+}
+
+// ------------------------------------------------------------------ candidates
+
+// Candidate array view: nseg segments of (1 << shift) slots; slot i is valid
+// when its offset in its segment is below that segment's count.
+struct Cands {
+  const uint2* c;
+  const uint32_t* cnt;
+  uint32_t slots;
+  uint32_t shift;
+  __device__ __forceinline__ bool valid(uint32_t i) const {
+    return (i & ((1u << shift) - 1u)) < cnt[i >> shift];
+  }
+};
+__device__ __forceinline__ Cands cands(const Row& R) {
+  const Misc* m = R.m;
+  return Cands{R.cand, m->seg_cnt, m->nseg << m->shift, m->shift};
+}
+
+__device__ __forceinline__ void reset_candidate_range(Misc* m) {
+  m->kmin = 0xffffffffu;
+  m->kmax = 0u;
+  m->res_max = 0u;
+}
+
 // ------------------------------------------------------------------ cluster exchange
 
-// Push the non-empty bins of the local histogram into merged buffer `buf` of every
-// CTA of the cluster (this one included), then cluster-sync. With one CTA
-// the local histogram is the merged one.
+// Push the non-empty bins of the local histogram into merged buffer `buf` of
+// every CTA of the cluster (this one included), then cluster-sync. With one
+// CTA the local histogram is the merged one.
 template <int T>
 __device__ __forceinline__ const uint32_t* merge_hist(Row& R, int buf) {
   __syncthreads();
   if (R.nclus == 1) return R.hist;
-  if (R.init_pending) { cluster_wait(); R.init_pending = false; }
+  wait_init(R);
   uint32_t* dst = buf ? R.merged1 : R.merged0;
   const uint32_t base = smem_addr(dst);
   for (int b = threadIdx.x; b < kBins; b += T) {
@@ -217,8 +263,8 @@ __device__ __forceinline__ const uint32_t* merge_hist(Row& R, int buf) {
   return dst;
 }
 
-// After the digit search on merged buffer `buf`: clear it for its next use. Peers only
-// write it again after a later cluster barrier.
+// After the digit search on merged buffer `buf`: clear it for its next use.
+// Peers only write it again after a later cluster barrier.
 template <int T>
 __device__ __forceinline__ void release_merged(Row& R, int buf) {
   if (R.nclus == 1) return;
@@ -226,60 +272,73 @@ __device__ __forceinline__ void release_merged(Row& R, int buf) {
   for (int i = threadIdx.x; i < kBins / 4; i += T) p[i] = make_uint4(0, 0, 0, 0);
 }
 
-// Copy the local candidate list into cand[] of every CTA of the cluster, then
-// cluster-sync. Afterwards cand[0, cand_count) holds the union (in an order
-// that may differ between CTAs) unless an overflow flag is set.
+// Fast-path exchange: this CTA's segment (and its count) goes to the same
+// segment of every peer. One cluster barrier, no remote atomics.
 template <int T>
-__device__ __forceinline__ void exchange(Row& R, uint32_t cap) {
-  __syncthreads();
-  if (R.nclus == 1) return;  // single CTA: local == cand, already counted
-  if (R.init_pending) { cluster_wait(); R.init_pending = false; }
+__device__ __forceinline__ void exchange_segments(Row& R) {
   Misc* m = R.m;
-  const uint32_t n = m->local_count;
-  const uint32_t n_put = n < cap ? n : cap;
-  if (threadIdx.x < R.nclus) {
-    const uint32_t q = threadIdx.x;
-    m->peer_base[q] = dsmem_atom_add(peer_addr(smem_addr(&m->cand_count), q), n);
-    if (n > cap) dsmem_red_or(peer_addr(smem_addr(&m->flags), q), 1u);
-  }
   __syncthreads();
-  const uint32_t cand_base = smem_addr(R.cand);
+  const uint32_t n = m->local_count;
+  if (threadIdx.x == 0) {
+    reset_candidate_range(m);
+    m->nseg = R.nclus;
+    m->shift = R.seg_shift;
+  }
+  if (R.nclus == 1) {
+    if (threadIdx.x == 0) m->seg_cnt[0] = n;
+    __syncthreads();
+    return;
+  }
+  wait_init(R);
+  const uint32_t seg = 1u << R.seg_shift;
+  const uint32_t n_put = n < seg ? n : seg;
+  const uint32_t off = R.rank << R.seg_shift;
+  if (threadIdx.x < R.nclus) dsmem_st_u32(peer_addr(smem_addr(&m->seg_cnt[R.rank]), threadIdx.x), n);
+  const uint2* mine = R.cand + off;
+  const uint32_t src = smem_addr(R.cand) + 8u * off;
   for (uint32_t q = 0; q < R.nclus; ++q) {
-    const uint32_t pb = m->peer_base[q];
-    const uint32_t dst = peer_addr(cand_base, q);
-    for (uint32_t i = threadIdx.x; i < n_put; i += T) {
-      if (pb + i < cap) dsmem_st_v2(dst + 8u * (pb + i), R.local[i]);
-    }
+    if (q == R.rank) continue;
+    const uint32_t dst = peer_addr(src, q);
+    for (uint32_t i = threadIdx.x; i < n_put; i += T) dsmem_st_v2(dst + 8u * i, mine[i]);
   }
   cluster_sync();
 }
 
-__device__ __forceinline__ void reset_lists(Row& R) {
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    R.m->cand_count = 0;
-    R.m->local_count = 0;
-    R.m->flags = 0;
-  }
-  __syncthreads();
-}
-
 // ------------------------------------------------------------------ position items
 
+// Rounds live in two register buffers; `b` picks one, element by element at
+// the point of use (keeps one copy of the code without a third buffer).
+template <int U, int S>
+struct Bufs {
+  const float4 (&a)[U];
+  const int (&na)[S];
+  const float4 (&b)[U];
+  const int (&nb)[S];
+  bool use_b;
+  __device__ __forceinline__ float4 v(int i) const { return use_b ? b[i] : a[i]; }
+  __device__ __forceinline__ int n(int s) const { return use_b ? nb[s] : na[s]; }
+};
+
 template <int T, int U, int W, class Keep>
-__device__ __forceinline__ void hist_round(Row& R, int r, const float4 (&v)[U],
-                                           const int (&n)[Geo<T, U, W>::kSlots], int level,
+__device__ __forceinline__ bool keep_slot(const Row& R, int r, const Bufs<U, Geo<T, U, W>::kSlots>& B, int s,
+                                          Keep keep) {
+  return B.use_b ? keep(R, r, B.b, s, B.nb[s]) : keep(R, r, B.a, s, B.na[s]);
+}
+
+template <int T, int U, int W, class Keep>
+__device__ __forceinline__ void hist_round(Row& R, int r, const Bufs<U, Geo<T, U, W>::kSlots>& B, int level,
                                            uint32_t d1, Keep keep) {
   using G = Geo<T, U, W>;
 #pragma unroll
   for (int s = 0; s < G::kSlots; ++s) {
-    if (n[s] == 0 || !keep(R, r, v, s, n[s])) continue;
+    const int ns = B.n(s);
+    if (ns == 0 || !keep_slot<T, U, W>(R, r, B, s, keep)) continue;
 #pragma unroll
     for (int j = 0; j < G::kVS; ++j)
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        if (4 * j + e < n[s]) {
-          const uint32_t kk = key_of(lane4(v[s * G::kVS + j], e));
+        if (4 * j + e < ns) {
+          const uint32_t kk = key_of(lane4(B.v(s * G::kVS + j), e));
           if (level == 1) atomicAdd(&R.hist[kk >> 21], 1u);
           else if ((kk >> 21) == d1) atomicAdd(&R.hist[(kk >> 10) & (kBins - 1)], 1u);
         }
@@ -291,21 +350,21 @@ __device__ __forceinline__ void hist_round(Row& R, int r, const float4 (&v)[U],
 // every position when `all`) to the list: a bit mask per thread, one warp
 // scan and one shared atomic per warp, then each lane writes its own items.
 template <int T, int U, int W, class Keep>
-__device__ __forceinline__ void filter_round(Row& R, int r, const float4 (&v)[U],
-                                             const int (&n)[Geo<T, U, W>::kSlots], float g, bool all,
-                                             uint32_t* counter, uint2* list, uint32_t cap, Keep keep) {
+__device__ __forceinline__ void filter_round(Row& R, int r, const Bufs<U, Geo<T, U, W>::kSlots>& B, float g,
+                                             bool all, uint32_t* counter, uint2* list, uint32_t cap, Keep keep) {
   using G = Geo<T, U, W>;
   static_assert(4 * U <= 32, "mask holds 32 positions");
   uint32_t mask = 0;
 #pragma unroll
   for (int s = 0; s < G::kSlots; ++s) {
-    const bool kept = n[s] > 0 && keep(R, r, v, s, n[s]);
+    const int ns = B.n(s);
+    const bool kept = ns > 0 && keep_slot<T, U, W>(R, r, B, s, keep);
 #pragma unroll
     for (int j = 0; j < G::kVS; ++j) {
-      const float4 q = v[s * G::kVS + j];
+      const float4 q = B.v(s * G::kVS + j);
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        const bool pe = kept && (4 * j + e < n[s]) && (all || lane4(q, e) >= g);
+        const bool pe = kept && (4 * j + e < ns) && (all || lane4(q, e) >= g);
         mask |= pe ? (1u << (4 * (s * G::kVS + j) + e)) : 0u;
       }
     }
@@ -323,7 +382,7 @@ __device__ __forceinline__ void filter_round(Row& R, int r, const float4 (&v)[U]
     uint32_t nib = (mask >> (4 * f)) & 15u;
     if (nib) {
       const int64_t p0 = slot_pos<T, U, W>(R, r, f / G::kVS) + 4 * (f % G::kVS);
-      const float4 q = v[f];
+      const float4 q = B.v(f);
       do {
         const int e = __ffs(nib) - 1;
         nib &= nib - 1;
@@ -334,107 +393,36 @@ __device__ __forceinline__ void filter_round(Row& R, int r, const float4 (&v)[U]
   }
 }
 
-// One pass of the streaming radix select: histogram digit (shift s, mask
-// wmask) of every kept composite that matches the prefix (tval under tmask).
-template <int T, int U, int W, class Keep>
-__device__ __forceinline__ void exact_hist_round(Row& R, int r, const float4 (&v)[U],
-                                                 const int (&n)[Geo<T, U, W>::kSlots], uint64_t tval,
-                                                 uint64_t tmask, int s, uint32_t wmask, Keep keep) {
-  using G = Geo<T, U, W>;
-#pragma unroll
-  for (int sl = 0; sl < G::kSlots; ++sl) {
-    if (n[sl] == 0 || !keep(R, r, v, sl, n[sl])) continue;
-    const int64_t pos = slot_pos<T, U, W>(R, r, sl);
-#pragma unroll
-    for (int j = 0; j < G::kVS; ++j)
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int o = 4 * j + e;
-        if (o < n[sl]) {
-          const uint64_t c = composite(key_of(lane4(v[sl * G::kVS + j], e)), (uint32_t)(pos + o));
-          if ((c & tmask) == tval) atomicAdd(&R.hist[(uint32_t)(c >> s) & wmask], 1u);
-        }
-      }
-  }
-}
-
-template <int T, int U, int W, class Keep>
-__device__ __forceinline__ void capture_round(Row& R, int r, const float4 (&v)[U],
-                                              const int (&n)[Geo<T, U, W>::kSlots], uint64_t Tc,
-                                              uint32_t* counter, uint2* list, uint32_t cap, Keep keep) {
-  using G = Geo<T, U, W>;
-#pragma unroll
-  for (int sl = 0; sl < G::kSlots; ++sl) {
-    const bool kept = n[sl] > 0 && keep(R, r, v, sl, n[sl]);
-    const int64_t pos = slot_pos<T, U, W>(R, r, sl);
-#pragma unroll
-    for (int j = 0; j < G::kVS; ++j)
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int o = 4 * j + e;
-        const uint32_t kk = key_of(lane4(v[sl * G::kVS + j], e));
-        const bool pe = kept && o < n[sl] && composite(kk, (uint32_t)(pos + o)) >= Tc;
-        warp_append(pe, kk, (uint32_t)(pos + o), counter, list, cap);
-      }
-  }
-}
-
 // ------------------------------------------------------------------ block items (stage A)
 
 template <int T, int U, int W>
-__device__ __forceinline__ void hist_round_blocks(Row& R, const float4 (&v)[U],
-                                                  const int (&n)[Geo<T, U, W>::kSlots], int level,
+__device__ __forceinline__ void hist_round_blocks(Row& R, const Bufs<U, Geo<T, U, W>::kSlots>& B, int level,
                                                   uint32_t d1) {
 #pragma unroll
   for (int s = 0; s < Geo<T, U, W>::kSlots; ++s) {
-    if (n[s] == 0) continue;
-    const uint32_t kk = slot_block_key<T, U, W>(v, s, n[s]);
+    const int ns = B.n(s);
+    if (ns == 0) continue;
+    const uint32_t kk = B.use_b ? slot_block_key<T, U, W>(B.b, s, ns) : slot_block_key<T, U, W>(B.a, s, ns);
     if (level == 1) atomicAdd(&R.hist[kk >> 21], 1u);
     else if ((kk >> 21) == d1) atomicAdd(&R.hist[(kk >> 10) & (kBins - 1)], 1u);
   }
 }
 
 template <int T, int U, int W>
-__device__ __forceinline__ void filter_round_blocks(Row& R, int r, const float4 (&v)[U],
-                                                    const int (&n)[Geo<T, U, W>::kSlots], uint32_t t,
-                                                    uint32_t* counter, uint2* list, uint32_t cap) {
+__device__ __forceinline__ void filter_round_blocks(Row& R, int r, const Bufs<U, Geo<T, U, W>::kSlots>& B,
+                                                    uint32_t t, uint32_t* counter, uint2* list, uint32_t cap) {
 #pragma unroll
   for (int s = 0; s < Geo<T, U, W>::kSlots; ++s) {
-    const uint32_t kk = n[s] > 0 ? slot_block_key<T, U, W>(v, s, n[s]) : 0u;
-    const bool pe = n[s] > 0 && kk >= t;
+    const int ns = B.n(s);
+    const uint32_t kk =
+        ns > 0 ? (B.use_b ? slot_block_key<T, U, W>(B.b, s, ns) : slot_block_key<T, U, W>(B.a, s, ns)) : 0u;
+    const bool pe = ns > 0 && kk >= t;
     const uint32_t bid = (uint32_t)(slot_pos<T, U, W>(R, r, s) / W);
     warp_append(pe, kk, bid, counter, list, cap);
   }
 }
 
-template <int T, int U, int W>
-__device__ __forceinline__ void exact_hist_round_blocks(Row& R, int r, const float4 (&v)[U],
-                                                        const int (&n)[Geo<T, U, W>::kSlots],
-                                                        uint64_t tval, uint64_t tmask, int s,
-                                                        uint32_t wmask) {
-#pragma unroll
-  for (int sl = 0; sl < Geo<T, U, W>::kSlots; ++sl) {
-    if (n[sl] == 0) continue;
-    const uint64_t c = composite(slot_block_key<T, U, W>(v, sl, n[sl]),
-                                 (uint32_t)(slot_pos<T, U, W>(R, r, sl) / W));
-    if ((c & tmask) == tval) atomicAdd(&R.hist[(uint32_t)(c >> s) & wmask], 1u);
-  }
-}
-
-template <int T, int U, int W>
-__device__ __forceinline__ void capture_round_blocks(Row& R, int r, const float4 (&v)[U],
-                                                     const int (&n)[Geo<T, U, W>::kSlots], uint64_t Tc,
-                                                     uint32_t* counter, uint2* list, uint32_t cap) {
-#pragma unroll
-  for (int sl = 0; sl < Geo<T, U, W>::kSlots; ++sl) {
-    const uint32_t kk = n[sl] > 0 ? slot_block_key<T, U, W>(v, sl, n[sl]) : 0u;
-    const uint32_t bid = (uint32_t)(slot_pos<T, U, W>(R, r, sl) / W);
-    const bool pe = n[sl] > 0 && composite(kk, bid) >= Tc;
-    warp_append(pe, kk, bid, counter, list, cap);
-  }
-}
-
-// ------------------------------------------------------------------ local select / output
+// ------------------------------------------------------------------ local select (radix, fallback)
 
 // Sample-rank target for the threshold estimate. With the whole slice sampled
 // the target is exact; otherwise a margin keeps the k-th item above the
@@ -458,11 +446,13 @@ __device__ __forceinline__ uint32_t bins_total(const uint32_t* bins, Misc* m) {
   return block_sum<T>(s, m);
 }
 
-// Exact MSD radix select over cand[0, n): the composite Tc with exactly K
-// entries >= Tc. Requires 1 <= K <= n and all composites distinct.
+// Exact MSD radix select over the valid candidates: the composite Tc with
+// exactly K of them >= Tc. Requires 1 <= K <= number of valid candidates and
+// all composites distinct.
 template <int T>
-__device__ __forceinline__ uint64_t select_local(Row& R, uint32_t n, uint32_t K, int64_t idx_limit) {
+__device__ __forceinline__ uint64_t select_local(Row& R, uint32_t K, int64_t idx_limit) {
   Misc* m = R.m;
+  const Cands cs = cands(R);
   uint64_t tval = 0, tmask = 0;
   uint32_t need = K;
   for (int di = 0; di < 6; ++di) {
@@ -474,8 +464,9 @@ __device__ __forceinline__ uint64_t select_local(Row& R, uint32_t n, uint32_t K,
       continue;
     }
     zero_bins<T>(R.hist);
-    for (uint32_t i = threadIdx.x; i < n; i += T) {
-      const uint2 e = R.cand[i];
+    for (uint32_t i = threadIdx.x; i < cs.slots; i += T) {
+      if (!cs.valid(i)) continue;
+      const uint2 e = cs.c[i];
       const uint64_t c = composite(e.x, e.y);
       if ((c & tmask) == tval) atomicAdd(&R.hist[(uint32_t)(c >> s) & ((1u << w) - 1u)], 1u);
     }
@@ -491,18 +482,19 @@ __device__ __forceinline__ uint64_t select_local(Row& R, uint32_t n, uint32_t K,
   return tval;
 }
 
-// Compact every cand entry with composite >= Tc into stage[] (as composites).
+// Compact every valid candidate with composite >= Tc into stage[] (as composites).
 template <int T>
-__device__ __forceinline__ uint32_t compact_selected(Row& R, uint32_t n, uint64_t Tc) {
+__device__ __forceinline__ uint32_t compact_selected(Row& R, uint64_t Tc) {
   Misc* m = R.m;
+  const Cands cs = cands(R);
   if (threadIdx.x == 0) m->aux[0] = 0;
   __syncthreads();
-  for (uint32_t base = 0; base < n; base += T) {
+  for (uint32_t base = 0; base < cs.slots; base += T) {
     const uint32_t i = base + threadIdx.x;
     uint64_t c = 0;
     bool pr = false;
-    if (i < n) {
-      const uint2 e = R.cand[i];
+    if (i < cs.slots && cs.valid(i)) {
+      const uint2 e = cs.c[i];
       c = composite(e.x, e.y);
       pr = c >= Tc;
     }
@@ -523,6 +515,8 @@ __device__ __forceinline__ uint32_t compact_selected(Row& R, uint32_t n, uint64_
   return cnt;
 }
 
+// ------------------------------------------------------------------ ordered output
+
 __device__ __forceinline__ void write_slot(int32_t* oi, float* ov, uint32_t slot, uint64_t c, const float* rowp) {
   const uint32_t key = (uint32_t)(c >> 32), idx = ~(uint32_t)c;
   oi[slot] = (int32_t)idx;
@@ -538,12 +532,15 @@ __device__ __forceinline__ void write_padding(const Row& R, int32_t* oi, float* 
   }
 }
 
-// Ordered output from stage[0, K) (any order): bitonic sort when one CTA owns
-// the row or own slices are large, else each CTA ranks its own items by counting.
-template <int T, class Owner>
-__device__ __forceinline__ void write_sorted_fallback(Row& R, uint32_t K, uint32_t kout, int32_t* oi, float* ov,
-                                                      Owner owner) {
+// Output fallback for candidate sets with heavily populated buckets: radix
+// select of the K-th composite, compaction, then a bitonic sort (one CTA or
+// large own slices) or a rank count per own item.
+template <int T>
+__device__ __noinline__ void sorted_fallback(Row R, bool exact, uint64_t Tc, uint32_t K, uint32_t kout,
+                                             int32_t* oi, float* ov, int64_t idx_limit, OwnSlice owner) {
   Misc* m = R.m;
+  const uint64_t T64 = exact ? Tc : select_local<T>(R, K, idx_limit);
+  compact_selected<T>(R, T64);
   const bool use_sort = (R.nclus == 1) || (K > 64u * R.nclus);
   if (use_sort) {
     uint32_t P = 2;
@@ -585,36 +582,60 @@ __device__ __forceinline__ void write_sorted_fallback(Row& R, uint32_t K, uint32
   __syncthreads();
 }
 
-// Select the top K of cand[0, N) and write them in order (see step 4 at the
-// top of lt_device.cuh). Returns false, having written nothing, when a bucket
-// at or above the k-th item's bucket holds more than kMaxBucket items.
-template <int T, class Owner>
-__device__ __forceinline__ bool bucket_select_sort(Row& R, uint32_t N, uint32_t K, uint32_t kout, int32_t* oi,
-                                                   float* ov, Owner owner) {
+// Select the top K of the valid candidates and write them in order (see step
+// 4 at the top of lt_device.cuh). Returns false, having written nothing, when
+// some bucket holds more than kMaxBucket candidates. Expects kmin, kmax,
+// res_max and aux[1] reset.
+template <int T>
+__device__ __forceinline__ bool bucket_select_sort(Row& R, uint32_t K, uint32_t kout, int32_t* oi, float* ov,
+                                                   OwnSlice owner) {
   constexpr int BPT = kBins / T;
   Misc* m = R.m;
-  uint32_t lo = 0xffffffffu, hi = 0u;
-  for (uint32_t i = threadIdx.x; i < N; i += T) {
-    const uint32_t kk = R.cand[i].x;
+  const Cands cs = cands(R);
+  // key range and count of the candidates (and a zeroed histogram)
+  uint32_t lo = 0xffffffffu, hi = 0u, nvalid = 0;
+  for (uint32_t i = threadIdx.x; i < cs.slots; i += T) {
+    if (!cs.valid(i)) continue;
+    const uint32_t kk = cs.c[i].x;
     lo = min(lo, kk);
     hi = max(hi, kk);
+    ++nvalid;
   }
-  block_minmax<T>(lo, hi, m);
+  lo = __reduce_min_sync(kFull, lo);
+  hi = __reduce_max_sync(kFull, hi);
+  nvalid = __reduce_add_sync(kFull, nvalid);
+  if (lane_id() == 0) {
+    atomicMin(&m->kmin, lo);
+    atomicMax(&m->kmax, hi);
+    atomicAdd(&m->aux[1], nvalid);
+  }
+  {
+    uint4* z = reinterpret_cast<uint4*>(R.hist);
+    for (int i = threadIdx.x; i < kBins / 4; i += T) z[i] = make_uint4(0, 0, 0, 0);
+  }
+  __syncthreads();
+  lo = m->kmin;
+  hi = m->kmax;
+  const uint32_t N = m->aux[1];
   if (hi == lo && N > (uint32_t)kMaxBucket) return false;
   const float scale = (float)kBins / ((float)(hi - lo) + 1.0f);
   auto bucket = [lo, scale](uint32_t key) -> uint32_t {
     const uint32_t b = (uint32_t)((float)(key - lo) * scale);
     return b > (uint32_t)(kBins - 1) ? (uint32_t)(kBins - 1) : b;
   };
-  zero_bins<T>(R.hist);
-  for (uint32_t i = threadIdx.x; i < N; i += T) atomicAdd(&R.hist[bucket(R.cand[i].x)], 1u);
+  for (uint32_t i = threadIdx.x; i < cs.slots; i += T)
+    if (cs.valid(i)) atomicAdd(&R.hist[bucket(cs.c[i].x)], 1u);
   __syncthreads();
-  // exclusive suffix starts -> aux; the bucket b* holding the K-th item
+  // exclusive suffix starts -> aux; the bucket b* holding the K-th item; the
+  // largest bucket
   uint32_t v[BPT];
   load_bins<T>(R.hist, v);
-  uint32_t tot = 0;
+  uint32_t tot = 0, mx = 0;
 #pragma unroll
-  for (int j = 0; j < BPT; ++j) tot += v[j];
+  for (int j = 0; j < BPT; ++j) {
+    tot += v[j];
+    mx = max(mx, v[j]);
+  }
   uint32_t a = block_suffix_excl<T>(tot, m);
 #pragma unroll
   for (int j = BPT - 1; j >= 0; --j) {
@@ -626,18 +647,15 @@ __device__ __forceinline__ bool bucket_select_sort(Row& R, uint32_t N, uint32_t 
     }
     a += v[j];
   }
+  mx = __reduce_max_sync(kFull, mx);
+  if (lane_id() == 0) atomicMax(&m->res_max, mx);
   __syncthreads();
+  if (m->res_max > (uint32_t)kMaxBucket) return false;
   const uint32_t bstar = m->res_digit, above = m->res_above, cstar = m->res_cnt;
-  uint32_t mx = 0;
-#pragma unroll
-  for (int j = 0; j < BPT; ++j)
-    if (threadIdx.x * BPT + j >= bstar) mx = max(mx, v[j]);
-  uint32_t dummy = 0;
-  block_minmax<T>(dummy, mx, m);
-  if (mx > (uint32_t)kMaxBucket) return false;
   // scatter the items of buckets >= b* into stage, grouped by bucket
-  for (uint32_t i = threadIdx.x; i < N; i += T) {
-    const uint2 e = R.cand[i];
+  for (uint32_t i = threadIdx.x; i < cs.slots; i += T) {
+    if (!cs.valid(i)) continue;
+    const uint2 e = cs.c[i];
     const uint32_t b = bucket(e.x);
     if (b >= bstar) {
       const uint32_t pos = atomicAdd(&R.aux[b], 1u);
@@ -661,41 +679,192 @@ __device__ __forceinline__ bool bucket_select_sort(Row& R, uint32_t N, uint32_t 
   return true;
 }
 
+// ------------------------------------------------------------------ streaming exact select (rare)
+
+// Streaming radix select over this stage's items: 11/11/10-bit digit passes
+// over the composites (skipping the constant high bits of ~index), each pass
+// re-reading the slice and merging histograms over DSMEM, then one capture
+// pass of the K items >= the K-th composite into a flat candidate array.
+// Returns that composite. Requires R.init_pending == false.
+template <int T, int U, int W, bool kBlocks, class Keep>
+__device__ __noinline__ uint64_t exact_select(Row R, const Params p, uint32_t K, int64_t idx_limit, Keep keep) {
+  using G = Geo<T, U, W>;
+  Misc* m = R.m;
+  const bool vec = p.vec_ok != 0;
+  float4 va[U];
+  int na[G::kSlots];
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    m->cand_count = 0;
+    m->aux[0] = 0;
+  }
+  __syncthreads();
+  uint64_t tval = 0, tmask = 0;
+  uint32_t need = K;
+  int buf = 0;
+  for (int di = 0; di < 6; ++di) {
+    const int sh = digit_shift(di), w = digit_width(di);
+    const uint64_t dmask = ((1ull << w) - 1ull) << sh;
+    const uint32_t wmask = (1u << w) - 1u;
+    if (di == 3 && idx_limit <= (int64_t(1) << 21)) {
+      tval |= dmask;
+      tmask |= dmask;
+      continue;
+    }
+    zero_bins<T>(R.hist);
+    for (int r = 0; r < R.rounds; ++r) {
+      load_round<T, U, W>(R, vec, r, va, na);
+#pragma unroll
+      for (int s = 0; s < G::kSlots; ++s) {
+        if (na[s] == 0) continue;
+        const int64_t pos = slot_pos<T, U, W>(R, r, s);
+        if (kBlocks) {
+          const uint64_t c = composite(slot_block_key<T, U, W>(va, s, na[s]), (uint32_t)(pos / W));
+          if ((c & tmask) == tval) atomicAdd(&R.hist[(uint32_t)(c >> sh) & wmask], 1u);
+        } else {
+          if (!keep(R, r, va, s, na[s])) continue;
+#pragma unroll
+          for (int j = 0; j < G::kVS; ++j)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int o = 4 * j + e;
+              if (o < na[s]) {
+                const uint64_t c = composite(key_of(lane4(va[s * G::kVS + j], e)), (uint32_t)(pos + o));
+                if ((c & tmask) == tval) atomicAdd(&R.hist[(uint32_t)(c >> sh) & wmask], 1u);
+              }
+            }
+        }
+      }
+    }
+    const uint32_t* bins = merge_hist<T>(R, buf);
+    find_digit<T>(bins, need, m);
+    const uint32_t d = m->res_digit, above = m->res_above, cnt = m->res_cnt;
+    release_merged<T>(R, buf);
+    buf ^= 1;
+    need -= above;
+    tval |= (uint64_t)d << sh;
+    tmask |= dmask;
+    if (cnt == need) break;
+  }
+  // capture the K items >= tval into stage[] (local), then into every CTA's
+  // candidate array at offsets reserved with remote atomics
+  uint2* lst = reinterpret_cast<uint2*>(R.stage);
+  const uint32_t lcap = R.stage_cap;
+  for (int r = 0; r < R.rounds; ++r) {
+    load_round<T, U, W>(R, vec, r, va, na);
+#pragma unroll
+    for (int s = 0; s < G::kSlots; ++s) {
+      const int64_t pos = slot_pos<T, U, W>(R, r, s);
+      if (kBlocks) {
+        const uint32_t kk = na[s] > 0 ? slot_block_key<T, U, W>(va, s, na[s]) : 0u;
+        const uint32_t bid = (uint32_t)(pos / W);
+        warp_append(na[s] > 0 && composite(kk, bid) >= tval, kk, bid, &m->aux[0], lst, lcap);
+      } else {
+        const bool kept = na[s] > 0 && keep(R, r, va, s, na[s]);
+#pragma unroll
+        for (int j = 0; j < G::kVS; ++j)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int o = 4 * j + e;
+            const uint32_t kk = key_of(lane4(va[s * G::kVS + j], e));
+            const bool pe = kept && o < na[s] && composite(kk, (uint32_t)(pos + o)) >= tval;
+            warp_append(pe, kk, (uint32_t)(pos + o), &m->aux[0], lst, lcap);
+          }
+      }
+    }
+  }
+  __syncthreads();
+  const uint32_t n = m->aux[0] < lcap ? m->aux[0] : lcap;
+  const uint32_t cap = (uint32_t)p.cap;
+  if (R.nclus == 1) {
+    for (uint32_t i = threadIdx.x; i < n; i += T) R.cand[i] = lst[i];
+    if (threadIdx.x == 0) m->cand_count = n;
+    __syncthreads();
+  } else {
+    if (threadIdx.x < R.nclus)
+      m->peer_base[threadIdx.x] = dsmem_atom_add(peer_addr(smem_addr(&m->cand_count), threadIdx.x), n);
+    __syncthreads();
+    const uint32_t cand_base = smem_addr(R.cand);
+    for (uint32_t q = 0; q < R.nclus; ++q) {
+      const uint32_t pb = m->peer_base[q];
+      const uint32_t dst = peer_addr(cand_base, q);
+      for (uint32_t i = threadIdx.x; i < n; i += T)
+        if (pb + i < cap) dsmem_st_v2(dst + 8u * (pb + i), lst[i]);
+    }
+    cluster_sync();
+  }
+  // flat layout: one segment holding the K captured items
+  if (threadIdx.x == 0) {
+    reset_candidate_range(m);
+    m->nseg = 1;
+    m->shift = 31 - __clz(cap);
+    m->seg_cnt[0] = m->cand_count < cap ? m->cand_count : cap;
+  }
+  __syncthreads();
+  return tval;
+}
+
 // ------------------------------------------------------------------ one selection stage
 
 // Estimate -> filter -> exchange over the items of this stage (positions, or
-// blocks when kBlocks). Returns true when the exact streaming select ran:
-// then cand[0, K) holds exactly the selected items and *Tc their threshold
-// composite. Returns false on the fast path: cand[0, cand_count) holds every
-// item >= a lower bound of the K-th item, with K <= cand_count <= cap.
-// va/vb hold rounds 0 and 1 on entry when `loaded`.
+// blocks when kBlocks); on a miss, the streaming exact select. Returns true
+// when the exact select ran (the candidate array then holds exactly the K
+// selected items and *Tc is their threshold composite); false on the fast
+// path (the candidates are every item >= a lower bound of the K-th item).
+// cur/nxt hold rounds 0 and 1 on entry when `loaded`; *regs_intact tells
+// whether they still do on return.
 template <int T, int U, int W, bool kBlocks, class Keep>
-__device__ __forceinline__ bool select_stage(Row& R, const Params& p, float4 (&va)[U],
-                                             int (&na)[Geo<T, U, W>::kSlots], float4 (&vb)[U],
-                                             int (&nb)[Geo<T, U, W>::kSlots], bool loaded, uint32_t K,
+__device__ __forceinline__ bool select_stage(Row& R, const Params& p, float4 (&cur)[U],
+                                             int (&nc)[Geo<T, U, W>::kSlots], float4 (&nxt)[U],
+                                             int (&nn)[Geo<T, U, W>::kSlots], bool loaded, uint32_t K,
                                              int64_t items, int64_t idx_limit, Keep keep, bool first,
                                              bool* regs_intact, uint64_t* Tc, int tr) {
+  using G = Geo<T, U, W>;
   Misc* m = R.m;
   const bool vec = p.vec_ok != 0;
-  const uint32_t cap = (uint32_t)p.cap;
   if (!first) {
-    // A later stage reuses the candidate lists: clear them, and make sure no
-    // peer pushes into them before this CTA has finished with the last stage.
-    reset_lists(R);
+    // A later stage reuses the candidate array: clear the counts, and make
+    // sure no peer pushes into it before this CTA has finished with it.
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      m->local_count = 0;
+      m->cand_count = 0;
+    }
+    __syncthreads();
     if (R.nclus > 1) {
-      if (R.init_pending) { cluster_wait(); R.init_pending = false; }
+      wait_init(R);
       cluster_sync();
     }
   }
-  uint32_t* counter = (R.nclus > 1) ? &m->local_count : &m->cand_count;
-  uint2* list = (R.nclus > 1) ? R.local : R.cand;
+  const uint32_t seg = 1u << R.seg_shift;
+  uint2* list = R.cand + (R.rank << R.seg_shift);
+  uint32_t* counter = &m->local_count;
+  const uint32_t cap = (uint32_t)p.cap;
   const bool full = R.rounds_max <= 2;
-  *regs_intact = R.rounds <= 2;
+  const bool resident = R.rounds <= 2;
+  *regs_intact = resident;
   *Tc = 0;
 
   if (!loaded) {
-    if (R.rounds > 0) load_round<T, U, W>(R, vec, 0, va, na); else clear_round(na);
-    if (R.rounds > 1) load_round<T, U, W>(R, vec, 1, vb, nb); else clear_round(nb);
+    // rounds 0 and 1 into cur and nxt (one load site: shift, then load)
+    clear_round(nc);
+    clear_round(nn);
+#pragma unroll 1
+    for (int i = 0; i < 2; ++i) {
+#pragma unroll
+      for (int u = 0; u < U; ++u) cur[u] = nxt[u];
+#pragma unroll
+      for (int s = 0; s < G::kSlots; ++s) nc[s] = nn[s];
+      if (i < R.rounds) load_round<T, U, W>(R, vec, i, nxt, nn);
+      else clear_round(nn);
+    }
+    if (R.rounds == 1) {  // round 0 ended up in nxt
+#pragma unroll
+      for (int u = 0; u < U; ++u) cur[u] = nxt[u];
+#pragma unroll
+      for (int s = 0; s < G::kSlots; ++s) nc[s] = nn[s];
+      clear_round(nn);
+    }
   }
 
   bool exact = p.force_exact != 0;
@@ -704,110 +873,82 @@ __device__ __forceinline__ bool select_stage(Row& R, const Params& p, float4 (&v
     // ---- threshold estimate from the digit histogram of the sample
     uint32_t t = 0;
     if (items > (int64_t)(cap / 2)) {
-      zero_bins<T>(R.hist);
-      if (kBlocks) {
-        hist_round_blocks<T, U, W>(R, va, na, 1, 0);
-        if (full) hist_round_blocks<T, U, W>(R, vb, nb, 1, 0);
-      } else {
-        hist_round<T, U, W>(R, 0, va, na, 1, 0, keep);
-        if (full) hist_round<T, U, W>(R, 1, vb, nb, 1, 0, keep);
-      }
-      stamp(p, tr + kTrHist);
-      const uint32_t* bins = merge_hist<T>(R, 0);
-      stamp(p, tr + kTrMerge);
-      const uint32_t ns = full ? (uint32_t)items : bins_total<T>(bins, m);
-      if (ns > 0) {
-        const uint32_t r = sample_target(K, ns, items, full);
-        find_digit<T>(bins, r, m);
-        const uint32_t d1 = m->res_digit, above1 = m->res_above, cnt1 = m->res_cnt;
-        release_merged<T>(R, 0);
-        const float predicted = full ? (float)(above1 + cnt1)
-                                     : (float)(above1 + cnt1) * ((float)items / (float)ns);
-        t = d1 << 21;
-        if (predicted > 0.5f * (float)cap) {
-          zero_bins<T>(R.hist);
-          if (kBlocks) {
-            hist_round_blocks<T, U, W>(R, va, na, 2, d1);
-            if (full) hist_round_blocks<T, U, W>(R, vb, nb, 2, d1);
-          } else {
-            hist_round<T, U, W>(R, 0, va, na, 2, d1, keep);
-            if (full) hist_round<T, U, W>(R, 1, vb, nb, 2, d1, keep);
-          }
-          const uint32_t* bins2 = merge_hist<T>(R, 1);
-          find_digit<T>(bins2, r - above1, m);
-          const uint32_t d2 = m->res_digit;
-          release_merged<T>(R, 1);
-          t |= d2 << 10;
+      const int nsr = full ? (R.rounds < 2 ? R.rounds : 2) : (R.rounds < 1 ? R.rounds : 1);
+      uint32_t r = 0, d1 = 0, above1 = 0;
+#pragma unroll 1
+      for (int level = 1; level <= 2; ++level) {
+        zero_bins<T>(R.hist);
+#pragma unroll 1
+        for (int q = 0; q < nsr; ++q) {
+          const Bufs<U, G::kSlots> B{cur, nc, nxt, nn, q != 0};
+          if (kBlocks) hist_round_blocks<T, U, W>(R, B, level, d1);
+          else hist_round<T, U, W>(R, q, B, level, d1, keep);
         }
-      } else {
-        release_merged<T>(R, 0);
+        if (level == 1) stamp(p, tr + kTrHist);
+        const uint32_t* bins = merge_hist<T>(R, level - 1);
+        if (level == 1) stamp(p, tr + kTrMerge);
+        if (level == 1) {
+          const uint32_t ns = full ? (uint32_t)items : bins_total<T>(bins, m);
+          if (ns == 0) {  // no sample: keep every item
+            release_merged<T>(R, 0);
+            break;
+          }
+          r = sample_target(K, ns, items, full);
+          find_digit<T>(bins, r, m);
+          d1 = m->res_digit;
+          above1 = m->res_above;
+          const uint32_t cnt1 = m->res_cnt;
+          release_merged<T>(R, 0);
+          t = d1 << 21;
+          const float predicted = full ? (float)(above1 + cnt1)
+                                       : (float)(above1 + cnt1) * ((float)items / (float)ns);
+          if (predicted <= 0.5f * (float)cap) break;  // one 11-bit level is selective enough
+        } else {
+          find_digit<T>(bins, r - above1, m);
+          t |= m->res_digit << 10;
+          release_merged<T>(R, 1);
+        }
       }
     }
     stamp(p, tr + kTrEstimate);
     // ---- filter every round against the threshold
     const bool all = (t == 0u);
     const float g = threshold_float(all ? 1u : t);
-    for (int r = 0; r < R.rounds; r += 2) {
-      if (kBlocks) filter_round_blocks<T, U, W>(R, r, va, na, t, counter, list, cap);
-      else filter_round<T, U, W>(R, r, va, na, g, all, counter, list, cap, keep);
-      if (r + 2 < R.rounds) load_round<T, U, W>(R, vec, r + 2, va, na);
-      if (r + 1 < R.rounds) {
-        if (kBlocks) filter_round_blocks<T, U, W>(R, r + 1, vb, nb, t, counter, list, cap);
-        else filter_round<T, U, W>(R, r + 1, vb, nb, g, all, counter, list, cap, keep);
-        if (r + 3 < R.rounds) load_round<T, U, W>(R, vec, r + 3, vb, nb);
+#pragma unroll 1
+    for (int r = 0; r < R.rounds; ++r) {
+      const Bufs<U, G::kSlots> B{cur, nc, nxt, nn, resident && r == 1};
+      if (kBlocks) filter_round_blocks<T, U, W>(R, r, B, t, counter, list, seg);
+      else filter_round<T, U, W>(R, r, B, g, all, counter, list, seg, keep);
+      if (!resident) {
+#pragma unroll
+        for (int i = 0; i < U; ++i) cur[i] = nxt[i];
+#pragma unroll
+        for (int s = 0; s < G::kSlots; ++s) nc[s] = nn[s];
+        if (r + 2 < R.rounds) load_round<T, U, W>(R, vec, r + 2, nxt, nn);
+        else clear_round(nn);
       }
     }
     stamp(p, tr + kTrFilter);
-    exchange<T>(R, cap);
+    exchange_segments<T>(R);
     stamp(p, tr + kTrExchange);
-    const uint32_t N = m->cand_count;
-    const bool overflow = (m->flags & 1u) || N > cap;
-    if (overflow || N < K) {
+    uint32_t total = 0;
+    bool overflow = false;
+    for (uint32_t q = 0; q < R.nclus; ++q) {
+      const uint32_t c = m->seg_cnt[q];
+      total += c;
+      overflow = overflow || c > seg;
+    }
+    if (overflow || total < K) {
       exact = true;
       stat = overflow ? kCntOverflow : kCntShort;
-      __syncthreads();
     }
   }
 
   if (exact && K > 0) {
-    // ---- streaming radix select: every pass re-reads the slice
     if (stat != kCntFast) bump(p, R, stat);
+    wait_init(R);
+    *Tc = exact_select<T, U, W, kBlocks>(R, p, K, idx_limit, keep);
     *regs_intact = false;
-    reset_lists(R);
-    uint64_t tval = 0, tmask = 0;
-    uint32_t need = K;
-    int buf = 0;
-    for (int di = 0; di < 6; ++di) {
-      const int s = digit_shift(di), w = digit_width(di);
-      const uint64_t dmask = ((1ull << w) - 1ull) << s;
-      if (di == 3 && idx_limit <= (int64_t(1) << 21)) {
-        tval |= dmask;
-        tmask |= dmask;
-        continue;
-      }
-      zero_bins<T>(R.hist);
-      for (int r = 0; r < R.rounds; ++r) {
-        load_round<T, U, W>(R, vec, r, va, na);
-        if (kBlocks) exact_hist_round_blocks<T, U, W>(R, r, va, na, tval, tmask, s, (1u << w) - 1u);
-        else exact_hist_round<T, U, W>(R, r, va, na, tval, tmask, s, (1u << w) - 1u, keep);
-      }
-      const uint32_t* bins = merge_hist<T>(R, buf);
-      find_digit<T>(bins, need, m);
-      const uint32_t d = m->res_digit, above = m->res_above, cnt = m->res_cnt;
-      release_merged<T>(R, buf);
-      buf ^= 1;
-      need -= above;
-      tval |= (uint64_t)d << s;
-      tmask |= dmask;
-      if (cnt == need) break;
-    }
-    *Tc = tval;
-    for (int r = 0; r < R.rounds; ++r) {
-      load_round<T, U, W>(R, vec, r, va, na);
-      if (kBlocks) capture_round_blocks<T, U, W>(R, r, va, na, tval, counter, list, cap);
-      else capture_round<T, U, W>(R, r, va, na, tval, counter, list, cap, keep);
-    }
-    exchange<T>(R, cap);
     stamp(p, tr + kTrExact);
     bump(p, R, kCntExact);
     return true;
@@ -818,28 +959,22 @@ __device__ __forceinline__ bool select_stage(Row& R, const Params& p, float4 (&v
 }
 
 // Select and write the top K positions of this row after select_stage.
-template <int T, class Owner>
+template <int T>
 __device__ __forceinline__ void output_positions(Row& R, const Params& p, bool exact, uint64_t Tc, uint32_t K,
-                                                 int64_t idx_limit, Owner owner) {
+                                                 int64_t idx_limit) {
   const uint32_t kout = (uint32_t)p.k;
   int32_t* oi = p.out_idx + R.row * (int64_t)kout;
   float* ov = p.out_val ? p.out_val + R.row * (int64_t)kout : nullptr;
   if (K == 0) {
     write_padding<T>(R, oi, ov, 0, kout);
-    return;
-  }
-  const uint32_t cap = (uint32_t)p.cap;
-  const uint32_t N = exact ? K : (R.m->cand_count < cap ? R.m->cand_count : cap);
-  if (!bucket_select_sort<T>(R, N, K, kout, oi, ov, owner)) {
-    const uint64_t T64 = exact ? Tc : select_local<T>(R, N, K, idx_limit);
-    compact_selected<T>(R, N, T64);
-    write_sorted_fallback<T>(R, K, kout, oi, ov, owner);
+  } else {
+    if (threadIdx.x == 0) R.m->aux[1] = 0;
+    __syncthreads();
+    const OwnSlice own = own_slice(R);
+    if (!bucket_select_sort<T>(R, K, kout, oi, ov, own))
+      sorted_fallback<T>(R, exact, Tc, K, kout, oi, ov, idx_limit, own);
   }
   stamp(p, kTrOutput);
-}
-
-__device__ __forceinline__ bool in_slice(const Row& R, uint32_t idx) {
-  return (int64_t)idx >= R.begin && (int64_t)idx < R.end;
 }
 
 }  // namespace lt

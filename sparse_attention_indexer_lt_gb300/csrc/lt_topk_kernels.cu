@@ -20,9 +20,8 @@ __global__ void __launch_bounds__(T, (T <= 256 ? 3 : 1)) topk_kernel(Params p) {
   uint64_t Tc;
   const bool exact = select_stage<T, U, 4, false>(R, p, va, na, vb, nb, false, K, R.L, p.row_stride,
                                                   KeepAll{}, true, &intact, &Tc, 0);
-  output_positions<T>(R, p, exact, Tc, K, p.row_stride,
-                      [&R](uint32_t idx) { return R.nclus == 1 || in_slice(R, idx); });
-  finish_row(R);
+  output_positions<T>(R, p, exact, Tc, K, p.row_stride);
+  wait_init(R);
 }
 
 const void* topk_kernel_ptr(int threads) {
