@@ -65,7 +65,8 @@ uint32_t next_pow2(uint32_t x) {
 struct Plan {
   int cluster = 1;
   int threads = kNarrowThreads;
-  uint32_t cap = 0;
+  uint32_t cap = 0;        // candidate slots: cluster * (1 << seg_shift)
+  uint32_t seg_shift = 0;  // log2 of the slots each CTA of the cluster may fill
   uint32_t sel_cap = 0;
   uint32_t smem = 0;
   const void* func = nullptr;
@@ -140,10 +141,12 @@ lt_status make_plan(int32_t rows, int64_t row_stride, int32_t k, bool blocked, i
   plan->func = blocked ? lt::blocked_kernel_ptr(threads, block) : lt::topk_kernel_ptr(threads);
   if (!plan->func) return LT_ERR_UNSUPPORTED;
 
+  // Candidate capacity: about 4k slots per row (the sampled threshold keeps
+  // roughly k to 1.5k items), split into one segment per CTA of the cluster,
+  // each segment at least 256 slots so uneven slices still fit.
   const uint32_t kmax = (uint32_t)(blocked ? (k > k_blocks ? k : k_blocks) : k);
-  uint32_t cap = next_pow2(4 * kmax);
-  cap = cap < 2048u ? 2048u : (cap > 4096u ? 4096u : cap);
-  plan->cap = cap;
+  uint32_t base_cap = next_pow2(4 * kmax);
+  base_cap = base_cap < 2048u ? 2048u : (base_cap > 4096u ? 4096u : base_cap);
   plan->sel_cap = next_pow2(kmax < 32u ? 32u : kmax);
 
   int c = 1;
@@ -153,6 +156,14 @@ lt_status make_plan(int32_t rows, int64_t row_stride, int32_t k, bool blocked, i
     while (c < 16 && (int64_t)rows * 2 * c <= di->sms && (int64_t)c * kWideRound < row_stride) c *= 2;
   }
   for (;;) {
+    uint32_t seg = base_cap;
+    if (c > 1) {
+      seg = next_pow2((base_cap + (uint32_t)c - 1) / (uint32_t)c);
+      if (seg < 256u) seg = 256u;
+    }
+    plan->cap = (uint32_t)c * seg;
+    plan->seg_shift = 0;
+    while ((1u << plan->seg_shift) < seg) ++plan->seg_shift;
     const uint32_t smem = lt::make_layout(c > 1, plan->cap, plan->sel_cap).total;
     if ((int)smem > di->smem_optin) return LT_ERR_UNSUPPORTED;
     st = prepare_kernel(dev, slot, plan->func, smem, c);
@@ -186,6 +197,7 @@ lt_status check_common(const float* scores, int32_t rows, int64_t row_stride, in
 lt_status launch(const Plan& plan, const lt::Params& prm, int32_t rows, void* stream) {
   lt::Params p = prm;
   p.cap = (int32_t)plan.cap;
+  p.seg_shift = (int32_t)plan.seg_shift;
   p.sel_cap = (int32_t)plan.sel_cap;
   p.clustered = plan.cluster > 1 ? 1 : 0;
   cudaLaunchConfig_t cfg = {};
