@@ -846,7 +846,8 @@ __device__ __forceinline__ bool select_stage(Row& R, const Params& p, float4 (&c
   *Tc = 0;
 
   if (!loaded) {
-    // rounds 0 and 1 into cur and nxt (one load site: shift, then load)
+    // rounds 0 and 1 into cur and nxt (one load site: shift, then load);
+    // with a single round, round 0 ends in cur and nxt is empty
     clear_round(nc);
     clear_round(nn);
 #pragma unroll 1
@@ -857,13 +858,6 @@ __device__ __forceinline__ bool select_stage(Row& R, const Params& p, float4 (&c
       for (int s = 0; s < G::kSlots; ++s) nc[s] = nn[s];
       if (i < R.rounds) load_round<T, U, W>(R, vec, i, nxt, nn);
       else clear_round(nn);
-    }
-    if (R.rounds == 1) {  // round 0 ended up in nxt
-#pragma unroll
-      for (int u = 0; u < U; ++u) cur[u] = nxt[u];
-#pragma unroll
-      for (int s = 0; s < G::kSlots; ++s) nc[s] = nn[s];
-      clear_round(nn);
     }
   }
 
