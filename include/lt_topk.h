@@ -104,7 +104,7 @@ lt_status lt_topk_blocked(const float* scores, const int32_t* lengths, int32_t r
  *                  number of CTAs that share one row (16 needs a device that
  *                  can schedule a 16-CTA cluster, else LT_ERR_UNSUPPORTED)
  *   force_threads  0 lets the planner choose; 256 (several CTAs per SM, for
- *                  large batches) or 1024 (one CTA per SM, for few rows)
+ *                  large batches) or 512 (one CTA per SM, for few rows)
  *   force_exact    nonzero skips the sampled-threshold fast path and runs the
  *                  streaming radix select on every row (same results)
  *   counters       NULL, or device int32[LT_NUM_COUNTERS] that the kernel

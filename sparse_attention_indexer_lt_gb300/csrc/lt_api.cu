@@ -3,7 +3,7 @@
 // Planning. One cluster of C CTAs owns one row. Two CTA shapes exist:
 //   narrow: 256 threads, several CTAs per SM -- used when the batch alone has
 //           at least one row per SM (C = 1: no cluster traffic at all);
-//   wide:   1024 threads, one CTA per SM -- used for few rows. C doubles (up
+//   wide:   512 threads, one CTA per SM -- used for few rows. C doubles (up
 //           to 16, the largest cluster a GPC can host) while the whole grid
 //           still fits on the SMs and each CTA still gets at least one round
 //           (16384 positions) of the row.
@@ -23,9 +23,9 @@
 namespace {
 
 constexpr int kMaxDevices = 64;
-constexpr int kWideThreads = 1024;
+constexpr int kWideThreads = 512;
 constexpr int kNarrowThreads = 256;
-constexpr int64_t kWideRound = 1024 * 4 * 4;  // positions per CTA per round (wide)
+constexpr int64_t kWideRound = 512 * 8 * 4;  // positions per CTA per round (wide)
 constexpr int kSlots = 10;                    // kernel variants
 
 struct DeviceInfo {

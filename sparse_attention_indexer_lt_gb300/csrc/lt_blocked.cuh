@@ -11,7 +11,8 @@ namespace lt {
 // block ids are also written in ascending order.
 template <int T, int W>
 __global__ void __launch_bounds__(T, (T <= 256 ? 3 : 1)) blocked_kernel(Params p) {
-  constexpr int U = (W / 4 > 4) ? W / 4 : 4;
+  constexpr int U0 = T <= 256 ? 4 : 8;  // float4 per thread per round
+  constexpr int U = (W / 4 > U0) ? W / 4 : U0;
   using G = Geo<T, U, W>;
   extern __shared__ __align__(128) unsigned char smem[];
   Row R;

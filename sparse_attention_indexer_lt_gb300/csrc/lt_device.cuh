@@ -301,9 +301,9 @@ __device__ __forceinline__ void load_bins(const uint32_t* bins, uint32_t (&v)[kB
 }
 
 // Exclusive suffix sum over threads of per-thread totals (the keys in bins
-// owned by threads with a larger index). Warp 0 scans the warp totals.
-// Contains two __syncthreads; the caller must __syncthreads before warp_a or
-// warp_b is written again.
+// owned by threads with a larger index). One __syncthreads; every thread then
+// adds the totals of the warps after its own (at most 16 broadcast reads).
+// The caller must __syncthreads before warp_a is written again.
 template <int T>
 __device__ __forceinline__ uint32_t block_suffix_excl(uint32_t tot, Misc* m) {
   constexpr int NW = T / 32;
@@ -316,19 +316,11 @@ __device__ __forceinline__ uint32_t block_suffix_excl(uint32_t tot, Misc* m) {
   }
   if (lane == 0) m->warp_a[warp] = incl;
   __syncthreads();
-  if (threadIdx.x < 32) {
-    const uint32_t w = threadIdx.x;
-    const uint32_t own = w < (uint32_t)NW ? m->warp_a[w] : 0u;
-    uint32_t suf = own;  // sum over warps >= w
+  uint32_t after = 0;
 #pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const uint32_t n = __shfl_down_sync(kFull, suf, o);
-      if (w + o < 32) suf += n;
-    }
-    if (w < (uint32_t)NW) m->warp_b[w] = suf - own;  // sum over warps > w
-  }
-  __syncthreads();
-  return m->warp_b[warp] + (incl - tot);
+  for (int w = 1; w < NW; ++w)
+    if (w > (int)warp) after += m->warp_a[w];
+  return after + (incl - tot);
 }
 
 // Find digit d with suffix(d + 1) < r <= suffix(d), suffix(d) = sum of bins[b >= d].

@@ -161,16 +161,20 @@ __device__ __forceinline__ void setup_row(Row& R, const Params& p, unsigned char
   }
   R.L = L;
   R.rowp = p.scores + R.row * p.row_stride;
-  int64_t per = (L + R.nclus - 1) / R.nclus;
-  per = (per + W - 1) / W * W;
+  // the cluster size, T, W and the slots per round are powers of two
+  const int cl2 = 31 - __clz((int)R.nclus);
+  int64_t per = (L + R.nclus - 1) >> cl2;
+  per = (per + W - 1) & ~(int64_t)(W - 1);
   const int64_t b = (int64_t)R.rank * per;
   R.begin = b < L ? b : L;
   R.end = (R.begin + per) < L ? (R.begin + per) : L;
   R.tbase = R.begin + (int64_t)threadIdx.x * W;
-  const int64_t nt = (R.end - R.begin + G::kTile - 1) / G::kTile;
-  R.rounds = (int)((nt + G::kSlots - 1) / G::kSlots);
-  const int64_t ntm = (per + G::kTile - 1) / G::kTile;
-  R.rounds_max = (int)((ntm + G::kSlots - 1) / G::kSlots);
+  constexpr int kTile2 = __builtin_ctz((unsigned)(T * W));
+  constexpr int kSl2 = __builtin_ctz((unsigned)G::kSlots);
+  const int64_t nt = (R.end - R.begin + G::kTile - 1) >> kTile2;
+  R.rounds = (int)((nt + G::kSlots - 1) >> kSl2);
+  const int64_t ntm = (per + G::kTile - 1) >> kTile2;
+  R.rounds_max = (int)((ntm + G::kSlots - 1) >> kSl2);
 
   Misc* m = R.m;
   if (threadIdx.x == 0) {
@@ -219,20 +223,41 @@ __device__ __forceinline__ void dsmem_st_u32(uint32_t addr, uint32_t v) {
 
 // ------------------------------------------------------------------ candidates
 
-// Candidate array view: nseg segments of (1 << shift) slots; slot i is valid
-// when its offset in its segment is below that segment's count.
+// Candidate array view: nseg segments of (1 << shift) slots, segment q
+// holding cnt[q] entries. Entries are numbered 0 .. total-1 across the
+// segments; at(i) maps a number to its slot through the running counts.
 struct Cands {
   const uint2* c;
-  const uint32_t* cnt;
-  uint32_t slots;
   uint32_t shift;
-  __device__ __forceinline__ bool valid(uint32_t i) const {
-    return (i & ((1u << shift) - 1u)) < cnt[i >> shift];
+  uint32_t nseg;
+  uint32_t total;
+  uint32_t start[kMaxCluster];  // entries before segment q
+  __device__ __forceinline__ uint2 at(uint32_t i) const {
+    uint32_t q = 0;
+#pragma unroll
+    for (int j = 1; j < kMaxCluster; ++j)
+      if ((uint32_t)j < nseg && start[j] <= i) q = j;
+    return c[(q << shift) + (i - start[q])];
   }
 };
 __device__ __forceinline__ Cands cands(const Row& R) {
   const Misc* m = R.m;
-  return Cands{R.cand, m->seg_cnt, m->nseg << m->shift, m->shift};
+  Cands cs;
+  cs.c = R.cand;
+  cs.shift = m->shift;
+  cs.nseg = m->nseg;
+  const uint32_t seg = 1u << cs.shift;
+  uint32_t acc = 0;
+#pragma unroll
+  for (int q = 0; q < kMaxCluster; ++q) {
+    cs.start[q] = acc;
+    if ((uint32_t)q < cs.nseg) {
+      const uint32_t n = m->seg_cnt[q];
+      acc += n < seg ? n : seg;
+    }
+  }
+  cs.total = acc;
+  return cs;
 }
 
 __device__ __forceinline__ void reset_candidate_range(Misc* m) {
@@ -296,10 +321,12 @@ __device__ __forceinline__ void exchange_segments(Row& R) {
   if (threadIdx.x < R.nclus) dsmem_st_u32(peer_addr(smem_addr(&m->seg_cnt[R.rank]), threadIdx.x), n);
   const uint2* mine = R.cand + off;
   const uint32_t src = smem_addr(R.cand) + 8u * off;
-  for (uint32_t q = 0; q < R.nclus; ++q) {
-    if (q == R.rank) continue;
-    const uint32_t dst = peer_addr(src, q);
-    for (uint32_t i = threadIdx.x; i < n_put; i += T) dsmem_st_v2(dst + 8u * i, mine[i]);
+  // (peer, entry) pairs flattened over the threads; peers rank+1 .. rank+nclus-1
+  const uint32_t pairs = n_put * (R.nclus - 1);
+  for (uint32_t x = threadIdx.x; x < pairs; x += T) {
+    const uint32_t d = x / n_put, i = x - d * n_put;
+    const uint32_t q = (R.rank + 1 + d) & (R.nclus - 1);
+    dsmem_st_v2(peer_addr(src + 8u * i, q), mine[i]);
   }
   cluster_sync();
 }
@@ -464,9 +491,8 @@ __device__ __forceinline__ uint64_t select_local(Row& R, uint32_t K, int64_t idx
       continue;
     }
     zero_bins<T>(R.hist);
-    for (uint32_t i = threadIdx.x; i < cs.slots; i += T) {
-      if (!cs.valid(i)) continue;
-      const uint2 e = cs.c[i];
+    for (uint32_t i = threadIdx.x; i < cs.total; i += T) {
+      const uint2 e = cs.at(i);
       const uint64_t c = composite(e.x, e.y);
       if ((c & tmask) == tval) atomicAdd(&R.hist[(uint32_t)(c >> s) & ((1u << w) - 1u)], 1u);
     }
@@ -489,12 +515,12 @@ __device__ __forceinline__ uint32_t compact_selected(Row& R, uint64_t Tc) {
   const Cands cs = cands(R);
   if (threadIdx.x == 0) m->aux[0] = 0;
   __syncthreads();
-  for (uint32_t base = 0; base < cs.slots; base += T) {
+  for (uint32_t base = 0; base < cs.total; base += T) {
     const uint32_t i = base + threadIdx.x;
     uint64_t c = 0;
     bool pr = false;
-    if (i < cs.slots && cs.valid(i)) {
-      const uint2 e = cs.c[i];
+    if (i < cs.total) {
+      const uint2 e = cs.at(i);
       c = composite(e.x, e.y);
       pr = c >= Tc;
     }
@@ -584,8 +610,8 @@ __device__ __noinline__ void sorted_fallback(Row R, bool exact, uint64_t Tc, uin
 
 // Select the top K of the valid candidates and write them in order (see step
 // 4 at the top of lt_device.cuh). Returns false, having written nothing, when
-// some bucket holds more than kMaxBucket candidates. Expects kmin, kmax,
-// res_max and aux[1] reset.
+// some bucket holds more than kMaxBucket candidates. Expects kmin, kmax and
+// res_max reset.
 template <int T>
 __device__ __forceinline__ bool bucket_select_sort(Row& R, uint32_t K, uint32_t kout, int32_t* oi, float* ov,
                                                    OwnSlice owner) {
@@ -593,21 +619,17 @@ __device__ __forceinline__ bool bucket_select_sort(Row& R, uint32_t K, uint32_t 
   Misc* m = R.m;
   const Cands cs = cands(R);
   // key range and count of the candidates (and a zeroed histogram)
-  uint32_t lo = 0xffffffffu, hi = 0u, nvalid = 0;
-  for (uint32_t i = threadIdx.x; i < cs.slots; i += T) {
-    if (!cs.valid(i)) continue;
-    const uint32_t kk = cs.c[i].x;
+  uint32_t lo = 0xffffffffu, hi = 0u;
+  for (uint32_t i = threadIdx.x; i < cs.total; i += T) {
+    const uint32_t kk = cs.at(i).x;
     lo = min(lo, kk);
     hi = max(hi, kk);
-    ++nvalid;
   }
   lo = __reduce_min_sync(kFull, lo);
   hi = __reduce_max_sync(kFull, hi);
-  nvalid = __reduce_add_sync(kFull, nvalid);
   if (lane_id() == 0) {
     atomicMin(&m->kmin, lo);
     atomicMax(&m->kmax, hi);
-    atomicAdd(&m->aux[1], nvalid);
   }
   {
     uint4* z = reinterpret_cast<uint4*>(R.hist);
@@ -616,15 +638,14 @@ __device__ __forceinline__ bool bucket_select_sort(Row& R, uint32_t K, uint32_t 
   __syncthreads();
   lo = m->kmin;
   hi = m->kmax;
-  const uint32_t N = m->aux[1];
+  const uint32_t N = cs.total;
   if (hi == lo && N > (uint32_t)kMaxBucket) return false;
   const float scale = (float)kBins / ((float)(hi - lo) + 1.0f);
   auto bucket = [lo, scale](uint32_t key) -> uint32_t {
     const uint32_t b = (uint32_t)((float)(key - lo) * scale);
     return b > (uint32_t)(kBins - 1) ? (uint32_t)(kBins - 1) : b;
   };
-  for (uint32_t i = threadIdx.x; i < cs.slots; i += T)
-    if (cs.valid(i)) atomicAdd(&R.hist[bucket(cs.c[i].x)], 1u);
+  for (uint32_t i = threadIdx.x; i < cs.total; i += T) atomicAdd(&R.hist[bucket(cs.at(i).x)], 1u);
   __syncthreads();
   // exclusive suffix starts -> aux; the bucket b* holding the K-th item; the
   // largest bucket
@@ -653,9 +674,8 @@ __device__ __forceinline__ bool bucket_select_sort(Row& R, uint32_t K, uint32_t 
   if (m->res_max > (uint32_t)kMaxBucket) return false;
   const uint32_t bstar = m->res_digit, above = m->res_above, cstar = m->res_cnt;
   // scatter the items of buckets >= b* into stage, grouped by bucket
-  for (uint32_t i = threadIdx.x; i < cs.slots; i += T) {
-    if (!cs.valid(i)) continue;
-    const uint2 e = cs.c[i];
+  for (uint32_t i = threadIdx.x; i < cs.total; i += T) {
+    const uint2 e = cs.at(i);
     const uint32_t b = bucket(e.x);
     if (b >= bstar) {
       const uint32_t pos = atomicAdd(&R.aux[b], 1u);
@@ -962,8 +982,6 @@ __device__ __forceinline__ void output_positions(Row& R, const Params& p, bool e
   if (K == 0) {
     write_padding<T>(R, oi, ov, 0, kout);
   } else {
-    if (threadIdx.x == 0) R.m->aux[1] = 0;
-    __syncthreads();
     const OwnSlice own = own_slice(R);
     if (!bucket_select_sort<T>(R, K, kout, oi, ov, own))
       sorted_fallback<T>(R, exact, Tc, K, kout, oi, ov, idx_limit, own);

@@ -2,7 +2,7 @@
 #pragma once
 
 namespace lt {
-// threads is 256 (batched rows, several CTAs per SM) or 1024 (few rows, one CTA per SM).
+// threads is 256 (batched rows, several CTAs per SM) or 512 (few rows, one CTA per SM).
 const void* topk_kernel_ptr(int threads);
 // nullptr for an unsupported block size.
 const void* blocked_kernel_ptr(int threads, int block);

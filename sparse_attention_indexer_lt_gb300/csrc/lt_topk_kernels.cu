@@ -26,7 +26,7 @@ __global__ void __launch_bounds__(T, (T <= 256 ? 3 : 1)) topk_kernel(Params p) {
 
 const void* topk_kernel_ptr(int threads) {
   if (threads == 256) return reinterpret_cast<const void*>(&topk_kernel<256, 4>);
-  if (threads == 1024) return reinterpret_cast<const void*>(&topk_kernel<1024, 4>);
+  if (threads == 512) return reinterpret_cast<const void*>(&topk_kernel<512, 8>);
   return nullptr;
 }
 

@@ -29,7 +29,7 @@ def test_blocked_workload_exact_path():
     parity_blocked(S[:4].numpy(), None, w.block, w.k_blocks, w.k, what="c5/exact", force_exact=True)
 
 
-@pytest.mark.parametrize("ft", [256, 1024])
+@pytest.mark.parametrize("ft", [256, 512])
 @pytest.mark.parametrize("block", [4, 8, 16, 32])
 @pytest.mark.parametrize("dist", ["normal", "coarse", "special", "equal", "asc"])
 def test_blocked_small(block, dist, ft):
@@ -39,7 +39,7 @@ def test_blocked_small(block, dist, ft):
                        force_threads=ft)
 
 
-@pytest.mark.parametrize("ft", [256, 1024])
+@pytest.mark.parametrize("ft", [256, 512])
 @pytest.mark.parametrize("fc", [1, 2, 4, 8, 16])
 def test_blocked_forced_plans(fc, ft):
     S, L = workloads.random_rows(2, 262144, seed=31, dist="bf16", lengths="ragged", min_len=1)
@@ -49,7 +49,7 @@ def test_blocked_forced_plans(fc, ft):
                    force_threads=ft)
 
 
-@pytest.mark.parametrize("ft", [256, 1024])
+@pytest.mark.parametrize("ft", [256, 512])
 def test_blocked_workload_both_cta_shapes(ft):
     S, L, w = workloads.make("c5_blocked_16")
     parity_blocked(S.numpy(), None, w.block, w.k_blocks, w.k, what=f"c5/{ft}", force_threads=ft)
