@@ -59,7 +59,7 @@ def test_invalid_arguments_rejected_without_launch(lib):
     assert _topk(lib, fake, None, 1, 16, 4, fake, None, fc=3) == 1  # cluster not a power of two
     assert _topk(lib, fake, None, 1, 16, 4096, fake, None) == 2  # k > LT_MAX_K
     assert _topk(lib, fake, None, 1, (1 << 30) + 1, 4, fake, None) == 2  # row too long
-    assert lib.lt_topk_ex(fake, None, 1, 16, 4, fake, None, 0, 512, 0, None, None, None) == 1  # bad thread count
+    assert lib.lt_topk_ex(fake, None, 1, 16, 4, fake, None, 0, 1024, 0, None, None, None) == 1  # bad thread count
     # rows == 0 is a valid no-op
     assert _topk(lib, None, None, 0, 16, 4, None, None) == 0
 
