@@ -67,6 +67,7 @@ struct Plan {
   int threads = kNarrowThreads;
   uint32_t cap = 0;        // candidate slots: cluster * (1 << seg_shift)
   uint32_t seg_shift = 0;  // log2 of the slots each CTA of the cluster may fill
+  uint32_t wstage = 0;     // per-warp candidate staging bytes (threads * 16 * float4 per round)
   uint32_t sel_cap = 0;
   uint32_t smem = 0;
   const void* func = nullptr;
@@ -139,6 +140,12 @@ lt_status make_plan(int32_t rows, int64_t row_stride, int32_t k, bool blocked, i
   if (slot < 0) return LT_ERR_UNSUPPORTED;
   plan->threads = threads;
   plan->func = blocked ? lt::blocked_kernel_ptr(threads, block) : lt::topk_kernel_ptr(threads);
+  {
+    // float4 loads per thread per round, as instantiated in the kernels
+    int u = threads == kNarrowThreads ? 4 : 8;
+    if (blocked && block / 4 > u) u = block / 4;
+    plan->wstage = (uint32_t)threads * 16u * (uint32_t)u;
+  }
   if (!plan->func) return LT_ERR_UNSUPPORTED;
 
   // Candidate capacity: about 4k slots per row (the sampled threshold keeps
@@ -164,7 +171,7 @@ lt_status make_plan(int32_t rows, int64_t row_stride, int32_t k, bool blocked, i
     plan->cap = (uint32_t)c * seg;
     plan->seg_shift = 0;
     while ((1u << plan->seg_shift) < seg) ++plan->seg_shift;
-    const uint32_t smem = lt::make_layout(c > 1, plan->cap, plan->sel_cap).total;
+    const uint32_t smem = lt::make_layout(c > 1, plan->cap, plan->sel_cap, plan->wstage).total;
     if ((int)smem > di->smem_optin) return LT_ERR_UNSUPPORTED;
     st = prepare_kernel(dev, slot, plan->func, smem, c);
     if (st != LT_OK && !(st == LT_ERR_UNSUPPORTED && force_cluster == 0 && c > 8)) return st;
@@ -198,6 +205,7 @@ lt_status launch(const Plan& plan, const lt::Params& prm, int32_t rows, void* st
   lt::Params p = prm;
   p.cap = (int32_t)plan.cap;
   p.seg_shift = (int32_t)plan.seg_shift;
+  p.wstage = (int32_t)plan.wstage;
   p.sel_cap = (int32_t)plan.sel_cap;
   p.clustered = plan.cluster > 1 ? 1 : 0;
   cudaLaunchConfig_t cfg = {};

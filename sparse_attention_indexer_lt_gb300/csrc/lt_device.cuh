@@ -90,6 +90,7 @@ struct Params {
   int32_t cap;          // candidate slots: clusters * (1 << seg_shift)
   int32_t seg_shift;    // log2 of the candidate slots one CTA may fill
   int32_t sel_cap;      // power of two >= max(k, k_blocks)
+  int32_t wstage;       // bytes of the per-warp candidate staging area (threads * 16 * U)
   int32_t force_exact;
   int32_t vec_ok;       // every row start is 16-byte aligned
   int32_t clustered;    // launched with cluster size > 1
@@ -113,13 +114,13 @@ struct Misc {
 };
 
 struct Layout {
-  uint32_t misc, hist, aux, merged0, merged1, cand, stage, total;
+  uint32_t misc, hist, aux, merged0, merged1, cand, stage, wstage, total;
 };
 
 __host__ __device__ inline uint32_t align_up_u32(uint32_t x, uint32_t a) { return (x + a - 1) / a * a; }
 
 // stage holds sel_cap + kMaxBucket composites (bucket scatter, fallback sort).
-__host__ __device__ inline Layout make_layout(bool clustered, uint32_t cap, uint32_t sel_cap) {
+__host__ __device__ inline Layout make_layout(bool clustered, uint32_t cap, uint32_t sel_cap, uint32_t wstage) {
   Layout l;
   uint32_t o = 0;
   l.misc = o;    o = align_up_u32(o + (uint32_t)sizeof(Misc), 16);
@@ -133,6 +134,8 @@ __host__ __device__ inline Layout make_layout(bool clustered, uint32_t cap, uint
   }
   l.cand = o;    o += cap * 8;
   l.stage = o;   o += (sel_cap + kMaxBucket) * 8;
+  o = align_up_u32(o, 16);
+  l.wstage = o;  o += wstage;
   l.total = align_up_u32(o, 128);
   return l;
 }
@@ -204,6 +207,14 @@ __device__ __forceinline__ uint32_t key_of(uint32_t u) {
   return ((u & 0x7fffffffu) > 0x7f800000u) ? 0u : k;
 }
 __device__ __forceinline__ uint32_t key_of(float x) { return key_of(__float_as_uint(x)); }
+
+// The same order map without the -0 and NaN fix-ups, for histogram digits
+// only: -0 lands one 11-bit bin below +0 and a positive NaN in the top bins.
+// Both can only lower the estimated threshold or push the row onto the exact
+// path, never change a result.
+__device__ __forceinline__ uint32_t raw_key(uint32_t u) {
+  return u ^ ((uint32_t)((int32_t)u >> 31) | 0x80000000u);
+}
 
 __device__ __forceinline__ uint64_t composite(uint32_t key, uint32_t idx) {
   return ((uint64_t)key << 32) | (uint64_t)(~idx);

@@ -36,6 +36,7 @@ struct Row {
   uint32_t* merged1;
   uint2* cand;           // nclus segments of (1 << seg_shift) slots
   uint64_t* stage;
+  float4* wst;           // this warp's staging area: [U][32] float4
   const float* rowp;
   int64_t row;
   int64_t L;             // valid positions of the row
@@ -59,7 +60,9 @@ struct OwnSlice {
 };
 __device__ __forceinline__ OwnSlice own_slice(const Row& R) { return OwnSlice{R.begin, R.end, R.nclus == 1}; }
 
-__device__ __forceinline__ float nan_f() { return __int_as_float(0x7fffffff); }
+// Filler of positions past the slice end: a NaN (never passes x >= g) whose
+// raw key is 0 (lands in the lowest histogram bin).
+__device__ __forceinline__ float nan_f() { return __int_as_float((int)0xffffffffu); }
 
 template <int T, int U, int W>
 __device__ __forceinline__ int64_t slot_pos(const Row& R, int r, int s) {
@@ -144,7 +147,7 @@ __device__ __forceinline__ void setup_row(Row& R, const Params& p, unsigned char
   R.nclus = p.clustered ? cluster_size() : 1u;
   R.rank = p.clustered ? cluster_rank() : 0u;
   R.row = (int64_t)(blockIdx.x / R.nclus);
-  const Layout lay = make_layout(p.clustered != 0, (uint32_t)p.cap, (uint32_t)p.sel_cap);
+  const Layout lay = make_layout(p.clustered != 0, (uint32_t)p.cap, (uint32_t)p.sel_cap, (uint32_t)p.wstage);
   R.m = reinterpret_cast<Misc*>(smem + lay.misc);
   R.hist = reinterpret_cast<uint32_t*>(smem + lay.hist);
   R.aux = reinterpret_cast<uint32_t*>(smem + lay.aux);
@@ -152,6 +155,7 @@ __device__ __forceinline__ void setup_row(Row& R, const Params& p, unsigned char
   R.merged1 = reinterpret_cast<uint32_t*>(smem + lay.merged1);
   R.cand = reinterpret_cast<uint2*>(smem + lay.cand);
   R.stage = reinterpret_cast<uint64_t*>(smem + lay.stage);
+  R.wst = reinterpret_cast<float4*>(smem + lay.wstage) + (threadIdx.x >> 5) * 32 * U;
   R.stage_cap = (uint32_t)p.sel_cap + kMaxBucket;
   R.seg_shift = (uint32_t)p.seg_shift;
   int64_t L = p.row_stride;
@@ -233,6 +237,7 @@ struct Cands {
   uint32_t total;
   uint32_t start[kMaxCluster];  // entries before segment q
   __device__ __forceinline__ uint2 at(uint32_t i) const {
+    if (nseg == 1) return c[i];
     uint32_t q = 0;
 #pragma unroll
     for (int j = 1; j < kMaxCluster; ++j)
@@ -333,40 +338,23 @@ __device__ __forceinline__ void exchange_segments(Row& R) {
 
 // ------------------------------------------------------------------ position items
 
-// Rounds live in two register buffers; `b` picks one, element by element at
-// the point of use (keeps one copy of the code without a third buffer).
-template <int U, int S>
-struct Bufs {
-  const float4 (&a)[U];
-  const int (&na)[S];
-  const float4 (&b)[U];
-  const int (&nb)[S];
-  bool use_b;
-  __device__ __forceinline__ float4 v(int i) const { return use_b ? b[i] : a[i]; }
-  __device__ __forceinline__ int n(int s) const { return use_b ? nb[s] : na[s]; }
-};
-
-template <int T, int U, int W, class Keep>
-__device__ __forceinline__ bool keep_slot(const Row& R, int r, const Bufs<U, Geo<T, U, W>::kSlots>& B, int s,
-                                          Keep keep) {
-  return B.use_b ? keep(R, r, B.b, s, B.nb[s]) : keep(R, r, B.a, s, B.na[s]);
-}
-
-template <int T, int U, int W, class Keep>
-__device__ __forceinline__ void hist_round(Row& R, int r, const Bufs<U, Geo<T, U, W>::kSlots>& B, int level,
-                                           uint32_t d1, Keep keep) {
+// Sample histogram of one round. level 1: top 11 bits of the raw key;
+// level 2: the next 11 bits of the items whose top 11 bits equal d1.
+template <int T, int U, int W, int kLevel, class Keep>
+__device__ __forceinline__ void hist_round(Row& R, int r, const float4 (&v)[U],
+                                           const int (&n)[Geo<T, U, W>::kSlots], uint32_t d1, Keep keep) {
   using G = Geo<T, U, W>;
 #pragma unroll
   for (int s = 0; s < G::kSlots; ++s) {
-    const int ns = B.n(s);
-    if (ns == 0 || !keep_slot<T, U, W>(R, r, B, s, keep)) continue;
+    const int ns = n[s];
+    if (ns == 0 || !keep(R, r, v, s, ns)) continue;
 #pragma unroll
     for (int j = 0; j < G::kVS; ++j)
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        if (4 * j + e < ns) {
-          const uint32_t kk = key_of(lane4(B.v(s * G::kVS + j), e));
-          if (level == 1) atomicAdd(&R.hist[kk >> 21], 1u);
+        if (ns == W || 4 * j + e < ns) {
+          const uint32_t kk = raw_key(__float_as_uint(lane4(v[s * G::kVS + j], e)));
+          if (kLevel == 1) atomicAdd(&R.hist[kk >> 21], 1u);
           else if ((kk >> 21) == d1) atomicAdd(&R.hist[(kk >> 10) & (kBins - 1)], 1u);
         }
       }
@@ -374,75 +362,102 @@ __device__ __forceinline__ void hist_round(Row& R, int r, const Bufs<U, Geo<T, U
 }
 
 // Append every kept position whose score passes the threshold (x >= g, or
-// every position when `all`) to the list: a bit mask per thread, one warp
-// scan and one shared atomic per warp, then each lane writes its own items.
+// every valid position when `all`) to the list. Each lane builds a bit mask
+// of its passing positions; one warp scan and one shared atomic reserve the
+// warp's slots; lanes with candidates stage their round in shared memory and
+// every lane then writes one candidate (the owner lane of candidate k is
+// found by a binary search over the warp's running counts).
 template <int T, int U, int W, class Keep>
-__device__ __forceinline__ void filter_round(Row& R, int r, const Bufs<U, Geo<T, U, W>::kSlots>& B, float g,
-                                             bool all, uint32_t* counter, uint2* list, uint32_t cap, Keep keep) {
+__device__ __forceinline__ void filter_round(Row& R, int r, const float4 (&v)[U],
+                                             const int (&n)[Geo<T, U, W>::kSlots], float g, bool all,
+                                             uint32_t* counter, uint2* list, uint32_t cap, Keep keep) {
   using G = Geo<T, U, W>;
   static_assert(4 * U <= 32, "mask holds 32 positions");
   uint32_t mask = 0;
 #pragma unroll
   for (int s = 0; s < G::kSlots; ++s) {
-    const int ns = B.n(s);
-    const bool kept = ns > 0 && keep_slot<T, U, W>(R, r, B, s, keep);
+    const int ns = n[s];
+    uint32_t sm = 0;
+    if (!all) {
+      // positions past the slice end hold NaN, which fails x >= g
 #pragma unroll
-    for (int j = 0; j < G::kVS; ++j) {
-      const float4 q = B.v(s * G::kVS + j);
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const bool pe = kept && (4 * j + e < ns) && (all || lane4(q, e) >= g);
-        mask |= pe ? (1u << (4 * (s * G::kVS + j) + e)) : 0u;
+      for (int j = 0; j < G::kVS; ++j) {
+        const float4 q = v[s * G::kVS + j];
+        const uint32_t b = 4 * j;
+        sm |= (q.x >= g ? 1u : 0u) << b;
+        sm |= (q.y >= g ? 1u : 0u) << (b + 1);
+        sm |= (q.z >= g ? 1u : 0u) << (b + 2);
+        sm |= (q.w >= g ? 1u : 0u) << (b + 3);
       }
+    } else {
+      sm = ns >= 32 ? 0xffffffffu : ((1u << ns) - 1u);
     }
+    if (sm != 0 && !keep(R, r, v, s, ns)) sm = 0;
+    mask |= sm << (4 * G::kVS * s);
   }
+  const uint32_t lane = lane_id();
   const uint32_t c = (uint32_t)__popc(mask);
   const uint32_t incl = warp_incl_scan(c);
   const uint32_t total = __shfl_sync(kFull, incl, 31);
   if (total == 0) return;
   uint32_t base = 0;
-  if (lane_id() == 31) base = atomicAdd(counter, total);
+  if (lane == 31) base = atomicAdd(counter, total);
   base = __shfl_sync(kFull, base, 31);
-  uint32_t pos = base + incl - c;
+  if (mask) {
 #pragma unroll
-  for (int f = 0; f < U; ++f) {
-    uint32_t nib = (mask >> (4 * f)) & 15u;
-    if (nib) {
-      const int64_t p0 = slot_pos<T, U, W>(R, r, f / G::kVS) + 4 * (f % G::kVS);
-      const float4 q = B.v(f);
-      do {
-        const int e = __ffs(nib) - 1;
-        nib &= nib - 1;
-        if (pos < cap) list[pos] = make_uint2(key_of(lane4(q, e)), (uint32_t)(p0 + e));
-        ++pos;
-      } while (nib);
+    for (int f = 0; f < U; ++f) R.wst[f * 32 + lane] = v[f];
+  }
+  __syncwarp();
+  const uint32_t excl = incl - c;
+  const float* stf = reinterpret_cast<const float*>(R.wst);
+  const uint32_t wbase = threadIdx.x & ~31u;
+  for (uint32_t k0 = 0; k0 < total; k0 += 32) {
+    const uint32_t k = k0 + lane;
+    const uint32_t kq = k < total ? k : total - 1;
+    uint32_t owner = 0;  // number of lanes whose running count is <= kq
+#pragma unroll
+    for (uint32_t step = 16; step; step >>= 1) {
+      const uint32_t x = __shfl_sync(kFull, incl, owner + step - 1);
+      if (x <= kq) owner += step;
+    }
+    const uint32_t oex = __shfl_sync(kFull, excl, owner);
+    uint32_t om = __shfl_sync(kFull, mask, owner);
+    if (k < total) {
+      for (uint32_t t = kq - oex; t > 0; --t) om &= om - 1;
+      const uint32_t bit = (uint32_t)(__ffs(om) - 1);
+      const uint32_t f = bit >> 2, e = bit & 3u;
+      const float x = stf[(f * 32 + owner) * 4 + e];
+      const int s = (int)(f / G::kVS), j = (int)(f % G::kVS);
+      const int64_t pos = R.begin + (int64_t)(wbase + owner) * W + (int64_t)(r + R.rounds * s) * G::kTile +
+                          4 * j + e;
+      if (base + k < cap) list[base + k] = make_uint2(key_of(x), (uint32_t)pos);
     }
   }
+  __syncwarp();
 }
 
 // ------------------------------------------------------------------ block items (stage A)
 
-template <int T, int U, int W>
-__device__ __forceinline__ void hist_round_blocks(Row& R, const Bufs<U, Geo<T, U, W>::kSlots>& B, int level,
-                                                  uint32_t d1) {
+template <int T, int U, int W, int kLevel>
+__device__ __forceinline__ void hist_round_blocks(Row& R, const float4 (&v)[U],
+                                                  const int (&n)[Geo<T, U, W>::kSlots], uint32_t d1) {
 #pragma unroll
   for (int s = 0; s < Geo<T, U, W>::kSlots; ++s) {
-    const int ns = B.n(s);
-    if (ns == 0) continue;
-    const uint32_t kk = B.use_b ? slot_block_key<T, U, W>(B.b, s, ns) : slot_block_key<T, U, W>(B.a, s, ns);
-    if (level == 1) atomicAdd(&R.hist[kk >> 21], 1u);
+    if (n[s] == 0) continue;
+    const uint32_t kk = slot_block_key<T, U, W>(v, s, n[s]);
+    if (kLevel == 1) atomicAdd(&R.hist[kk >> 21], 1u);
     else if ((kk >> 21) == d1) atomicAdd(&R.hist[(kk >> 10) & (kBins - 1)], 1u);
   }
 }
 
 template <int T, int U, int W>
-__device__ __forceinline__ void filter_round_blocks(Row& R, int r, const Bufs<U, Geo<T, U, W>::kSlots>& B,
-                                                    uint32_t t, uint32_t* counter, uint2* list, uint32_t cap) {
+__device__ __forceinline__ void filter_round_blocks(Row& R, int r, const float4 (&v)[U],
+                                                    const int (&n)[Geo<T, U, W>::kSlots], uint32_t t,
+                                                    uint32_t* counter, uint2* list, uint32_t cap) {
 #pragma unroll
   for (int s = 0; s < Geo<T, U, W>::kSlots; ++s) {
-    const int ns = B.n(s);
-    const uint32_t kk =
-        ns > 0 ? (B.use_b ? slot_block_key<T, U, W>(B.b, s, ns) : slot_block_key<T, U, W>(B.a, s, ns)) : 0u;
+    const int ns = n[s];
+    const uint32_t kk = ns > 0 ? slot_block_key<T, U, W>(v, s, ns) : 0u;
     const bool pe = ns > 0 && kk >= t;
     const uint32_t bid = (uint32_t)(slot_pos<T, U, W>(R, r, s) / W);
     warp_append(pe, kk, bid, counter, list, cap);
@@ -892,13 +907,24 @@ __device__ __forceinline__ bool select_stage(Row& R, const Params& p, float4 (&c
 #pragma unroll 1
       for (int level = 1; level <= 2; ++level) {
         zero_bins<T>(R.hist);
-#pragma unroll 1
-        for (int q = 0; q < nsr; ++q) {
-          const Bufs<U, G::kSlots> B{cur, nc, nxt, nn, q != 0};
-          if (kBlocks) hist_round_blocks<T, U, W>(R, B, level, d1);
-          else hist_round<T, U, W>(R, q, B, level, d1, keep);
+        if (level == 1) {
+          if (kBlocks) {
+            if (nsr > 0) hist_round_blocks<T, U, W, 1>(R, cur, nc, 0);
+            if (nsr > 1) hist_round_blocks<T, U, W, 1>(R, nxt, nn, 0);
+          } else {
+            if (nsr > 0) hist_round<T, U, W, 1>(R, 0, cur, nc, 0, keep);
+            if (nsr > 1) hist_round<T, U, W, 1>(R, 1, nxt, nn, 0, keep);
+          }
+          stamp(p, tr + kTrHist);
+        } else {
+          if (kBlocks) {
+            if (nsr > 0) hist_round_blocks<T, U, W, 2>(R, cur, nc, d1);
+            if (nsr > 1) hist_round_blocks<T, U, W, 2>(R, nxt, nn, d1);
+          } else {
+            if (nsr > 0) hist_round<T, U, W, 2>(R, 0, cur, nc, d1, keep);
+            if (nsr > 1) hist_round<T, U, W, 2>(R, 1, nxt, nn, d1, keep);
+          }
         }
-        if (level == 1) stamp(p, tr + kTrHist);
         const uint32_t* bins = merge_hist<T>(R, level - 1);
         if (level == 1) stamp(p, tr + kTrMerge);
         if (level == 1) {
@@ -928,12 +954,20 @@ __device__ __forceinline__ bool select_stage(Row& R, const Params& p, float4 (&c
     // ---- filter every round against the threshold
     const bool all = (t == 0u);
     const float g = threshold_float(all ? 1u : t);
+    if (resident) {
+      if (R.rounds > 0) {
+        if (kBlocks) filter_round_blocks<T, U, W>(R, 0, cur, nc, t, counter, list, seg);
+        else filter_round<T, U, W>(R, 0, cur, nc, g, all, counter, list, seg, keep);
+      }
+      if (R.rounds > 1) {
+        if (kBlocks) filter_round_blocks<T, U, W>(R, 1, nxt, nn, t, counter, list, seg);
+        else filter_round<T, U, W>(R, 1, nxt, nn, g, all, counter, list, seg, keep);
+      }
+    } else {
 #pragma unroll 1
-    for (int r = 0; r < R.rounds; ++r) {
-      const Bufs<U, G::kSlots> B{cur, nc, nxt, nn, resident && r == 1};
-      if (kBlocks) filter_round_blocks<T, U, W>(R, r, B, t, counter, list, seg);
-      else filter_round<T, U, W>(R, r, B, g, all, counter, list, seg, keep);
-      if (!resident) {
+      for (int r = 0; r < R.rounds; ++r) {
+        if (kBlocks) filter_round_blocks<T, U, W>(R, r, cur, nc, t, counter, list, seg);
+        else filter_round<T, U, W>(R, r, cur, nc, g, all, counter, list, seg, keep);
 #pragma unroll
         for (int i = 0; i < U; ++i) cur[i] = nxt[i];
 #pragma unroll
