@@ -227,48 +227,36 @@ __device__ __forceinline__ void dsmem_st_u32(uint32_t addr, uint32_t v) {
 
 // ------------------------------------------------------------------ candidates
 
-// Candidate array view: nseg segments of (1 << shift) slots, segment q
-// holding cnt[q] entries. Entries are numbered 0 .. total-1 across the
-// segments; at(i) maps a number to its slot through the running counts.
-struct Cands {
-  const uint2* c;
-  uint32_t shift;
-  uint32_t nseg;
-  uint32_t total;
-  uint32_t start[kMaxCluster];  // entries before segment q
-  __device__ __forceinline__ uint2 at(uint32_t i) const {
-    if (nseg == 1) return c[i];
-    uint32_t q = 0;
-#pragma unroll
-    for (int j = 1; j < kMaxCluster; ++j)
-      if ((uint32_t)j < nseg && start[j] <= i) q = j;
-    return c[(q << shift) + (i - start[q])];
-  }
-};
-__device__ __forceinline__ Cands cands(const Row& R) {
+// Visit every candidate: the array holds nseg segments of (1 << shift) slots,
+// segment q holding seg_cnt[q] entries. Warps are spread over the segments
+// (several warps per segment when there are fewer segments than warps).
+template <int T, class F>
+__device__ __forceinline__ void for_each_cand(const Row& R, F f) {
+  constexpr uint32_t NW = T / 32;
   const Misc* m = R.m;
-  Cands cs;
-  cs.c = R.cand;
-  cs.shift = m->shift;
-  cs.nseg = m->nseg;
-  const uint32_t seg = 1u << cs.shift;
-  uint32_t acc = 0;
-#pragma unroll
-  for (int q = 0; q < kMaxCluster; ++q) {
-    cs.start[q] = acc;
-    if ((uint32_t)q < cs.nseg) {
-      const uint32_t n = m->seg_cnt[q];
-      acc += n < seg ? n : seg;
+  const uint32_t nseg = m->nseg, shift = m->shift;
+  const uint32_t seg = 1u << shift;
+  const uint32_t warp = threadIdx.x >> 5, lane = lane_id();
+  if (nseg >= NW) {
+    for (uint32_t q = warp; q < nseg; q += NW) {
+      const uint32_t n = min(m->seg_cnt[q], seg);
+      const uint2* c = R.cand + (q << shift);
+      for (uint32_t j = lane; j < n; j += 32) f(c[j]);
     }
+  } else {
+    const uint32_t per = NW / nseg;  // warps per segment (powers of two)
+    const uint32_t q = warp / per, sub = warp - q * per;
+    const uint32_t n = min(m->seg_cnt[q], seg);
+    const uint2* c = R.cand + (q << shift);
+    for (uint32_t j = sub * 32 + lane; j < n; j += per * 32) f(c[j]);
   }
-  cs.total = acc;
-  return cs;
 }
 
 __device__ __forceinline__ void reset_candidate_range(Misc* m) {
   m->kmin = 0xffffffffu;
   m->kmax = 0u;
   m->res_max = 0u;
+  m->aux[1] = 0u;
 }
 
 // ------------------------------------------------------------------ cluster exchange
@@ -276,15 +264,24 @@ __device__ __forceinline__ void reset_candidate_range(Misc* m) {
 // Push the non-empty bins of the local histogram into merged buffer `buf` of
 // every CTA of the cluster (this one included), then cluster-sync. With one
 // CTA the local histogram is the merged one.
+// With lo_rank > 0 only the bins at or above this CTA's own lo_rank-th key
+// are pushed: the cluster-wide lo_rank-th key is at least that large, so every
+// bin at or above its digit still arrives complete (used with a full sample).
 template <int T>
-__device__ __forceinline__ const uint32_t* merge_hist(Row& R, int buf) {
+__device__ __forceinline__ const uint32_t* merge_hist(Row& R, int buf, uint32_t lo_rank = 0) {
   __syncthreads();
   if (R.nclus == 1) return R.hist;
+  uint32_t dlo = 0;
+  if (lo_rank > 0) {
+    if (threadIdx.x == 0) R.m->res_digit = 0;  // stays 0 when this CTA holds fewer than lo_rank keys
+    find_digit<T>(R.hist, lo_rank, R.m);
+    dlo = R.m->res_digit;
+  }
   wait_init(R);
   uint32_t* dst = buf ? R.merged1 : R.merged0;
   const uint32_t base = smem_addr(dst);
   for (int b = threadIdx.x; b < kBins; b += T) {
-    const uint32_t v = R.hist[b];
+    const uint32_t v = (uint32_t)b >= dlo ? R.hist[b] : 0u;
     if (v) {
       for (uint32_t q = 0; q < R.nclus; ++q) dsmem_red_add(peer_addr(base + 4u * b, q), v);
     }
@@ -494,7 +491,6 @@ __device__ __forceinline__ uint32_t bins_total(const uint32_t* bins, Misc* m) {
 template <int T>
 __device__ __forceinline__ uint64_t select_local(Row& R, uint32_t K, int64_t idx_limit) {
   Misc* m = R.m;
-  const Cands cs = cands(R);
   uint64_t tval = 0, tmask = 0;
   uint32_t need = K;
   for (int di = 0; di < 6; ++di) {
@@ -506,11 +502,10 @@ __device__ __forceinline__ uint64_t select_local(Row& R, uint32_t K, int64_t idx
       continue;
     }
     zero_bins<T>(R.hist);
-    for (uint32_t i = threadIdx.x; i < cs.total; i += T) {
-      const uint2 e = cs.at(i);
+    for_each_cand<T>(R, [&](uint2 e) {
       const uint64_t c = composite(e.x, e.y);
       if ((c & tmask) == tval) atomicAdd(&R.hist[(uint32_t)(c >> s) & ((1u << w) - 1u)], 1u);
-    }
+    });
     __syncthreads();
     find_digit<T>(R.hist, need, m);
     const uint32_t d = m->res_digit, above = m->res_above, cnt = m->res_cnt;
@@ -523,33 +518,19 @@ __device__ __forceinline__ uint64_t select_local(Row& R, uint32_t K, int64_t idx
   return tval;
 }
 
-// Compact every valid candidate with composite >= Tc into stage[] (as composites).
+// Compact every candidate with composite >= Tc into stage[] (as composites).
 template <int T>
 __device__ __forceinline__ uint32_t compact_selected(Row& R, uint64_t Tc) {
   Misc* m = R.m;
-  const Cands cs = cands(R);
   if (threadIdx.x == 0) m->aux[0] = 0;
   __syncthreads();
-  for (uint32_t base = 0; base < cs.total; base += T) {
-    const uint32_t i = base + threadIdx.x;
-    uint64_t c = 0;
-    bool pr = false;
-    if (i < cs.total) {
-      const uint2 e = cs.at(i);
-      c = composite(e.x, e.y);
-      pr = c >= Tc;
+  for_each_cand<T>(R, [&](uint2 e) {
+    const uint64_t c = composite(e.x, e.y);
+    if (c >= Tc) {
+      const uint32_t pos = atomicAdd(&m->aux[0], 1u);
+      if (pos < R.stage_cap) R.stage[pos] = c;
     }
-    const unsigned msk = __ballot_sync(kFull, pr);
-    if (msk) {
-      const uint32_t lane = lane_id();
-      const int leader = __ffs(msk) - 1;
-      uint32_t b = 0;
-      if ((int)lane == leader) b = atomicAdd(&m->aux[0], (uint32_t)__popc(msk));
-      b = __shfl_sync(kFull, b, leader);
-      const uint32_t pos = b + (uint32_t)__popc(msk & ((1u << lane) - 1u));
-      if (pr && pos < R.stage_cap) R.stage[pos] = c;
-    }
-  }
+  });
   __syncthreads();
   const uint32_t cnt = m->aux[0];
   __syncthreads();
@@ -632,19 +613,20 @@ __device__ __forceinline__ bool bucket_select_sort(Row& R, uint32_t K, uint32_t 
                                                    OwnSlice owner) {
   constexpr int BPT = kBins / T;
   Misc* m = R.m;
-  const Cands cs = cands(R);
   // key range and count of the candidates (and a zeroed histogram)
-  uint32_t lo = 0xffffffffu, hi = 0u;
-  for (uint32_t i = threadIdx.x; i < cs.total; i += T) {
-    const uint32_t kk = cs.at(i).x;
-    lo = min(lo, kk);
-    hi = max(hi, kk);
-  }
+  uint32_t lo = 0xffffffffu, hi = 0u, nloc = 0;
+  for_each_cand<T>(R, [&](uint2 e) {
+    lo = min(lo, e.x);
+    hi = max(hi, e.x);
+    ++nloc;
+  });
+  nloc = __reduce_add_sync(kFull, nloc);
   lo = __reduce_min_sync(kFull, lo);
   hi = __reduce_max_sync(kFull, hi);
   if (lane_id() == 0) {
     atomicMin(&m->kmin, lo);
     atomicMax(&m->kmax, hi);
+    atomicAdd(&m->aux[1], nloc);
   }
   {
     uint4* z = reinterpret_cast<uint4*>(R.hist);
@@ -653,14 +635,14 @@ __device__ __forceinline__ bool bucket_select_sort(Row& R, uint32_t K, uint32_t 
   __syncthreads();
   lo = m->kmin;
   hi = m->kmax;
-  const uint32_t N = cs.total;
+  const uint32_t N = m->aux[1];
   if (hi == lo && N > (uint32_t)kMaxBucket) return false;
   const float scale = (float)kBins / ((float)(hi - lo) + 1.0f);
   auto bucket = [lo, scale](uint32_t key) -> uint32_t {
     const uint32_t b = (uint32_t)((float)(key - lo) * scale);
     return b > (uint32_t)(kBins - 1) ? (uint32_t)(kBins - 1) : b;
   };
-  for (uint32_t i = threadIdx.x; i < cs.total; i += T) atomicAdd(&R.hist[bucket(cs.at(i).x)], 1u);
+  for_each_cand<T>(R, [&](uint2 e) { atomicAdd(&R.hist[bucket(e.x)], 1u); });
   __syncthreads();
   // exclusive suffix starts -> aux; the bucket b* holding the K-th item; the
   // largest bucket
@@ -689,14 +671,13 @@ __device__ __forceinline__ bool bucket_select_sort(Row& R, uint32_t K, uint32_t 
   if (m->res_max > (uint32_t)kMaxBucket) return false;
   const uint32_t bstar = m->res_digit, above = m->res_above, cstar = m->res_cnt;
   // scatter the items of buckets >= b* into stage, grouped by bucket
-  for (uint32_t i = threadIdx.x; i < cs.total; i += T) {
-    const uint2 e = cs.at(i);
+  for_each_cand<T>(R, [&](uint2 e) {
     const uint32_t b = bucket(e.x);
     if (b >= bstar) {
       const uint32_t pos = atomicAdd(&R.aux[b], 1u);
       if (pos < R.stage_cap) R.stage[pos] = composite(e.x, e.y);
     }
-  }
+  });
   __syncthreads();
   const uint32_t M = above + cstar;
   for (uint32_t i = threadIdx.x; i < M; i += T) {
@@ -925,7 +906,8 @@ __device__ __forceinline__ bool select_stage(Row& R, const Params& p, float4 (&c
             if (nsr > 1) hist_round<T, U, W, 2>(R, 1, nxt, nn, d1, keep);
           }
         }
-        const uint32_t* bins = merge_hist<T>(R, level - 1);
+        const uint32_t lo_rank = (level == 1 && full && R.nclus >= 8) ? (K < (uint32_t)items ? K : (uint32_t)items) : 0u;
+        const uint32_t* bins = merge_hist<T>(R, level - 1, lo_rank);
         if (level == 1) stamp(p, tr + kTrMerge);
         if (level == 1) {
           const uint32_t ns = full ? (uint32_t)items : bins_total<T>(bins, m);
