@@ -152,27 +152,42 @@ class Clocks:
 
 # ------------------------------------------------------------------ timing helpers
 
-def timed_launches(launch, steps: int, warmup: int, world: int):
-    """Run warmup untimed steps, then exactly `steps` steps with an event pair
-    around each launch. A sleep kernel queued first keeps the GPU busy while
-    the host enqueues the steps, so the events see GPU time only.
-    Returns (total_ms from first start to last end, [per-launch ms])."""
+def timed_steps(launch, steps: int, warmup: int, world: int) -> float:
+    """The timed region: `warmup` untimed steps, then exactly `steps` steps
+    launched back to back between two CUDA events on the launching stream,
+    bracketed by a barrier and a device synchronize on both sides. A sleep
+    kernel queued first keeps the GPU busy while the host enqueues the steps,
+    so the events see GPU time only. Returns milliseconds for all steps."""
     for i in range(warmup):
         launch(i)
     torch.cuda.synchronize()
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier(world)
     torch.cuda.synchronize()
     torch.cuda._sleep(int(2e6 + steps * 1e5))  # covers the host-side enqueue of all steps
+    a.record()
+    for i in range(steps):
+        launch(warmup + i)
+    b.record()
+    torch.cuda.synchronize()
+    barrier(world)
+    return a.elapsed_time(b)
+
+
+def launch_durations(launch, steps: int, world: int, offset: int = 0):
+    """Diagnostic pass: an event pair around every launch (each launch then
+    also pays its own launch latency). Returns per-launch milliseconds."""
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    barrier(world)
+    torch.cuda.synchronize()
+    torch.cuda._sleep(int(2e6 + steps * 1e5))
     for i in range(steps):
         ev[i][0].record()
-        launch(warmup + i)
+        launch(offset + i)
         ev[i][1].record()
     torch.cuda.synchronize()
     barrier(world)
-    per = [a.elapsed_time(b) for a, b in ev]
-    total = ev[0][0].elapsed_time(ev[-1][1])
-    return total, per
+    return [x.elapsed_time(y) for x, y in ev]
 
 
 def l2_bytes():
@@ -234,16 +249,17 @@ def bench_ours(args, world, rank):
         lt.topk(copies[i % ncopies], None, w.k, out_idx=oi, out_val=ov)
 
     with Clocks(dev.index) as clk:
-        total_ms, per = timed_launches(step, args.steps, args.warmup, world)
+        total_ms = timed_steps(step, args.steps, args.warmup, world)
+        per = launch_durations(step, args.steps, world, offset=args.warmup + args.steps)
         # warm-L2 latency (the indexer that produced the row has just written it)
-        warm_total, warm_per = timed_launches(lambda i: lt.topk(base, None, w.k, out_idx=oi, out_val=ov),
-                                              args.steps, args.warmup, world)
+        warm_ms = timed_steps(lambda i: lt.topk(base, None, w.k, out_idx=oi, out_val=ov),
+                              args.steps, args.warmup, world)
         batched = [] if args.no_batched else bench_batched(lt, dev, args, world, peak, L2)
         ttk = bench_torch_topk(base, w.k, args, world)
     clocks = clk.summary()
     total_ms = max_over_ranks(total_ms, world)
     us_per_row = total_ms * 1000.0 / (args.steps * w.rows * world)
-    kern_ms = statistics.mean(per)
+    kern_ms = total_ms / args.steps  # average launch duration over the timed region
     achieved = (4 * w.row_stride * w.rows) / (kern_ms * 1e-3) / 1e9
     traffic = profile_traffic("topk_kernel", HEADLINE)
     plan = lt.plan(w.rows, w.row_stride, w.k)
@@ -267,8 +283,9 @@ def bench_ours(args, world, rank):
         "config": {"workload": HEADLINE, "rows": w.rows, "n": w.row_stride, "k": w.k,
                    "l2": f"rotating {ncopies} input copies ({ncopies * row_bytes >> 20} MiB > 2x L2)",
                    "plan": plan, "parallelism": "replicas" if world > 1 else "single GPU",
-                   "warm_l2_us_per_row": round(statistics.median(warm_per) * 1000.0, 3),
-                   "kernel_us_median": round(statistics.median(per) * 1000.0, 3)},
+                   "timing": "events around the back-to-back launches of the timed steps",
+                   "warm_l2_us_per_row": round(warm_ms * 1000.0 / args.steps, 3),
+                   "isolated_launch_us_median": round(statistics.median(per) * 1000.0, 3)},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 5), "traffic": traffic,
                      "peak_kind": f"{peak_kind} copy bandwidth (burst)",
@@ -305,10 +322,10 @@ def bench_batched(lt, dev, args, world, peak, L2):
         else:
             def step(i, c=copies, n=ncopies):
                 lt.topk(c[i % n], ld, w.k, out_idx=oi, out_val=ov)
-        total_ms, per = timed_launches(step, steps, max(3, args.warmup), world)
+        total_ms = timed_steps(step, steps, max(3, args.warmup), world)
         total_ms = max_over_ranks(total_ms, world)
         step_ms = total_ms / steps
-        kern_ms = statistics.mean(per)
+        kern_ms = step_ms
         gbs = nbytes / (kern_ms * 1e-3) / 1e9
         out.append({
             "workload": name, "rows": w.rows, "read_bytes": nbytes,
@@ -348,10 +365,10 @@ def bench_only(args, world):
         else:
             lt.topk(c, ld, w.k, out_idx=oi, out_val=ov)
 
-    total_ms, per = timed_launches(step, args.steps, args.warmup, world)
-    kern = statistics.mean(per)
-    return {"workload": args.only, "steps": args.steps, "kernel_us_mean": round(kern * 1000, 3),
-            "step_us": round(total_ms * 1000 / args.steps, 3), "read_bytes": nbytes,
+    total_ms = timed_steps(step, args.steps, args.warmup, world)
+    kern = total_ms / args.steps
+    return {"workload": args.only, "steps": args.steps, "step_us": round(kern * 1000, 3),
+            "read_bytes": nbytes,
             "hbm_gbs": round(nbytes / (kern * 1e-3) / 1e9, 1), "copies": ncopies,
             "plan": lt.plan(w.rows, w.row_stride, w.k, blocked=w.blocked, k_blocks=w.k_blocks)}
 
@@ -403,8 +420,8 @@ def bench_trace(args):
 
 def bench_torch_topk(x, k, args, world):
     steps = max(3, min(args.steps, 50))
-    _, per = timed_launches(lambda i: torch.topk(x, k, dim=1, sorted=True), steps, 3, world)
-    return round(statistics.median(per) * 1000.0, 3)
+    ms = timed_steps(lambda i: torch.topk(x, k, dim=1, sorted=True), steps, 3, world)
+    return round(ms * 1000.0 / steps, 3)
 
 
 def bench_e2e(lt, S, w, dev, args, world):

@@ -7,8 +7,10 @@
 //           to 16, the largest cluster a GPC can host) while the whole grid
 //           still fits on the SMs and each CTA still gets at least one round
 //           (16384 positions) of the row.
-// A 16-CTA cluster is non-portable: the plan asks the occupancy calculator
-// whether one can be scheduled with the chosen shared memory, halving C if not.
+// A 16-CTA cluster is non-portable. The plan asks the occupancy calculator how
+// many clusters of the chosen shape can be resident at once and halves C until
+// all rows fit in one wave (a cluster must sit inside one GPC, so eight
+// 8-CTA clusters of one-CTA-per-SM kernels may not fit where 128 SMs would).
 
 #include <cuda_runtime.h>
 
@@ -106,7 +108,15 @@ lt_status prepare_kernel(int dev, int slot, const void* func, uint32_t smem, int
   return LT_OK;
 }
 
-bool cluster_fits(const void* func, int cluster, int threads, uint32_t smem) {
+// Clusters of this shape that can be resident at once (0 when none fits).
+// Queried once per device, kernel, cluster size and shared-memory size.
+struct ActiveEntry {
+  uint32_t smem = 0;
+  int n = -1;
+};
+ActiveEntry g_active[kMaxDevices][kSlots][5];
+
+int active_clusters_query(const void* func, int cluster, int threads, uint32_t smem) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)cluster);
   cfg.blockDim = dim3((unsigned)threads);
@@ -121,9 +131,24 @@ bool cluster_fits(const void* func, int cluster, int threads, uint32_t smem) {
   int n = 0;
   if (cudaOccupancyMaxActiveClusters(&n, func, &cfg) != cudaSuccess) {
     (void)cudaGetLastError();  // clear the error this query may leave behind
-    return false;
+    return 0;
   }
-  return n > 0;
+  return n;
+}
+
+int active_clusters(int dev, int slot, const void* func, int cluster, int threads, uint32_t smem) {
+  int lc = 0;
+  while ((1 << lc) < cluster) ++lc;
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    const ActiveEntry& e = g_active[dev][slot][lc];
+    if (e.n >= 0 && e.smem == smem) return e.n;
+  }
+  const int n = active_clusters_query(func, cluster, threads, smem);
+  std::lock_guard<std::mutex> lk(g_mu);
+  g_active[dev][slot][lc].smem = smem;
+  g_active[dev][slot][lc].n = n;
+  return n;
 }
 
 lt_status make_plan(int32_t rows, int64_t row_stride, int32_t k, bool blocked, int32_t block,
@@ -175,7 +200,10 @@ lt_status make_plan(int32_t rows, int64_t row_stride, int32_t k, bool blocked, i
     if ((int)smem > di->smem_optin) return LT_ERR_UNSUPPORTED;
     st = prepare_kernel(dev, slot, plan->func, smem, c);
     if (st != LT_OK && !(st == LT_ERR_UNSUPPORTED && force_cluster == 0 && c > 8)) return st;
-    if (st == LT_OK && (c == 1 || cluster_fits(plan->func, c, threads, smem))) {
+    // automatic plans also want every row's cluster resident at once (one
+    // wave): large clusters need that many SMs free inside one GPC
+    const int need = force_cluster > 0 ? 1 : (rows < 1 ? 1 : rows);
+    if (st == LT_OK && (c == 1 || active_clusters(dev, slot, plan->func, c, threads, smem) >= need)) {
       plan->cluster = c;
       plan->smem = smem;
       break;
