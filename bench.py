@@ -58,6 +58,8 @@ def parse():
     ap.add_argument("--force-cluster", type=int, default=0)
     ap.add_argument("--only", choices=sorted(workloads.CONFIGS), default=None,
                     help="time one workload's kernel alone (for profilers); prints a short JSON line")
+    ap.add_argument("--kernel", choices=["auto", "resident", "stream"], default="auto",
+                    help="force the top-k kernel in --only / --trace runs")
     return ap.parse_args()
 
 
@@ -341,6 +343,9 @@ def bench_batched(lt, dev, args, world, peak, L2):
     return out
 
 
+KERNEL_IDS = {"auto": 0, "resident": 1, "stream": 2}
+
+
 def bench_only(args, world):
     """One workload, one kernel: warmup + steps launches on rotating copies."""
     import sparse_attention_indexer_lt_gb300 as lt
@@ -363,14 +368,15 @@ def bench_only(args, world):
         if w.blocked:
             lt.topk_blocked(c, ld, w.block, w.k_blocks, w.k, out_idx=oi, out_val=ov, out_blocks=ob)
         else:
-            lt.topk(c, ld, w.k, out_idx=oi, out_val=ov)
+            lt.topk(c, ld, w.k, out_idx=oi, out_val=ov, force_kernel=KERNEL_IDS[args.kernel])
 
     total_ms = timed_steps(step, args.steps, args.warmup, world)
     kern = total_ms / args.steps
     return {"workload": args.only, "steps": args.steps, "step_us": round(kern * 1000, 3),
             "read_bytes": nbytes,
             "hbm_gbs": round(nbytes / (kern * 1e-3) / 1e9, 1), "copies": ncopies,
-            "plan": lt.plan(w.rows, w.row_stride, w.k, blocked=w.blocked, k_blocks=w.k_blocks)}
+            "plan": lt.plan(w.rows, w.row_stride, w.k, blocked=w.blocked, k_blocks=w.k_blocks,
+                            force_kernel=0 if w.blocked else KERNEL_IDS[args.kernel])}
 
 
 TRACE_NAMES = ["start", "hist", "merge", "estimate", "filter", "exchange", "exact", "output",
@@ -388,9 +394,10 @@ def bench_trace(args):
     base = S.to(dev)
     copies = [base] + [base.clone() for _ in range(3)]
     ld = None if L is None else L.to(dev)
+    kid = 0 if w.blocked else KERNEL_IDS[args.kernel]
     pl = lt.plan(w.rows, w.row_stride, w.k, blocked=w.blocked, k_blocks=w.k_blocks,
-                 force_cluster=args.force_cluster, force_threads=args.force_threads)
-    ctas = w.rows * pl["cluster"]
+                 force_cluster=args.force_cluster, force_threads=args.force_threads, force_kernel=kid)
+    ctas = pl["grid"]  # persistent kernels: the first row of each CTA is traced
     tr = torch.full((ctas, 16), -1, dtype=torch.int64, device=dev)
     kw = dict(force_cluster=args.force_cluster, force_threads=args.force_threads)
     for i in range(max(3, args.warmup) + 1):
@@ -399,7 +406,7 @@ def bench_trace(args):
         if w.blocked:
             lt.topk_blocked(c, ld, w.block, w.k_blocks, w.k, trace=tr, **kw)
         else:
-            lt.topk(c, ld, w.k, trace=tr, **kw)
+            lt.topk(c, ld, w.k, trace=tr, force_kernel=kid, **kw)
         torch.cuda.synchronize()
     t = tr.cpu()
     start = t[:, 0]

@@ -31,7 +31,8 @@
  *   out_blocks  int32  [rows][k_blocks] or NULL (two-level only)
  * A row with L_r < k fills slots [L_r, k) with index -1 and value -inf.
  * Rows whose start is 16-byte aligned (scores 16-byte aligned and row_stride a
- * multiple of 4) use 128-bit loads; any other alignment takes scalar loads.
+ * multiple of 4) use 128-bit loads (batches of such rows: bulk copies into
+ * shared memory); any other alignment takes scalar loads.
  *
  * Errors. Argument errors return LT_ERR_INVALID_ARG or LT_ERR_UNSUPPORTED
  * synchronously and launch nothing. A failed launch returns LT_ERR_CUDA
@@ -97,6 +98,15 @@ lt_status lt_topk_blocked(const float* scores, const int32_t* lengths, int32_t r
                           int64_t row_stride, int32_t block, int32_t k_blocks, int32_t k,
                           int32_t* out_idx, float* out_val, int32_t* out_blocks, void* stream);
 
+/* Kernels (force_kernel, lt_plan_info.kernel). */
+#define LT_KERNEL_AUTO 0
+/* Register-resident: each CTA holds its first rounds of the row in registers
+ * and streams the rest with 128-bit loads; any alignment; one row per cluster. */
+#define LT_KERNEL_RESIDENT 1
+/* Streamed: 16-byte aligned rows move into a shared-memory ring by bulk
+ * copies; persistent CTAs walk the rows and prefetch the next one. */
+#define LT_KERNEL_STREAM 2
+
 /*
  * Launch-plan control, for tests and measurement (not needed for normal use).
  *
@@ -107,24 +117,32 @@ lt_status lt_topk_blocked(const float* scores, const int32_t* lengths, int32_t r
  *                  large batches) or 512 (one CTA per SM, for few rows)
  *   force_exact    nonzero skips the sampled-threshold fast path and runs the
  *                  streaming radix select on every row (same results)
+ *   force_kernel   LT_KERNEL_AUTO lets the planner choose (currently always
+ *                  register-resident); LT_KERNEL_STREAM on unaligned rows
+ *                  returns LT_ERR_UNSUPPORTED
  *   counters       NULL, or device int32[LT_NUM_COUNTERS] that the kernel
  *                  increments atomically, once per row: [0] rows finished on
  *                  the fast path, [1] rows finished on the streaming radix
  *                  select, [2] rows whose candidate set overflowed, [3] rows
- *                  whose sampled threshold kept fewer than k candidates.
+ *                  whose sampled threshold kept fewer than k candidates,
+ *                  [4] rows of the streamed kernel during which a wait for a
+ *                  bulk copy gave up after its poll limit (a hardware fault;
+ *                  that row's output is undefined -- never seen in practice).
  *                  For the two-level call, each row counts once per stage.
  *   trace          NULL, or device int64[grid CTAs * 16] receiving, from
  *                  thread 0 of each CTA, global-timer nanoseconds at phase
  *                  boundaries (entry, sample histogram, first cluster merge,
  *                  threshold, filter, candidate exchange, exact select,
  *                  output; the two-level kernel's second stage uses slots
- *                  9..14). CTA b of the grid is row b / cluster_size.
+ *                  9..14). CTA b of the grid is row b / cluster_size; a CTA
+ *                  of the streamed kernel serves several rows and traces its
+ *                  third (or, with fewer, its last).
  */
-#define LT_NUM_COUNTERS 4
+#define LT_NUM_COUNTERS 5
 lt_status lt_topk_ex(const float* scores, const int32_t* lengths, int32_t rows,
                      int64_t row_stride, int32_t k, int32_t* out_idx, float* out_val,
                      int32_t force_cluster, int32_t force_threads, int32_t force_exact,
-                     int32_t* counters, int64_t* trace, void* stream);
+                     int32_t force_kernel, int32_t* counters, int64_t* trace, void* stream);
 lt_status lt_topk_blocked_ex(const float* scores, const int32_t* lengths, int32_t rows,
                              int64_t row_stride, int32_t block, int32_t k_blocks, int32_t k,
                              int32_t* out_idx, float* out_val, int32_t* out_blocks,
@@ -134,13 +152,21 @@ lt_status lt_topk_blocked_ex(const float* scores, const int32_t* lengths, int32_
 /*
  * lt_topk_plan -- the launch the planner would make, without launching.
  * blocked selects the two-level kernel (block and k_blocks are ignored
- * otherwise). Writes the CTAs per row (cluster size), threads per CTA and
- * dynamic shared memory bytes per CTA to the non-NULL host pointers.
+ * otherwise); aligned says whether the rows will be 16-byte aligned. Fills
+ * *info (host memory, owned by the caller).
  */
+typedef struct lt_plan_info {
+  int32_t kernel;           /* LT_KERNEL_RESIDENT or LT_KERNEL_STREAM */
+  int32_t cluster_size;     /* CTAs that share one row */
+  int32_t threads_per_cta;
+  int32_t smem_bytes;       /* dynamic shared memory per CTA */
+  int32_t grid_ctas;        /* CTAs launched (streamed: persistent, rows grid-stride) */
+  int32_t ring_stages;      /* streamed kernel: shared-memory ring stages, else 0 */
+} lt_plan_info;
 lt_status lt_topk_plan(int32_t rows, int64_t row_stride, int32_t k, int32_t blocked,
                        int32_t block, int32_t k_blocks, int32_t force_cluster,
-                       int32_t force_threads, int32_t* cluster_size, int32_t* threads_per_cta,
-                       int32_t* smem_bytes);
+                       int32_t force_threads, int32_t force_kernel, int32_t aligned,
+                       lt_plan_info* info);
 
 /* Static description of a status code. */
 const char* lt_status_string(lt_status status);

@@ -17,11 +17,20 @@ from pathlib import Path
 import torch
 
 __all__ = ["topk", "topk_blocked", "plan", "load", "library_path", "LtError", "NUM_COUNTERS",
-           "status_string", "version"]
+           "status_string", "version", "PlanInfo", "KERNEL_AUTO", "KERNEL_RESIDENT", "KERNEL_STREAM"]
 
 _LIB_PATH = Path(__file__).resolve().parent / "liblt_topk.so"
 _lib = None
-NUM_COUNTERS = 4
+NUM_COUNTERS = 5
+KERNEL_AUTO, KERNEL_RESIDENT, KERNEL_STREAM = 0, 1, 2
+_KERNEL_NAMES = {KERNEL_RESIDENT: "resident", KERNEL_STREAM: "stream"}
+
+
+class PlanInfo(ctypes.Structure):
+    """Mirror of lt_plan_info."""
+    _fields_ = [("kernel", ctypes.c_int32), ("cluster_size", ctypes.c_int32),
+                ("threads_per_cta", ctypes.c_int32), ("smem_bytes", ctypes.c_int32),
+                ("grid_ctas", ctypes.c_int32), ("ring_stages", ctypes.c_int32)]
 
 
 class LtError(RuntimeError):
@@ -49,14 +58,14 @@ def load() -> ctypes.CDLL:
     i32, i64, vp = ctypes.c_int32, ctypes.c_int64, ctypes.c_void_p
     lib.lt_topk.argtypes = [vp, vp, i32, i64, i32, vp, vp, vp]
     lib.lt_topk.restype = ctypes.c_int
-    lib.lt_topk_ex.argtypes = [vp, vp, i32, i64, i32, vp, vp, i32, i32, i32, vp, vp, vp]
+    lib.lt_topk_ex.argtypes = [vp, vp, i32, i64, i32, vp, vp, i32, i32, i32, i32, vp, vp, vp]
     lib.lt_topk_ex.restype = ctypes.c_int
     lib.lt_topk_blocked.argtypes = [vp, vp, i32, i64, i32, i32, i32, vp, vp, vp, vp]
     lib.lt_topk_blocked.restype = ctypes.c_int
     lib.lt_topk_blocked_ex.argtypes = [vp, vp, i32, i64, i32, i32, i32, vp, vp, vp, i32, i32, i32, vp, vp,
                                        vp]
     lib.lt_topk_blocked_ex.restype = ctypes.c_int
-    lib.lt_topk_plan.argtypes = [i32, i64, i32, i32, i32, i32, i32, i32, vp, vp, vp]
+    lib.lt_topk_plan.argtypes = [i32, i64, i32, i32, i32, i32, i32, i32, i32, i32, vp]
     lib.lt_topk_plan.restype = ctypes.c_int
     lib.lt_status_string.argtypes = [ctypes.c_int]
     lib.lt_status_string.restype = ctypes.c_char_p
@@ -124,8 +133,9 @@ def _counters(c, device):
 def topk(scores: torch.Tensor, lengths: torch.Tensor | None = None, k: int = 512, *,
          out_idx: torch.Tensor | None = None, out_val: torch.Tensor | None = None,
          with_values: bool = True, force_cluster: int = 0, force_threads: int = 0,
-         force_exact: bool = False, counters: torch.Tensor | None = None,
-         trace: torch.Tensor | None = None, stream: torch.cuda.Stream | None = None):
+         force_exact: bool = False, force_kernel: int = KERNEL_AUTO,
+         counters: torch.Tensor | None = None, trace: torch.Tensor | None = None,
+         stream: torch.cuda.Stream | None = None):
     """Per-row top-k by (score desc, index asc); returns (idx int32 [rows, k], val float32 [rows, k] or None)."""
     lib = load()
     rows, n = _check_scores(scores)
@@ -141,7 +151,8 @@ def topk(scores: torch.Tensor, lengths: torch.Tensor | None = None, k: int = 512
         s = (stream or torch.cuda.current_stream(dev)).cuda_stream
         st = lib.lt_topk_ex(_ptr(scores), _ptr(lengths), rows, max(n, 1), int(k), _ptr(out_idx),
                             _ptr(out_val), int(force_cluster), int(force_threads),
-                            int(bool(force_exact)), _ptr(counters), _ptr(trace), ctypes.c_void_p(s))
+                            int(bool(force_exact)), int(force_kernel), _ptr(counters), _ptr(trace),
+                            ctypes.c_void_p(s))
     if st != 0:
         raise LtError("lt_topk", st)
     return out_idx, out_val
@@ -176,14 +187,16 @@ def topk_blocked(scores: torch.Tensor, lengths: torch.Tensor | None = None, bloc
 
 def plan(rows: int, row_stride: int, k: int, *, blocked: bool = False, block: int = 8,
          k_blocks: int = 2048, force_cluster: int = 0, force_threads: int = 0,
-         device: int | None = None) -> dict:
-    """The launch the planner would make: {'cluster', 'threads', 'smem'}."""
+         force_kernel: int = KERNEL_AUTO, aligned: bool = True, device: int | None = None) -> dict:
+    """The launch the planner would make: {'kernel', 'cluster', 'threads', 'smem', 'grid', 'stages'}."""
     lib = load()
-    c, t, s = ctypes.c_int32(), ctypes.c_int32(), ctypes.c_int32()
+    info = PlanInfo()
     with torch.cuda.device(device if device is not None else torch.cuda.current_device()):
         st = lib.lt_topk_plan(int(rows), int(row_stride), int(k), int(bool(blocked)), int(block),
-                              int(k_blocks), int(force_cluster), int(force_threads), ctypes.byref(c),
-                              ctypes.byref(t), ctypes.byref(s))
+                              int(k_blocks), int(force_cluster), int(force_threads), int(force_kernel),
+                              int(bool(aligned)), ctypes.byref(info))
     if st != 0:
         raise LtError("lt_topk_plan", st)
-    return {"cluster": c.value, "threads": t.value, "smem": s.value}
+    return {"kernel": _KERNEL_NAMES.get(info.kernel, str(info.kernel)), "cluster": info.cluster_size,
+            "threads": info.threads_per_cta, "smem": info.smem_bytes, "grid": info.grid_ctas,
+            "stages": info.ring_stages}

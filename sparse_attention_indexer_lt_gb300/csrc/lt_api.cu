@@ -21,6 +21,7 @@
 #include "../../include/lt_topk.h"
 #include "lt_device.cuh"
 #include "lt_launch.h"
+#include "lt_stream.cuh"
 
 namespace {
 
@@ -28,12 +29,17 @@ constexpr int kMaxDevices = 64;
 constexpr int kWideThreads = 512;
 constexpr int kNarrowThreads = 256;
 constexpr int64_t kWideRound = 512 * 8 * 4;  // positions per CTA per round (wide)
-constexpr int kSlots = 10;                    // kernel variants
+constexpr int kSlots = 12;                    // kernel variants
+// the streamed kernel's launch bounds: CTAs per SM for 256 / 512 threads
+constexpr int stream_ctas_per_sm(int threads) { return threads == 256 ? 3 : 2; }
+constexpr int kStreamMaxStages = 8;
 
 struct DeviceInfo {
   bool ready = false;
   int sms = 0;
   int smem_optin = 0;
+  int smem_per_sm = 0;
+  int smem_reserved = 0;
 };
 
 std::mutex g_mu;
@@ -51,8 +57,9 @@ int block_index(int block) {
   }
 }
 
-int kernel_slot(bool blocked, int block, int threads) {
+int kernel_slot(bool blocked, int block, int threads, bool stream = false) {
   const int wide = threads == kWideThreads ? 1 : 0;
+  if (stream) return 10 + wide;
   if (!blocked) return wide;
   const int b = block_index(block);
   return b < 0 ? -1 : 2 + 2 * b + wide;
@@ -65,8 +72,11 @@ uint32_t next_pow2(uint32_t x) {
 }
 
 struct Plan {
+  int kernel = LT_KERNEL_RESIDENT;
   int cluster = 1;
   int threads = kNarrowThreads;
+  int grid = 0;             // CTAs launched
+  uint32_t stages = 0;      // streamed kernel: ring stages
   uint32_t cap = 0;        // candidate slots: cluster * (1 << seg_shift)
   uint32_t seg_shift = 0;  // log2 of the slots each CTA of the cluster may fill
   uint32_t wstage = 0;     // per-warp candidate staging bytes (threads * 16 * float4 per round)
@@ -84,6 +94,10 @@ lt_status device_info(DeviceInfo** out, int* dev_out) {
   if (!d.ready) {
     if (cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return LT_ERR_CUDA;
     if (cudaDeviceGetAttribute(&d.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
+      return LT_ERR_CUDA;
+    if (cudaDeviceGetAttribute(&d.smem_per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) != cudaSuccess)
+      return LT_ERR_CUDA;
+    if (cudaDeviceGetAttribute(&d.smem_reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev) != cudaSuccess)
       return LT_ERR_CUDA;
     d.ready = true;
   }
@@ -151,13 +165,30 @@ int active_clusters(int dev, int slot, const void* func, int cluster, int thread
   return n;
 }
 
+lt_status make_stream_plan(int32_t rows, int64_t row_stride, int32_t k, int32_t force_cluster,
+                           int32_t force_threads, DeviceInfo* di, int dev, Plan* plan);
+
 lt_status make_plan(int32_t rows, int64_t row_stride, int32_t k, bool blocked, int32_t block,
-                    int32_t k_blocks, int32_t force_cluster, int32_t force_threads, Plan* plan,
-                    int* dev_out) {
+                    int32_t k_blocks, int32_t force_cluster, int32_t force_threads, int32_t force_kernel,
+                    bool aligned, Plan* plan, int* dev_out) {
   DeviceInfo* di = nullptr;
   int dev = 0;
   lt_status st = device_info(&di, &dev);
   if (st != LT_OK) return st;
+  // The streamed kernel (bulk copies need 16-byte aligned rows) runs only
+  // when asked for: measured on GB300 it does not yet beat the register-
+  // resident kernel on the batched shapes, whose loads are all in flight from
+  // their first instruction and which keeps three CTAs per SM.
+  bool stream = false;
+  if (force_kernel == LT_KERNEL_STREAM) {
+    if (blocked || !aligned) return LT_ERR_UNSUPPORTED;
+    stream = true;
+  }
+  if (stream) {
+    st = make_stream_plan(rows, row_stride, k, force_cluster, force_threads, di, dev, plan);
+    if (st == LT_OK) *dev_out = dev;
+    return st;
+  }
 
   int threads = force_threads;
   if (threads == 0) threads = (int64_t)rows >= di->sms ? kNarrowThreads : kWideThreads;
@@ -212,8 +243,80 @@ lt_status make_plan(int32_t rows, int64_t row_stride, int32_t k, bool blocked, i
     c /= 2;
   }
   if ((int64_t)rows * plan->cluster > 0x7fffffffLL) return LT_ERR_UNSUPPORTED;
+  plan->grid = rows * plan->cluster;
   *dev_out = dev;
   return LT_OK;
+}
+
+// Streamed kernel: three (256 threads) or two (512) CTAs per SM, as many ring
+// stages as fit in that share of an SM's shared memory, persistent CTAs (each
+// walks rows grid-stride). C doubles while every row's cluster still fits on the SMs
+// twice over and each CTA keeps at least two chunks of the row.
+lt_status make_stream_plan(int32_t rows, int64_t row_stride, int32_t k, int32_t force_cluster,
+                           int32_t force_threads, DeviceInfo* di, int dev, Plan* plan) {
+  int threads = force_threads;
+  if (threads == 0) threads = (int64_t)rows >= 2 * di->sms ? kNarrowThreads : kWideThreads;
+  const int slot = kernel_slot(false, 4, threads, true);
+  plan->kernel = LT_KERNEL_STREAM;
+  plan->threads = threads;
+  plan->func = lt::stream_kernel_ptr(threads);
+  if (!plan->func) return LT_ERR_UNSUPPORTED;
+  plan->wstage = 0;
+  const uint32_t chunk_pos = threads == kNarrowThreads ? (uint32_t)lt::SGeo<256, 4>::kChunk
+                                                       : (uint32_t)lt::SGeo<512, 2>::kChunk;
+  const uint32_t kmax = (uint32_t)k;
+  uint32_t base_cap = next_pow2(4 * kmax);
+  base_cap = base_cap < 2048u ? 2048u : (base_cap > 4096u ? 4096u : base_cap);
+  plan->sel_cap = next_pow2(kmax < 32u ? 32u : kmax);
+  const int cps = stream_ctas_per_sm(threads);
+  const int slots_total = di->sms * cps;
+  int c = 1;
+  if (force_cluster > 0) {
+    c = force_cluster;
+  } else {
+    while (c < 16 && (int64_t)rows * 2 * c <= slots_total && (int64_t)c * 2 * chunk_pos < row_stride) c *= 2;
+  }
+  const uint32_t budget = (uint32_t)(di->smem_per_sm / cps - di->smem_reserved);
+  for (;;) {
+    uint32_t seg = base_cap;
+    if (c > 1) {
+      seg = next_pow2((base_cap + (uint32_t)c - 1) / (uint32_t)c);
+      if (seg < 256u) seg = 256u;
+    }
+    plan->cap = (uint32_t)c * seg;
+    plan->seg_shift = 0;
+    while ((1u << plan->seg_shift) < seg) ++plan->seg_shift;
+    uint32_t ns = kStreamMaxStages;
+    while (ns > 2 && lt::make_stream_layout(c > 1, plan->cap, plan->sel_cap, ns, 4 * chunk_pos).total > budget) --ns;
+    const uint32_t smem = lt::make_stream_layout(c > 1, plan->cap, plan->sel_cap, ns, 4 * chunk_pos).total;
+    if ((int)smem > di->smem_optin) return LT_ERR_UNSUPPORTED;
+    lt_status st = prepare_kernel(dev, slot, plan->func, smem, c);
+    if (st != LT_OK && !(st == LT_ERR_UNSUPPORTED && force_cluster == 0 && c > 8)) return st;
+    int resident = 0;
+    if (st == LT_OK) {
+      if (c == 1) {
+        int per_sm = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, plan->func, threads, smem) != cudaSuccess) {
+          (void)cudaGetLastError();
+          per_sm = 0;
+        }
+        resident = per_sm * di->sms;
+      } else {
+        resident = active_clusters(dev, slot, plan->func, c, threads, smem);
+      }
+    }
+    const int need = force_cluster > 0 ? 1 : (c == 1 ? 1 : rows);
+    if (resident >= need) {
+      plan->cluster = c;
+      plan->smem = smem;
+      plan->stages = ns;
+      const int64_t clusters = rows < resident ? rows : resident;
+      plan->grid = (int)(clusters * c);
+      return LT_OK;
+    }
+    if (force_cluster > 0 || c == 1) return LT_ERR_UNSUPPORTED;
+    c /= 2;
+  }
 }
 
 lt_status check_common(const float* scores, int32_t rows, int64_t row_stride, int32_t k,
@@ -229,15 +332,16 @@ lt_status check_common(const float* scores, int32_t rows, int64_t row_stride, in
   return LT_OK;
 }
 
-lt_status launch(const Plan& plan, const lt::Params& prm, int32_t rows, void* stream) {
+lt_status launch(const Plan& plan, const lt::Params& prm, void* stream) {
   lt::Params p = prm;
   p.cap = (int32_t)plan.cap;
   p.seg_shift = (int32_t)plan.seg_shift;
   p.wstage = (int32_t)plan.wstage;
   p.sel_cap = (int32_t)plan.sel_cap;
   p.clustered = plan.cluster > 1 ? 1 : 0;
+  p.ring_stages = (int32_t)plan.stages;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)((int64_t)rows * plan.cluster));
+  cfg.gridDim = dim3((unsigned)plan.grid);
   cfg.blockDim = dim3((unsigned)plan.threads);
   cfg.dynamicSmemBytes = plan.smem;
   cfg.stream = static_cast<cudaStream_t>(stream);
@@ -262,14 +366,16 @@ extern "C" {
 
 lt_status lt_topk_ex(const float* scores, const int32_t* lengths, int32_t rows, int64_t row_stride,
                      int32_t k, int32_t* out_idx, float* out_val, int32_t force_cluster,
-                     int32_t force_threads, int32_t force_exact, int32_t* counters, int64_t* trace,
-                     void* stream) {
+                     int32_t force_threads, int32_t force_exact, int32_t force_kernel, int32_t* counters,
+                     int64_t* trace, void* stream) {
   lt_status st = check_common(scores, rows, row_stride, k, out_idx, force_cluster, force_threads);
   if (st != LT_OK) return st;
+  if (force_kernel < LT_KERNEL_AUTO || force_kernel > LT_KERNEL_STREAM) return LT_ERR_INVALID_ARG;
   if (rows == 0) return LT_OK;
   Plan plan;
   int dev = 0;
-  st = make_plan(rows, row_stride, k, false, 4, 1, force_cluster, force_threads, &plan, &dev);
+  st = make_plan(rows, row_stride, k, false, 4, 1, force_cluster, force_threads, force_kernel,
+                 aligned16(scores, row_stride), &plan, &dev);
   if (st != LT_OK) return st;
   lt::Params p = {};
   p.scores = scores;
@@ -285,12 +391,13 @@ lt_status lt_topk_ex(const float* scores, const int32_t* lengths, int32_t rows, 
   p.k_blocks = 1;
   p.force_exact = force_exact ? 1 : 0;
   p.vec_ok = aligned16(scores, row_stride) ? 1 : 0;
-  return launch(plan, p, rows, stream);
+  return launch(plan, p, stream);
 }
 
 lt_status lt_topk(const float* scores, const int32_t* lengths, int32_t rows, int64_t row_stride,
                   int32_t k, int32_t* out_idx, float* out_val, void* stream) {
-  return lt_topk_ex(scores, lengths, rows, row_stride, k, out_idx, out_val, 0, 0, 0, nullptr, nullptr, stream);
+  return lt_topk_ex(scores, lengths, rows, row_stride, k, out_idx, out_val, 0, 0, 0, LT_KERNEL_AUTO, nullptr,
+                    nullptr, stream);
 }
 
 lt_status lt_topk_blocked_ex(const float* scores, const int32_t* lengths, int32_t rows,
@@ -305,7 +412,8 @@ lt_status lt_topk_blocked_ex(const float* scores, const int32_t* lengths, int32_
   if (rows == 0) return LT_OK;
   Plan plan;
   int dev = 0;
-  st = make_plan(rows, row_stride, k, true, block, k_blocks, force_cluster, force_threads, &plan, &dev);
+  st = make_plan(rows, row_stride, k, true, block, k_blocks, force_cluster, force_threads, LT_KERNEL_AUTO,
+                 aligned16(scores, row_stride), &plan, &dev);
   if (st != LT_OK) return st;
   lt::Params p = {};
   p.scores = scores;
@@ -321,7 +429,7 @@ lt_status lt_topk_blocked_ex(const float* scores, const int32_t* lengths, int32_
   p.k_blocks = k_blocks;
   p.force_exact = force_exact ? 1 : 0;
   p.vec_ok = aligned16(scores, row_stride) ? 1 : 0;
-  return launch(plan, p, rows, stream);
+  return launch(plan, p, stream);
 }
 
 lt_status lt_topk_blocked(const float* scores, const int32_t* lengths, int32_t rows,
@@ -332,22 +440,27 @@ lt_status lt_topk_blocked(const float* scores, const int32_t* lengths, int32_t r
 }
 
 lt_status lt_topk_plan(int32_t rows, int64_t row_stride, int32_t k, int32_t blocked, int32_t block,
-                       int32_t k_blocks, int32_t force_cluster, int32_t force_threads,
-                       int32_t* cluster_size, int32_t* threads_per_cta, int32_t* smem_bytes) {
-  if (rows < 1 || row_stride < 1 || k < 1) return LT_ERR_INVALID_ARG;
+                       int32_t k_blocks, int32_t force_cluster, int32_t force_threads, int32_t force_kernel,
+                       int32_t aligned, lt_plan_info* info) {
+  if (rows < 1 || row_stride < 1 || k < 1 || info == nullptr) return LT_ERR_INVALID_ARG;
   if (!(force_threads == 0 || force_threads == kNarrowThreads || force_threads == kWideThreads))
     return LT_ERR_INVALID_ARG;
+  if (force_kernel < LT_KERNEL_AUTO || force_kernel > LT_KERNEL_STREAM) return LT_ERR_INVALID_ARG;
   if (blocked && block_index(block) < 0) return LT_ERR_UNSUPPORTED;
   if (k > LT_MAX_K || row_stride > LT_MAX_ROW_STRIDE) return LT_ERR_UNSUPPORTED;
   if (blocked && (k_blocks < 1 || k_blocks > LT_MAX_K)) return LT_ERR_INVALID_ARG;
   Plan plan;
   int dev = 0;
   lt_status st = make_plan(rows, row_stride, k, blocked != 0, blocked ? block : 4, blocked ? k_blocks : 1,
-                           force_cluster, force_threads, &plan, &dev);
+                           force_cluster, force_threads, force_kernel, aligned != 0 && row_stride % 4 == 0,
+                           &plan, &dev);
   if (st != LT_OK) return st;
-  if (cluster_size) *cluster_size = plan.cluster;
-  if (threads_per_cta) *threads_per_cta = plan.threads;
-  if (smem_bytes) *smem_bytes = (int32_t)plan.smem;
+  info->kernel = plan.kernel;
+  info->cluster_size = plan.cluster;
+  info->threads_per_cta = plan.threads;
+  info->smem_bytes = (int32_t)plan.smem;
+  info->grid_ctas = plan.grid;
+  info->ring_stages = (int32_t)plan.stages;
   return LT_OK;
 }
 
@@ -361,6 +474,6 @@ const char* lt_status_string(lt_status status) {
   }
 }
 
-int32_t lt_version(void) { return 200; }
+int32_t lt_version(void) { return 300; }
 
 }  // extern "C"

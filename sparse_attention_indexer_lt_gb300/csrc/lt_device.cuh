@@ -57,8 +57,11 @@ constexpr int kMaxCluster = 16;
 constexpr int kMaxWarps = 32;
 constexpr int kMaxBucket = 64;    // largest bucket ranked by counting
 constexpr unsigned kFull = 0xffffffffu;
+// A second 11-bit level refines the sampled threshold only when the first
+// predicts more candidates than this fraction of the candidate capacity.
+constexpr float kLevel2Frac = 0.75f;
 
-enum Counter { kCntFast = 0, kCntExact = 1, kCntOverflow = 2, kCntShort = 3 };
+enum Counter { kCntFast = 0, kCntExact = 1, kCntOverflow = 2, kCntShort = 3, kCntTimeout = 4 };
 
 // Phase timestamps (nanoseconds of the global timer) written by thread 0 of
 // each CTA when a trace buffer is given: slot i of CTA b at trace[b * 16 + i].
@@ -94,6 +97,7 @@ struct Params {
   int32_t force_exact;
   int32_t vec_ok;       // every row start is 16-byte aligned
   int32_t clustered;    // launched with cluster size > 1
+  int32_t ring_stages;  // streamed kernel: shared-memory ring stages
 };
 
 // ------------------------------------------------------------------ smem layout

@@ -48,7 +48,17 @@ struct Row {
   int rounds;            // rounds of this CTA's slice
   int rounds_max;        // cluster-wide maximum
   bool init_pending;     // the start-up cluster barrier has not been waited on
+  int64_t* trace;        // phase timestamps of this row (nullable)
 };
+
+// Phase timestamp of this row (thread 0 of each CTA), when traced.
+__device__ __forceinline__ void stamp(const Row& R, int slot) {
+  if (R.trace != nullptr && threadIdx.x == 0) {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    R.trace[(int64_t)blockIdx.x * kTraceSlots + slot] = (int64_t)t;
+  }
+}
 
 // Items of this CTA's own slice (ranks in the output are written by their owner).
 struct OwnSlice {
@@ -141,12 +151,14 @@ struct KeepBlocks {
 
 // ------------------------------------------------------------------ setup
 
+// row < 0: the row of this CTA's cluster (one row per cluster); otherwise the
+// given row (persistent kernels).
 template <int T, int U, int W>
-__device__ __forceinline__ void setup_row(Row& R, const Params& p, unsigned char* smem) {
+__device__ __forceinline__ void setup_row(Row& R, const Params& p, unsigned char* smem, int64_t row = -1) {
   using G = Geo<T, U, W>;
   R.nclus = p.clustered ? cluster_size() : 1u;
   R.rank = p.clustered ? cluster_rank() : 0u;
-  R.row = (int64_t)(blockIdx.x / R.nclus);
+  R.row = row >= 0 ? row : (int64_t)(blockIdx.x / R.nclus);
   const Layout lay = make_layout(p.clustered != 0, (uint32_t)p.cap, (uint32_t)p.sel_cap, (uint32_t)p.wstage);
   R.m = reinterpret_cast<Misc*>(smem + lay.misc);
   R.hist = reinterpret_cast<uint32_t*>(smem + lay.hist);
@@ -157,6 +169,7 @@ __device__ __forceinline__ void setup_row(Row& R, const Params& p, unsigned char
   R.stage = reinterpret_cast<uint64_t*>(smem + lay.stage);
   R.wst = reinterpret_cast<float4*>(smem + lay.wstage) + (threadIdx.x >> 5) * 32 * U;
   R.stage_cap = (uint32_t)p.sel_cap + kMaxBucket;
+  R.trace = p.trace;
   R.seg_shift = (uint32_t)p.seg_shift;
   int64_t L = p.row_stride;
   if (p.lengths) {
@@ -896,7 +909,7 @@ __device__ __forceinline__ bool select_stage(Row& R, const Params& p, float4 (&c
             if (nsr > 0) hist_round<T, U, W, 1>(R, 0, cur, nc, 0, keep);
             if (nsr > 1) hist_round<T, U, W, 1>(R, 1, nxt, nn, 0, keep);
           }
-          stamp(p, tr + kTrHist);
+          stamp(R, tr + kTrHist);
         } else {
           if (kBlocks) {
             if (nsr > 0) hist_round_blocks<T, U, W, 2>(R, cur, nc, d1);
@@ -908,7 +921,7 @@ __device__ __forceinline__ bool select_stage(Row& R, const Params& p, float4 (&c
         }
         const uint32_t lo_rank = (level == 1 && full && R.nclus >= 8) ? (K < (uint32_t)items ? K : (uint32_t)items) : 0u;
         const uint32_t* bins = merge_hist<T>(R, level - 1, lo_rank);
-        if (level == 1) stamp(p, tr + kTrMerge);
+        if (level == 1) stamp(R, tr + kTrMerge);
         if (level == 1) {
           const uint32_t ns = full ? (uint32_t)items : bins_total<T>(bins, m);
           if (ns == 0) {  // no sample: keep every item
@@ -924,7 +937,7 @@ __device__ __forceinline__ bool select_stage(Row& R, const Params& p, float4 (&c
           t = d1 << 21;
           const float predicted = full ? (float)(above1 + cnt1)
                                        : (float)(above1 + cnt1) * ((float)items / (float)ns);
-          if (predicted <= 0.5f * (float)cap) break;  // one 11-bit level is selective enough
+          if (predicted <= kLevel2Frac * (float)cap) break;  // one 11-bit level is selective enough
         } else {
           find_digit<T>(bins, r - above1, m);
           t |= m->res_digit << 10;
@@ -932,7 +945,7 @@ __device__ __forceinline__ bool select_stage(Row& R, const Params& p, float4 (&c
         }
       }
     }
-    stamp(p, tr + kTrEstimate);
+    stamp(R, tr + kTrEstimate);
     // ---- filter every round against the threshold
     const bool all = (t == 0u);
     const float g = threshold_float(all ? 1u : t);
@@ -958,9 +971,9 @@ __device__ __forceinline__ bool select_stage(Row& R, const Params& p, float4 (&c
         else clear_round(nn);
       }
     }
-    stamp(p, tr + kTrFilter);
+    stamp(R, tr + kTrFilter);
     exchange_segments<T>(R);
-    stamp(p, tr + kTrExchange);
+    stamp(R, tr + kTrExchange);
     uint32_t total = 0;
     bool overflow = false;
     for (uint32_t q = 0; q < R.nclus; ++q) {
@@ -979,11 +992,11 @@ __device__ __forceinline__ bool select_stage(Row& R, const Params& p, float4 (&c
     wait_init(R);
     *Tc = exact_select<T, U, W, kBlocks>(R, p, K, idx_limit, keep);
     *regs_intact = false;
-    stamp(p, tr + kTrExact);
+    stamp(R, tr + kTrExact);
     bump(p, R, kCntExact);
     return true;
   }
-  stamp(p, tr + kTrExact);
+  stamp(R, tr + kTrExact);
   if (K > 0) bump(p, R, kCntFast);
   return false;
 }
@@ -1002,7 +1015,7 @@ __device__ __forceinline__ void output_positions(Row& R, const Params& p, bool e
     if (!bucket_select_sort<T>(R, K, kout, oi, ov, own))
       sorted_fallback<T>(R, exact, Tc, K, kout, oi, ov, idx_limit, own);
   }
-  stamp(p, kTrOutput);
+  stamp(R, kTrOutput);
 }
 
 }  // namespace lt

@@ -8,4 +8,6 @@ const void* topk_kernel_ptr(int threads);
 const void* blocked_kernel_ptr(int threads, int block);
 const void* blocked_kernel_ptr_narrow(int block);
 const void* blocked_kernel_ptr_wide(int block);
+// the streamed top-k kernel: 256 threads (three CTAs per SM) or 512 (two)
+const void* stream_kernel_ptr(int threads);
 }  // namespace lt

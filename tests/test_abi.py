@@ -45,8 +45,8 @@ def test_status_strings_and_version(lib):
 P = ctypes.c_void_p
 
 
-def _topk(lib, scores, lengths, rows, stride, k, oi, ov, fc=0):
-    return lib.lt_topk_ex(scores, lengths, rows, stride, k, oi, ov, fc, 0, 0, None, None, None)
+def _topk(lib, scores, lengths, rows, stride, k, oi, ov, fc=0, fk=0):
+    return lib.lt_topk_ex(scores, lengths, rows, stride, k, oi, ov, fc, 0, 0, fk, None, None, None)
 
 
 def test_invalid_arguments_rejected_without_launch(lib):
@@ -59,7 +59,9 @@ def test_invalid_arguments_rejected_without_launch(lib):
     assert _topk(lib, fake, None, 1, 16, 4, fake, None, fc=3) == 1  # cluster not a power of two
     assert _topk(lib, fake, None, 1, 16, 4096, fake, None) == 2  # k > LT_MAX_K
     assert _topk(lib, fake, None, 1, (1 << 30) + 1, 4, fake, None) == 2  # row too long
-    assert lib.lt_topk_ex(fake, None, 1, 16, 4, fake, None, 0, 1024, 0, None, None, None) == 1  # bad thread count
+    assert lib.lt_topk_ex(fake, None, 1, 16, 4, fake, None, 0, 1024, 0, 0, None, None, None) == 1  # bad threads
+    assert _topk(lib, fake, None, 1, 16, 4, fake, None, fk=3) == 1  # unknown kernel
+    assert _topk(lib, fake, None, 1, 16, 4, fake, None, fk=-1) == 1
     # rows == 0 is a valid no-op
     assert _topk(lib, None, None, 0, 16, 4, None, None) == 0
 
@@ -72,6 +74,16 @@ def test_blocked_invalid_arguments(lib):
     assert f(fake, None, 1, 64, 6, 4, 4, fake, None, None, 0, 0, 0, None, None, None) == 2   # block unsupported
     assert f(fake, None, 1, 64, 8, 5000, 4, fake, None, None, 0, 0, 0, None, None, None) == 2
     assert f(None, None, 0, 64, 8, 4, 4, None, None, None, 0, 0, 0, None, None, None) == 0
+
+
+def test_plan_rejects_bad_arguments(lib):
+    from sparse_attention_indexer_lt_gb300 import PlanInfo
+    info = PlanInfo()
+    f = lib.lt_topk_plan
+    assert f(0, 64, 4, 0, 4, 1, 0, 0, 0, 1, ctypes.byref(info)) == 1      # rows < 1
+    assert f(1, 64, 4, 0, 4, 1, 0, 0, 0, 1, None) == 1                    # no output struct
+    assert f(1, 64, 4, 0, 4, 1, 0, 0, 7, 1, ctypes.byref(info)) == 1      # unknown kernel
+    assert f(1, 64, 4, 1, 6, 4, 0, 0, 0, 1, ctypes.byref(info)) == 2      # block unsupported
 
 
 def test_binding_refuses_cpu_tensors():

@@ -8,6 +8,9 @@ from _gpu import counters, gpu_topk, parity_topk
 
 pytestmark = pytest.mark.gpu
 
+# 1: register-resident kernel, 2: streamed kernel (bulk copies into a shared-memory ring)
+KERNELS = [1, 2]
+
 
 @pytest.fixture(scope="module", autouse=True)
 def _built():
@@ -27,12 +30,24 @@ def test_workload_parity_and_fast_path(name):
     assert cnt[1] == 0, cnt
 
 
+@pytest.mark.parametrize("kernel", KERNELS)
+@pytest.mark.parametrize("name", ["c1_single_4096", "c2_decode_262144", "c3_ragged_64", "c4_prefill_4096"])
+def test_workload_parity_each_kernel(name, kernel):
+    S, L, w = workloads.make(name)
+    c = counters()
+    parity_topk(S.numpy(), None if L is None else L.numpy(), w.k, what=f"{name}/kernel {kernel}",
+                counters=c, force_kernel=kernel)
+    cnt = c.cpu().numpy()
+    assert cnt[0] == w.rows and cnt[1] == 0 and cnt[4] == 0, cnt
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
 @pytest.mark.parametrize("name", ["c1_single_4096", "c2_decode_262144", "c3_ragged_64"])
-def test_workload_parity_exact_path(name):
+def test_workload_parity_exact_path(name, kernel):
     S, L, w = workloads.make(name)
     c = counters()
     parity_topk(S.numpy(), None if L is None else L.numpy(), w.k, what=name + "/exact",
-                force_exact=True, counters=c)
+                force_exact=True, counters=c, force_kernel=kernel)
     assert c.cpu().numpy()[1] == w.rows
 
 
@@ -45,18 +60,20 @@ def test_prefill_rows_exact_path_subset():
 DISTS = ["normal", "bf16", "coarse", "equal", "asc", "desc", "special", "tail"]
 
 
+@pytest.mark.parametrize("kernel", KERNELS)
 @pytest.mark.parametrize("dist", DISTS)
 @pytest.mark.parametrize("shape", [(3, 1000), (2, 5000), (2, 40000), (1, 300000)])
-def test_small_distributions(dist, shape):
+def test_small_distributions(dist, shape, kernel):
     rows, stride = shape
     S, L = workloads.random_rows(rows, stride, seed=hash((dist, stride)) % 1000, dist=dist,
                                  lengths="ragged", min_len=0)
     for k in (1, 64, 512):
-        parity_topk(S.numpy(), L.numpy(), k, what=f"{dist}{shape} k={k}")
+        parity_topk(S.numpy(), L.numpy(), k, what=f"{dist}{shape} k={k}", force_kernel=kernel)
 
 
+@pytest.mark.parametrize("kernel", KERNELS)
 @pytest.mark.parametrize("k", [1, 512, 2048])
-def test_edge_lengths_and_poisoned_padding(k):
+def test_edge_lengths_and_poisoned_padding(k, kernel):
     stride = 20000
     lens = [0, 1, 2, 3, 4, 5, 7, 8, 9, k - 1, k, k + 1, 1023, 1024, 1025, 8191, 8192, 8193,
             16383, 16384, 16385, stride - 1, stride]
@@ -65,22 +82,23 @@ def test_edge_lengths_and_poisoned_padding(k):
     S = S.numpy().copy()
     for r, l in enumerate(lens):
         S[r, l:] = np.inf  # never read: positions >= L must not be selected
-    parity_topk(S, np.array(lens, np.int32), k, what=f"edges k={k}")
+    parity_topk(S, np.array(lens, np.int32), k, what=f"edges k={k}", force_kernel=kernel)
 
 
+@pytest.mark.parametrize("kernel", KERNELS)
 @pytest.mark.parametrize("ft", [256, 512])
 @pytest.mark.parametrize("fc", [1, 2, 4, 8, 16])
-def test_forced_plans_agree(fc, ft):
+def test_forced_plans_agree(fc, ft, kernel):
+    kw = dict(force_cluster=fc, force_threads=ft, force_kernel=kernel)
     S, L = workloads.random_rows(4, 100000, seed=9, dist="bf16", lengths="ragged", min_len=1)
-    parity_topk(S.numpy(), L.numpy(), 512, what=f"cluster {fc}x{ft}", force_cluster=fc, force_threads=ft)
-    S2, L2 = workloads.random_rows(3, 70001, seed=10, dist="special", lengths="ragged")
-    parity_topk(S2.numpy(), L2.numpy(), 300, what=f"cluster {fc}x{ft} special", force_cluster=fc,
-                force_threads=ft)
-    parity_topk(S2.numpy(), L2.numpy(), 300, what=f"cluster {fc}x{ft} special exact", force_cluster=fc,
-                force_threads=ft, force_exact=True)
+    parity_topk(S.numpy(), L.numpy(), 512, what=f"cluster {fc}x{ft}", **kw)
+    # the resident kernel also gets an unaligned stride; the streamed one needs aligned rows
+    S2, L2 = workloads.random_rows(3, 70001 if kernel == 1 else 70004, seed=10, dist="special",
+                                   lengths="ragged")
+    parity_topk(S2.numpy(), L2.numpy(), 300, what=f"cluster {fc}x{ft} special", **kw)
+    parity_topk(S2.numpy(), L2.numpy(), 300, what=f"cluster {fc}x{ft} special exact", force_exact=True, **kw)
     S3, L3 = workloads.random_rows(5, 9000, seed=11, dist="coarse", lengths="ragged")
-    parity_topk(S3.numpy(), L3.numpy(), 700, what=f"cluster {fc}x{ft} coarse", force_cluster=fc,
-                force_threads=ft)
+    parity_topk(S3.numpy(), L3.numpy(), 700, what=f"cluster {fc}x{ft} coarse", **kw)
 
 
 @pytest.mark.parametrize("ft", [256, 512])
@@ -102,19 +120,40 @@ def test_unaligned_rows_take_the_scalar_path():
     oi, ov = oracle.topk(big[:, 1:].contiguous().numpy(), None, 512)
     assert np.array_equal(idx.cpu().numpy(), oi)
     assert np.array_equal(val.cpu().numpy().view(np.uint32), ov.view(np.uint32))
+    # the streamed kernel needs 16-byte aligned rows and says so
+    with pytest.raises(lt.LtError):
+        lt.topk(s, None, 512, force_kernel=2)
 
 
+@pytest.mark.parametrize("kernel", KERNELS)
 @pytest.mark.parametrize("k", [1000, 2048])
-def test_large_k(k):
+def test_large_k(k, kernel):
     S, L = workloads.random_rows(3, 262144, seed=12, dist="bf16", lengths="ragged", min_len=1000)
-    parity_topk(S.numpy(), L.numpy(), k, what=f"k={k}")
+    parity_topk(S.numpy(), L.numpy(), k, what=f"k={k}", force_kernel=kernel)
 
 
-def test_rows_longer_than_one_register_pass():
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_rows_longer_than_one_register_pass(kernel):
     S, L = workloads.random_rows(2, 1048576, seed=13, dist="normal")
-    parity_topk(S.numpy(), None, 512, what="1M positions")
+    parity_topk(S.numpy(), None, 512, what="1M positions", force_kernel=kernel)
     S, L = workloads.random_rows(2, 600000, seed=14, dist="tail", lengths="ragged")
-    parity_topk(S.numpy(), L.numpy(), 512, what="600K ragged", force_cluster=4)
+    parity_topk(S.numpy(), L.numpy(), 512, what="600K ragged", force_cluster=4, force_kernel=kernel)
+
+
+@pytest.mark.parametrize("ft", [256, 512])
+def test_streamed_rows_walk_more_rows_than_ctas(ft):
+    """Persistent CTAs: many short and empty rows, several rows per CTA, chunks of
+    the next row in flight while a row is selected."""
+    import sparse_attention_indexer_lt_gb300 as lt
+    rows = 1500
+    S, L = workloads.random_rows(rows, 6000, seed=16, dist="bf16", lengths="ragged", min_len=0)
+    L = L.numpy().copy()
+    L[::7] = 0
+    c = counters()
+    parity_topk(S.numpy(), L, 256, what=f"walk {ft}", force_kernel=2, force_threads=ft, counters=c)
+    pl = lt.plan(rows, 6000, 256, force_kernel=2, force_threads=ft)
+    assert pl["kernel"] == "stream" and pl["grid"] < rows and pl["stages"] >= 2
+    assert c.cpu().numpy()[4] == 0
 
 
 def test_determinism_repeated_runs():
