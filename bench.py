@@ -85,12 +85,21 @@ def barrier(world):
 
 
 def max_over_ranks(x: float, world: int) -> float:
+    """The slowest rank's time (every rank gets it)."""
     if world == 1:
         return x
     import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def whole_job_us_per_row(max_total_ms: float, steps: int, rows_per_rank: int, world: int) -> float:
+    """Replicas: every rank runs `steps` steps of `rows_per_rank` rows; the job's
+    time is the slowest rank's, so the whole-job figure is that time over all
+    rows processed by all ranks."""
+    return max_total_ms * 1000.0 / (steps * rows_per_rank * world)
 
 
 # ------------------------------------------------------------------ clocks
@@ -260,7 +269,7 @@ def bench_ours(args, world, rank):
         ttk = bench_torch_topk(base, w.k, args, world)
     clocks = clk.summary()
     total_ms = max_over_ranks(total_ms, world)
-    us_per_row = total_ms * 1000.0 / (args.steps * w.rows * world)
+    us_per_row = whole_job_us_per_row(total_ms, args.steps, w.rows, world)
     kern_ms = total_ms / args.steps  # average launch duration over the timed region
     achieved = (4 * w.row_stride * w.rows) / (kern_ms * 1e-3) / 1e9
     traffic = profile_traffic("topk_kernel", HEADLINE)
