@@ -377,7 +377,8 @@ def bench_only(args, world):
         if w.blocked:
             lt.topk_blocked(c, ld, w.block, w.k_blocks, w.k, out_idx=oi, out_val=ov, out_blocks=ob)
         else:
-            lt.topk(c, ld, w.k, out_idx=oi, out_val=ov, force_kernel=KERNEL_IDS[args.kernel])
+            lt.topk(c, ld, w.k, out_idx=oi, out_val=ov, force_kernel=KERNEL_IDS[args.kernel],
+                    force_cluster=args.force_cluster, force_threads=args.force_threads)
 
     total_ms = timed_steps(step, args.steps, args.warmup, world)
     kern = total_ms / args.steps
@@ -385,7 +386,9 @@ def bench_only(args, world):
             "read_bytes": nbytes,
             "hbm_gbs": round(nbytes / (kern * 1e-3) / 1e9, 1), "copies": ncopies,
             "plan": lt.plan(w.rows, w.row_stride, w.k, blocked=w.blocked, k_blocks=w.k_blocks,
-                            force_kernel=0 if w.blocked else KERNEL_IDS[args.kernel])}
+                            force_kernel=0 if w.blocked else KERNEL_IDS[args.kernel],
+                            force_cluster=0 if w.blocked else args.force_cluster,
+                            force_threads=0 if w.blocked else args.force_threads)}
 
 
 TRACE_NAMES = ["start", "hist", "merge", "estimate", "filter", "exchange", "exact", "output",

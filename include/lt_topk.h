@@ -93,6 +93,11 @@ lt_status lt_topk(const float* scores, const int32_t* lengths, int32_t rows, int
  *   block     4, 8, 16 or 32 (the pages use 8)
  *   k_blocks  1 <= k_blocks <= LT_MAX_K
  *   k         1 <= k <= LT_MAX_K
+ *
+ * With k_blocks >= k every block holding one of the row's plain top-k
+ * positions is kept, so stage B equals the plain top-k of the row; the
+ * library then computes the two stages independently, side by side (same
+ * results, bit for bit).
  */
 lt_status lt_topk_blocked(const float* scores, const int32_t* lengths, int32_t rows,
                           int64_t row_stride, int32_t block, int32_t k_blocks, int32_t k,
@@ -128,7 +133,9 @@ lt_status lt_topk_blocked(const float* scores, const int32_t* lengths, int32_t r
  *                  [4] rows of the streamed kernel during which a wait for a
  *                  bulk copy gave up after its poll limit (a hardware fault;
  *                  that row's output is undefined -- never seen in practice).
- *                  For the two-level call, each row counts once per stage.
+ *                  For the two-level call, each row counts once per stage
+ *                  (with k_blocks >= k and out_blocks NULL, only stage B
+ *                  runs: once).
  *   trace          NULL, or device int64[grid CTAs * 16] receiving, from
  *                  thread 0 of each CTA, global-timer nanoseconds at phase
  *                  boundaries (entry, sample histogram, first cluster merge,

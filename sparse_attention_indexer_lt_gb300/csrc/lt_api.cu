@@ -276,7 +276,11 @@ lt_status make_stream_plan(int32_t rows, int64_t row_stride, int32_t k, int32_t 
   } else {
     while (c < 16 && (int64_t)rows * 2 * c <= slots_total && (int64_t)c * 2 * chunk_pos < row_stride) c *= 2;
   }
-  const uint32_t budget = (uint32_t)(di->smem_per_sm / cps - di->smem_reserved);
+  // shared memory per CTA: the SM's share when several CTAs per SM are
+  // wanted; the whole opt-in amount when the grid is one CTA per SM anyway
+  const bool sparse = (int64_t)rows * c <= di->sms;
+  const uint32_t budget = sparse ? (uint32_t)di->smem_optin
+                                 : (uint32_t)(di->smem_per_sm / cps - di->smem_reserved);
   for (;;) {
     uint32_t seg = base_cap;
     if (c > 1) {
@@ -410,12 +414,19 @@ lt_status lt_topk_blocked_ex(const float* scores, const int32_t* lengths, int32_
   if (block < 1 || k_blocks < 1) return LT_ERR_INVALID_ARG;
   if (k_blocks > LT_MAX_K || block_index(block) < 0) return LT_ERR_UNSUPPORTED;
   if (rows == 0) return LT_OK;
+  // k_blocks >= k: stage B equals the plain top-k, so the stages run as two
+  // independent groups of clusters (see lt_blocked.cuh); the stage-A group
+  // exists only when the kept blocks are wanted.
+  const bool split = k_blocks >= k;
+  const int groups = (split && out_blocks != nullptr) ? 2 : 1;
+  if ((int64_t)rows * groups > 0x7fffffffLL) return LT_ERR_UNSUPPORTED;
   Plan plan;
   int dev = 0;
-  st = make_plan(rows, row_stride, k, true, block, k_blocks, force_cluster, force_threads, LT_KERNEL_AUTO,
-                 aligned16(scores, row_stride), &plan, &dev);
+  st = make_plan(rows * groups, row_stride, k, true, block, k_blocks, force_cluster, force_threads,
+                 LT_KERNEL_AUTO, aligned16(scores, row_stride), &plan, &dev);
   if (st != LT_OK) return st;
   lt::Params p = {};
+  p.split = split ? 1 : 0;
   p.scores = scores;
   p.lengths = lengths;
   p.row_stride = row_stride;
@@ -451,7 +462,11 @@ lt_status lt_topk_plan(int32_t rows, int64_t row_stride, int32_t k, int32_t bloc
   if (blocked && (k_blocks < 1 || k_blocks > LT_MAX_K)) return LT_ERR_INVALID_ARG;
   Plan plan;
   int dev = 0;
-  lt_status st = make_plan(rows, row_stride, k, blocked != 0, blocked ? block : 4, blocked ? k_blocks : 1,
+  // the two-level call with k_blocks >= k launches two groups of clusters
+  // (plain top-k, stage A) when kept blocks are wanted, as assumed here
+  const int groups = (blocked && k_blocks >= k) ? 2 : 1;
+  if ((int64_t)rows * groups > 0x7fffffffLL) return LT_ERR_UNSUPPORTED;
+  lt_status st = make_plan(rows * groups, row_stride, k, blocked != 0, blocked ? block : 4, blocked ? k_blocks : 1,
                            force_cluster, force_threads, force_kernel, aligned != 0 && row_stride % 4 == 0,
                            &plan, &dev);
   if (st != LT_OK) return st;

@@ -9,6 +9,15 @@ namespace lt {
 // key of the block's best score), ties by lowest block id; stage B selects the
 // top k positions inside the kept blocks, ties by lowest position. The kept
 // block ids are also written in ascending order.
+//
+// With k_blocks >= k the stages are independent: every block holding one of
+// the row's plain top-k positions is kept (each block ranked above it has its
+// own maximum, a distinct position ranked above that position, so fewer than
+// k blocks rank above it), hence stage B returns exactly the plain top-k. The
+// launch then holds two groups of clusters (split): group 1 (clusters
+// [0, rows)) computes the plain top-k of its row, group 2 (clusters
+// [rows, 2 rows), launched only when out_blocks is wanted) stage A alone. Both
+// read the row once, side by side, instead of one stage after the other.
 template <int T, int W>
 __global__ void __launch_bounds__(T, (T <= 256 ? 3 : 1)) blocked_kernel(Params p) {
   constexpr int U0 = T <= 256 ? 4 : 8;  // float4 per thread per round
@@ -17,10 +26,22 @@ __global__ void __launch_bounds__(T, (T <= 256 ? 3 : 1)) blocked_kernel(Params p
   extern __shared__ __align__(128) unsigned char smem[];
   Row R;
   stamp(p, kTrStart);
-  setup_row<T, U, W>(R, p, smem);
+  const int64_t cid = (int64_t)(blockIdx.x / (p.clustered ? cluster_size() : 1u));
+  const int role = p.split ? (cid < p.rows ? 1 : 2) : 0;  // 0: both stages in turn
+  setup_row<T, U, W>(R, p, smem, p.split ? cid % p.rows : cid);
   Misc* m = R.m;
   float4 va[U], vb[U];
   int na[G::kSlots], nb[G::kSlots];
+  if (role == 1) {
+    const uint32_t K = (uint32_t)(R.L < (int64_t)p.k ? R.L : (int64_t)p.k);
+    bool intact;
+    uint64_t Tc;
+    const bool exact = select_stage<T, U, W, false>(R, p, va, na, vb, nb, false, K, R.L, p.row_stride, KeepAll{},
+                                                    true, &intact, &Tc, kTrStageB);
+    output_positions<T>(R, p, exact, Tc, K, p.row_stride);
+    wait_init(R);
+    return;
+  }
   const int64_t nblocks = (R.L + W - 1) / W;
   const uint32_t KA = (uint32_t)(nblocks < (int64_t)p.k_blocks ? nblocks : (int64_t)p.k_blocks);
 
@@ -49,42 +70,76 @@ __global__ void __launch_bounds__(T, (T <= 256 ? 3 : 1)) blocked_kernel(Params p
   const uint32_t n_before = block_sum<T>(before, m);
   const uint32_t ncand = block_sum<T>(ncand_part, m);
   if (p.out_blocks) {
-    uint32_t* ids = R.hist;  // own kept ids as ~id, so a descending sort is ascending
-    if (threadIdx.x == 0) m->own_count = 0;
-    __syncthreads();
-    for (uint32_t base = 0; base < KA; base += T) {
-      const uint32_t i = base + threadIdx.x;
-      uint32_t bid = 0;
-      bool mine = false;
-      if (i < KA) {
-        bid = ~(uint32_t)R.stage[i];
-        mine = (int64_t)bid >= b0 && (int64_t)bid < b1;
-      }
-      const unsigned msk = __ballot_sync(kFull, mine);
-      if (msk) {
-        const uint32_t lane = lane_id();
-        const int leader = __ffs(msk) - 1;
-        uint32_t bb = 0;
-        if ((int)lane == leader) bb = atomicAdd(&m->own_count, (uint32_t)__popc(msk));
-        bb = __shfl_sync(kFull, bb, leader);
-        const uint32_t pos = bb + (uint32_t)__popc(msk & ((1u << lane) - 1u));
-        if (mine && pos < (uint32_t)kBins) ids[pos] = ~bid;
-      }
-    }
-    __syncthreads();
-    const uint32_t n_own = m->own_count < (uint32_t)kBins ? m->own_count : (uint32_t)kBins;
-    uint32_t P = 2;
-    while (P < n_own) P <<= 1;
-    for (uint32_t i = n_own + threadIdx.x; i < P; i += T) ids[i] = 0u;
-    __syncthreads();
-    bitonic_sort_desc<T>(ids, P);
     int32_t* ob = p.out_blocks + R.row * (int64_t)p.k_blocks;
-    for (uint32_t i = threadIdx.x; i < n_own; i += T) ob[n_before + i] = (int32_t)(~ids[i]);
-    if (R.rank == 0) {
-      for (uint32_t j = KA + threadIdx.x; j < (uint32_t)p.k_blocks; j += T) ob[j] = -1;
+    const int64_t nbo = b1 - b0;
+    if (nbo <= 32 * (int64_t)kBins) {
+      // a bitmap of this CTA's kept blocks, then an ascending prefix over its
+      // words: each thread writes the ids of its own words in order
+      uint32_t* bits = R.hist;
+      const uint32_t words = (uint32_t)((nbo + 31) >> 5);
+      for (uint32_t i = threadIdx.x; i < words; i += T) bits[i] = 0u;
+      __syncthreads();
+      for (uint32_t i = threadIdx.x; i < KA; i += T) {
+        const uint32_t bid = ~(uint32_t)R.stage[i];
+        if ((int64_t)bid >= b0 && (int64_t)bid < b1) {
+          const uint32_t o = (uint32_t)((int64_t)bid - b0);
+          atomicOr(&bits[o >> 5], 1u << (o & 31u));
+        }
+      }
+      __syncthreads();
+      const uint32_t wpt = (words + T - 1) / T;
+      const uint32_t w0 = threadIdx.x * wpt;
+      const uint32_t w1 = min(w0 + wpt, words);
+      uint32_t cnt = 0;
+      for (uint32_t w = w0; w < w1; ++w) cnt += (uint32_t)__popc(bits[w]);
+      uint32_t out = n_before + block_prefix_excl<T>(cnt, m);
+      for (uint32_t w = w0; w < w1; ++w)
+        for (uint32_t x = bits[w]; x; x &= x - 1u)
+          ob[out++] = (int32_t)(b0 + 32 * (int64_t)w + (__ffs(x) - 1));
+      if (R.rank == 0) {
+        for (uint32_t j = KA + threadIdx.x; j < (uint32_t)p.k_blocks; j += T) ob[j] = -1;
+      }
+    } else {
+      uint32_t* ids = R.hist;  // own kept ids as ~id, so a descending sort is ascending
+      if (threadIdx.x == 0) m->own_count = 0;
+      __syncthreads();
+      for (uint32_t base = 0; base < KA; base += T) {
+        const uint32_t i = base + threadIdx.x;
+        uint32_t bid = 0;
+        bool mine = false;
+        if (i < KA) {
+          bid = ~(uint32_t)R.stage[i];
+          mine = (int64_t)bid >= b0 && (int64_t)bid < b1;
+        }
+        const unsigned msk = __ballot_sync(kFull, mine);
+        if (msk) {
+          const uint32_t lane = lane_id();
+          const int leader = __ffs(msk) - 1;
+          uint32_t bb = 0;
+          if ((int)lane == leader) bb = atomicAdd(&m->own_count, (uint32_t)__popc(msk));
+          bb = __shfl_sync(kFull, bb, leader);
+          const uint32_t pos = bb + (uint32_t)__popc(msk & ((1u << lane) - 1u));
+          if (mine && pos < (uint32_t)kBins) ids[pos] = ~bid;
+        }
+      }
+      __syncthreads();
+      const uint32_t n_own = m->own_count < (uint32_t)kBins ? m->own_count : (uint32_t)kBins;
+      uint32_t P = 2;
+      while (P < n_own) P <<= 1;
+      for (uint32_t i = n_own + threadIdx.x; i < P; i += T) ids[i] = 0u;
+      __syncthreads();
+      bitonic_sort_desc<T>(ids, P);
+      for (uint32_t i = threadIdx.x; i < n_own; i += T) ob[n_before + i] = (int32_t)(~ids[i]);
+      if (R.rank == 0) {
+        for (uint32_t j = KA + threadIdx.x; j < (uint32_t)p.k_blocks; j += T) ob[j] = -1;
+      }
     }
   }
   __syncthreads();
+  if (role == 2) {
+    wait_init(R);
+    return;
+  }
 
   // ---- stage B: the top k among the positions of the kept blocks
   const uint32_t KB = ncand < (uint32_t)p.k ? ncand : (uint32_t)p.k;

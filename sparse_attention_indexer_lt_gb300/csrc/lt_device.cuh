@@ -56,6 +56,7 @@ constexpr int kBins = 2048;       // 11-bit digits / linear buckets
 constexpr int kMaxCluster = 16;
 constexpr int kMaxWarps = 32;
 constexpr int kMaxBucket = 64;    // largest bucket ranked by counting
+constexpr int kOutBuckets = 1024; // linear key buckets of the ordered output
 constexpr unsigned kFull = 0xffffffffu;
 // A second 11-bit level refines the sampled threshold only when the first
 // predicts more candidates than this fraction of the candidate capacity.
@@ -98,6 +99,7 @@ struct Params {
   int32_t vec_ok;       // every row start is 16-byte aligned
   int32_t clustered;    // launched with cluster size > 1
   int32_t ring_stages;  // streamed kernel: shared-memory ring stages
+  int32_t split;        // two-level kernel: stages run as independent cluster groups
 };
 
 // ------------------------------------------------------------------ smem layout
@@ -110,7 +112,10 @@ struct Misc {
   uint32_t res_digit, res_above, res_cnt, res_max;
   uint32_t kmin, kmax;   // candidate key range (bucket select)
   uint32_t nseg, shift;  // current candidate layout: nseg segments of 1 << shift slots
+  uint32_t local_min, local_max;  // key range of this CTA's candidates (fast path)
   uint32_t seg_cnt[kMaxCluster];  // entries in each segment (may exceed the segment: overflow)
+  uint32_t seg_min[kMaxCluster];  // key range of each segment's entries
+  uint32_t seg_max[kMaxCluster];
   uint32_t peer_base[kMaxCluster];
   uint32_t warp_a[kMaxWarps];
   uint32_t warp_b[kMaxWarps];
@@ -336,6 +341,23 @@ __device__ __forceinline__ uint32_t block_suffix_excl(uint32_t tot, Misc* m) {
   for (int w = 1; w < NW; ++w)
     if (w > (int)warp) after += m->warp_a[w];
   return after + (incl - tot);
+}
+
+// Exclusive prefix sum over threads of per-thread values (the sum over threads
+// with a smaller index). One __syncthreads; the caller must __syncthreads
+// before warp_a is written again.
+template <int T>
+__device__ __forceinline__ uint32_t block_prefix_excl(uint32_t x, Misc* m) {
+  constexpr int NW = T / 32;
+  const uint32_t lane = lane_id(), warp = threadIdx.x >> 5;
+  const uint32_t incl = warp_incl_scan(x);
+  if (lane == 31) m->warp_a[warp] = incl;
+  __syncthreads();
+  uint32_t before = 0;
+#pragma unroll
+  for (int w = 0; w < NW - 1; ++w)
+    if (w < (int)warp) before += m->warp_a[w];
+  return before + incl - x;
 }
 
 // Find digit d with suffix(d + 1) < r <= suffix(d), suffix(d) = sum of bins[b >= d].

@@ -197,6 +197,8 @@ __device__ __forceinline__ void setup_row(Row& R, const Params& p, unsigned char
   if (threadIdx.x == 0) {
     m->cand_count = 0;
     m->local_count = 0;
+    m->local_min = 0xffffffffu;
+    m->local_max = 0u;
     m->flags = 0;
     m->own_count = 0;
   }
@@ -324,8 +326,13 @@ __device__ __forceinline__ void exchange_segments(Row& R) {
     m->nseg = R.nclus;
     m->shift = R.seg_shift;
   }
+  const uint32_t kmn = m->local_min, kmx = m->local_max;
   if (R.nclus == 1) {
-    if (threadIdx.x == 0) m->seg_cnt[0] = n;
+    if (threadIdx.x == 0) {
+      m->seg_cnt[0] = n;
+      m->seg_min[0] = kmn;
+      m->seg_max[0] = kmx;
+    }
     __syncthreads();
     return;
   }
@@ -333,7 +340,11 @@ __device__ __forceinline__ void exchange_segments(Row& R) {
   const uint32_t seg = 1u << R.seg_shift;
   const uint32_t n_put = n < seg ? n : seg;
   const uint32_t off = R.rank << R.seg_shift;
-  if (threadIdx.x < R.nclus) dsmem_st_u32(peer_addr(smem_addr(&m->seg_cnt[R.rank]), threadIdx.x), n);
+  if (threadIdx.x < R.nclus) {
+    dsmem_st_u32(peer_addr(smem_addr(&m->seg_cnt[R.rank]), threadIdx.x), n);
+    dsmem_st_u32(peer_addr(smem_addr(&m->seg_min[R.rank]), threadIdx.x), kmn);
+    dsmem_st_u32(peer_addr(smem_addr(&m->seg_max[R.rank]), threadIdx.x), kmx);
+  }
   const uint2* mine = R.cand + off;
   const uint32_t src = smem_addr(R.cand) + 8u * off;
   // (peer, entry) pairs flattened over the threads; peers rank+1 .. rank+nclus-1
@@ -421,6 +432,7 @@ __device__ __forceinline__ void filter_round(Row& R, int r, const float4 (&v)[U]
   const uint32_t excl = incl - c;
   const float* stf = reinterpret_cast<const float*>(R.wst);
   const uint32_t wbase = threadIdx.x & ~31u;
+  uint32_t kmn = 0xffffffffu, kmx = 0u;
   for (uint32_t k0 = 0; k0 < total; k0 += 32) {
     const uint32_t k = k0 + lane;
     const uint32_t kq = k < total ? k : total - 1;
@@ -440,8 +452,17 @@ __device__ __forceinline__ void filter_round(Row& R, int r, const float4 (&v)[U]
       const int s = (int)(f / G::kVS), j = (int)(f % G::kVS);
       const int64_t pos = R.begin + (int64_t)(wbase + owner) * W + (int64_t)(r + R.rounds * s) * G::kTile +
                           4 * j + e;
-      if (base + k < cap) list[base + k] = make_uint2(key_of(x), (uint32_t)pos);
+      const uint32_t kk = key_of(x);
+      kmn = min(kmn, kk);
+      kmx = max(kmx, kk);
+      if (base + k < cap) list[base + k] = make_uint2(kk, (uint32_t)pos);
     }
+  }
+  kmn = __reduce_min_sync(kFull, kmn);
+  kmx = __reduce_max_sync(kFull, kmx);
+  if (lane == 0) {
+    atomicMin(&R.m->local_min, kmn);
+    atomicMax(&R.m->local_max, kmx);
   }
   __syncwarp();
 }
@@ -619,48 +640,56 @@ __device__ __noinline__ void sorted_fallback(Row R, bool exact, uint64_t Tc, uin
 
 // Select the top K of the valid candidates and write them in order (see step
 // 4 at the top of lt_device.cuh). Returns false, having written nothing, when
-// some bucket holds more than kMaxBucket candidates. Expects kmin, kmax and
+// some bucket holds more than kMaxBucket candidates. With have_range the
+// caller knows the candidates' key range [lo, hi] and count N and the
+// histogram is already zero (the fast path clears it before the filter and
+// the exchange's barrier follows); otherwise one pass finds them. Expects
 // res_max reset.
 template <int T>
 __device__ __forceinline__ bool bucket_select_sort(Row& R, uint32_t K, uint32_t kout, int32_t* oi, float* ov,
-                                                   OwnSlice owner) {
-  constexpr int BPT = kBins / T;
+                                                   OwnSlice owner, bool have_range, uint32_t lo, uint32_t hi,
+                                                   uint32_t N) {
+  constexpr int NB = kOutBuckets;
+  constexpr int BPT = NB / T;
+  static_assert(NB % T == 0 && NB <= kBins, "bucket count");
   Misc* m = R.m;
-  // key range and count of the candidates (and a zeroed histogram)
-  uint32_t lo = 0xffffffffu, hi = 0u, nloc = 0;
-  for_each_cand<T>(R, [&](uint2 e) {
-    lo = min(lo, e.x);
-    hi = max(hi, e.x);
-    ++nloc;
-  });
-  nloc = __reduce_add_sync(kFull, nloc);
-  lo = __reduce_min_sync(kFull, lo);
-  hi = __reduce_max_sync(kFull, hi);
-  if (lane_id() == 0) {
-    atomicMin(&m->kmin, lo);
-    atomicMax(&m->kmax, hi);
-    atomicAdd(&m->aux[1], nloc);
+  if (!have_range) {
+    uint32_t l = 0xffffffffu, h = 0u, nloc = 0;
+    for_each_cand<T>(R, [&](uint2 e) {
+      l = min(l, e.x);
+      h = max(h, e.x);
+      ++nloc;
+    });
+    nloc = __reduce_add_sync(kFull, nloc);
+    l = __reduce_min_sync(kFull, l);
+    h = __reduce_max_sync(kFull, h);
+    if (lane_id() == 0) {
+      atomicMin(&m->kmin, l);
+      atomicMax(&m->kmax, h);
+      atomicAdd(&m->aux[1], nloc);
+    }
+    {
+      uint4* z = reinterpret_cast<uint4*>(R.hist);
+      for (int i = threadIdx.x; i < NB / 4; i += T) z[i] = make_uint4(0, 0, 0, 0);
+    }
+    __syncthreads();
+    lo = m->kmin;
+    hi = m->kmax;
+    N = m->aux[1];
   }
-  {
-    uint4* z = reinterpret_cast<uint4*>(R.hist);
-    for (int i = threadIdx.x; i < kBins / 4; i += T) z[i] = make_uint4(0, 0, 0, 0);
-  }
-  __syncthreads();
-  lo = m->kmin;
-  hi = m->kmax;
-  const uint32_t N = m->aux[1];
   if (hi == lo && N > (uint32_t)kMaxBucket) return false;
-  const float scale = (float)kBins / ((float)(hi - lo) + 1.0f);
+  const float scale = (float)NB / ((float)(hi - lo) + 1.0f);
   auto bucket = [lo, scale](uint32_t key) -> uint32_t {
     const uint32_t b = (uint32_t)((float)(key - lo) * scale);
-    return b > (uint32_t)(kBins - 1) ? (uint32_t)(kBins - 1) : b;
+    return b > (uint32_t)(NB - 1) ? (uint32_t)(NB - 1) : b;
   };
   for_each_cand<T>(R, [&](uint2 e) { atomicAdd(&R.hist[bucket(e.x)], 1u); });
   __syncthreads();
   // exclusive suffix starts -> aux; the bucket b* holding the K-th item; the
   // largest bucket
   uint32_t v[BPT];
-  load_bins<T>(R.hist, v);
+#pragma unroll
+  for (int j = 0; j < BPT; ++j) v[j] = R.hist[threadIdx.x * BPT + j];
   uint32_t tot = 0, mx = 0;
 #pragma unroll
   for (int j = 0; j < BPT; ++j) {
@@ -697,10 +726,10 @@ __device__ __forceinline__ bool bucket_select_sort(Row& R, uint32_t K, uint32_t 
     const uint64_t c = R.stage[i];
     if (!owner(~(uint32_t)c)) continue;
     const uint32_t b = bucket((uint32_t)(c >> 32));
-    const uint32_t e = R.aux[b], s = e - R.hist[b];
+    const uint32_t e = R.aux[b], s0 = e - R.hist[b];
     uint32_t r = 0;
-    for (uint32_t j = s; j < e; ++j) r += (R.stage[j] > c) ? 1u : 0u;
-    const uint32_t rank = s + r;
+    for (uint32_t j = s0; j < e; ++j) r += (R.stage[j] > c) ? 1u : 0u;
+    const uint32_t rank = s0 + r;
     if (rank < K) write_slot(oi, ov, rank, c, R.rowp);
   }
   write_padding<T>(R, oi, ov, K, kout);
@@ -857,6 +886,8 @@ __device__ __forceinline__ bool select_stage(Row& R, const Params& p, float4 (&c
     __syncthreads();
     if (threadIdx.x == 0) {
       m->local_count = 0;
+      m->local_min = 0xffffffffu;
+      m->local_max = 0u;
       m->cand_count = 0;
     }
     __syncthreads();
@@ -946,6 +977,12 @@ __device__ __forceinline__ bool select_stage(Row& R, const Params& p, float4 (&c
       }
     }
     stamp(R, tr + kTrEstimate);
+    {
+      // the output's bucket counts start from zero; the exchange's barrier
+      // orders these stores before them
+      uint4* z = reinterpret_cast<uint4*>(R.hist);
+      for (int i = threadIdx.x; i < kOutBuckets / 4; i += T) z[i] = make_uint4(0, 0, 0, 0);
+    }
     // ---- filter every round against the threshold
     const bool all = (t == 0u);
     const float g = threshold_float(all ? 1u : t);
@@ -1012,7 +1049,20 @@ __device__ __forceinline__ void output_positions(Row& R, const Params& p, bool e
     write_padding<T>(R, oi, ov, 0, kout);
   } else {
     const OwnSlice own = own_slice(R);
-    if (!bucket_select_sort<T>(R, K, kout, oi, ov, own))
+    // fast path: the filter recorded each segment's key range and count
+    const Misc* m = R.m;
+    uint32_t lo = 0xffffffffu, hi = 0u, n = 0;
+    if (!exact) {
+      const uint32_t seg = 1u << m->shift;
+      for (uint32_t q = 0; q < m->nseg; ++q) {
+        const uint32_t c = m->seg_cnt[q];
+        if (c == 0) continue;
+        n += min(c, seg);
+        lo = min(lo, m->seg_min[q]);
+        hi = max(hi, m->seg_max[q]);
+      }
+    }
+    if (!bucket_select_sort<T>(R, K, kout, oi, ov, own, !exact, lo, hi, n))
       sorted_fallback<T>(R, exact, Tc, K, kout, oi, ov, idx_limit, own);
   }
   stamp(R, kTrOutput);

@@ -295,15 +295,24 @@ __device__ __forceinline__ void filter_chunk(Row& R, const float* buf, int c, in
     }
     mask |= b << (4 * u);
   }
-  if (mask == 0) return;
-  uint32_t slot = atomicAdd(counter, (uint32_t)__popc(mask));
-  for (; mask; mask &= mask - 1u, ++slot) {
-    const uint32_t bit = (uint32_t)(__ffs(mask) - 1);
-    const uint32_t f = threadIdx.x + T * (bit >> 2), e = bit & 3u;
-    if (slot < cap) {
-      const float x = buf[4 * f + e];
-      list[slot] = make_uint2(key_of(x), (uint32_t)(R.begin + (int64_t)(chunk_rel(c, rounds, f) + e)));
+  if (__ballot_sync(kFull, mask != 0) == 0) return;
+  uint32_t kmn = 0xffffffffu, kmx = 0u;
+  if (mask) {
+    uint32_t slot = atomicAdd(counter, (uint32_t)__popc(mask));
+    for (; mask; mask &= mask - 1u, ++slot) {
+      const uint32_t bit = (uint32_t)(__ffs(mask) - 1);
+      const uint32_t f = threadIdx.x + T * (bit >> 2), e = bit & 3u;
+      const uint32_t kk = key_of(buf[4 * f + e]);
+      kmn = min(kmn, kk);
+      kmx = max(kmx, kk);
+      if (slot < cap) list[slot] = make_uint2(kk, (uint32_t)(R.begin + (int64_t)(chunk_rel(c, rounds, f) + e)));
     }
+  }
+  kmn = __reduce_min_sync(kFull, kmn);
+  kmx = __reduce_max_sync(kFull, kmx);
+  if (lane_id() == 0) {
+    atomicMin(&R.m->local_min, kmn);
+    atomicMax(&R.m->local_max, kmx);
   }
 }
 
@@ -378,6 +387,12 @@ __device__ __forceinline__ void stream_row(Row& R, const Params& p, uint64_t* ba
       }
     }
     stamp(R, kTrEstimate);
+    {
+      // the output's bucket counts start from zero; the exchange's barrier
+      // orders these stores before them
+      uint4* z = reinterpret_cast<uint4*>(R.hist);
+      for (int i = threadIdx.x; i < kOutBuckets / 4; i += T) z[i] = make_uint4(0, 0, 0, 0);
+    }
     const bool all = (t == 0u);
     const float g = threshold_float(all ? 1u : t);
 #pragma unroll 1
