@@ -169,6 +169,8 @@ typedef struct lt_plan_info {
   int32_t smem_bytes;       /* dynamic shared memory per CTA */
   int32_t grid_ctas;        /* CTAs launched (streamed: persistent, rows grid-stride) */
   int32_t ring_stages;      /* streamed kernel: shared-memory ring stages, else 0 */
+  int32_t one_round;        /* register-resident top-k: every CTA's slice is one
+                               register round (the compact single-round variant) */
 } lt_plan_info;
 lt_status lt_topk_plan(int32_t rows, int64_t row_stride, int32_t k, int32_t blocked,
                        int32_t block, int32_t k_blocks, int32_t force_cluster,

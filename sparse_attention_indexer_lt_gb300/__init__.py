@@ -30,7 +30,8 @@ class PlanInfo(ctypes.Structure):
     """Mirror of lt_plan_info."""
     _fields_ = [("kernel", ctypes.c_int32), ("cluster_size", ctypes.c_int32),
                 ("threads_per_cta", ctypes.c_int32), ("smem_bytes", ctypes.c_int32),
-                ("grid_ctas", ctypes.c_int32), ("ring_stages", ctypes.c_int32)]
+                ("grid_ctas", ctypes.c_int32), ("ring_stages", ctypes.c_int32),
+                ("one_round", ctypes.c_int32)]
 
 
 class LtError(RuntimeError):
@@ -188,7 +189,8 @@ def topk_blocked(scores: torch.Tensor, lengths: torch.Tensor | None = None, bloc
 def plan(rows: int, row_stride: int, k: int, *, blocked: bool = False, block: int = 8,
          k_blocks: int = 2048, force_cluster: int = 0, force_threads: int = 0,
          force_kernel: int = KERNEL_AUTO, aligned: bool = True, device: int | None = None) -> dict:
-    """The launch the planner would make: {'kernel', 'cluster', 'threads', 'smem', 'grid', 'stages'}."""
+    """The launch the planner would make: {'kernel', 'cluster', 'threads', 'smem', 'grid', 'stages',
+    'one_round'}."""
     lib = load()
     info = PlanInfo()
     with torch.cuda.device(device if device is not None else torch.cuda.current_device()):
@@ -199,4 +201,4 @@ def plan(rows: int, row_stride: int, k: int, *, blocked: bool = False, block: in
         raise LtError("lt_topk_plan", st)
     return {"kernel": _KERNEL_NAMES.get(info.kernel, str(info.kernel)), "cluster": info.cluster_size,
             "threads": info.threads_per_cta, "smem": info.smem_bytes, "grid": info.grid_ctas,
-            "stages": info.ring_stages}
+            "stages": info.ring_stages, "one_round": bool(info.one_round)}

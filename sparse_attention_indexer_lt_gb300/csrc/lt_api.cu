@@ -29,7 +29,7 @@ constexpr int kMaxDevices = 64;
 constexpr int kWideThreads = 512;
 constexpr int kNarrowThreads = 256;
 constexpr int64_t kWideRound = 512 * 8 * 4;  // positions per CTA per round (wide)
-constexpr int kSlots = 12;                    // kernel variants
+constexpr int kSlots = 14;                    // kernel variants
 // the streamed kernel's launch bounds: CTAs per SM for 256 / 512 threads
 constexpr int stream_ctas_per_sm(int threads) { return threads == 256 ? 3 : 2; }
 constexpr int kStreamMaxStages = 8;
@@ -57,10 +57,10 @@ int block_index(int block) {
   }
 }
 
-int kernel_slot(bool blocked, int block, int threads, bool stream = false) {
+int kernel_slot(bool blocked, int block, int threads, bool stream = false, bool one_round = false) {
   const int wide = threads == kWideThreads ? 1 : 0;
   if (stream) return 10 + wide;
-  if (!blocked) return wide;
+  if (!blocked) return (one_round ? 12 : 0) + wide;
   const int b = block_index(block);
   return b < 0 ? -1 : 2 + 2 * b + wide;
 }
@@ -76,6 +76,7 @@ struct Plan {
   int cluster = 1;
   int threads = kNarrowThreads;
   int grid = 0;             // CTAs launched
+  bool one_round = false;   // top-k: every slice fits one register round
   uint32_t stages = 0;      // streamed kernel: ring stages
   uint32_t cap = 0;        // candidate slots: cluster * (1 << seg_shift)
   uint32_t seg_shift = 0;  // log2 of the slots each CTA of the cluster may fill
@@ -192,10 +193,22 @@ lt_status make_plan(int32_t rows, int64_t row_stride, int32_t k, bool blocked, i
 
   int threads = force_threads;
   if (threads == 0) threads = (int64_t)rows >= di->sms ? kNarrowThreads : kWideThreads;
-  const int slot = kernel_slot(blocked, block, threads);
-  if (slot < 0) return LT_ERR_UNSUPPORTED;
+  if (kernel_slot(blocked, block, threads) < 0) return LT_ERR_UNSUPPORTED;
   plan->threads = threads;
-  plan->func = blocked ? lt::blocked_kernel_ptr(threads, block) : lt::topk_kernel_ptr(threads);
+  // the top-k kernel has a variant for slices of one register round
+  auto pick = [&](int c, int* slot) -> const void* {
+    if (blocked) {
+      *slot = kernel_slot(true, block, threads);
+      return lt::blocked_kernel_ptr(threads, block);
+    }
+    int64_t per = (row_stride + c - 1) / c;
+    per = (per + 3) & ~(int64_t)3;
+    plan->one_round = per <= lt::topk_round_positions(threads);
+    *slot = kernel_slot(false, 4, threads, false, plan->one_round);
+    return lt::topk_kernel_ptr(threads, plan->one_round);
+  };
+  int slot = 0;
+  plan->func = pick(1, &slot);
   {
     // float4 loads per thread per round, as instantiated in the kernels
     int u = threads == kNarrowThreads ? 4 : 8;
@@ -219,6 +232,8 @@ lt_status make_plan(int32_t rows, int64_t row_stride, int32_t k, bool blocked, i
     while (c < 16 && (int64_t)rows * 2 * c <= di->sms && (int64_t)c * kWideRound < row_stride) c *= 2;
   }
   for (;;) {
+    plan->func = pick(c, &slot);
+    if (!plan->func) return LT_ERR_UNSUPPORTED;
     uint32_t seg = base_cap;
     if (c > 1) {
       seg = next_pow2((base_cap + (uint32_t)c - 1) / (uint32_t)c);
@@ -476,6 +491,7 @@ lt_status lt_topk_plan(int32_t rows, int64_t row_stride, int32_t k, int32_t bloc
   info->smem_bytes = (int32_t)plan.smem;
   info->grid_ctas = plan.grid;
   info->ring_stages = (int32_t)plan.stages;
+  info->one_round = plan.one_round ? 1 : 0;
   return LT_OK;
 }
 
@@ -489,6 +505,6 @@ const char* lt_status_string(lt_status status) {
   }
 }
 
-int32_t lt_version(void) { return 300; }
+int32_t lt_version(void) { return 310; }
 
 }  // extern "C"

@@ -1038,6 +1038,110 @@ __device__ __forceinline__ bool select_stage(Row& R, const Params& p, float4 (&c
   return false;
 }
 
+// ------------------------------------------------------------------ single-round path
+
+template <int U, int S>
+struct RoundRegs {
+  float4 v[U];
+  int n[S];
+};
+
+// Second 11-bit level of the threshold for the single-round path: the next
+// 11 key bits of the items in first-level bin d1, merged over the cluster; r2
+// is the rank sought inside that bin. Rare (heavily populated first-level
+// bins), so it lives out of line and the common path stays compact.
+template <int T, int U, int W>
+__device__ __noinline__ uint32_t refine_level2(Row R, RoundRegs<U, Geo<T, U, W>::kSlots> rr, uint32_t d1,
+                                               uint32_t r2) {
+  zero_bins<T>(R.hist);
+  hist_round<T, U, W, 2>(R, 0, rr.v, rr.n, d1, KeepAll{});
+  const uint32_t* bins = merge_hist<T>(R, 1);
+  find_digit<T>(bins, r2, R.m);
+  const uint32_t d2 = R.m->res_digit;
+  release_merged<T>(R, 1);
+  return (d1 << 21) | (d2 << 10);
+}
+
+// Single-round path: every CTA's slice is one register round, so the sample
+// is the whole slice and its histogram is exact. The same steps as
+// select_stage (first stage, every position kept) without the second
+// register buffer, the streaming filter and the inline second estimate level:
+// the code a row executes once per CTA is what its latency pays to fetch.
+template <int T, int U, int W>
+__device__ __forceinline__ bool select_one(Row& R, const Params& p, float4 (&v)[U], int (&n)[Geo<T, U, W>::kSlots],
+                                           uint32_t K, uint64_t* Tc) {
+  using G = Geo<T, U, W>;
+  Misc* m = R.m;
+  const uint32_t seg = 1u << R.seg_shift;
+  uint2* list = R.cand + (R.rank << R.seg_shift);
+  const uint32_t cap = (uint32_t)p.cap;
+  *Tc = 0;
+  if (R.rounds > 0) load_round<T, U, W>(R, p.vec_ok != 0, 0, v, n);
+  else clear_round(n);
+
+  bool exact = p.force_exact != 0;
+  int stat = kCntFast;
+  if (!exact && K > 0) {
+    uint32_t t = 0;
+    if (R.L > (int64_t)(cap / 2)) {
+      zero_bins<T>(R.hist);
+      hist_round<T, U, W, 1>(R, 0, v, n, 0, KeepAll{});
+      stamp(R, kTrHist);
+      // K <= L: with large clusters each CTA pushes only the bins at or above
+      // its own K-th digit (the cluster's K-th key is at least as large)
+      const uint32_t* bins = merge_hist<T>(R, 0, R.nclus >= 8 ? K : 0u);
+      stamp(R, kTrMerge);
+      find_digit<T>(bins, K, m);
+      const uint32_t d1 = m->res_digit, above1 = m->res_above, cnt1 = m->res_cnt;
+      release_merged<T>(R, 0);
+      t = d1 << 21;
+      if ((float)(above1 + cnt1) > kLevel2Frac * (float)cap) {
+        RoundRegs<U, G::kSlots> rr;
+#pragma unroll
+        for (int u = 0; u < U; ++u) rr.v[u] = v[u];
+#pragma unroll
+        for (int s = 0; s < G::kSlots; ++s) rr.n[s] = n[s];
+        t = refine_level2<T, U, W>(R, rr, d1, K - above1);
+      }
+    }
+    stamp(R, kTrEstimate);
+    {
+      // the output's bucket counts start from zero; the exchange's barrier
+      // orders these stores before them
+      uint4* z = reinterpret_cast<uint4*>(R.hist);
+      for (int i = threadIdx.x; i < kOutBuckets / 4; i += T) z[i] = make_uint4(0, 0, 0, 0);
+    }
+    const bool all = (t == 0u);
+    filter_round<T, U, W>(R, 0, v, n, threshold_float(all ? 1u : t), all, &m->local_count, list, seg,
+                          KeepAll{});
+    stamp(R, kTrFilter);
+    exchange_segments<T>(R);
+    stamp(R, kTrExchange);
+    uint32_t total = 0;
+    bool overflow = false;
+    for (uint32_t q = 0; q < R.nclus; ++q) {
+      const uint32_t c = m->seg_cnt[q];
+      total += c;
+      overflow = overflow || c > seg;
+    }
+    if (overflow || total < K) {
+      exact = true;
+      stat = overflow ? kCntOverflow : kCntShort;
+    }
+  }
+  if (exact && K > 0) {
+    if (stat != kCntFast) bump(p, R, stat);
+    wait_init(R);
+    *Tc = exact_select<T, U, W, false>(R, p, K, p.row_stride, KeepAll{});
+    stamp(R, kTrExact);
+    bump(p, R, kCntExact);
+    return true;
+  }
+  stamp(R, kTrExact);
+  if (K > 0) bump(p, R, kCntFast);
+  return false;
+}
+
 // Select and write the top K positions of this row after select_stage.
 template <int T>
 __device__ __forceinline__ void output_positions(Row& R, const Params& p, bool exact, uint64_t Tc, uint32_t K,

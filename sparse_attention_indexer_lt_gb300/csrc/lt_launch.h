@@ -2,8 +2,10 @@
 #pragma once
 
 namespace lt {
-// threads is 256 (batched rows, several CTAs per SM) or 512 (few rows, one CTA per SM).
-const void* topk_kernel_ptr(int threads);
+// threads is 256 (batched rows, several CTAs per SM) or 512 (few rows, one CTA per SM);
+// one_round: the variant for slices of at most topk_round_positions(threads) positions.
+const void* topk_kernel_ptr(int threads, bool one_round);
+int64_t topk_round_positions(int threads);
 // nullptr for an unsupported block size.
 const void* blocked_kernel_ptr(int threads, int block);
 const void* blocked_kernel_ptr_narrow(int block);
