@@ -364,13 +364,18 @@ lt_status launch(const Plan& plan, const lt::Params& prm, void* stream) {
   cfg.blockDim = dim3((unsigned)plan.threads);
   cfg.dynamicSmemBytes = plan.smem;
   cfg.stream = static_cast<cudaStream_t>(stream);
-  cudaLaunchAttribute attr;
-  attr.id = cudaLaunchAttributeClusterDimension;
-  attr.val.clusterDim.x = (unsigned)plan.cluster;
-  attr.val.clusterDim.y = 1;
-  attr.val.clusterDim.z = 1;
-  cfg.attrs = &attr;
-  cfg.numAttrs = plan.cluster > 1 ? 1 : 0;
+  // programmatic dependent launch: this kernel's shared-memory setup may
+  // overlap the previous kernel of the stream; every kernel waits for that
+  // kernel's completion before it touches global memory
+  cudaLaunchAttribute attrs[2];
+  attrs[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attrs[0].val.programmaticStreamSerializationAllowed = 1;
+  attrs[1].id = cudaLaunchAttributeClusterDimension;
+  attrs[1].val.clusterDim.x = (unsigned)plan.cluster;
+  attrs[1].val.clusterDim.y = 1;
+  attrs[1].val.clusterDim.z = 1;
+  cfg.attrs = attrs;
+  cfg.numAttrs = plan.cluster > 1 ? 2 : 1;
   void* args[] = {&p};
   return cudaLaunchKernelExC(&cfg, plan.func, args) == cudaSuccess ? LT_OK : LT_ERR_CUDA;
 }

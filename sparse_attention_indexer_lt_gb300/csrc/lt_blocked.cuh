@@ -26,6 +26,7 @@ __global__ void __launch_bounds__(T, (T <= 256 ? 3 : 1)) blocked_kernel(Params p
   extern __shared__ __align__(128) unsigned char smem[];
   Row R;
   stamp(p, kTrStart);
+  grid_dependents_launch();
   const int64_t cid = (int64_t)(blockIdx.x / (p.clustered ? cluster_size() : 1u));
   const int role = p.split ? (cid < p.rows ? 1 : 2) : 0;  // 0: both stages in turn
   setup_row<T, U, W>(R, p, smem, p.split ? cid % p.rows : cid);

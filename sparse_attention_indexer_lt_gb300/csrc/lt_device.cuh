@@ -194,6 +194,21 @@ __device__ __forceinline__ void dsmem_st_v2(uint32_t addr, uint2 v) {
   asm volatile("st.shared::cluster.v2.u32 [%0], {%1, %2};" :: "r"(addr), "r"(v.x), "r"(v.y) : "memory");
 }
 
+// Programmatic dependent launch. A kernel launched with programmatic stream
+// serialization may start while the previous kernel of its stream still runs:
+// everything before grid_dependency_wait() overlaps that kernel (so it must
+// not touch global memory the previous kernel may write), and the wait returns
+// once the previous grid has completed and its writes are visible. Without the
+// launch attribute (or with no previous kernel) the wait returns at once.
+__device__ __forceinline__ void grid_dependency_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+// Lets the next kernel of the stream start launching (its CTAs still wait for
+// this grid to complete before touching global memory).
+__device__ __forceinline__ void grid_dependents_launch() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 __device__ __forceinline__ void stamp(const Params& p, int slot) {
   if (p.trace != nullptr && threadIdx.x == 0) {
     uint64_t t;

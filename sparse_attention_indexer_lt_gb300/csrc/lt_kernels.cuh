@@ -171,6 +171,29 @@ __device__ __forceinline__ void setup_row(Row& R, const Params& p, unsigned char
   R.stage_cap = (uint32_t)p.sel_cap + kMaxBucket;
   R.trace = p.trace;
   R.seg_shift = (uint32_t)p.seg_shift;
+
+  // shared-memory initialisation first: it overlaps the previous kernel of
+  // the stream under programmatic dependent launch
+  Misc* m = R.m;
+  if (threadIdx.x == 0) {
+    m->cand_count = 0;
+    m->local_count = 0;
+    m->local_min = 0xffffffffu;
+    m->local_max = 0u;
+    m->flags = 0;
+    m->own_count = 0;
+  }
+  if (p.clustered) {
+    uint4* z0 = reinterpret_cast<uint4*>(R.merged0);
+    uint4* z1 = reinterpret_cast<uint4*>(R.merged1);
+    for (int i = threadIdx.x; i < kBins / 4; i += T) {
+      z0[i] = make_uint4(0, 0, 0, 0);
+      z1[i] = make_uint4(0, 0, 0, 0);
+    }
+  }
+  // lengths, scores and the outputs may belong to the previous kernel
+  grid_dependency_wait();
+
   int64_t L = p.row_stride;
   if (p.lengths) {
     L = (int64_t)p.lengths[R.row];
@@ -192,24 +215,6 @@ __device__ __forceinline__ void setup_row(Row& R, const Params& p, unsigned char
   R.rounds = (int)((nt + G::kSlots - 1) >> kSl2);
   const int64_t ntm = (per + G::kTile - 1) >> kTile2;
   R.rounds_max = (int)((ntm + G::kSlots - 1) >> kSl2);
-
-  Misc* m = R.m;
-  if (threadIdx.x == 0) {
-    m->cand_count = 0;
-    m->local_count = 0;
-    m->local_min = 0xffffffffu;
-    m->local_max = 0u;
-    m->flags = 0;
-    m->own_count = 0;
-  }
-  if (p.clustered) {
-    uint4* z0 = reinterpret_cast<uint4*>(R.merged0);
-    uint4* z1 = reinterpret_cast<uint4*>(R.merged1);
-    for (int i = threadIdx.x; i < kBins / 4; i += T) {
-      z0[i] = make_uint4(0, 0, 0, 0);
-      z1[i] = make_uint4(0, 0, 0, 0);
-    }
-  }
   __syncthreads();
   R.init_pending = false;
   if (R.nclus > 1) {

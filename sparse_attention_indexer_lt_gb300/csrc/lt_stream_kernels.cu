@@ -25,6 +25,9 @@ __global__ void __launch_bounds__(T, kMinCtas) stream_kernel(Params p) {
     for (uint32_t i = 0; i < ns; ++i) mbar_init(&bars[i], 1);
     mbar_fence_init();
   }
+  grid_dependents_launch();
+  // the producer reads lengths and scores, which the previous kernel may write
+  grid_dependency_wait();
   Prod& P = *reinterpret_cast<Prod*>(smem + sl.prod);  // thread 0 only
   if (threadIdx.x == 0) {
     P.scores = p.scores;

@@ -13,6 +13,7 @@ __global__ void __launch_bounds__(T, (T <= 256 ? 3 : 1)) topk_kernel(Params p) {
   using G = Geo<T, U, 4>;
   Row R;
   stamp(p, kTrStart);
+  grid_dependents_launch();
   setup_row<T, U, 4>(R, p, smem);
   float4 va[U];
   int na[G::kSlots];

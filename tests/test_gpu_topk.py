@@ -178,3 +178,23 @@ def test_values_optional_and_side_stream():
     assert val is None
     oi, _ = oracle.topk(S.numpy(), None, 128)
     assert np.array_equal(idx.cpu().numpy(), oi)
+
+
+def test_dependent_launch_orders_with_neighbouring_kernels():
+    """The kernels start under programmatic dependent launch: a score row written
+    by the kernel just before must be read complete, and a kernel just after that
+    rewrites the scores must not change the result (no host synchronisation)."""
+    import oracle
+    import sparse_attention_indexer_lt_gb300 as lt
+    S, _ = workloads.random_rows(4, 262144, seed=17, dist="tail")
+    base = S.cuda()
+    for threads in (0, 256, 512):
+        scaled = base * 2.0                      # producer kernel, then top-k at once
+        idx, val = lt.topk(scaled, None, 512, force_threads=threads)
+        scaled.fill_(float("inf"))               # overwrites the scores right after
+        idx2, _ = lt.topk(base * 2.0, None, 512, force_threads=threads)  # back to back
+        torch.cuda.synchronize()
+        oi, ov = oracle.topk((S * 2.0).numpy(), None, 512)
+        assert np.array_equal(idx.cpu().numpy(), oi)
+        assert np.array_equal(val.cpu().numpy().view(np.uint32), ov.view(np.uint32))
+        assert np.array_equal(idx2.cpu().numpy(), oi)
