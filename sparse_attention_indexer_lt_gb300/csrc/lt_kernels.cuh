@@ -134,6 +134,7 @@ __device__ __forceinline__ uint32_t slot_block_key(const float4 (&v)[U], int s, 
 }
 
 struct KeepAll {
+  static constexpr bool kAll = true;
   template <class V>
   __device__ __forceinline__ bool operator()(const Row&, int, const V&, int, int) const { return true; }
 };
@@ -142,6 +143,7 @@ struct KeepAll {
 // composite is >= the stage-A threshold composite Tc.
 template <int T, int U, int W>
 struct KeepBlocks {
+  static constexpr bool kAll = false;
   uint64_t Tc;
   __device__ __forceinline__ bool operator()(const Row& R, int r, const float4 (&v)[U], int s, int nv) const {
     const uint32_t bid = (uint32_t)(slot_pos<T, U, W>(R, r, s) / W);
@@ -387,16 +389,13 @@ __device__ __forceinline__ void hist_round(Row& R, int r, const float4 (&v)[U],
   }
 }
 
-// Append every kept position whose score passes the threshold (x >= g, or
-// every valid position when `all`) to the list. Each lane builds a bit mask
-// of its passing positions; one warp scan and one shared atomic reserve the
-// warp's slots; lanes with candidates stage their round in shared memory and
-// every lane then writes one candidate (the owner lane of candidate k is
-// found by a binary search over the warp's running counts).
+// Bit mask of this lane's passing positions in round r: bit 4*f + e is
+// element e of float4 f (x >= g, or every valid position when `all`), for
+// kept slots only.
 template <int T, int U, int W, class Keep>
-__device__ __forceinline__ void filter_round(Row& R, int r, const float4 (&v)[U],
-                                             const int (&n)[Geo<T, U, W>::kSlots], float g, bool all,
-                                             uint32_t* counter, uint2* list, uint32_t cap, Keep keep) {
+__device__ __forceinline__ uint32_t round_mask(const Row& R, int r, const float4 (&v)[U],
+                                               const int (&n)[Geo<T, U, W>::kSlots], float g, bool all,
+                                               Keep keep) {
   using G = Geo<T, U, W>;
   static_assert(4 * U <= 32, "mask holds 32 positions");
   uint32_t mask = 0;
@@ -421,6 +420,18 @@ __device__ __forceinline__ void filter_round(Row& R, int r, const float4 (&v)[U]
     if (sm != 0 && !keep(R, r, v, s, ns)) sm = 0;
     mask |= sm << (4 * G::kVS * s);
   }
+  return mask;
+}
+
+// Append the positions of round r flagged in each lane's mask to the list:
+// one warp scan and one shared atomic reserve the warp's slots; lanes with
+// candidates stage their round in shared memory and every lane then writes
+// one candidate (the owner lane of candidate k is found by a binary search
+// over the warp's running counts). Records the key range of what it appends.
+template <int T, int U, int W>
+__device__ __forceinline__ void extract_round(Row& R, int r, const float4 (&v)[U], uint32_t mask,
+                                              uint32_t* counter, uint2* list, uint32_t cap) {
+  using G = Geo<T, U, W>;
   const uint32_t lane = lane_id();
   const uint32_t c = (uint32_t)__popc(mask);
   const uint32_t incl = warp_incl_scan(c);
@@ -470,6 +481,68 @@ __device__ __forceinline__ void filter_round(Row& R, int r, const float4 (&v)[U]
     atomicMax(&R.m->local_max, kmx);
   }
   __syncwarp();
+}
+
+// Append every kept position whose score passes the threshold (x >= g, or
+// every valid position when `all`) to the list.
+template <int T, int U, int W, class Keep>
+__device__ __forceinline__ void filter_round(Row& R, int r, const float4 (&v)[U],
+                                             const int (&n)[Geo<T, U, W>::kSlots], float g, bool all,
+                                             uint32_t* counter, uint2* list, uint32_t cap, Keep keep) {
+  extract_round<T, U, W>(R, r, v, round_mask<T, U, W>(R, r, v, n, g, all, keep), counter, list, cap);
+}
+
+// The streaming filter of the plain top-k (every position kept, W = 4) over
+// rounds 0 .. rounds-1, rounds 0 and 1 already in a and b. The two register
+// buffers alternate (round r + 2 loads into the buffer round r just left), and
+// a round lying wholly inside the slice loads and compares without any
+// validity bookkeeping, from per-thread slot pointers.
+template <int T, int U>
+__device__ __forceinline__ void filter_rounds_all(Row& R, bool vec, float4 (&a)[U], int (&na)[U], float4 (&b)[U],
+                                                  int (&nb)[U], float g, bool all, uint32_t* counter, uint2* list,
+                                                  uint32_t cap) {
+  using G = Geo<T, U, 4>;
+  static_assert(G::kSlots == U, "one float4 per slot");
+  const int rounds = R.rounds;
+  const int64_t len = R.end - R.begin;
+  const float* p0 = R.rowp + R.tbase;
+  const int64_t sstride = (int64_t)rounds * G::kTile;
+  auto whole = [&](int r) { return (int64_t)(r + rounds * (U - 1) + 1) * G::kTile <= len; };
+  auto load = [&](int r, float4 (&v)[U], int (&n)[U]) {
+    if (vec && whole(r)) {
+      const float* pr = p0 + (int64_t)r * G::kTile;
+#pragma unroll
+      for (int s = 0; s < U; ++s) {
+        v[s] = ldg4(pr + s * sstride);
+        n[s] = 4;
+      }
+    } else {
+      load_round<T, U, 4>(R, vec, r, v, n);
+    }
+  };
+  auto filt = [&](int r, const float4 (&v)[U], const int (&n)[U]) {
+    uint32_t mask = 0;
+    if (!all && whole(r)) {
+#pragma unroll
+      for (int s = 0; s < U; ++s) {
+        const float4 q = v[s];
+        mask |= ((q.x >= g ? 1u : 0u) | (q.y >= g ? 2u : 0u) | (q.z >= g ? 4u : 0u) | (q.w >= g ? 8u : 0u))
+                << (4 * s);
+      }
+    } else {
+      mask = round_mask<T, U, 4>(R, r, v, n, g, all, KeepAll{});
+    }
+    extract_round<T, U, 4>(R, r, v, mask, counter, list, cap);
+  };
+#pragma unroll 1
+  for (int r = 0; r < rounds; r += 2) {
+    filt(r, a, na);
+    if (r + 2 < rounds) load(r + 2, a, na);
+    if (r + 1 < rounds) {
+      filt(r + 1, b, nb);
+      if (r + 3 < rounds) load(r + 3, b, nb);
+    }
+  }
 }
 
 // ------------------------------------------------------------------ block items (stage A)
@@ -1000,6 +1073,8 @@ __device__ __forceinline__ bool select_stage(Row& R, const Params& p, float4 (&c
         if (kBlocks) filter_round_blocks<T, U, W>(R, 1, nxt, nn, t, counter, list, seg);
         else filter_round<T, U, W>(R, 1, nxt, nn, g, all, counter, list, seg, keep);
       }
+    } else if constexpr (!kBlocks && W == 4 && Keep::kAll) {
+      filter_rounds_all<T, U>(R, vec, cur, nc, nxt, nn, g, all, counter, list, seg);
     } else {
 #pragma unroll 1
       for (int r = 0; r < R.rounds; ++r) {
