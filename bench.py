@@ -404,7 +404,11 @@ def bench_trace(args):
     dev = torch.device("cuda", torch.cuda.current_device())
     S, L, w = workloads.make(args.trace)
     base = S.to(dev)
-    copies = [base] + [base.clone() for _ in range(3)]
+    # as many rotating copies as the timed bench uses, so the traced launch reads cold rows
+    nbytes = workloads.read_bytes(L, w.rows, w.row_stride)
+    L2 = l2_bytes()
+    ncopies = workloads.l2_rotation_copies(nbytes, L2) if nbytes < 4 * L2 else 1
+    copies = [base] + [base.clone() for _ in range(max(1, ncopies) - 1)]
     ld = None if L is None else L.to(dev)
     kid = 0 if w.blocked else KERNEL_IDS[args.kernel]
     pl = lt.plan(w.rows, w.row_stride, w.k, blocked=w.blocked, k_blocks=w.k_blocks,

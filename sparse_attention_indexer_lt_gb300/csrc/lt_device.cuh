@@ -55,7 +55,7 @@ namespace lt {
 constexpr int kBins = 2048;       // 11-bit digits / linear buckets
 constexpr int kMaxCluster = 16;
 constexpr int kMaxWarps = 32;
-constexpr int kMaxBucket = 64;    // largest bucket ranked by counting
+constexpr int kMaxBucket = 256;   // largest bucket ranked by counting
 constexpr int kOutBuckets = 1024; // linear key buckets of the ordered output
 constexpr unsigned kFull = 0xffffffffu;
 // A second 11-bit level refines the sampled threshold only when the first
