@@ -52,9 +52,70 @@ __global__ void __launch_bounds__(T, (T <= 256 ? 3 : 1)) blocked_kernel(Params p
   const bool exactA = select_stage<T, U, W, true>(R, p, va, na, vb, nb, false, KA, nblocks, nblocks,
                                                   KeepAll{}, true, &intact, &TcA, 0);
   uint64_t TA = 0;
+  bool from_segments = false;  // stage-A-only clusters on the fast path
   if (KA > 0) {
-    TA = exactA ? TcA : select_local<T>(R, KA, nblocks);
-    compact_selected<T>(R, TA);  // stage[0, KA) = kept block composites
+    // (the bitmap of this CTA's blocks lives in the histogram area)
+    if (role == 2 && !exactA && (R.end - R.begin + W - 1) / W <= 32 * (int64_t)kBins) {
+      const uint32_t seg = 1u << m->shift;
+      uint32_t lo = 0xffffffffu, hi = 0u;
+      for (uint32_t q = 0; q < m->nseg; ++q) {
+        if (m->seg_cnt[q] == 0) continue;
+        lo = min(lo, m->seg_min[q]);
+        hi = max(hi, m->seg_max[q]);
+      }
+      (void)seg;
+      from_segments = threshold_by_buckets<T>(R, KA, lo, hi, &TA);
+    }
+    if (!from_segments) {
+      TA = exactA ? TcA : select_local<T>(R, KA, nblocks);
+      compact_selected<T>(R, TA);  // stage[0, KA) = kept block composites
+    }
+  }
+  if (from_segments) {
+    // kept blocks straight from the candidate segments: this CTA's own kept
+    // blocks are the entries of its own segment >= TA, the lower-ranked
+    // slices' kept blocks precede them
+    const int64_t b0s = R.begin / W, b1s = (R.end + W - 1) / W;
+    const uint32_t seg = 1u << m->shift;
+    uint32_t before = 0;
+    for (uint32_t q = 0; q < R.rank; ++q) {
+      const uint32_t n = min(m->seg_cnt[q], seg);
+      const uint2* c = R.cand + (q << m->shift);
+      for (uint32_t j = threadIdx.x; j < n; j += T) before += composite(c[j].x, c[j].y) >= TA ? 1u : 0u;
+    }
+    const uint32_t n_before = block_sum<T>(before, m);
+    if (p.out_blocks) {
+      int32_t* ob = p.out_blocks + R.row * (int64_t)p.k_blocks;
+      const int64_t nbo = b1s - b0s;
+      uint32_t* bits = R.hist;
+      const uint32_t words = (uint32_t)((nbo + 31) >> 5);
+      for (uint32_t i = threadIdx.x; i < words; i += T) bits[i] = 0u;
+      __syncthreads();
+      const uint32_t n_own = min(m->seg_cnt[R.rank], seg);
+      const uint2* own = R.cand + (R.rank << m->shift);
+      for (uint32_t j = threadIdx.x; j < n_own; j += T) {
+        if (composite(own[j].x, own[j].y) >= TA) {
+          const uint32_t o = (uint32_t)((int64_t)own[j].y - b0s);
+          atomicOr(&bits[o >> 5], 1u << (o & 31u));
+        }
+      }
+      __syncthreads();
+      const uint32_t wpt = (words + T - 1) / T;
+      const uint32_t w0 = threadIdx.x * wpt;
+      const uint32_t w1 = min(w0 + wpt, words);
+      uint32_t cnt = 0;
+      for (uint32_t w = w0; w < w1; ++w) cnt += (uint32_t)__popc(bits[w]);
+      uint32_t out = n_before + block_prefix_excl<T>(cnt, m);
+      for (uint32_t w = w0; w < w1; ++w)
+        for (uint32_t x = bits[w]; x; x &= x - 1u)
+          ob[out++] = (int32_t)(b0s + 32 * (int64_t)w + (__ffs(x) - 1));
+      if (R.rank == 0) {
+        for (uint32_t j = KA + threadIdx.x; j < (uint32_t)p.k_blocks; j += T) ob[j] = -1;
+      }
+    }
+    __syncthreads();
+    wait_init(R);
+    return;
   }
 
   // ---- kept block ids in ascending order: this CTA's own kept blocks,

@@ -563,13 +563,24 @@ template <int T, int U, int W>
 __device__ __forceinline__ void filter_round_blocks(Row& R, int r, const float4 (&v)[U],
                                                     const int (&n)[Geo<T, U, W>::kSlots], uint32_t t,
                                                     uint32_t* counter, uint2* list, uint32_t cap) {
+  uint32_t kmn = 0xffffffffu, kmx = 0u;
 #pragma unroll
   for (int s = 0; s < Geo<T, U, W>::kSlots; ++s) {
     const int ns = n[s];
     const uint32_t kk = ns > 0 ? slot_block_key<T, U, W>(v, s, ns) : 0u;
     const bool pe = ns > 0 && kk >= t;
+    if (pe) {
+      kmn = min(kmn, kk);
+      kmx = max(kmx, kk);
+    }
     const uint32_t bid = (uint32_t)(slot_pos<T, U, W>(R, r, s) / W);
     warp_append(pe, kk, bid, counter, list, cap);
+  }
+  kmn = __reduce_min_sync(kFull, kmn);
+  kmx = __reduce_max_sync(kFull, kmx);
+  if (lane_id() == 0 && kmn <= kmx) {
+    atomicMin(&R.m->local_min, kmn);
+    atomicMax(&R.m->local_max, kmx);
   }
 }
 
@@ -647,6 +658,65 @@ __device__ __forceinline__ uint32_t compact_selected(Row& R, uint64_t Tc) {
   const uint32_t cnt = m->aux[0];
   __syncthreads();
   return cnt;
+}
+
+// Composite of the K-th largest fast-path candidate (segmented candidates,
+// key range [lo, hi], histogram zeroed and a barrier passed since): 1024
+// linear key buckets, a suffix scan for the bucket b* holding the K-th item,
+// then the exact rank of the items of b* among themselves. Returns false,
+// deciding nothing, when b* holds more than kMaxBucket items.
+template <int T>
+__device__ __forceinline__ bool threshold_by_buckets(Row& R, uint32_t K, uint32_t lo, uint32_t hi, uint64_t* Tc) {
+  constexpr int NB = kOutBuckets;
+  constexpr int BPT = NB / T;
+  Misc* m = R.m;
+  const float scale = (float)NB / ((float)(hi - lo) + 1.0f);
+  auto bucket = [lo, scale](uint32_t key) -> uint32_t {
+    const uint32_t b = (uint32_t)((float)(key - lo) * scale);
+    return b > (uint32_t)(NB - 1) ? (uint32_t)(NB - 1) : b;
+  };
+  if (threadIdx.x == 0) m->aux[2] = 0u;
+  for_each_cand<T>(R, [&](uint2 e) { atomicAdd(&R.hist[bucket(e.x)], 1u); });
+  __syncthreads();
+  uint32_t v[BPT];
+#pragma unroll
+  for (int j = 0; j < BPT; ++j) v[j] = R.hist[threadIdx.x * BPT + j];
+  uint32_t tot = 0;
+#pragma unroll
+  for (int j = 0; j < BPT; ++j) tot += v[j];
+  uint32_t a = block_suffix_excl<T>(tot, m);
+#pragma unroll
+  for (int j = BPT - 1; j >= 0; --j) {
+    if (a < K && K <= a + v[j]) {
+      m->res_digit = threadIdx.x * BPT + j;
+      m->res_above = a;
+      m->res_cnt = v[j];
+    }
+    a += v[j];
+  }
+  __syncthreads();
+  const uint32_t bstar = m->res_digit, above = m->res_above, cstar = m->res_cnt;
+  if (cstar > (uint32_t)kMaxBucket) return false;
+  for_each_cand<T>(R, [&](uint2 e) {
+    if (bucket(e.x) == bstar) {
+      const uint32_t pos = atomicAdd(&m->aux[2], 1u);
+      if (pos < R.stage_cap) R.stage[pos] = composite(e.x, e.y);
+    }
+  });
+  __syncthreads();
+  const uint32_t need = K - above;  // 1 <= need <= cstar
+  for (uint32_t i = threadIdx.x; i < cstar; i += T) {
+    const uint64_t c = R.stage[i];
+    uint32_t r = 0;
+    for (uint32_t j = 0; j < cstar; ++j) r += (R.stage[j] > c) ? 1u : 0u;
+    if (r == need - 1) {
+      m->aux[4] = (uint32_t)c;
+      m->aux[5] = (uint32_t)(c >> 32);
+    }
+  }
+  __syncthreads();
+  *Tc = ((uint64_t)m->aux[5] << 32) | m->aux[4];
+  return true;
 }
 
 // ------------------------------------------------------------------ ordered output
