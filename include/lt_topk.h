@@ -143,7 +143,15 @@ lt_status lt_topk_blocked(const float* scores, const int32_t* lengths, int32_t r
  *                  output; the two-level kernel's second stage uses slots
  *                  9..14). CTA b of the grid is row b / cluster_size; a CTA
  *                  of the streamed kernel serves several rows and traces its
- *                  third (or, with fewer, its last).
+ *                  third (or, with fewer, its last). The entry timestamp is
+ *                  written before the launch waits for the previous kernel
+ *                  of the stream: give traced launches their own buffer or
+ *                  synchronise between them.
+ *
+ * Every launch uses programmatic dependent launch: a kernel may start while
+ * the previous kernel of the stream finishes, and waits for it (device-side)
+ * before it reads lengths or scores or writes outputs, counters or trace
+ * slots other than the entry timestamp.
  */
 #define LT_NUM_COUNTERS 5
 lt_status lt_topk_ex(const float* scores, const int32_t* lengths, int32_t rows,

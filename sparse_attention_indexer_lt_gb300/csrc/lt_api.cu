@@ -9,8 +9,12 @@
 //           (16384 positions) of the row.
 // A 16-CTA cluster is non-portable. The plan asks the occupancy calculator how
 // many clusters of the chosen shape can be resident at once and halves C until
-// all rows fit in one wave (a cluster must sit inside one GPC, so eight
-// 8-CTA clusters of one-CTA-per-SM kernels may not fit where 128 SMs would).
+// all rows fit in one wave (a cluster must sit inside one GPC, so sixteen
+// 8-CTA clusters of one-CTA-per-SM kernels may not all fit although 128 SMs
+// would). When every CTA's slice is a single register round the top-k kernel
+// is its compact single-round variant. The two-level call with k_blocks >= k
+// plans twice the rows (its plain top-k and stage-A groups run side by side).
+// The streamed kernel is used only when asked for (force_kernel).
 
 #include <cuda_runtime.h>
 

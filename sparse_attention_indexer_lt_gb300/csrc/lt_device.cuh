@@ -18,20 +18,25 @@
 //      than the k-th key (exact when the sample is the whole slice).
 //   3. filter + candidate exchange. Every key >= t is appended to this CTA's
 //      segment of its candidate array (one warp scan and one shared atomic
-//      per warp and round); each CTA then stores its segment and its count
-//      into the same segment of every peer over DSMEM, so after one cluster
-//      barrier every CTA holds the same candidate multiset.
-//   4. select + order. The candidates are spread over 2048 buckets that are
-//      linear in the key between the smallest and largest candidate key; a
-//      suffix scan of the bucket counts finds the bucket of the k-th item and
-//      the first output slot of every bucket above it; an item's slot is its
-//      bucket's first slot plus the number of items of its bucket with a
-//      larger composite (key << 32 | ~index). The composite is unique, and
-//      among equal keys the larger ~index -- the lower index -- wins: the
+//      per warp and round), recording the segment's key range; each CTA then
+//      stores its segment, count and key range into the same segment of every
+//      peer over DSMEM, so after one cluster barrier every CTA holds the same
+//      candidate multiset.
+//   4. select + order. The candidates are spread over kOutBuckets buckets
+//      that are linear in the key between the smallest and largest candidate
+//      key; a suffix scan of the bucket counts finds the bucket of the k-th
+//      item and the first output slot of every bucket above it; an item's
+//      slot is its bucket's first slot plus the number of items of its bucket
+//      with a larger composite (key << 32 | ~index). The composite is unique,
+//      and among equal keys the larger ~index -- the lower index -- wins: the
 //      lowest-index tie fill is the low word of the composite. When a bucket
-//      holds too many items (massive ties), an MSD radix select over the
-//      composites and a bitonic sort take over.
+//      holds more than kMaxBucket items (massive ties), an MSD radix select
+//      over the composites and a bitonic sort take over.
 //   5. each CTA writes the slots of the items that came from its own slice.
+//
+// Every kernel is launched with programmatic dependent launch: it initialises
+// shared memory while the previous kernel of its stream finishes, then waits
+// for that grid (griddepcontrol.wait) before touching global memory.
 //
 // When the sampled threshold keeps fewer than k candidates or more than the
 // candidate capacity (adversarial orderings, massive ties), the row falls
@@ -42,8 +47,9 @@
 //
 // No kernel here waits on a flag: the only cross-CTA synchronisation is the
 // hardware cluster barrier, which every thread of every CTA reaches the same
-// number of times, and no CTA touches a peer's shared memory after the last
-// cluster barrier.
+// number of times (every branch that contains one depends only on values all
+// CTAs of the cluster share), and no CTA touches a peer's shared memory after
+// the last cluster barrier. The streamed kernel's mbarrier waits are bounded.
 
 #pragma once
 

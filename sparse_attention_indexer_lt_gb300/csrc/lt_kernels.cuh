@@ -9,10 +9,12 @@
 // the two-level kernel W = block (stage A items are blocks, stage B items are
 // the positions of the kept blocks).
 //
-// Code layout: everything a normal row executes is inlined once; the paths
-// only adversarial rows take (the streaming exact select, the radix-select +
-// bitonic fallback of the output, scalar loads of ragged slot ends) are
-// separate functions, so the hot code stays small enough to fetch quickly.
+// Code layout: a row's code runs once per CTA, so its latency includes
+// fetching that code. Everything a normal row executes is inlined once; the
+// paths only adversarial rows take (the streaming exact select, the
+// radix-select + bitonic fallback of the output, the single-round path's
+// second estimate level) are separate functions, and slices of one register
+// round use select_one, which has no streaming code at all.
 
 #pragma once
 
