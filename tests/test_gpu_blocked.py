@@ -75,3 +75,27 @@ def test_blocked_optional_outputs():
     assert val is None and blk is None
     oi, _, _ = oracle.topk_blocked(S.numpy(), None, 8, 100, 50)
     assert np.array_equal(idx.cpu().numpy(), oi)
+
+
+def test_blocked_split_without_kept_blocks_runs_one_stage():
+    """k_blocks >= k and no out_blocks: only the plain top-k group runs (one count
+    per row), and its result still equals the literal two-level oracle."""
+    import oracle
+    import sparse_attention_indexer_lt_gb300 as lt
+    S, L = workloads.random_rows(6, 50000, seed=35, dist="bf16", lengths="ragged", min_len=100)
+    c = counters()
+    idx, val, blk = lt.topk_blocked(S.cuda(), L.cuda(), 8, 2048, 512, with_blocks=False, counters=c)
+    torch.cuda.synchronize()
+    assert blk is None
+    oi, ov, _ = oracle.topk_blocked(S.numpy(), L.numpy(), 8, 2048, 512)
+    assert np.array_equal(idx.cpu().numpy(), oi)
+    assert np.array_equal(val.cpu().numpy().view(np.uint32), ov.view(np.uint32))
+    assert c.cpu().numpy()[0] + c.cpu().numpy()[1] == 6
+
+
+@pytest.mark.parametrize("kb,k", [(2048, 512), (100, 512)])
+def test_blocked_split_and_sequential_exact_paths(kb, k):
+    """Forced streaming radix select in both the side-by-side (kb >= k) and the
+    one-after-the-other (kb < k) launches."""
+    S, L = workloads.random_rows(3, 90000, seed=36, dist="coarse", lengths="ragged", min_len=1)
+    parity_blocked(S.numpy(), L.numpy(), 8, kb, k, what=f"exact kb={kb}", force_exact=True)
