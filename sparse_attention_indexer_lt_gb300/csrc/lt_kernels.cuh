@@ -1012,6 +1012,67 @@ __device__ __noinline__ uint64_t exact_select(Row R, const Params p, uint32_t K,
   return tval;
 }
 
+// Threshold estimate of a single-CTA, 256-thread row from its spread round-0
+// sample (not the whole slice) with two 8-bit digit levels of 256 bins, one
+// bin per thread: the top 8 bits of the raw key, then the next 8 bits of the
+// keys in the chosen bin. The threshold resolves 16 key bits -- 1/128 of an
+// octave, each bf16 value its own bin -- with two one-bin-per-thread scans
+// instead of 2048-bin ones. Returns the lower edge of the 16-bit bin holding
+// the r-th largest sample key.
+template <int T, int U, int W>
+__device__ __forceinline__ uint32_t estimate_small(Row& R, const float4 (&v)[U],
+                                                   const int (&n)[Geo<T, U, W>::kSlots], uint32_t K,
+                                                   int64_t items) {
+  using G = Geo<T, U, W>;
+  static_assert(T == 256 && W == 4, "one 8-bit bin per thread, position items");
+  Misc* m = R.m;
+  uint32_t* h1 = R.hist;
+  uint32_t* h2 = R.hist + 256;
+  h1[threadIdx.x] = 0u;
+  h2[threadIdx.x] = 0u;
+  __syncthreads();
+#pragma unroll
+  for (int s = 0; s < G::kSlots; ++s) {
+    const int ns = n[s];
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+      if (e < ns) atomicAdd(&h1[raw_key(__float_as_uint(lane4(v[s], e))) >> 24], 1u);
+  }
+  // sample size from the geometry: round 0 holds tiles 0, rounds, 2 rounds, ...
+  const int64_t len = R.end - R.begin;
+  uint32_t nsamp = 0;
+#pragma unroll
+  for (int s = 0; s < G::kSlots; ++s) {
+    const int64_t t0 = (int64_t)R.rounds * s * G::kTile;
+    if (t0 < len) nsamp += (uint32_t)(len - t0 < G::kTile ? len - t0 : G::kTile);
+  }
+  const uint32_t r = sample_target(K, nsamp, items, false);
+  __syncthreads();
+  const uint32_t v1 = h1[threadIdx.x];
+  uint32_t a = block_suffix_excl<T>(v1, m);
+  if (a < r && r <= a + v1) {
+    m->res_digit = threadIdx.x;
+    m->res_above = a;
+  }
+  __syncthreads();
+  const uint32_t d1 = m->res_digit, r2 = r - m->res_above;
+#pragma unroll
+  for (int s = 0; s < G::kSlots; ++s) {
+    const int ns = n[s];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const uint32_t kk = raw_key(__float_as_uint(lane4(v[s], e)));
+      if (e < ns && (kk >> 24) == d1) atomicAdd(&h2[(kk >> 16) & 255u], 1u);
+    }
+  }
+  __syncthreads();
+  const uint32_t v2 = h2[threadIdx.x];
+  a = block_suffix_excl<T>(v2, m);
+  if (a < r2 && r2 <= a + v2) m->res_digit = threadIdx.x;
+  __syncthreads();
+  return (d1 << 24) | (m->res_digit << 16);
+}
+
 // ------------------------------------------------------------------ one selection stage
 
 // Estimate -> filter -> exchange over the items of this stage (positions, or
@@ -1076,7 +1137,14 @@ __device__ __forceinline__ bool select_stage(Row& R, const Params& p, float4 (&c
   if (!exact && K > 0) {
     // ---- threshold estimate from the digit histogram of the sample
     uint32_t t = 0;
-    if (items > (int64_t)(cap / 2)) {
+    bool estimated = false;
+    if constexpr (!kBlocks && T == 256 && W == 4 && Keep::kAll) {
+      if (items > (int64_t)(cap / 2) && !full && R.nclus == 1 && first) {
+        t = estimate_small<T, U, W>(R, cur, nc, K, items);
+        estimated = true;
+      }
+    }
+    if (!estimated && items > (int64_t)(cap / 2)) {
       const int nsr = full ? (R.rounds < 2 ? R.rounds : 2) : (R.rounds < 1 ? R.rounds : 1);
       uint32_t r = 0, d1 = 0, above1 = 0;
 #pragma unroll 1
