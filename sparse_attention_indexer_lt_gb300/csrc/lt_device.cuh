@@ -187,9 +187,6 @@ __device__ __forceinline__ uint32_t peer_addr(uint32_t local_addr, uint32_t rank
 __device__ __forceinline__ void dsmem_red_add(uint32_t addr, uint32_t v) {
   asm volatile("red.relaxed.cluster.shared::cluster.add.u32 [%0], %1;" :: "r"(addr), "r"(v) : "memory");
 }
-__device__ __forceinline__ void dsmem_red_or(uint32_t addr, uint32_t v) {
-  asm volatile("red.relaxed.cluster.shared::cluster.or.b32 [%0], %1;" :: "r"(addr), "r"(v) : "memory");
-}
 __device__ __forceinline__ uint32_t dsmem_atom_add(uint32_t addr, uint32_t v) {
   uint32_t old;
   asm volatile("atom.relaxed.cluster.shared::cluster.add.u32 %0, [%1], %2;"
