@@ -17,8 +17,9 @@
 //      that bucket is still wide. The result is a key threshold t no larger
 //      than the k-th key (exact when the sample is the whole slice).
 //   3. filter + candidate exchange. Every key >= t is appended to this CTA's
-//      segment of its candidate array (one warp scan and one shared atomic
-//      per warp and round), recording the segment's key range; each CTA then
+//      segment of its candidate array (one shared atomic per lane and round
+//      that has candidates; the lane then walks its own flagged elements),
+//      recording the segment's key range; each CTA then
 //      stores its segment, count and key range into the same segment of every
 //      peer over DSMEM, so after one cluster barrier every CTA holds the same
 //      candidate multiset.

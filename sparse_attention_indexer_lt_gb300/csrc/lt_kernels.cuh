@@ -425,64 +425,46 @@ __device__ __forceinline__ uint32_t round_mask(const Row& R, int r, const float4
   return mask;
 }
 
-// Append the positions of round r flagged in each lane's mask to the list:
-// one warp scan and one shared atomic reserve the warp's slots; lanes with
-// candidates stage their round in shared memory and every lane then writes
-// one candidate (the owner lane of candidate k is found by a binary search
-// over the warp's running counts). Records the key range of what it appends.
+// Append the positions of round r flagged in this lane's mask to the list.
+// One shared atomic reserves the lane's slots; the lane stages its round in
+// its own slots of the warp's staging area (read back by index, by this lane
+// only) and walks its set bits, so the warp takes as many steps as its
+// busiest lane holds candidates. Bit 4*f + e is element e of float4 f, i.e.
+// slot f / kVS, float4 f % kVS. kmn/kmx collect the lane's key range.
 template <int T, int U, int W>
-__device__ __forceinline__ void extract_round(Row& R, int r, const float4 (&v)[U], uint32_t mask,
-                                              uint32_t* counter, uint2* list, uint32_t cap) {
+__device__ __forceinline__ void extract_lane(const Row& R, int r, const float4 (&v)[U], uint32_t mask,
+                                             uint32_t* counter, uint2* list, uint32_t cap, uint32_t& kmn,
+                                             uint32_t& kmx) {
   using G = Geo<T, U, W>;
+  if (mask == 0) return;
+  uint32_t o = atomicAdd(counter, (uint32_t)__popc(mask));
   const uint32_t lane = lane_id();
-  const uint32_t c = (uint32_t)__popc(mask);
-  const uint32_t incl = warp_incl_scan(c);
-  const uint32_t total = __shfl_sync(kFull, incl, 31);
-  if (total == 0) return;
-  uint32_t base = 0;
-  if (lane == 31) base = atomicAdd(counter, total);
-  base = __shfl_sync(kFull, base, 31);
-  if (mask) {
 #pragma unroll
-    for (int f = 0; f < U; ++f) R.wst[f * 32 + lane] = v[f];
-  }
-  __syncwarp();
-  const uint32_t excl = incl - c;
-  const float* stf = reinterpret_cast<const float*>(R.wst);
-  const uint32_t wbase = threadIdx.x & ~31u;
-  uint32_t kmn = 0xffffffffu, kmx = 0u;
-  for (uint32_t k0 = 0; k0 < total; k0 += 32) {
-    const uint32_t k = k0 + lane;
-    const uint32_t kq = k < total ? k : total - 1;
-    uint32_t owner = 0;  // number of lanes whose running count is <= kq
-#pragma unroll
-    for (uint32_t step = 16; step; step >>= 1) {
-      const uint32_t x = __shfl_sync(kFull, incl, owner + step - 1);
-      if (x <= kq) owner += step;
-    }
-    const uint32_t oex = __shfl_sync(kFull, excl, owner);
-    uint32_t om = __shfl_sync(kFull, mask, owner);
-    if (k < total) {
-      for (uint32_t t = kq - oex; t > 0; --t) om &= om - 1;
-      const uint32_t bit = (uint32_t)(__ffs(om) - 1);
-      const uint32_t f = bit >> 2, e = bit & 3u;
-      const float x = stf[(f * 32 + owner) * 4 + e];
-      const int s = (int)(f / G::kVS), j = (int)(f % G::kVS);
-      const int64_t pos = R.begin + (int64_t)(wbase + owner) * W + (int64_t)(r + R.rounds * s) * G::kTile +
-                          4 * j + e;
-      const uint32_t kk = key_of(x);
-      kmn = min(kmn, kk);
-      kmx = max(kmx, kk);
-      if (base + k < cap) list[base + k] = make_uint2(kk, (uint32_t)pos);
-    }
-  }
+  for (int f = 0; f < U; ++f) R.wst[f * 32 + lane] = v[f];
+  const float* st = reinterpret_cast<const float*>(R.wst) + 4 * lane;
+  // row-relative positions fit 32 bits (a row holds fewer than 2^31)
+  const uint32_t p0 = (uint32_t)R.tbase + (uint32_t)r * (uint32_t)G::kTile;
+  const uint32_t sstride = (uint32_t)R.rounds * (uint32_t)G::kTile;
+  do {
+    const uint32_t bit = (uint32_t)(__ffs(mask) - 1);
+    mask &= mask - 1u;
+    const uint32_t f = bit >> 2, e = bit & 3u;
+    const uint32_t kk = key_of(st[128 * f + e]);
+    kmn = min(kmn, kk);
+    kmx = max(kmx, kk);
+    if (o < cap) list[o] = make_uint2(kk, p0 + (f / G::kVS) * sstride + 4 * (f % G::kVS) + e);
+    ++o;
+  } while (mask);
+}
+
+// Fold the warp's key range into the CTA's (local_min / local_max).
+__device__ __forceinline__ void flush_key_range(const Row& R, uint32_t kmn, uint32_t kmx) {
   kmn = __reduce_min_sync(kFull, kmn);
   kmx = __reduce_max_sync(kFull, kmx);
-  if (lane == 0) {
+  if (lane_id() == 0 && kmn <= kmx) {
     atomicMin(&R.m->local_min, kmn);
     atomicMax(&R.m->local_max, kmx);
   }
-  __syncwarp();
 }
 
 // Append every kept position whose score passes the threshold (x >= g, or
@@ -491,7 +473,9 @@ template <int T, int U, int W, class Keep>
 __device__ __forceinline__ void filter_round(Row& R, int r, const float4 (&v)[U],
                                              const int (&n)[Geo<T, U, W>::kSlots], float g, bool all,
                                              uint32_t* counter, uint2* list, uint32_t cap, Keep keep) {
-  extract_round<T, U, W>(R, r, v, round_mask<T, U, W>(R, r, v, n, g, all, keep), counter, list, cap);
+  uint32_t kmn = 0xffffffffu, kmx = 0u;
+  extract_lane<T, U, W>(R, r, v, round_mask<T, U, W>(R, r, v, n, g, all, keep), counter, list, cap, kmn, kmx);
+  flush_key_range(R, kmn, kmx);
 }
 
 // The streaming filter of the plain top-k (every position kept, W = 4) over
@@ -522,6 +506,7 @@ __device__ __forceinline__ void filter_rounds_all(Row& R, bool vec, float4 (&a)[
       load_round<T, U, 4>(R, vec, r, v, n);
     }
   };
+  uint32_t kmn = 0xffffffffu, kmx = 0u;
   auto filt = [&](int r, const float4 (&v)[U], const int (&n)[U]) {
     uint32_t mask = 0;
     if (!all && whole(r)) {
@@ -534,7 +519,7 @@ __device__ __forceinline__ void filter_rounds_all(Row& R, bool vec, float4 (&a)[
     } else {
       mask = round_mask<T, U, 4>(R, r, v, n, g, all, KeepAll{});
     }
-    extract_round<T, U, 4>(R, r, v, mask, counter, list, cap);
+    extract_lane<T, U, 4>(R, r, v, mask, counter, list, cap, kmn, kmx);
   };
 #pragma unroll 1
   for (int r = 0; r < rounds; r += 2) {
@@ -545,6 +530,7 @@ __device__ __forceinline__ void filter_rounds_all(Row& R, bool vec, float4 (&a)[
       if (r + 3 < rounds) load(r + 3, b, nb);
     }
   }
+  flush_key_range(R, kmn, kmx);
 }
 
 // ------------------------------------------------------------------ block items (stage A)
