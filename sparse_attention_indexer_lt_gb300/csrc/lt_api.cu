@@ -84,7 +84,7 @@ struct Plan {
   uint32_t stages = 0;      // streamed kernel: ring stages
   uint32_t cap = 0;        // candidate slots: cluster * (1 << seg_shift)
   uint32_t seg_shift = 0;  // log2 of the slots each CTA of the cluster may fill
-  uint32_t wstage = 0;     // per-warp candidate staging bytes (threads * 16 * float4 per round)
+  uint32_t wstage = 0;     // candidate staging bytes (threads * 16 * kStageF4)
   uint32_t sel_cap = 0;
   uint32_t smem = 0;
   const void* func = nullptr;
@@ -213,12 +213,8 @@ lt_status make_plan(int32_t rows, int64_t row_stride, int32_t k, bool blocked, i
   };
   int slot = 0;
   plan->func = pick(1, &slot);
-  {
-    // float4 loads per thread per round, as instantiated in the kernels
-    int u = threads == kNarrowThreads ? 4 : 8;
-    if (blocked && block / 4 > u) u = block / 4;
-    plan->wstage = (uint32_t)threads * 16u * (uint32_t)u;
-  }
+  // candidate staging: kStageF4 float4 per thread
+  plan->wstage = (uint32_t)threads * 16u * (uint32_t)lt::kStageF4;
   if (!plan->func) return LT_ERR_UNSUPPORTED;
 
   // Candidate capacity: about 4k slots per row (the sampled threshold keeps

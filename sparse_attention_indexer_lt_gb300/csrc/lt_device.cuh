@@ -64,6 +64,7 @@ constexpr int kMaxCluster = 16;
 constexpr int kMaxWarps = 32;
 constexpr int kMaxBucket = 256;   // largest bucket ranked by counting
 constexpr int kOutBuckets = 1024; // linear key buckets of the ordered output
+constexpr int kStageF4 = 8;        // float4 staging slots per lane (two 4-float4 rounds or one of 8)
 constexpr unsigned kFull = 0xffffffffu;
 // A second 11-bit level refines the sampled threshold only when the first
 // predicts more candidates than this fraction of the candidate capacity.
@@ -101,7 +102,7 @@ struct Params {
   int32_t cap;          // candidate slots: clusters * (1 << seg_shift)
   int32_t seg_shift;    // log2 of the candidate slots one CTA may fill
   int32_t sel_cap;      // power of two >= max(k, k_blocks)
-  int32_t wstage;       // bytes of the per-warp candidate staging area (threads * 16 * U)
+  int32_t wstage;       // bytes of the candidate staging area (threads * 16 * kStageF4)
   int32_t force_exact;
   int32_t vec_ok;       // every row start is 16-byte aligned
   int32_t clustered;    // launched with cluster size > 1
@@ -267,8 +268,34 @@ __device__ __forceinline__ float value_of(uint32_t key, const float* rowp, uint3
   return __uint_as_float(b);
 }
 
+// All ones when x >= g (ordered: false for NaN), else zero.
+__device__ __forceinline__ uint32_t ge_bits(float x, float g) {
+  uint32_t r;
+  asm("set.ge.u32.f32 %0, %1, %2;" : "=r"(r) : "f"(x), "f"(g));
+  return r;
+}
+
+// (a & c) | (b & ~c): the bits of a where c is set, of b elsewhere.
+__device__ __forceinline__ uint32_t bit_merge(uint32_t a, uint32_t b, uint32_t c) {
+  uint32_t r;
+  asm("lop3.b32 %0, %1, %2, %3, 0xE4;" : "=r"(r) : "r"(a), "r"(b), "r"(c));
+  return r;
+}
+
 __device__ __forceinline__ float lane4(const float4& q, int e) {
   return e == 0 ? q.x : e == 1 ? q.y : e == 2 ? q.z : q.w;
+}
+
+// Bit 4*f + e set when element e of v[f] >= g (NaN never passes): compare i
+// gives all ones or zero, and bit i is taken from it while the bits below i
+// are kept.
+template <int U>
+__device__ __forceinline__ uint32_t ge_mask(const float4 (&v)[U], float g) {
+  static_assert(4 * U <= 32, "mask holds 32 positions");
+  uint32_t m = ge_bits(v[0].x, g);
+#pragma unroll
+  for (int i = 1; i < 4 * U; ++i) m = bit_merge(m, ge_bits(lane4(v[i / 4], i % 4), g), (1u << i) - 1u);
+  return 4 * U == 32 ? m : (m & ((1u << (4 * U)) - 1u));
 }
 
 // ------------------------------------------------------------------ warp / block helpers

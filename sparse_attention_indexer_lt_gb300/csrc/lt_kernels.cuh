@@ -38,7 +38,7 @@ struct Row {
   uint32_t* merged1;
   uint2* cand;           // nclus segments of (1 << seg_shift) slots
   uint64_t* stage;
-  float4* wst;           // this warp's staging area: [U][32] float4
+  float4* wst;           // this warp's staging area: [kStageF4][32] float4
   const float* rowp;
   int64_t row;
   int64_t L;             // valid positions of the row
@@ -171,7 +171,8 @@ __device__ __forceinline__ void setup_row(Row& R, const Params& p, unsigned char
   R.merged1 = reinterpret_cast<uint32_t*>(smem + lay.merged1);
   R.cand = reinterpret_cast<uint2*>(smem + lay.cand);
   R.stage = reinterpret_cast<uint64_t*>(smem + lay.stage);
-  R.wst = reinterpret_cast<float4*>(smem + lay.wstage) + (threadIdx.x >> 5) * 32 * U;
+  static_assert(U <= kStageF4, "a lane stages at most kStageF4 float4");
+  R.wst = reinterpret_cast<float4*>(smem + lay.wstage) + (threadIdx.x >> 5) * 32 * kStageF4;
   R.stage_cap = (uint32_t)p.sel_cap + kMaxBucket;
   R.trace = p.trace;
   R.seg_shift = (uint32_t)p.seg_shift;
@@ -478,21 +479,53 @@ __device__ __forceinline__ void filter_round(Row& R, int r, const float4 (&v)[U]
   flush_key_range(R, kmn, kmx);
 }
 
+// Per-lane walk over the staged float4s of one or two rounds (see
+// filter_rounds_all): bit 4*F + e of mask is element e of staged float4 F,
+// float4 F < U being slot F of round r (first position p0 of this lane) and
+// F >= U slot F - U of round r + 1. kPos: every flagged score is > 0 (the
+// threshold is positive), so its key is its bits with the sign bit set.
+template <int T, int U, bool kPos>
+__device__ __forceinline__ void walk_lane(const Row& R, uint32_t mask, uint32_t p0, uint32_t sstride,
+                                          uint32_t* counter, uint2* list, uint32_t cap, uint32_t& kmn,
+                                          uint32_t& kmx) {
+  constexpr uint32_t kTile = (uint32_t)Geo<T, U, 4>::kTile;
+  if (mask == 0) return;
+  uint32_t o = atomicAdd(counter, (uint32_t)__popc(mask));
+  const float* st = reinterpret_cast<const float*>(R.wst) + 4 * lane_id();
+  do {
+    const uint32_t bit = (uint32_t)(__ffs(mask) - 1);
+    mask &= mask - 1u;
+    const uint32_t F = bit >> 2, e = bit & 3u;
+    const uint32_t u = __float_as_uint(st[128 * F + e]);
+    const uint32_t kk = kPos ? (u | 0x80000000u) : key_of(u);
+    kmn = min(kmn, kk);
+    kmx = max(kmx, kk);
+    const uint32_t pos = p0 + (F >= (uint32_t)U ? kTile : 0u) + (F & (uint32_t)(U - 1)) * sstride + e;
+    if (o < cap) list[o] = make_uint2(kk, pos);
+    ++o;
+  } while (mask);
+}
+
 // The streaming filter of the plain top-k (every position kept, W = 4) over
 // rounds 0 .. rounds-1, rounds 0 and 1 already in a and b. The two register
 // buffers alternate (round r + 2 loads into the buffer round r just left), and
 // a round lying wholly inside the slice loads and compares without any
-// validity bookkeeping, from per-thread slot pointers.
-template <int T, int U>
+// validity bookkeeping, from per-thread slot pointers. A round's flagged
+// lanes stage it in shared memory before its buffer reloads, so the next
+// loads leave before the candidates are written; with 16-position rounds
+// (U = 4) both rounds of a pair share one walk over a 32-bit mask.
+template <int T, int U, bool kPos>
 __device__ __forceinline__ void filter_rounds_all(Row& R, bool vec, float4 (&a)[U], int (&na)[U], float4 (&b)[U],
                                                   int (&nb)[U], float g, bool all, uint32_t* counter, uint2* list,
                                                   uint32_t cap) {
   using G = Geo<T, U, 4>;
   static_assert(G::kSlots == U, "one float4 per slot");
+  constexpr bool kPair = 8 * U <= 32;
   const int rounds = R.rounds;
   const int64_t len = R.end - R.begin;
   const float* p0 = R.rowp + R.tbase;
   const int64_t sstride = (int64_t)rounds * G::kTile;
+  const uint32_t lane = lane_id();
   auto whole = [&](int r) { return (int64_t)(r + rounds * (U - 1) + 1) * G::kTile <= len; };
   auto load = [&](int r, float4 (&v)[U], int (&n)[U]) {
     if (vec && whole(r)) {
@@ -506,28 +539,38 @@ __device__ __forceinline__ void filter_rounds_all(Row& R, bool vec, float4 (&a)[
       load_round<T, U, 4>(R, vec, r, v, n);
     }
   };
-  uint32_t kmn = 0xffffffffu, kmx = 0u;
-  auto filt = [&](int r, const float4 (&v)[U], const int (&n)[U]) {
-    uint32_t mask = 0;
-    if (!all && whole(r)) {
-#pragma unroll
-      for (int s = 0; s < U; ++s) {
-        const float4 q = v[s];
-        mask |= ((q.x >= g ? 1u : 0u) | (q.y >= g ? 2u : 0u) | (q.z >= g ? 4u : 0u) | (q.w >= g ? 8u : 0u))
-                << (4 * s);
-      }
-    } else {
-      mask = round_mask<T, U, 4>(R, r, v, n, g, all, KeepAll{});
-    }
-    extract_lane<T, U, 4>(R, r, v, mask, counter, list, cap, kmn, kmx);
+  auto mask_of = [&](int r, const float4 (&v)[U], const int (&n)[U]) -> uint32_t {
+    if (!all && whole(r)) return ge_mask<U>(v, g);
+    return round_mask<T, U, 4>(R, r, v, n, g, all, KeepAll{});
   };
+  auto stage = [&](int F0, const float4 (&v)[U]) {
+#pragma unroll
+    for (int f = 0; f < U; ++f) R.wst[(F0 + f) * 32 + lane] = v[f];
+  };
+  const uint32_t q0 = (uint32_t)R.tbase, ss = (uint32_t)sstride;
+  uint32_t kmn = 0xffffffffu, kmx = 0u;
 #pragma unroll 1
   for (int r = 0; r < rounds; r += 2) {
-    filt(r, a, na);
+    const uint32_t ma = mask_of(r, a, na);
+    if (ma) stage(0, a);
     if (r + 2 < rounds) load(r + 2, a, na);
-    if (r + 1 < rounds) {
-      filt(r + 1, b, nb);
-      if (r + 3 < rounds) load(r + 3, b, nb);
+    const uint32_t pr = q0 + (uint32_t)r * (uint32_t)G::kTile;
+    if constexpr (kPair) {
+      uint32_t mb = 0;
+      if (r + 1 < rounds) {
+        mb = mask_of(r + 1, b, nb);
+        if (mb) stage(U, b);
+        if (r + 3 < rounds) load(r + 3, b, nb);
+      }
+      walk_lane<T, U, kPos>(R, ma | (mb << (4 * U)), pr, ss, counter, list, cap, kmn, kmx);
+    } else {
+      walk_lane<T, U, kPos>(R, ma, pr, ss, counter, list, cap, kmn, kmx);
+      if (r + 1 < rounds) {
+        const uint32_t mb = mask_of(r + 1, b, nb);
+        if (mb) stage(0, b);
+        if (r + 3 < rounds) load(r + 3, b, nb);
+        walk_lane<T, U, kPos>(R, mb, pr + (uint32_t)G::kTile, ss, counter, list, cap, kmn, kmx);
+      }
     }
   }
   flush_key_range(R, kmn, kmx);
@@ -1017,12 +1060,13 @@ __device__ __forceinline__ uint32_t estimate_small(Row& R, const float4 (&v)[U],
   h1[threadIdx.x] = 0u;
   h2[threadIdx.x] = 0u;
   __syncthreads();
+  // positions past the slice end hold NaN (raw key 0): counted in the lowest
+  // bins, they can only lower the threshold
+  (void)n;
 #pragma unroll
   for (int s = 0; s < G::kSlots; ++s) {
-    const int ns = n[s];
 #pragma unroll
-    for (int e = 0; e < 4; ++e)
-      if (e < ns) atomicAdd(&h1[raw_key(__float_as_uint(lane4(v[s], e))) >> 24], 1u);
+    for (int e = 0; e < 4; ++e) atomicAdd(&h1[raw_key(__float_as_uint(lane4(v[s], e))) >> 24], 1u);
   }
   // sample size from the geometry: round 0 holds tiles 0, rounds, 2 rounds, ...
   const int64_t len = R.end - R.begin;
@@ -1044,11 +1088,10 @@ __device__ __forceinline__ uint32_t estimate_small(Row& R, const float4 (&v)[U],
   const uint32_t d1 = m->res_digit, r2 = r - m->res_above;
 #pragma unroll
   for (int s = 0; s < G::kSlots; ++s) {
-    const int ns = n[s];
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
       const uint32_t kk = raw_key(__float_as_uint(lane4(v[s], e)));
-      if (e < ns && (kk >> 24) == d1) atomicAdd(&h2[(kk >> 16) & 255u], 1u);
+      if ((kk >> 24) == d1) atomicAdd(&h2[(kk >> 16) & 255u], 1u);
     }
   }
   __syncthreads();
@@ -1200,7 +1243,8 @@ __device__ __forceinline__ bool select_stage(Row& R, const Params& p, float4 (&c
         else filter_round<T, U, W>(R, 1, nxt, nn, g, all, counter, list, seg, keep);
       }
     } else if constexpr (!kBlocks && W == 4 && Keep::kAll) {
-      filter_rounds_all<T, U>(R, vec, cur, nc, nxt, nn, g, all, counter, list, seg);
+      if (!all && g > 0.0f) filter_rounds_all<T, U, true>(R, vec, cur, nc, nxt, nn, g, all, counter, list, seg);
+      else filter_rounds_all<T, U, false>(R, vec, cur, nc, nxt, nn, g, all, counter, list, seg);
     } else {
 #pragma unroll 1
       for (int r = 0; r < R.rounds; ++r) {
