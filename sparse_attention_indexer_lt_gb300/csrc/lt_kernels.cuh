@@ -114,6 +114,30 @@ __device__ __forceinline__ void load_round(const Row& R, bool vec, int r, float4
   }
 }
 
+// Four-position slots (W = 4): round r lies wholly inside the slice.
+template <int T, int U>
+__device__ __forceinline__ bool round_whole(const Row& R, int r) {
+  return (int64_t)(r + R.rounds * (U - 1) + 1) * Geo<T, U, 4>::kTile <= R.end - R.begin;
+}
+
+// Load round r of four-position slots: a whole round takes U vector loads
+// from this thread's slot pointers, others go through load_round.
+template <int T, int U>
+__device__ __forceinline__ void load_round4(const Row& R, bool vec, int r, float4 (&v)[U], int (&n)[U]) {
+  using G = Geo<T, U, 4>;
+  if (vec && round_whole<T, U>(R, r)) {
+    const float* pr = R.rowp + R.tbase + (int64_t)r * G::kTile;
+    const int64_t sstride = (int64_t)R.rounds * G::kTile;
+#pragma unroll
+    for (int s = 0; s < U; ++s) {
+      v[s] = ldg4(pr + s * sstride);
+      n[s] = 4;
+    }
+  } else {
+    load_round<T, U, 4>(R, vec, r, v, n);
+  }
+}
+
 template <int S>
 __device__ __forceinline__ void clear_round(int (&n)[S]) {
 #pragma unroll
@@ -269,11 +293,12 @@ __device__ __forceinline__ void for_each_cand(const Row& R, F f) {
       for (uint32_t j = lane; j < n; j += 32) f(c[j]);
     }
   } else {
-    const uint32_t per = NW / nseg;  // warps per segment (powers of two)
-    const uint32_t q = warp / per, sub = warp - q * per;
+    // 2^lp warps per segment (nseg and NW are powers of two)
+    const uint32_t lp = (uint32_t)(__clz(nseg) - __clz((int)NW));
+    const uint32_t q = warp >> lp, sub = warp & ((1u << lp) - 1u);
     const uint32_t n = min(m->seg_cnt[q], seg);
     const uint2* c = R.cand + (q << shift);
-    for (uint32_t j = sub * 32 + lane; j < n; j += per * 32) f(c[j]);
+    for (uint32_t j = sub * 32 + lane; j < n; j += 32u << lp) f(c[j]);
   }
 }
 
@@ -522,32 +547,17 @@ __device__ __forceinline__ void filter_rounds_all(Row& R, bool vec, float4 (&a)[
   static_assert(G::kSlots == U, "one float4 per slot");
   constexpr bool kPair = 8 * U <= 32;
   const int rounds = R.rounds;
-  const int64_t len = R.end - R.begin;
-  const float* p0 = R.rowp + R.tbase;
-  const int64_t sstride = (int64_t)rounds * G::kTile;
   const uint32_t lane = lane_id();
-  auto whole = [&](int r) { return (int64_t)(r + rounds * (U - 1) + 1) * G::kTile <= len; };
-  auto load = [&](int r, float4 (&v)[U], int (&n)[U]) {
-    if (vec && whole(r)) {
-      const float* pr = p0 + (int64_t)r * G::kTile;
-#pragma unroll
-      for (int s = 0; s < U; ++s) {
-        v[s] = ldg4(pr + s * sstride);
-        n[s] = 4;
-      }
-    } else {
-      load_round<T, U, 4>(R, vec, r, v, n);
-    }
-  };
+  auto load = [&](int r, float4 (&v)[U], int (&n)[U]) { load_round4<T, U>(R, vec, r, v, n); };
   auto mask_of = [&](int r, const float4 (&v)[U], const int (&n)[U]) -> uint32_t {
-    if (!all && whole(r)) return ge_mask<U>(v, g);
+    if (!all && round_whole<T, U>(R, r)) return ge_mask<U>(v, g);
     return round_mask<T, U, 4>(R, r, v, n, g, all, KeepAll{});
   };
   auto stage = [&](int F0, const float4 (&v)[U]) {
 #pragma unroll
     for (int f = 0; f < U; ++f) R.wst[(F0 + f) * 32 + lane] = v[f];
   };
-  const uint32_t q0 = (uint32_t)R.tbase, ss = (uint32_t)sstride;
+  const uint32_t q0 = (uint32_t)R.tbase, ss = (uint32_t)rounds * (uint32_t)G::kTile;
   uint32_t kmn = 0xffffffffu, kmx = 0u;
 #pragma unroll 1
   for (int r = 0; r < rounds; r += 2) {
@@ -1145,6 +1155,15 @@ __device__ __forceinline__ bool select_stage(Row& R, const Params& p, float4 (&c
   *regs_intact = resident;
   *Tc = 0;
 
+  if constexpr (!kBlocks && W == 4) {
+    if (!loaded) {
+      if (R.rounds > 0) load_round4<T, U>(R, vec, 0, cur, nc);
+      else clear_round(nc);
+      if (R.rounds > 1) load_round4<T, U>(R, vec, 1, nxt, nn);
+      else clear_round(nn);
+      loaded = true;
+    }
+  }
   if (!loaded) {
     // rounds 0 and 1 into cur and nxt (one load site: shift, then load);
     // with a single round, round 0 ends in cur and nxt is empty
