@@ -367,8 +367,8 @@ __device__ __forceinline__ void load_bins(const uint32_t* bins, uint32_t (&v)[kB
 }
 
 // Exclusive suffix sum over threads of per-thread totals (the keys in bins
-// owned by threads with a larger index). One __syncthreads; every thread then
-// adds the totals of the warps after its own (at most 16 broadcast reads).
+// owned by threads with a larger index). One __syncthreads; each lane then
+// reads one warp total and one warp reduction adds those after its warp.
 // The caller must __syncthreads before warp_a is written again.
 template <int T>
 __device__ __forceinline__ uint32_t block_suffix_excl(uint32_t tot, Misc* m) {
@@ -382,10 +382,7 @@ __device__ __forceinline__ uint32_t block_suffix_excl(uint32_t tot, Misc* m) {
   }
   if (lane == 0) m->warp_a[warp] = incl;
   __syncthreads();
-  uint32_t after = 0;
-#pragma unroll
-  for (int w = 1; w < NW; ++w)
-    if (w > (int)warp) after += m->warp_a[w];
+  const uint32_t after = __reduce_add_sync(kFull, (lane > warp && lane < (uint32_t)NW) ? m->warp_a[lane] : 0u);
   return after + (incl - tot);
 }
 
@@ -394,42 +391,63 @@ __device__ __forceinline__ uint32_t block_suffix_excl(uint32_t tot, Misc* m) {
 // before warp_a is written again.
 template <int T>
 __device__ __forceinline__ uint32_t block_prefix_excl(uint32_t x, Misc* m) {
-  constexpr int NW = T / 32;
+  static_assert(T % 32 == 0 && T / 32 <= kMaxWarps, "whole warps");
   const uint32_t lane = lane_id(), warp = threadIdx.x >> 5;
   const uint32_t incl = warp_incl_scan(x);
   if (lane == 31) m->warp_a[warp] = incl;
   __syncthreads();
-  uint32_t before = 0;
-#pragma unroll
-  for (int w = 0; w < NW - 1; ++w)
-    if (w < (int)warp) before += m->warp_a[w];
+  const uint32_t before = __reduce_add_sync(kFull, lane < warp ? m->warp_a[lane] : 0u);
   return before + incl - x;
 }
 
-// Find digit d with suffix(d + 1) < r <= suffix(d), suffix(d) = sum of bins[b >= d].
-// Requires 1 <= r <= sum(bins). Results land in m->res_*. Ends with __syncthreads.
-template <int T>
-__device__ __forceinline__ void find_digit(const uint32_t* bins, uint32_t r, Misc* m) {
-  constexpr int BPT = kBins / T;
-  uint32_t v[BPT];
-  load_bins<T>(bins, v);
+// Thread t owns bins t*BPT .. t*BPT + BPT-1 with counts v[]. Finds the bin d
+// with suffix(d + 1) < r <= suffix(d), suffix(d) = sum of bins >= d, for
+// 1 <= r <= sum. Warp totals locate the warp holding it; only that warp
+// scans its lanes. Results land in m->res_digit / res_above / res_cnt. Ends
+// with __syncthreads; the caller must __syncthreads before warp_a is written
+// again.
+template <int T, int BPT>
+__device__ __forceinline__ void find_rank(const uint32_t (&v)[BPT], uint32_t r, Misc* m) {
+  constexpr int NW = T / 32;
+  const uint32_t lane = lane_id(), warp = threadIdx.x >> 5;
   uint32_t tot = 0;
 #pragma unroll
   for (int j = 0; j < BPT; ++j) tot += v[j];
-  uint32_t acc = block_suffix_excl<T>(tot, m);
-  if (acc < r && r <= acc + tot) {
+  const uint32_t wsum = __reduce_add_sync(kFull, tot);
+  if (lane == 0) m->warp_a[warp] = wsum;
+  __syncthreads();
+  const uint32_t after_w =
+      __reduce_add_sync(kFull, (lane > warp && lane < (uint32_t)NW) ? m->warp_a[lane] : 0u);
+  if (after_w < r && r <= after_w + wsum) {
+    uint32_t incl = tot;  // sum over lanes >= lane
 #pragma unroll
-    for (int j = BPT - 1; j >= 0; --j) {
-      if (acc + v[j] >= r) {
-        m->res_digit = (uint32_t)(threadIdx.x * BPT + j);
-        m->res_above = acc;
-        m->res_cnt = v[j];
-        break;
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t n = __shfl_down_sync(kFull, incl, o);
+      if (lane + o < 32) incl += n;
+    }
+    uint32_t acc = after_w + incl - tot;
+    if (acc < r && r <= acc + tot) {
+#pragma unroll
+      for (int j = BPT - 1; j >= 0; --j) {
+        if (acc + v[j] >= r) {
+          m->res_digit = (uint32_t)(threadIdx.x * BPT + j);
+          m->res_above = acc;
+          m->res_cnt = v[j];
+          break;
+        }
+        acc += v[j];
       }
-      acc += v[j];
     }
   }
   __syncthreads();
+}
+
+// find_rank over the kBins bins of a histogram.
+template <int T>
+__device__ __forceinline__ void find_digit(const uint32_t* bins, uint32_t r, Misc* m) {
+  uint32_t v[kBins / T];
+  load_bins<T>(bins, v);
+  find_rank<T, kBins / T>(v, r, m);
 }
 
 // Bitonic sort of s[0, n) descending; n a power of two >= 2. Ends with __syncthreads.

@@ -1088,13 +1088,8 @@ __device__ __forceinline__ uint32_t estimate_small(Row& R, const float4 (&v)[U],
   }
   const uint32_t r = sample_target(K, nsamp, items, false);
   __syncthreads();
-  const uint32_t v1 = h1[threadIdx.x];
-  uint32_t a = block_suffix_excl<T>(v1, m);
-  if (a < r && r <= a + v1) {
-    m->res_digit = threadIdx.x;
-    m->res_above = a;
-  }
-  __syncthreads();
+  const uint32_t v1[1] = {h1[threadIdx.x]};
+  find_rank<T, 1>(v1, r, m);
   const uint32_t d1 = m->res_digit, r2 = r - m->res_above;
 #pragma unroll
   for (int s = 0; s < G::kSlots; ++s) {
@@ -1105,10 +1100,8 @@ __device__ __forceinline__ uint32_t estimate_small(Row& R, const float4 (&v)[U],
     }
   }
   __syncthreads();
-  const uint32_t v2 = h2[threadIdx.x];
-  a = block_suffix_excl<T>(v2, m);
-  if (a < r2 && r2 <= a + v2) m->res_digit = threadIdx.x;
-  __syncthreads();
+  const uint32_t v2[1] = {h2[threadIdx.x]};
+  find_rank<T, 1>(v2, r2, m);
   return (d1 << 24) | (m->res_digit << 16);
 }
 
@@ -1280,13 +1273,9 @@ __device__ __forceinline__ bool select_stage(Row& R, const Params& p, float4 (&c
     stamp(R, tr + kTrFilter);
     exchange_segments<T>(R);
     stamp(R, tr + kTrExchange);
-    uint32_t total = 0;
-    bool overflow = false;
-    for (uint32_t q = 0; q < R.nclus; ++q) {
-      const uint32_t c = m->seg_cnt[q];
-      total += c;
-      overflow = overflow || c > seg;
-    }
+    const uint32_t cq = lane_id() < R.nclus ? m->seg_cnt[lane_id()] : 0u;
+    const uint32_t total = __reduce_add_sync(kFull, cq);
+    const bool overflow = __any_sync(kFull, cq > seg);
     if (overflow || total < K) {
       exact = true;
       stat = overflow ? kCntOverflow : kCntShort;
@@ -1386,13 +1375,9 @@ __device__ __forceinline__ bool select_one(Row& R, const Params& p, float4 (&v)[
     stamp(R, kTrFilter);
     exchange_segments<T>(R);
     stamp(R, kTrExchange);
-    uint32_t total = 0;
-    bool overflow = false;
-    for (uint32_t q = 0; q < R.nclus; ++q) {
-      const uint32_t c = m->seg_cnt[q];
-      total += c;
-      overflow = overflow || c > seg;
-    }
+    const uint32_t cq = lane_id() < R.nclus ? m->seg_cnt[lane_id()] : 0u;
+    const uint32_t total = __reduce_add_sync(kFull, cq);
+    const bool overflow = __any_sync(kFull, cq > seg);
     if (overflow || total < K) {
       exact = true;
       stat = overflow ? kCntOverflow : kCntShort;
@@ -1426,14 +1411,19 @@ __device__ __forceinline__ void output_positions(Row& R, const Params& p, bool e
     const Misc* m = R.m;
     uint32_t lo = 0xffffffffu, hi = 0u, n = 0;
     if (!exact) {
-      const uint32_t seg = 1u << m->shift;
-      for (uint32_t q = 0; q < m->nseg; ++q) {
-        const uint32_t c = m->seg_cnt[q];
-        if (c == 0) continue;
-        n += min(c, seg);
-        lo = min(lo, m->seg_min[q]);
-        hi = max(hi, m->seg_max[q]);
+      // lane q reads segment q's count and key range
+      const uint32_t q = lane_id();
+      uint32_t c = 0, mn = 0xffffffffu, mx = 0u;
+      if (q < m->nseg) {
+        c = min(m->seg_cnt[q], 1u << m->shift);
+        if (c) {
+          mn = m->seg_min[q];
+          mx = m->seg_max[q];
+        }
       }
+      n = __reduce_add_sync(kFull, c);
+      lo = __reduce_min_sync(kFull, mn);
+      hi = __reduce_max_sync(kFull, mx);
     }
     if (!bucket_select_sort<T>(R, K, kout, oi, ov, own, !exact, lo, hi, n))
       sorted_fallback<T>(R, exact, Tc, K, kout, oi, ov, idx_limit, own);

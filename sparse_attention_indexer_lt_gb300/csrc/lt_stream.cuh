@@ -405,13 +405,9 @@ __device__ __forceinline__ void stream_row(Row& R, const Params& p, uint64_t* ba
     stamp(R, kTrFilter);
     exchange_segments<T>(R);
     stamp(R, kTrExchange);
-    uint32_t total = 0;
-    bool overflow = false;
-    for (uint32_t q = 0; q < R.nclus; ++q) {
-      const uint32_t cq = m->seg_cnt[q];
-      total += cq;
-      overflow = overflow || cq > seg;
-    }
+    const uint32_t cs = lane_id() < R.nclus ? m->seg_cnt[lane_id()] : 0u;
+    const uint32_t total = __reduce_add_sync(kFull, cs);
+    const bool overflow = __any_sync(kFull, cs > seg);
     if (overflow || total < K) {
       exact = true;
       stat = overflow ? kCntOverflow : kCntShort;
