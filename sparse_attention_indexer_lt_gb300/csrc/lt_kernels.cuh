@@ -922,7 +922,6 @@ __device__ __forceinline__ bool bucket_select_sort(Row& R, uint32_t K, uint32_t 
     if (rank < K) write_slot(oi, ov, rank, c, R.rowp);
   }
   write_padding<T>(R, oi, ov, K, kout);
-  __syncthreads();
   return true;
 }
 
@@ -1343,7 +1342,15 @@ __device__ __forceinline__ bool select_one(Row& R, const Params& p, float4 (&v)[
     uint32_t t = 0;
     if (R.L > (int64_t)(cap / 2)) {
       zero_bins<T>(R.hist);
-      hist_round<T, U, W, 1>(R, 0, v, n, 0, KeepAll{});
+      // every position of the round: the NaN fillers past the slice end have
+      // raw key 0 and land in bin 0, below any threshold but t = 0 ("all")
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        atomicAdd(&R.hist[raw_key(__float_as_uint(v[u].x)) >> 21], 1u);
+        atomicAdd(&R.hist[raw_key(__float_as_uint(v[u].y)) >> 21], 1u);
+        atomicAdd(&R.hist[raw_key(__float_as_uint(v[u].z)) >> 21], 1u);
+        atomicAdd(&R.hist[raw_key(__float_as_uint(v[u].w)) >> 21], 1u);
+      }
       stamp(R, kTrHist);
       // K <= L: with large clusters each CTA pushes only the bins at or above
       // its own K-th digit (the cluster's K-th key is at least as large)
@@ -1370,8 +1377,14 @@ __device__ __forceinline__ bool select_one(Row& R, const Params& p, float4 (&v)[
       for (int i = threadIdx.x; i < kOutBuckets / 4; i += T) z[i] = make_uint4(0, 0, 0, 0);
     }
     const bool all = (t == 0u);
-    filter_round<T, U, W>(R, 0, v, n, threshold_float(all ? 1u : t), all, &m->local_count, list, seg,
-                          KeepAll{});
+    {
+      // positions past the slice end hold NaN, which fails x >= g
+      const uint32_t mask = all ? round_mask<T, U, W>(R, 0, v, n, 0.0f, true, KeepAll{})
+                                : ge_mask<U>(v, threshold_float(t));
+      uint32_t kmn = 0xffffffffu, kmx = 0u;
+      extract_lane<T, U, W>(R, 0, v, mask, &m->local_count, list, seg, kmn, kmx);
+      flush_key_range(R, kmn, kmx);
+    }
     stamp(R, kTrFilter);
     exchange_segments<T>(R);
     stamp(R, kTrExchange);
