@@ -549,8 +549,10 @@ __device__ __forceinline__ void filter_rounds_all(Row& R, bool vec, float4 (&a)[
   const int rounds = R.rounds;
   const uint32_t lane = lane_id();
   auto load = [&](int r, float4 (&v)[U], int (&n)[U]) { load_round4<T, U>(R, vec, r, v, n); };
+  // kPos (never "all"): positions past the slice end hold NaN, which fails
+  // x >= g, so every round takes the plain compare mask
   auto mask_of = [&](int r, const float4 (&v)[U], const int (&n)[U]) -> uint32_t {
-    if (!all && round_whole<T, U>(R, r)) return ge_mask<U>(v, g);
+    if (kPos || (!all && round_whole<T, U>(R, r))) return ge_mask<U>(v, g);
     return round_mask<T, U, 4>(R, r, v, n, g, all, KeepAll{});
   };
   auto stage = [&](int F0, const float4 (&v)[U]) {
