@@ -382,12 +382,23 @@ __device__ __forceinline__ void exchange_segments(Row& R) {
   }
   const uint2* mine = R.cand + off;
   const uint32_t src = smem_addr(R.cand) + 8u * off;
-  // (peer, entry) pairs flattened over the threads; peers rank+1 .. rank+nclus-1
+  // (peer, entry) pairs flattened over the threads; peers rank+1 .. rank+nclus-1.
+  // x / n_put from a float estimate and one correction (x < 2^22 is exact
+  // in a float and the estimate is off by at most one).
   const uint32_t pairs = n_put * (R.nclus - 1);
+  const float inv = 1.0f / (float)(n_put > 0 ? n_put : 1u);
   for (uint32_t x = threadIdx.x; x < pairs; x += T) {
-    const uint32_t d = x / n_put, i = x - d * n_put;
+    uint32_t d = (uint32_t)((float)x * inv);
+    int32_t i = (int32_t)x - (int32_t)(d * n_put);
+    if (i < 0) {
+      --d;
+      i += (int32_t)n_put;
+    } else if (i >= (int32_t)n_put) {
+      ++d;
+      i -= (int32_t)n_put;
+    }
     const uint32_t q = (R.rank + 1 + d) & (R.nclus - 1);
-    dsmem_st_v2(peer_addr(src + 8u * i, q), mine[i]);
+    dsmem_st_v2(peer_addr(src + 8u * (uint32_t)i, q), mine[i]);
   }
   cluster_sync();
 }
