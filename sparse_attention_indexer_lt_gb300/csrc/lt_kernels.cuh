@@ -147,16 +147,18 @@ __device__ __forceinline__ void clear_round(int (&n)[S]) {
 // Key of the block held in slot s (max of the keys of its valid positions).
 template <int T, int U, int W>
 __device__ __forceinline__ uint32_t slot_block_key(const float4 (&v)[U], int s, int nv) {
+  // key_of is monotone on non-NaN scores and maps NaN lowest; fmaxf skips a
+  // NaN operand, so the key of the float maximum is the maximum key (an
+  // all-NaN block gives NaN, key 0). Positions past the slice end hold NaN.
   constexpr int VS = Geo<T, U, W>::kVS;
-  uint32_t best = 0;
+  (void)nv;
+  float best = fmaxf(fmaxf(v[s * VS].x, v[s * VS].y), fmaxf(v[s * VS].z, v[s * VS].w));
 #pragma unroll
-  for (int j = 0; j < VS; ++j)
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const uint32_t kk = key_of(lane4(v[s * VS + j], e));
-      if (4 * j + e < nv && kk > best) best = kk;
-    }
-  return best;
+  for (int j = 1; j < VS; ++j) {
+    const float4 q = v[s * VS + j];
+    best = fmaxf(best, fmaxf(fmaxf(q.x, q.y), fmaxf(q.z, q.w)));
+  }
+  return key_of(best);
 }
 
 struct KeepAll {
