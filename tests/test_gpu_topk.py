@@ -141,6 +141,20 @@ def test_rows_longer_than_one_register_pass(kernel):
 
 
 @pytest.mark.parametrize("ft", [256, 512])
+@pytest.mark.parametrize("dist", ["desc", "coarse", "special", "normal", "equal"])
+def test_streaming_filter_thresholds_of_any_sign(dist, ft):
+    """Single-CTA rows of many register rounds (the sampled estimate and the
+    streaming filter): negative and zero thresholds ("desc"), heavy ties
+    ("coarse", "equal": the latter overflows onto the exact path), special
+    values, and positive thresholds, which take the sign-bit key shortcut."""
+    S, L = workloads.random_rows(6, 45000, seed=21 + len(dist), dist=dist, lengths="ragged",
+                                 min_len=20000)
+    for k in (64, 512, 2048):
+        parity_topk(S.numpy(), L.numpy(), k, what=f"{dist} stream k={k} t={ft}", force_cluster=1,
+                    force_threads=ft)
+
+
+@pytest.mark.parametrize("ft", [256, 512])
 def test_streamed_rows_walk_more_rows_than_ctas(ft):
     """Persistent CTAs: many short and empty rows, several rows per CTA, chunks of
     the next row in flight while a row is selected."""
