@@ -39,7 +39,7 @@ __global__ void __launch_bounds__(T, (T <= 256 ? 3 : 1)) blocked_kernel(Params p
     uint64_t Tc;
     const bool exact = select_stage<T, U, W, false>(R, p, va, na, vb, nb, false, K, R.L, p.row_stride, KeepAll{},
                                                     true, &intact, &Tc, kTrStageB);
-    output_positions<T>(R, p, exact, Tc, K, p.row_stride);
+    output_positions<T>(R, p, exact, Tc, K, p.row_stride, true);
     wait_init(R);
     return;
   }
@@ -210,7 +210,7 @@ __global__ void __launch_bounds__(T, (T <= 256 ? 3 : 1)) blocked_kernel(Params p
   const bool exactB = select_stage<T, U, W, false>(R, p, va, na, vb, nb, intact, KB, (int64_t)ncand,
                                                    p.row_stride, KeepBlocks<T, U, W>{TA}, false,
                                                    &intact_b, &TcB, kTrStageB);
-  output_positions<T>(R, p, exactB, TcB, KB, p.row_stride);
+  output_positions<T>(R, p, exactB, TcB, KB, p.row_stride, true);
   wait_init(R);
 }
 

@@ -19,10 +19,11 @@
 //   3. filter + candidate exchange. Every key >= t is appended to this CTA's
 //      segment of its candidate array (one shared atomic per lane and round
 //      that has candidates; the lane then walks its own flagged elements),
-//      recording the segment's key range; each CTA then
-//      stores its segment, count and key range into the same segment of every
-//      peer over DSMEM, so after one cluster barrier every CTA holds the same
-//      candidate multiset.
+//      recording the segment's key range; each CTA then stores its count
+//      and key range into every peer and its segment into the same segment
+//      of rank 0 over DSMEM, so after one cluster barrier rank 0 holds every
+//      candidate. (The two-level kernel's block stage stores segments into
+//      every peer: each CTA then writes its own kept blocks.)
 //   4. select + order. The candidates are spread over kOutBuckets buckets
 //      that are linear in the key between the smallest and largest candidate
 //      key; a suffix scan of the bucket counts finds the bucket of the k-th
@@ -33,7 +34,8 @@
 //      lowest-index tie fill is the low word of the composite. When a bucket
 //      holds more than kMaxBucket items (massive ties), an MSD radix select
 //      over the composites and a bitonic sort take over.
-//   5. each CTA writes the slots of the items that came from its own slice.
+//   5. rank 0 writes every slot. (After the exact path every CTA holds the
+//      selected items and writes the slots of those from its own slice.)
 //
 // Every kernel is launched with programmatic dependent launch: it initialises
 // shared memory while the previous kernel of its stream finishes, then waits

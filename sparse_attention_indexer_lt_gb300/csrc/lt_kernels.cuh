@@ -351,10 +351,12 @@ __device__ __forceinline__ void release_merged(Row& R, int buf) {
   for (int i = threadIdx.x; i < kBins / 4; i += T) p[i] = make_uint4(0, 0, 0, 0);
 }
 
-// Fast-path exchange: this CTA's segment (and its count) goes to the same
-// segment of every peer. One cluster barrier, no remote atomics.
+// Fast-path exchange: this CTA's count and key range go to every peer, its
+// segment to the same segment of every peer, or with `gather` to rank 0 only
+// (which then orders and writes the whole row). One cluster barrier, no
+// remote atomics.
 template <int T>
-__device__ __forceinline__ void exchange_segments(Row& R) {
+__device__ __forceinline__ void exchange_segments(Row& R, bool gather) {
   Misc* m = R.m;
   __syncthreads();
   const uint32_t n = m->local_count;
@@ -384,6 +386,13 @@ __device__ __forceinline__ void exchange_segments(Row& R) {
   }
   const uint2* mine = R.cand + off;
   const uint32_t src = smem_addr(R.cand) + 8u * off;
+  if (gather) {
+    if (R.rank != 0) {
+      for (uint32_t i = threadIdx.x; i < n_put; i += T) dsmem_st_v2(peer_addr(src + 8u * i, 0), mine[i]);
+    }
+    cluster_sync();
+    return;
+  }
   // (peer, entry) pairs flattened over the threads; peers rank+1 .. rank+nclus-1.
   // x / n_put from a float estimate and one correction (x < 2^22 is exact
   // in a float and the estimate is off by at most one).
@@ -1285,7 +1294,7 @@ __device__ __forceinline__ bool select_stage(Row& R, const Params& p, float4 (&c
       }
     }
     stamp(R, tr + kTrFilter);
-    exchange_segments<T>(R);
+    exchange_segments<T>(R, !kBlocks);
     stamp(R, tr + kTrExchange);
     const uint32_t cq = lane_id() < R.nclus ? m->seg_cnt[lane_id()] : 0u;
     const uint32_t total = __reduce_add_sync(kFull, cq);
@@ -1401,7 +1410,7 @@ __device__ __forceinline__ bool select_one(Row& R, const Params& p, float4 (&v)[
       flush_key_range(R, kmn, kmx);
     }
     stamp(R, kTrFilter);
-    exchange_segments<T>(R);
+    exchange_segments<T>(R, true);
     stamp(R, kTrExchange);
     const uint32_t cq = lane_id() < R.nclus ? m->seg_cnt[lane_id()] : 0u;
     const uint32_t total = __reduce_add_sync(kFull, cq);
@@ -1425,9 +1434,19 @@ __device__ __forceinline__ bool select_one(Row& R, const Params& p, float4 (&v)[
 }
 
 // Select and write the top K positions of this row after select_stage.
+// gather: the fast-path exchange gathered every candidate in rank 0, which
+// writes the whole row alone; the other CTAs are done.
 template <int T>
-__device__ __forceinline__ void output_positions(Row& R, const Params& p, bool exact, uint64_t Tc, uint32_t K,
-                                                 int64_t idx_limit) {
+__device__ __forceinline__ void output_positions(Row& R0, const Params& p, bool exact, uint64_t Tc, uint32_t K,
+                                                 int64_t idx_limit, bool gather) {
+  Row R = R0;
+  if (gather && !exact && R.nclus > 1) {
+    if (R.rank != 0) {
+      stamp(R, kTrOutput);
+      return;
+    }
+    R.nclus = 1;  // rank 0 owns every position
+  }
   const uint32_t kout = (uint32_t)p.k;
   int32_t* oi = p.out_idx + R.row * (int64_t)kout;
   float* ov = p.out_val ? p.out_val + R.row * (int64_t)kout : nullptr;

@@ -403,7 +403,7 @@ __device__ __forceinline__ void stream_row(Row& R, const Params& p, uint64_t* ba
     }
     consumed = true;
     stamp(R, kTrFilter);
-    exchange_segments<T>(R);
+    exchange_segments<T>(R, false);
     stamp(R, kTrExchange);
     const uint32_t cs = lane_id() < R.nclus ? m->seg_cnt[lane_id()] : 0u;
     const uint32_t total = __reduce_add_sync(kFull, cs);
@@ -431,7 +431,7 @@ __device__ __forceinline__ void stream_row(Row& R, const Params& p, uint64_t* ba
     stamp(R, kTrExact);
     if (K > 0) bump(p, R, kCntFast);
   }
-  output_positions<T>(R, p, exact, Tc, K, p.row_stride);
+  output_positions<T>(R, p, exact, Tc, K, p.row_stride, false);
 }
 
 }  // namespace lt

@@ -29,7 +29,7 @@ __global__ void __launch_bounds__(T, (T <= 256 ? 3 : 1)) topk_kernel(Params p) {
     exact = select_stage<T, U, 4, false>(R, p, va, na, vb, nb, false, K, R.L, p.row_stride, KeepAll{}, true,
                                          &intact, &Tc, 0);
   }
-  output_positions<T>(R, p, exact, Tc, K, p.row_stride);
+  output_positions<T>(R, p, exact, Tc, K, p.row_stride, true);
   wait_init(R);
 }
 
