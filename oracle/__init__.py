@@ -46,6 +46,8 @@ def _load():
         lib.lt_oracle_topk.restype = ctypes.c_int
         lib.lt_oracle_topk_blocked.argtypes = [vp, vp, i64, i64, i64, i64, i64, vp, vp, vp, i32]
         lib.lt_oracle_topk_blocked.restype = ctypes.c_int
+        lib.lt_oracle_topk_candidates.argtypes = [vp, vp, i64, i64, i64, vp, i64, i64, vp, vp, i32]
+        lib.lt_oracle_topk_candidates.restype = ctypes.c_int
         _lib = lib
     return _lib
 
@@ -101,3 +103,26 @@ def topk_blocked(scores, lengths, block: int, k_blocks: int, k: int, nthreads: i
     if rc != 0:
         raise ValueError("lt_oracle_topk_blocked: invalid argument")
     return idx, val, blk
+
+
+def topk_candidates(scores, lengths, cand_blocks, block: int, k: int, nthreads: int | None = None):
+    """Top-k among the positions of the listed blocks: (idx int32 [rows, k], val float32 [rows, k]).
+
+    cand_blocks: int [rows, n_cand]; ids outside [0, nblocks) are ignored and
+    repeated ids count once.
+    """
+    s, ln = _prep(scores, lengths)
+    rows, stride = s.shape
+    cb = np.ascontiguousarray(np.asarray(cand_blocks, dtype=np.int32))
+    if cb.ndim == 1:
+        cb = cb[None, :]
+    if cb.ndim != 2 or cb.shape[0] != rows:
+        raise ValueError("cand_blocks must be [rows, n_cand]")
+    idx = np.empty((rows, k), dtype=np.int32)
+    val = np.empty((rows, k), dtype=np.float32)
+    rc = _load().lt_oracle_topk_candidates(_ptr(s), _ptr(ln), rows, stride, int(block), _ptr(cb),
+                                           cb.shape[1], int(k), _ptr(idx), _ptr(val),
+                                           int(nthreads or default_threads()))
+    if rc != 0:
+        raise ValueError("lt_oracle_topk_candidates: invalid argument")
+    return idx, val

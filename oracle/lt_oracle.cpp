@@ -19,15 +19,23 @@
 //     min(k, L), pad the rest with (-1, -inf). Under that rule the answer is
 //     unique.
 //
-//   * Two-level selection. "Layer 20 selects up to 2048 eight-position blocks
-//     as candidates; later indexer-source layers restrict their top-512 to
-//     those candidates" (SGLang and Miles day-0 support for DeepSeek-V4.1,
+//   * Two-level selection. In the cross-layer sharing of DeepSeek-V4.1 one
+//     layer picks at most 2048 candidate blocks of eight positions and the
+//     later indexer-source layers take their top-512 only among the positions
+//     of those blocks (SGLang and Miles day-0 support for DeepSeek-V4.1,
 //     xhh.club, Q&A on cross-layer sharing). Literal steps, in the order the
 //     page gives them: (1) block score = max of the block's valid scores;
 //     (2) stable-sort blocks by block score descending, keep the first
 //     min(k_blocks, nblocks) (ties: lowest block index); (3) gather the
 //     valid positions of the kept blocks in ascending index order; (4) stable
 //     sort those by score descending, keep min(k, ncand).
+//
+//   * Candidate-restricted selection with the candidates given (the later
+//     layers' side of that sharing, where the block list arrives from the
+//     earlier layer). The pages say nothing about the list's form; reading:
+//     block ids outside [0, nblocks) are ignored (-1 pads a short list),
+//     repeated ids count once, the list's order does not matter. Steps (3)
+//     and (4) above on the listed blocks.
 //
 // Float order (the pages are silent; reading stated here and in the design doc):
 // IEEE order on numbers, so -0.0 == +0.0 and +-inf are ordinary extremes;
@@ -125,6 +133,25 @@ void blocked_row(const float* s, int64_t L, int64_t B, int64_t k_blocks, int64_t
   write_row(s, cand, k, out_idx, out_val);
 }
 
+void candidates_row(const float* s, int64_t L, int64_t B, const int32_t* listed, int64_t n_listed,
+                    int64_t k, int32_t* out_idx, float* out_val) {
+  // the listed blocks that hold valid positions, each once, ascending
+  const int64_t nb = (L + B - 1) / B;
+  std::vector<int64_t> blocks;
+  blocks.reserve(n_listed);
+  for (int64_t j = 0; j < n_listed; ++j)
+    if (listed[j] >= 0 && listed[j] < nb) blocks.push_back(listed[j]);
+  std::sort(blocks.begin(), blocks.end());
+  blocks.erase(std::unique(blocks.begin(), blocks.end()), blocks.end());
+  // (3) their valid positions, ascending; (4) stable sort by score descending
+  std::vector<int64_t> cand;
+  cand.reserve(blocks.size() * B);
+  for (int64_t b : blocks)
+    for (int64_t i = b * B; i < std::min(L, (b + 1) * B); ++i) cand.push_back(i);
+  stable_sort_desc(s, cand);
+  write_row(s, cand, k, out_idx, out_val);
+}
+
 template <class F>
 void parallel_rows(int64_t rows, int32_t nthreads, F f) {
   if (nthreads <= 1 || rows <= 1) {
@@ -168,6 +195,22 @@ int lt_oracle_topk_blocked(const float* scores, const int32_t* lengths, int64_t 
     blocked_row(scores + r * row_stride, row_length(lengths, r, row_stride), block, k_blocks,
                 k, out_idx + r * k, out_val ? out_val + r * k : nullptr,
                 out_blocks ? out_blocks + r * k_blocks : nullptr);
+  });
+  return 0;
+}
+
+// cand_blocks: n_cand block ids per row (row-major), host memory.
+int lt_oracle_topk_candidates(const float* scores, const int32_t* lengths, int64_t rows,
+                              int64_t row_stride, int64_t block, const int32_t* cand_blocks,
+                              int64_t n_cand, int64_t k, int32_t* out_idx, float* out_val,
+                              int32_t nthreads) {
+  if (rows < 0 || row_stride < 0 || block < 1 || n_cand < 0 || k < 1 ||
+      (rows > 0 && (!scores || !out_idx || (n_cand > 0 && !cand_blocks))))
+    return 1;
+  parallel_rows(rows, nthreads, [=](int64_t r) {
+    candidates_row(scores + r * row_stride, row_length(lengths, r, row_stride), block,
+                   cand_blocks ? cand_blocks + r * n_cand : nullptr, n_cand, k, out_idx + r * k,
+                   out_val ? out_val + r * k : nullptr);
   });
   return 0;
 }

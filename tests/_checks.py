@@ -53,6 +53,17 @@ def brute_blocked_row(s, L: int, B: int, k_blocks: int, k: int):
     return out_idx, out_blocks
 
 
+def brute_candidates_row(s, L: int, B: int, listed, k: int):
+    """Top-k among the positions of the listed blocks, restated with Python tuples:
+    the listed ids that name a block of [0, L) form a set; its valid positions
+    are ranked like brute_topk_row."""
+    nb = (L + B - 1) // B
+    blocks = {int(b) for b in listed if 0 <= int(b) < nb}
+    cand = [i for i in range(L) if i // B in blocks]
+    order = sorted(cand, key=lambda i: _sort_key(float(s[i]), i))[:k]
+    return order + [-1] * (k - len(order))
+
+
 def _rank_tuple(x: np.ndarray):
     """(nan, -x) as two arrays usable for lexicographic comparison."""
     nan = np.isnan(x)

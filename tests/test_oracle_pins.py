@@ -15,7 +15,7 @@ import torch
 
 import oracle
 import workloads
-from _checks import (brute_blocked_row, brute_topk_row, check_invariants, equal_outputs,
+from _checks import (brute_blocked_row, brute_candidates_row, brute_topk_row, check_invariants, equal_outputs,
                      lexsort_topk_row)
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
@@ -214,6 +214,65 @@ def test_blocked_workload_rows_invariants():
         assert np.all(np.diff(b) > 0) and b.size == w.k_blocks
         # every output position lies in a kept block
         assert np.isin(idx[r] // w.block, b).all()
+
+
+def test_candidates_against_brute_force_small():
+    rng = np.random.default_rng(5)
+    for trial in range(300):
+        B = int(rng.choice([1, 2, 3, 4, 8]))
+        n = int(rng.integers(0, 40))
+        s = np.array(rng.choice([0.0, 1.0, 2.0, -1.0, float("nan"), -0.0], size=40), dtype=np.float32)
+        nc = int(rng.integers(0, 12))
+        listed = rng.integers(-2, 14, size=nc).astype(np.int32)  # pads, repeats, ids past the row
+        k = int(rng.integers(1, 20))
+        idx, val = oracle.topk_candidates(s[None], np.array([n], np.int32), listed[None], B, k, nthreads=1)
+        assert idx[0].tolist() == brute_candidates_row(s, n, B, listed, k), (s, n, B, listed, k)
+        assert check_invariants_subset(s, idx[0], val[0])
+
+
+def check_invariants_subset(s, idx, val):
+    """Picks are distinct, values are bit copies, pads are (-1, -inf) after the picks."""
+    picks = idx[idx >= 0]
+    n = picks.size
+    return (np.unique(picks).size == n and np.all(idx[n:] == -1) and np.all(np.isneginf(val[n:]))
+            and np.array_equal(val[:n].view(np.uint32), s[picks].view(np.uint32)))
+
+
+@pytest.mark.parametrize("dist", ["normal", "coarse", "bf16", "special"])
+def test_candidates_reproduce_both_other_functions(dist):
+    """Special cases that reduce to the other two functions: listing every block
+    gives the plain top-k; listing the blocks stage A kept gives the two-level
+    result."""
+    S, L = workloads.random_rows(6, 3000, seed=22, dist=dist, lengths="ragged")
+    S = S.numpy()
+    L = L.numpy()
+    B = 8
+    every = np.tile(np.arange((3000 + B - 1) // B, dtype=np.int32), (6, 1))
+    for k in (1, 64, 300):
+        i1, v1 = oracle.topk_candidates(S, L, every, B, k)
+        i2, v2 = oracle.topk(S, L, k)
+        assert equal_outputs(i1, v1, i2, v2)
+    for kb, k in [(16, 100), (40, 64), (300, 512)]:
+        i3, v3, blk = oracle.topk_blocked(S, L, B, kb, k)
+        i4, v4 = oracle.topk_candidates(S, L, blk, B, k)
+        assert equal_outputs(i3, v3, i4, v4)
+
+
+def test_candidates_ignore_order_repeats_and_padding():
+    rng = np.random.default_rng(6)
+    S, L = workloads.random_rows(4, 5000, seed=23, dist="bf16", lengths="ragged")
+    S = S.numpy()
+    L = L.numpy()
+    listed = np.stack([np.sort(rng.choice(625, size=50, replace=False)) for _ in range(4)]).astype(np.int32)
+    i1, v1 = oracle.topk_candidates(S, L, listed, 8, 128)
+    shuffled = np.stack([rng.permutation(r) for r in listed])
+    noisy = np.concatenate([shuffled, listed[:, :10], np.full((4, 7), -1, np.int32),
+                            np.full((4, 3), 10 ** 6, np.int32)], axis=1)
+    i2, v2 = oracle.topk_candidates(S, L, noisy, 8, 128)
+    assert equal_outputs(i1, v1, i2, v2)
+    # no listed block: every slot is padding
+    i3, v3 = oracle.topk_candidates(S, L, np.full((4, 5), -1, np.int32), 8, 16)
+    assert np.all(i3 == -1) and np.all(np.isneginf(v3))
 
 
 # ---------------------------------------------------------------- the pins have teeth
