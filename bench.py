@@ -317,10 +317,15 @@ def bench_ours(args, world, rank):
 def bench_batched(lt, dev, args, world, peak, L2):
     out = []
     steps = max(3, min(args.steps, 50))
-    for name in ("c3_ragged_64", "c4_prefill_4096", "c5_blocked_16"):
+    for name in ("c3_ragged_64", "c4_prefill_4096", "c5_blocked_16", "c6_listed_16"):
         S, L, w = workloads.make(name)
+        listed = name.startswith("c6")
         nbytes = workloads.read_bytes(L, w.rows, w.row_stride)
+        # copies rotate over what a step touches (whole rows, for every kernel here)
         ncopies = workloads.l2_rotation_copies(nbytes, L2) if nbytes < 4 * L2 else 1
+        cand = workloads.listed_blocks(name).to(dev) if listed else None
+        if listed:  # the method reads the listed blocks' scores and the list, not the whole row
+            nbytes = 4 * cand.numel() * w.block + 4 * cand.numel()
         base = S.to(dev)
         copies = [base] + [base.clone() for _ in range(ncopies - 1)]
         ld = None if L is None else L.to(dev)
@@ -330,6 +335,9 @@ def bench_batched(lt, dev, args, world, peak, L2):
         if w.blocked:
             def step(i, c=copies, n=ncopies):
                 lt.topk_blocked(c[i % n], ld, w.block, w.k_blocks, w.k, out_idx=oi, out_val=ov, out_blocks=ob)
+        elif listed:
+            def step(i, c=copies, n=ncopies):
+                lt.topk_candidates(c[i % n], cand, ld, w.block, w.k, out_idx=oi, out_val=ov)
         else:
             def step(i, c=copies, n=ncopies):
                 lt.topk(c[i % n], ld, w.k, out_idx=oi, out_val=ov)
@@ -345,8 +353,11 @@ def bench_batched(lt, dev, args, world, peak, L2):
             "kernel_us": round(kern_ms * 1000.0, 2),
             "hbm_gbs": round(gbs, 1), "frac_of_peak": round(gbs / peak, 4),
             "l2": f"{ncopies} rotating copies" if ncopies > 1 else "input larger than 4x L2",
-            "plan": lt.plan(w.rows, w.row_stride, w.k, blocked=w.blocked, k_blocks=w.k_blocks),
+            "plan": lt.plan(w.rows, w.row_stride, w.k, blocked=w.blocked or listed,
+                            k_blocks=1 if listed else w.k_blocks),
         })
+        if listed:
+            out[-1]["bytes"] = "listed blocks' scores + the list (the kernel scans the whole row)"
         del copies, base
         torch.cuda.empty_cache()
     return out
@@ -371,11 +382,18 @@ def bench_only(args, world):
     oi = torch.empty(w.rows, w.k, dtype=torch.int32, device=dev)
     ov = torch.empty(w.rows, w.k, dtype=torch.float32, device=dev)
     ob = torch.empty(w.rows, w.k_blocks, dtype=torch.int32, device=dev) if w.blocked else None
+    listed = args.only.startswith("c6")
+    cand = workloads.listed_blocks(args.only).to(dev) if listed else None
+    if listed:
+        nbytes = 4 * cand.numel() * w.block + 4 * cand.numel()
 
     def step(i):
         c = copies[i % ncopies]
         if w.blocked:
             lt.topk_blocked(c, ld, w.block, w.k_blocks, w.k, out_idx=oi, out_val=ov, out_blocks=ob)
+        elif listed:
+            lt.topk_candidates(c, cand, ld, w.block, w.k, out_idx=oi, out_val=ov,
+                               force_cluster=args.force_cluster, force_threads=args.force_threads)
         else:
             lt.topk(c, ld, w.k, out_idx=oi, out_val=ov, force_kernel=KERNEL_IDS[args.kernel],
                     force_cluster=args.force_cluster, force_threads=args.force_threads)
@@ -385,8 +403,9 @@ def bench_only(args, world):
     return {"workload": args.only, "steps": args.steps, "step_us": round(kern * 1000, 3),
             "read_bytes": nbytes,
             "hbm_gbs": round(nbytes / (kern * 1e-3) / 1e9, 1), "copies": ncopies,
-            "plan": lt.plan(w.rows, w.row_stride, w.k, blocked=w.blocked, k_blocks=w.k_blocks,
-                            force_kernel=0 if w.blocked else KERNEL_IDS[args.kernel],
+            "plan": lt.plan(w.rows, w.row_stride, w.k, blocked=w.blocked or listed,
+                            k_blocks=1 if listed else w.k_blocks,
+                            force_kernel=0 if (w.blocked or listed) else KERNEL_IDS[args.kernel],
                             force_cluster=0 if w.blocked else args.force_cluster,
                             force_threads=0 if w.blocked else args.force_threads)}
 
@@ -410,8 +429,10 @@ def bench_trace(args):
     ncopies = workloads.l2_rotation_copies(nbytes, L2) if nbytes < 4 * L2 else 1
     copies = [base] + [base.clone() for _ in range(max(1, ncopies) - 1)]
     ld = None if L is None else L.to(dev)
-    kid = 0 if w.blocked else KERNEL_IDS[args.kernel]
-    pl = lt.plan(w.rows, w.row_stride, w.k, blocked=w.blocked, k_blocks=w.k_blocks,
+    listed = args.trace.startswith("c6")
+    cand = workloads.listed_blocks(args.trace).to(dev) if listed else None
+    kid = 0 if (w.blocked or listed) else KERNEL_IDS[args.kernel]
+    pl = lt.plan(w.rows, w.row_stride, w.k, blocked=w.blocked or listed, k_blocks=1 if listed else w.k_blocks,
                  force_cluster=args.force_cluster, force_threads=args.force_threads, force_kernel=kid)
     ctas = pl["grid"]  # persistent kernels: the first row of each CTA is traced
     tr = torch.full((ctas, 16), -1, dtype=torch.int64, device=dev)
@@ -421,6 +442,8 @@ def bench_trace(args):
         c = copies[i % len(copies)]
         if w.blocked:
             lt.topk_blocked(c, ld, w.block, w.k_blocks, w.k, trace=tr, **kw)
+        elif listed:
+            lt.topk_candidates(c, cand, ld, w.block, w.k, trace=tr, **kw)
         else:
             lt.topk(c, ld, w.k, trace=tr, force_kernel=kid, **kw)
         torch.cuda.synchronize()

@@ -103,6 +103,32 @@ lt_status lt_topk_blocked(const float* scores, const int32_t* lengths, int32_t r
                           int64_t row_stride, int32_t block, int32_t k_blocks, int32_t k,
                           int32_t* out_idx, float* out_val, int32_t* out_blocks, void* stream);
 
+/*
+ * lt_topk_candidates -- top-k restricted to the positions of given blocks.
+ *
+ * The later layers' side of the cross-layer candidate sharing (SGLang and
+ * Miles day-0 support for DeepSeek-V4.1, Q&A on cross-layer sharing): one
+ * layer publishes its kept blocks (for example out_blocks of
+ * lt_topk_blocked) and a later layer ranks its own scores only inside them.
+ * Per row (L = L_r, nblocks = ceil(L / block)): the candidate positions are
+ * the valid positions i < L of the listed blocks; keep the first
+ * min(k, ncand) by (score desc, position asc), written as for lt_topk.
+ *
+ *   block        4, 8, 16 or 32; ceil(row_stride / block) <= 65536, else
+ *                LT_ERR_UNSUPPORTED
+ *   cand_blocks  device int32[rows][n_cand], owned by the caller, read only:
+ *                block ids in any order; ids outside [0, nblocks) are
+ *                ignored (-1 pads a short list), a repeated id counts once
+ *   n_cand       >= 0 (0: every row is all padding)
+ *   k            1 <= k <= LT_MAX_K
+ * Errors as for lt_topk; cand_blocks NULL with n_cand > 0 and rows > 0, a
+ * negative n_cand or block < 1 return LT_ERR_INVALID_ARG.
+ */
+lt_status lt_topk_candidates(const float* scores, const int32_t* lengths, int32_t rows,
+                             int64_t row_stride, int32_t block, const int32_t* cand_blocks,
+                             int32_t n_cand, int32_t k, int32_t* out_idx, float* out_val,
+                             void* stream);
+
 /* Kernels (force_kernel, lt_plan_info.kernel). */
 #define LT_KERNEL_AUTO 0
 /* Register-resident: each CTA holds its first rounds of the row in registers
@@ -163,6 +189,11 @@ lt_status lt_topk_blocked_ex(const float* scores, const int32_t* lengths, int32_
                              int32_t* out_idx, float* out_val, int32_t* out_blocks,
                              int32_t force_cluster, int32_t force_threads, int32_t force_exact,
                              int32_t* counters, int64_t* trace, void* stream);
+lt_status lt_topk_candidates_ex(const float* scores, const int32_t* lengths, int32_t rows,
+                                int64_t row_stride, int32_t block, const int32_t* cand_blocks,
+                                int32_t n_cand, int32_t k, int32_t* out_idx, float* out_val,
+                                int32_t force_cluster, int32_t force_threads, int32_t force_exact,
+                                int32_t* counters, int64_t* trace, void* stream);
 
 /*
  * lt_topk_plan -- the launch the planner would make, without launching.

@@ -66,6 +66,11 @@ def load() -> ctypes.CDLL:
     lib.lt_topk_blocked_ex.argtypes = [vp, vp, i32, i64, i32, i32, i32, vp, vp, vp, i32, i32, i32, vp, vp,
                                        vp]
     lib.lt_topk_blocked_ex.restype = ctypes.c_int
+    lib.lt_topk_candidates.argtypes = [vp, vp, i32, i64, i32, vp, i32, i32, vp, vp, vp]
+    lib.lt_topk_candidates.restype = ctypes.c_int
+    lib.lt_topk_candidates_ex.argtypes = [vp, vp, i32, i64, i32, vp, i32, i32, vp, vp, i32, i32, i32, vp,
+                                          vp, vp]
+    lib.lt_topk_candidates_ex.restype = ctypes.c_int
     lib.lt_topk_plan.argtypes = [i32, i64, i32, i32, i32, i32, i32, i32, i32, i32, vp]
     lib.lt_topk_plan.restype = ctypes.c_int
     lib.lt_status_string.argtypes = [ctypes.c_int]
@@ -184,6 +189,38 @@ def topk_blocked(scores: torch.Tensor, lengths: torch.Tensor | None = None, bloc
     if st != 0:
         raise LtError("lt_topk_blocked", st)
     return out_idx, out_val, out_blocks
+
+
+def topk_candidates(scores: torch.Tensor, cand_blocks: torch.Tensor, lengths: torch.Tensor | None = None,
+                    block: int = 8, k: int = 512, *, out_idx: torch.Tensor | None = None,
+                    out_val: torch.Tensor | None = None, with_values: bool = True, force_cluster: int = 0,
+                    force_threads: int = 0, force_exact: bool = False,
+                    counters: torch.Tensor | None = None, trace: torch.Tensor | None = None,
+                    stream: torch.cuda.Stream | None = None):
+    """Top-k among the positions of the listed blocks (cand_blocks int32 [rows, n_cand] on the same
+    device; ids outside the row's blocks are ignored, repeats count once); returns
+    (idx [rows, k], val [rows, k] or None)."""
+    lib = load()
+    rows, n = _check_scores(scores)
+    dev = scores.device
+    lengths = _check_lengths(lengths, rows, dev)
+    if (not isinstance(cand_blocks, torch.Tensor) or cand_blocks.device != dev
+            or cand_blocks.dtype != torch.int32 or cand_blocks.dim() != 2 or cand_blocks.shape[0] != rows
+            or not cand_blocks.is_contiguous()):
+        raise ValueError("cand_blocks must be a contiguous int32 tensor [rows, n_cand] on the scores' device")
+    out_idx = _out(out_idx, (rows, k), torch.int32, dev, "out_idx")
+    out_val = _out(out_val, (rows, k), torch.float32, dev, "out_val") if with_values else None
+    counters = _counters(counters, dev)
+    with torch.cuda.device(dev):
+        s = (stream or torch.cuda.current_stream(dev)).cuda_stream
+        st = lib.lt_topk_candidates_ex(_ptr(scores), _ptr(lengths), rows, max(n, 1), int(block),
+                                       _ptr(cand_blocks), int(cand_blocks.shape[1]), int(k), _ptr(out_idx),
+                                       _ptr(out_val), int(force_cluster), int(force_threads),
+                                       int(bool(force_exact)), _ptr(counters), _ptr(trace),
+                                       ctypes.c_void_p(s))
+    if st != 0:
+        raise LtError("lt_topk_candidates", st)
+    return out_idx, out_val
 
 
 def plan(rows: int, row_stride: int, k: int, *, blocked: bool = False, block: int = 8,

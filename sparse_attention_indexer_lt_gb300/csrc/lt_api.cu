@@ -470,6 +470,52 @@ lt_status lt_topk_blocked(const float* scores, const int32_t* lengths, int32_t r
                             out_blocks, 0, 0, 0, nullptr, nullptr, stream);
 }
 
+lt_status lt_topk_candidates_ex(const float* scores, const int32_t* lengths, int32_t rows,
+                                int64_t row_stride, int32_t block, const int32_t* cand_blocks,
+                                int32_t n_cand, int32_t k, int32_t* out_idx, float* out_val,
+                                int32_t force_cluster, int32_t force_threads, int32_t force_exact,
+                                int32_t* counters, int64_t* trace, void* stream) {
+  lt_status st = check_common(scores, rows, row_stride, k, out_idx, force_cluster, force_threads);
+  if (st != LT_OK) return st;
+  if (block < 1 || n_cand < 0 || (n_cand > 0 && cand_blocks == nullptr && rows > 0))
+    return LT_ERR_INVALID_ARG;
+  if (block_index(block) < 0) return LT_ERR_UNSUPPORTED;
+  // every CTA holds a bitmap of the row's blocks in kBins words
+  if ((row_stride + block - 1) / block > (int64_t)32 * lt::kBins) return LT_ERR_UNSUPPORTED;
+  if (rows == 0) return LT_OK;
+  Plan plan;
+  int dev = 0;
+  st = make_plan(rows, row_stride, k, true, block, 1, force_cluster, force_threads, LT_KERNEL_AUTO,
+                 aligned16(scores, row_stride), &plan, &dev);
+  if (st != LT_OK) return st;
+  lt::Params p = {};
+  p.external = 1;
+  p.cand_blocks = cand_blocks;
+  p.n_cand = n_cand;
+  p.scores = scores;
+  p.lengths = lengths;
+  p.row_stride = row_stride;
+  p.out_idx = out_idx;
+  p.out_val = out_val;
+  p.out_blocks = nullptr;
+  p.counters = counters;
+  p.trace = trace;
+  p.rows = rows;
+  p.k = k;
+  p.k_blocks = 1;
+  p.force_exact = force_exact ? 1 : 0;
+  p.vec_ok = aligned16(scores, row_stride) ? 1 : 0;
+  return launch(plan, p, stream);
+}
+
+lt_status lt_topk_candidates(const float* scores, const int32_t* lengths, int32_t rows,
+                             int64_t row_stride, int32_t block, const int32_t* cand_blocks,
+                             int32_t n_cand, int32_t k, int32_t* out_idx, float* out_val,
+                             void* stream) {
+  return lt_topk_candidates_ex(scores, lengths, rows, row_stride, block, cand_blocks, n_cand, k,
+                               out_idx, out_val, 0, 0, 0, nullptr, nullptr, stream);
+}
+
 lt_status lt_topk_plan(int32_t rows, int64_t row_stride, int32_t k, int32_t blocked, int32_t block,
                        int32_t k_blocks, int32_t force_cluster, int32_t force_threads, int32_t force_kernel,
                        int32_t aligned, lt_plan_info* info) {
@@ -510,6 +556,6 @@ const char* lt_status_string(lt_status status) {
   }
 }
 
-int32_t lt_version(void) { return 310; }
+int32_t lt_version(void) { return 320; }
 
 }  // extern "C"

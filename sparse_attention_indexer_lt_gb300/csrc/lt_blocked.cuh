@@ -28,11 +28,44 @@ __global__ void __launch_bounds__(T, (T <= 256 ? 3 : 1)) blocked_kernel(Params p
   stamp(p, kTrStart);
   grid_dependents_launch();
   const int64_t cid = (int64_t)(blockIdx.x / (p.clustered ? cluster_size() : 1u));
-  const int role = p.split ? (cid < p.rows ? 1 : 2) : 0;  // 0: both stages in turn
+  // 0: both stages in turn; 1 / 2: plain top-k / stage A side by side;
+  // 3: stage B over a given block list
+  const int role = p.external ? 3 : (p.split ? (cid < p.rows ? 1 : 2) : 0);
   setup_row<T, U, W>(R, p, smem, p.split ? cid % p.rows : cid);
   Misc* m = R.m;
   float4 va[U], vb[U];
   int na[G::kSlots], nb[G::kSlots];
+  if (role == 3) {
+    // a bitmap of the row's listed blocks in the output's bucket-start area
+    // (unused until the ordered output); every CTA holds the whole row's, so
+    // it counts the candidate positions itself
+    const int64_t nblocks = (R.L + W - 1) / W;
+    const uint32_t words = (uint32_t)((nblocks + 31) >> 5);  // <= kBins: checked by the host
+    uint32_t* bits = R.aux;
+    for (uint32_t i = threadIdx.x; i < words; i += T) bits[i] = 0u;
+    __syncthreads();
+    const int32_t* listed = p.cand_blocks + R.row * (int64_t)p.n_cand;
+    for (int32_t j = (int32_t)threadIdx.x; j < p.n_cand; j += T) {
+      const int32_t b = listed[j];
+      if (b >= 0 && (int64_t)b < nblocks) atomicOr(&bits[b >> 5], 1u << (b & 31));
+    }
+    __syncthreads();
+    uint32_t cnt = 0;
+    for (uint32_t i = threadIdx.x; i < words; i += T) cnt += (uint32_t)__popc(bits[i]);
+    const uint32_t nlisted = block_sum<T>(cnt, m);
+    const int64_t lastb = nblocks - 1;
+    const bool last = nblocks > 0 && ((bits[lastb >> 5] >> (lastb & 31)) & 1u) != 0u;
+    const int64_t ncand = (int64_t)nlisted * W - (last ? nblocks * W - R.L : 0);
+    const uint32_t K = (uint32_t)(ncand < (int64_t)p.k ? ncand : (int64_t)p.k);
+    bool intact;
+    uint64_t Tc;
+    const bool exact = select_stage<T, U, W, false>(R, p, va, na, vb, nb, false, K, ncand, p.row_stride,
+                                                    KeepListed<T, U, W>{bits, words * 32u}, true, &intact,
+                                                    &Tc, 0);
+    output_positions<T>(R, p, exact, Tc, K, p.row_stride, true);
+    wait_init(R);
+    return;
+  }
   if (role == 1) {
     const uint32_t K = (uint32_t)(R.L < (int64_t)p.k ? R.L : (int64_t)p.k);
     bool intact;

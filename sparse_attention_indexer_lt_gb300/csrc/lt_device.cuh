@@ -110,6 +110,9 @@ struct Params {
   int32_t clustered;    // launched with cluster size > 1
   int32_t ring_stages;  // streamed kernel: shared-memory ring stages
   int32_t split;        // two-level kernel: stages run as independent cluster groups
+  const int32_t* cand_blocks;  // listed-candidate call: n_cand block ids per row
+  int32_t n_cand;
+  int32_t external;     // two-level kernel: stage B over the listed blocks only
 };
 
 // ------------------------------------------------------------------ smem layout

@@ -169,6 +169,19 @@ struct KeepAll {
 
 // Stage B of the two-level kernel: keep a slot (one block) when its block
 // composite is >= the stage-A threshold composite Tc.
+// Keep the positions of listed blocks: bit b of bits[b >> 5] marks block b of
+// the row; blocks at or past nbits are not listed.
+template <int T, int U, int W>
+struct KeepListed {
+  static constexpr bool kAll = false;
+  const uint32_t* bits;
+  uint32_t nbits;
+  __device__ __forceinline__ bool operator()(const Row& R, int r, const float4 (&)[U], int s, int) const {
+    const int64_t bid = slot_pos<T, U, W>(R, r, s) / W;
+    return bid < (int64_t)nbits && ((bits[bid >> 5] >> (bid & 31)) & 1u) != 0u;
+  }
+};
+
 template <int T, int U, int W>
 struct KeepBlocks {
   static constexpr bool kAll = false;

@@ -63,5 +63,19 @@ def parity_blocked(S, L, block, k_blocks, k, what="", **kw):
     return gi, gv, gb
 
 
+def parity_candidates(S, L, cand, block, k, what="", **kw):
+    S = np.ascontiguousarray(np.asarray(S, dtype=np.float32))
+    Ln = None if L is None else np.asarray(L, dtype=np.int32)
+    C = np.ascontiguousarray(np.asarray(cand, dtype=np.int32))
+    s, l = to_dev(S, Ln)
+    gi, gv = lt.topk_candidates(s, torch.as_tensor(C).cuda(), l, block, k, **kw)
+    torch.cuda.synchronize()
+    gi = gi.cpu().numpy()
+    gv = None if gv is None else gv.cpu().numpy()
+    oi, ov = oracle.topk_candidates(S, Ln, C, block, k)
+    assert_same(gi, gv, oi, ov, what)
+    return gi, gv
+
+
 def counters():
     return torch.zeros(lt.NUM_COUNTERS, dtype=torch.int32, device="cuda")

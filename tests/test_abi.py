@@ -25,8 +25,8 @@ def declared_functions():
 
 def test_header_declares_the_entry_points():
     names = declared_functions()
-    for n in ["lt_topk", "lt_topk_blocked", "lt_topk_ex", "lt_topk_blocked_ex", "lt_topk_plan",
-              "lt_status_string", "lt_version"]:
+    for n in ["lt_topk", "lt_topk_blocked", "lt_topk_ex", "lt_topk_blocked_ex", "lt_topk_candidates",
+              "lt_topk_candidates_ex", "lt_topk_plan", "lt_status_string", "lt_version"]:
         assert n in names
 
 
@@ -74,6 +74,24 @@ def test_blocked_invalid_arguments(lib):
     assert f(fake, None, 1, 64, 6, 4, 4, fake, None, None, 0, 0, 0, None, None, None) == 2   # block unsupported
     assert f(fake, None, 1, 64, 8, 5000, 4, fake, None, None, 0, 0, 0, None, None, None) == 2
     assert f(None, None, 0, 64, 8, 4, 4, None, None, None, 0, 0, 0, None, None, None) == 0
+
+
+def test_candidates_invalid_arguments(lib):
+    fake = P(0x1000)
+    f = lib.lt_topk_candidates_ex
+
+    def call(scores, rows, stride, block, cand, n_cand, k, oi):
+        return f(scores, None, rows, stride, block, cand, n_cand, k, oi, None, 0, 0, 0, None, None, None)
+
+    assert call(fake, 1, 64, 0, fake, 4, 4, fake) == 1          # block < 1
+    assert call(fake, 1, 64, 8, fake, -1, 4, fake) == 1         # n_cand < 0
+    assert call(fake, 1, 64, 8, None, 4, 4, fake) == 1          # no list for n_cand > 0
+    assert call(fake, 1, 64, 8, fake, 4, 0, fake) == 1          # k < 1
+    assert call(None, 1, 64, 8, fake, 4, 4, fake) == 1          # scores NULL
+    assert call(fake, 1, 64, 6, fake, 4, 4, fake) == 2          # block unsupported
+    assert call(fake, 1, 64, 8, fake, 4, 4096, fake) == 2       # k > LT_MAX_K
+    assert call(fake, 1, 262148, 4, fake, 4, 4, fake) == 2      # more than 65536 blocks per row
+    assert call(None, 0, 64, 8, None, 4, 4, None) == 0          # rows == 0: nothing to do
 
 
 def test_plan_rejects_bad_arguments(lib):

@@ -4,9 +4,9 @@ This module draws random numbers and lays them out; it holds none of the
 selection arithmetic. Both the CUDA path and the CPU oracle consume what it
 returns, so parity never depends on it.
 
-Workloads (the pages quote "million-token context, batch size 1" for the
-Lightning TopK figure and 4:1 CSA compression, so one row at 1M tokens has
-262,144 compressed positions; the rest are the batched shapes the
+Workloads (the pages give the Lightning TopK figure for a context of a
+million tokens at batch size 1, and CSA compresses 4:1, so one row at 1M
+tokens has 262,144 compressed positions; the rest are the batched shapes the
 deployment implies):
 
   c1_single_4096     1 x 4096, N(0,1) rounded to bf16 (ties occur), k=512
@@ -18,6 +18,8 @@ deployment implies):
                      N(0,1) fp32, k=512
   c5_blocked_16      16 x 262144, N(0,1) fp32, blocks of 8, top-2048 blocks,
                      then top-512 positions inside them
+  c6_listed_16       the c5 rows; per row 2048 distinct 8-blocks drawn
+                     uniformly (listed_blocks), top-512 among their positions
 
 RNG: ``torch.Generator('cpu').manual_seed(seed)``; draw order lengths, scores,
 tail positions, tail addends.
@@ -57,6 +59,9 @@ CONFIGS = {
                               k_blocks=2048,
                               description="two-level: 16 rows x 262144 fp32, top-2048 of "
                                           "32768 8-blocks, then top-512"),
+    "c6_listed_16": Workload("c6_listed_16", 16, 262144, 512, block=8, k_blocks=2048,
+                             description="listed candidates: the c5 rows, top-512 among 2048 "
+                                         "given 8-blocks per row"),
 }
 
 
@@ -85,7 +90,7 @@ def make(name: str, seed: int = 0):
         r = torch.arange(w.rows, dtype=torch.int64)
         lengths = ((126976 + r + 1) // 4).to(torch.int32)
         scores = torch.randn(w.rows, w.row_stride, generator=g)
-    elif name == "c5_blocked_16":
+    elif name in ("c5_blocked_16", "c6_listed_16"):
         scores = torch.randn(w.rows, w.row_stride, generator=g)
     else:  # pragma: no cover
         raise KeyError(name)
@@ -150,3 +155,14 @@ def read_bytes(lengths, rows: int, stride: int) -> int:
 def l2_rotation_copies(bytes_per_copy: int, l2_bytes: int) -> int:
     """Number of distinct input copies whose total exceeds twice the L2 size."""
     return max(1, math.ceil(2 * l2_bytes / max(1, bytes_per_copy)) + 1)
+
+
+def listed_blocks(name: str, seed: int = 0) -> torch.Tensor:
+    """The block list of a listed-candidates workload: per row, k_blocks distinct
+    block ids drawn uniformly from the row's blocks, ascending (the form an
+    earlier layer publishes; which blocks does not change the work)."""
+    w = CONFIGS[name]
+    g = torch.Generator("cpu").manual_seed(1000 + seed)
+    nb = (w.row_stride + w.block - 1) // w.block
+    rows = [torch.sort(torch.randperm(nb, generator=g)[:w.k_blocks]).values for _ in range(w.rows)]
+    return torch.stack(rows).to(torch.int32).contiguous()
