@@ -357,7 +357,8 @@ def bench_batched(lt, dev, args, world, peak, L2):
                             k_blocks=1 if listed else w.k_blocks),
         })
         if listed:
-            out[-1]["bytes"] = "listed blocks' scores + the list (the kernel scans the whole row)"
+            out[-1]["bytes"] = "listed blocks' scores + the list"
+            out[-1]["plan"] = {"kernel": "listed", "cluster": 1, "threads": 512, "grid": w.rows}
         del copies, base
         torch.cuda.empty_cache()
     return out
@@ -403,11 +404,11 @@ def bench_only(args, world):
     return {"workload": args.only, "steps": args.steps, "step_us": round(kern * 1000, 3),
             "read_bytes": nbytes,
             "hbm_gbs": round(nbytes / (kern * 1e-3) / 1e9, 1), "copies": ncopies,
-            "plan": lt.plan(w.rows, w.row_stride, w.k, blocked=w.blocked or listed,
-                            k_blocks=1 if listed else w.k_blocks,
-                            force_kernel=0 if (w.blocked or listed) else KERNEL_IDS[args.kernel],
-                            force_cluster=0 if w.blocked else args.force_cluster,
-                            force_threads=0 if w.blocked else args.force_threads)}
+            "plan": ({"kernel": "listed", "cluster": 1, "threads": 512, "grid": w.rows} if listed else
+                     lt.plan(w.rows, w.row_stride, w.k, blocked=w.blocked, k_blocks=w.k_blocks,
+                             force_kernel=0 if w.blocked else KERNEL_IDS[args.kernel],
+                             force_cluster=0 if w.blocked else args.force_cluster,
+                             force_threads=0 if w.blocked else args.force_threads))}
 
 
 TRACE_NAMES = ["start", "hist", "merge", "estimate", "filter", "exchange", "exact", "output",

@@ -33,7 +33,7 @@ constexpr int kMaxDevices = 64;
 constexpr int kWideThreads = 512;
 constexpr int kNarrowThreads = 256;
 constexpr int64_t kWideRound = 512 * 8 * 4;  // positions per CTA per round (wide)
-constexpr int kSlots = 14;                    // kernel variants
+constexpr int kSlots = 18;                    // kernel variants
 // the streamed kernel's launch bounds: CTAs per SM for 256 / 512 threads
 constexpr int stream_ctas_per_sm(int threads) { return threads == 256 ? 3 : 2; }
 constexpr int kStreamMaxStages = 8;
@@ -61,6 +61,7 @@ int block_index(int block) {
   }
 }
 
+// slots 14..17: the listed-candidate kernel, by block size
 int kernel_slot(bool blocked, int block, int threads, bool stream = false, bool one_round = false) {
   const int wide = threads == kWideThreads ? 1 : 0;
   if (stream) return 10 + wide;
@@ -485,9 +486,36 @@ lt_status lt_topk_candidates_ex(const float* scores, const int32_t* lengths, int
   if (rows == 0) return LT_OK;
   Plan plan;
   int dev = 0;
-  st = make_plan(rows, row_stride, k, true, block, 1, force_cluster, force_threads, LT_KERNEL_AUTO,
-                 aligned16(scores, row_stride), &plan, &dev);
-  if (st != LT_OK) return st;
+  // A list of at most one register round of blocks goes to the listed
+  // kernel, which reads only those blocks; longer lists, forced cluster
+  // shapes and force_exact scan whole rows with the two-level kernel.
+  bool gathered = force_exact == 0 && (force_cluster == 0 || force_cluster == 1) &&
+                  (force_threads == 0 || force_threads == kWideThreads) &&
+                  (int64_t)n_cand <= lt::listed_round_blocks(block);
+  if (gathered) {
+    DeviceInfo* di = nullptr;
+    st = device_info(&di, &dev);
+    if (st != LT_OK) return st;
+    plan.threads = kWideThreads;
+    plan.cluster = 1;
+    plan.grid = rows;
+    plan.cap = 512u * 8u * 4u;  // a slot for every gathered position: no overflow
+    plan.seg_shift = 14;
+    plan.wstage = (uint32_t)kWideThreads * 16u * (uint32_t)lt::kStageF4;
+    plan.sel_cap = next_pow2(k < 32 ? 32u : (uint32_t)k);
+    plan.func = lt::listed_kernel_ptr(block);
+    plan.smem = lt::make_layout(false, plan.cap, plan.sel_cap, plan.wstage).total;
+    gathered = plan.func != nullptr && (int)plan.smem <= di->smem_optin;
+    if (gathered) {
+      st = prepare_kernel(dev, 14 + block_index(block), plan.func, plan.smem, 1);
+      if (st != LT_OK) return st;
+    }
+  }
+  if (!gathered) {
+    st = make_plan(rows, row_stride, k, true, block, 1, force_cluster, force_threads, LT_KERNEL_AUTO,
+                   aligned16(scores, row_stride), &plan, &dev);
+    if (st != LT_OK) return st;
+  }
   lt::Params p = {};
   p.external = 1;
   p.cand_blocks = cand_blocks;

@@ -12,4 +12,8 @@ const void* blocked_kernel_ptr_narrow(int block);
 const void* blocked_kernel_ptr_wide(int block);
 // the streamed top-k kernel: 256 threads (three CTAs per SM) or 512 (two)
 const void* stream_kernel_ptr(int threads);
+// listed-candidate kernel (512 threads, one CTA per row, only the listed
+// blocks read): nullptr for an unsupported block size
+const void* listed_kernel_ptr(int block);
+int64_t listed_round_blocks(int block);
 }  // namespace lt

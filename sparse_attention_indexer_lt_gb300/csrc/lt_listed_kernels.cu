@@ -1,0 +1,196 @@
+// lt_listed_kernels.cu -- top-k among the positions of a short block list,
+// reading only those blocks.
+#include "lt_kernels.cuh"
+#include "lt_launch.h"
+
+namespace lt {
+
+// The i-th of a thread's block ids (i < B).
+template <int B>
+__device__ __forceinline__ uint32_t pick_id(const uint32_t (&a)[B], uint32_t i) {
+  uint32_t r = a[0];
+#pragma unroll
+  for (int j = 1; j < B; ++j) r = (i == (uint32_t)j) ? a[j] : r;
+  return r;
+}
+
+// One CTA per row. The row's listed blocks (ids outside the row ignored,
+// repeats once) fit one register round of T threads x U float4: thread t
+// loads the t-th group of BPT blocks of the ascending unique list, so the
+// CTA reads only those blocks' scores. Then the single-round selection:
+// exact 11-bit histogram of the keys of every gathered score (key_of: NaN
+// lowest, like the fillers past the list), so the threshold -- the lower
+// edge of the bin holding the K-th key -- keeps at least K; filter; ordered
+// output. The candidate area holds every gathered position, so no row can
+// overflow it. Should a filter ever keep fewer than K, it is redone keeping
+// every position.
+template <int T, int W>
+__global__ void __launch_bounds__(T, 1) listed_kernel(Params p) {
+  constexpr int U = 8;          // float4 per thread: the round
+  constexpr int VS = W / 4;     // float4 per block
+  constexpr int BPT = U / VS;   // blocks per thread
+  using G = Geo<T, U, W>;
+  static_assert(G::kSlots == BPT, "a slot is a block");
+  extern __shared__ __align__(128) unsigned char smem[];
+  Row R;
+  stamp(p, kTrStart);
+  grid_dependents_launch();
+  setup_row<T, U, W>(R, p, smem);
+  Misc* m = R.m;
+  const int64_t nblocks = (R.L + W - 1) / W;
+  const uint32_t words = (uint32_t)((nblocks + 31) >> 5);  // <= kBins: checked by the host
+
+  // (1) bitmap of the listed blocks, then their ids ascending in the
+  // candidate area (free until the filter)
+  uint32_t* bits = R.aux;
+  for (uint32_t i = threadIdx.x; i < words; i += T) bits[i] = 0u;
+  __syncthreads();
+  {
+    // the list (at most T * BPT entries: host) read with all loads in flight
+    const int32_t* listed = p.cand_blocks + R.row * (int64_t)p.n_cand;
+    int32_t lb[BPT];
+#pragma unroll
+    for (int i = 0; i < BPT; ++i) {
+      const int32_t j = (int32_t)threadIdx.x + i * T;
+      lb[i] = j < p.n_cand ? __ldg(listed + j) : -1;
+    }
+#pragma unroll
+    for (int i = 0; i < BPT; ++i) {
+      const int32_t b = lb[i];
+      if (b >= 0 && (int64_t)b < nblocks) atomicOr(&bits[b >> 5], 1u << (b & 31));
+    }
+  }
+  __syncthreads();
+  const uint32_t wpt = (words + T - 1) / T;
+  const uint32_t w0 = threadIdx.x * wpt;
+  const uint32_t w1 = min(w0 + wpt, words);
+  uint32_t cnt = 0;
+  for (uint32_t w = w0; w < w1; ++w) cnt += (uint32_t)__popc(bits[w]);
+  uint32_t* ids = reinterpret_cast<uint32_t*>(R.cand);
+  uint32_t o = block_prefix_excl<T>(cnt, m);
+  for (uint32_t w = w0; w < w1; ++w)
+    for (uint32_t x = bits[w]; x; x &= x - 1u) ids[o++] = 32u * w + (uint32_t)(__ffs(x) - 1);
+  if (threadIdx.x == T - 1) m->aux[0] = o;  // the number of unique listed blocks (<= T * BPT: host)
+  const int64_t lastb = nblocks - 1;
+  const bool last = nblocks > 0 && ((bits[lastb >> 5] >> (lastb & 31)) & 1u) != 0u;
+  __syncthreads();
+  const uint32_t n_u = m->aux[0];
+
+  // (2) this thread's blocks, gathered; positions past the list or the row
+  // hold NaN (n[j] counts a block's valid positions)
+  uint32_t bid[BPT];
+#pragma unroll
+  for (int j = 0; j < BPT; ++j) {
+    const uint32_t u = threadIdx.x * BPT + j;
+    bid[j] = u < n_u ? ids[u] : 0u;
+  }
+  __syncthreads();  // the id list is in registers: the candidate area is free
+  float4 v[U];
+  int n[BPT];
+  const bool vec = p.vec_ok != 0;
+#pragma unroll
+  for (int j = 0; j < BPT; ++j) {
+    const uint32_t u = threadIdx.x * BPT + j;
+    const int64_t pos0 = (int64_t)bid[j] * W;
+    int64_t nv = u < n_u ? R.L - pos0 : 0;
+    nv = nv < 0 ? 0 : (nv > W ? W : nv);
+    n[j] = (int)nv;
+#pragma unroll
+    for (int q = 0; q < VS; ++q) {
+      const int64_t left = nv - 4 * q;
+      if (vec && left >= 4) v[j * VS + q] = ldg4(R.rowp + pos0 + 4 * q);
+      else v[j * VS + q] = load4_scalar(R.rowp + pos0 + 4 * q, left < 0 ? 0 : (left > 4 ? 4 : (int)left));
+    }
+  }
+  const int64_t ncand = (int64_t)n_u * W - (last ? nblocks * W - R.L : 0);
+  const uint32_t K = (uint32_t)(ncand < (int64_t)p.k ? ncand : (int64_t)p.k);
+  const uint32_t cap = (uint32_t)p.cap;
+
+  if (K > 0) {
+    // (3) threshold from the exact histogram of the gathered keys (the NaN
+    // fillers have key 0 and land in bin 0, below any threshold but t = 0,
+    // "all")
+    uint32_t t = 0;
+    if (ncand > (int64_t)(cap / 2)) {
+      zero_bins<T>(R.hist);
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        atomicAdd(&R.hist[key_of(v[u].x) >> 21], 1u);
+        atomicAdd(&R.hist[key_of(v[u].y) >> 21], 1u);
+        atomicAdd(&R.hist[key_of(v[u].z) >> 21], 1u);
+        atomicAdd(&R.hist[key_of(v[u].w) >> 21], 1u);
+      }
+      stamp(R, kTrHist);
+      __syncthreads();
+      find_digit<T>(R.hist, K, m);
+      t = m->res_digit << 21;
+    }
+    stamp(R, kTrEstimate);
+    {
+      // the output's bucket counts start from zero; the exchange's barrier
+      // orders these stores before them
+      uint4* z = reinterpret_cast<uint4*>(R.hist);
+      for (int i = threadIdx.x; i < kOutBuckets / 4; i += T) z[i] = make_uint4(0, 0, 0, 0);
+    }
+    // (4) filter: every gathered position whose score passes (NaN fillers fail)
+#pragma unroll 1
+    for (int pass = 0; pass < 2; ++pass) {
+      const bool all = pass == 1 || t == 0u;
+      uint32_t mask = all ? round_mask<T, U, W>(R, 0, v, n, 0.0f, true, KeepAll{})
+                          : ge_mask<U>(v, threshold_float(t));
+      uint32_t kmn = 0xffffffffu, kmx = 0u;
+      if (mask) {
+        uint2* list = R.cand;
+        uint32_t oc = atomicAdd(&m->local_count, (uint32_t)__popc(mask));
+        const uint32_t lane = lane_id();
+#pragma unroll
+        for (int f = 0; f < U; ++f) R.wst[f * 32 + lane] = v[f];
+        const float* st = reinterpret_cast<const float*>(R.wst) + 4 * lane;
+        do {
+          const uint32_t bit = (uint32_t)(__ffs(mask) - 1);
+          mask &= mask - 1u;
+          const uint32_t F = bit >> 2, e = bit & 3u;
+          const uint32_t kk = key_of(st[128 * F + e]);
+          kmn = min(kmn, kk);
+          kmx = max(kmx, kk);
+          const uint32_t pos = pick_id<BPT>(bid, F / VS) * W + 4u * (F % VS) + e;
+          if (oc < cap) list[oc] = make_uint2(kk, pos);
+          ++oc;
+        } while (mask);
+      }
+      flush_key_range(R, kmn, kmx);
+      stamp(R, kTrFilter);
+      exchange_segments<T>(R, false);  // one CTA: segment 0 is the whole list
+      stamp(R, kTrExchange);
+      if (m->seg_cnt[0] >= K) break;
+      // fewer than K kept (the threshold above guarantees at least K): start
+      // over keeping every position
+      __syncthreads();
+      if (threadIdx.x == 0) {
+        m->local_count = 0;
+        m->local_min = 0xffffffffu;
+        m->local_max = 0u;
+      }
+      __syncthreads();
+    }
+    stamp(R, kTrExact);
+    bump(p, R, kCntFast);
+  }
+  output_positions<T>(R, p, false, 0, K, p.row_stride, false);
+  wait_init(R);
+}
+
+const void* listed_kernel_ptr(int block) {
+  switch (block) {
+    case 4: return reinterpret_cast<const void*>(&listed_kernel<512, 4>);
+    case 8: return reinterpret_cast<const void*>(&listed_kernel<512, 8>);
+    case 16: return reinterpret_cast<const void*>(&listed_kernel<512, 16>);
+    case 32: return reinterpret_cast<const void*>(&listed_kernel<512, 32>);
+    default: return nullptr;
+  }
+}
+
+// Blocks one listed-kernel CTA gathers in its single register round.
+int64_t listed_round_blocks(int block) { return 512 * 8 * 4 / block; }
+
+}  // namespace lt
