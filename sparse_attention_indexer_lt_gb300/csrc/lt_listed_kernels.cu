@@ -15,9 +15,8 @@ __device__ __forceinline__ uint32_t pick_id(const uint32_t (&a)[B], uint32_t i) 
 }
 
 // One CTA per row. The row's listed blocks (ids outside the row ignored,
-// repeats once) fit one register round of T threads x U float4: thread t
-// loads the t-th group of BPT blocks of the ascending unique list, so the
-// CTA reads only those blocks' scores. Then the single-round selection:
+// repeats once) fit one register round of T threads x U float4, gathered from
+// the ascending unique list, so the CTA reads only those blocks' scores. Then the single-round selection:
 // exact 11-bit histogram of the keys of every gathered score (key_of: NaN
 // lowest, like the fillers past the list), so the threshold -- the lower
 // edge of the bin holding the K-th key -- keeps at least K; filter; ordered
@@ -76,31 +75,33 @@ __global__ void __launch_bounds__(T, 1) listed_kernel(Params p) {
   __syncthreads();
   const uint32_t n_u = m->aux[0];
 
-  // (2) this thread's blocks, gathered; positions past the list or the row
-  // hold NaN (n[j] counts a block's valid positions)
-  uint32_t bid[BPT];
+  // (2) the gathered round: warp w takes blocks [w * U * LPB, (w + 1) * U * LPB)
+  // of the list; its float4 f of lane l is float4 l % VS of block
+  // w * U * LPB + f * LPB + l / VS, so the lanes of one load share whole
+  // blocks (each 32-byte sector of a block is requested once). Positions past
+  // the list or the row hold NaN; nf[f] counts a float4's valid positions.
+  constexpr int LPB = 32 / VS;  // blocks per warp load
+  const uint32_t lane = lane_id();
+  const uint32_t q = lane % VS;
+  const uint32_t ubase = (threadIdx.x >> 5) * (U * LPB) + lane / VS;
+  uint32_t bidf[U];
 #pragma unroll
-  for (int j = 0; j < BPT; ++j) {
-    const uint32_t u = threadIdx.x * BPT + j;
-    bid[j] = u < n_u ? ids[u] : 0u;
+  for (int f = 0; f < U; ++f) {
+    const uint32_t u = ubase + f * LPB;
+    bidf[f] = u < n_u ? ids[u] : 0u;
   }
   __syncthreads();  // the id list is in registers: the candidate area is free
   float4 v[U];
-  int n[BPT];
+  int nf[U];
   const bool vec = p.vec_ok != 0;
 #pragma unroll
-  for (int j = 0; j < BPT; ++j) {
-    const uint32_t u = threadIdx.x * BPT + j;
-    const int64_t pos0 = (int64_t)bid[j] * W;
-    int64_t nv = u < n_u ? R.L - pos0 : 0;
-    nv = nv < 0 ? 0 : (nv > W ? W : nv);
-    n[j] = (int)nv;
-#pragma unroll
-    for (int q = 0; q < VS; ++q) {
-      const int64_t left = nv - 4 * q;
-      if (vec && left >= 4) v[j * VS + q] = ldg4(R.rowp + pos0 + 4 * q);
-      else v[j * VS + q] = load4_scalar(R.rowp + pos0 + 4 * q, left < 0 ? 0 : (left > 4 ? 4 : (int)left));
-    }
+  for (int f = 0; f < U; ++f) {
+    const int64_t p0 = (int64_t)bidf[f] * W + 4 * q;
+    int64_t nv = ubase + f * LPB < n_u ? R.L - p0 : 0;
+    nv = nv < 0 ? 0 : (nv > 4 ? 4 : nv);
+    nf[f] = (int)nv;
+    if (vec && nv == 4) v[f] = ldg4(R.rowp + p0);
+    else v[f] = load4_scalar(R.rowp + p0, (int)nv);
   }
   const int64_t ncand = (int64_t)n_u * W - (last ? nblocks * W - R.L : 0);
   const uint32_t K = (uint32_t)(ncand < (int64_t)p.k ? ncand : (int64_t)p.k);
@@ -136,13 +137,17 @@ __global__ void __launch_bounds__(T, 1) listed_kernel(Params p) {
 #pragma unroll 1
     for (int pass = 0; pass < 2; ++pass) {
       const bool all = pass == 1 || t == 0u;
-      uint32_t mask = all ? round_mask<T, U, W>(R, 0, v, n, 0.0f, true, KeepAll{})
-                          : ge_mask<U>(v, threshold_float(t));
+      uint32_t mask = 0;
+      if (all) {
+#pragma unroll
+        for (int f = 0; f < U; ++f) mask |= ((1u << nf[f]) - 1u) << (4 * f);
+      } else {
+        mask = ge_mask<U>(v, threshold_float(t));
+      }
       uint32_t kmn = 0xffffffffu, kmx = 0u;
       if (mask) {
         uint2* list = R.cand;
         uint32_t oc = atomicAdd(&m->local_count, (uint32_t)__popc(mask));
-        const uint32_t lane = lane_id();
 #pragma unroll
         for (int f = 0; f < U; ++f) R.wst[f * 32 + lane] = v[f];
         const float* st = reinterpret_cast<const float*>(R.wst) + 4 * lane;
@@ -153,7 +158,7 @@ __global__ void __launch_bounds__(T, 1) listed_kernel(Params p) {
           const uint32_t kk = key_of(st[128 * F + e]);
           kmn = min(kmn, kk);
           kmx = max(kmx, kk);
-          const uint32_t pos = pick_id<BPT>(bid, F / VS) * W + 4u * (F % VS) + e;
+          const uint32_t pos = pick_id<U>(bidf, F) * W + 4u * q + e;
           if (oc < cap) list[oc] = make_uint2(kk, pos);
           ++oc;
         } while (mask);
