@@ -433,8 +433,12 @@ def bench_trace(args):
     listed = args.trace.startswith("c6")
     cand = workloads.listed_blocks(args.trace).to(dev) if listed else None
     kid = 0 if (w.blocked or listed) else KERNEL_IDS[args.kernel]
-    pl = lt.plan(w.rows, w.row_stride, w.k, blocked=w.blocked or listed, k_blocks=1 if listed else w.k_blocks,
-                 force_cluster=args.force_cluster, force_threads=args.force_threads, force_kernel=kid)
+    if listed and args.force_cluster in (0, 1) and args.force_threads in (0, 512):
+        # a list of at most one register round of blocks takes the listed kernel: one CTA per row
+        pl = {"kernel": "listed", "cluster": 1, "threads": 512, "grid": w.rows}
+    else:
+        pl = lt.plan(w.rows, w.row_stride, w.k, blocked=w.blocked or listed, k_blocks=1 if listed else w.k_blocks,
+                     force_cluster=args.force_cluster, force_threads=args.force_threads, force_kernel=kid)
     ctas = pl["grid"]  # persistent kernels: the first row of each CTA is traced
     tr = torch.full((ctas, 16), -1, dtype=torch.int64, device=dev)
     kw = dict(force_cluster=args.force_cluster, force_threads=args.force_threads)
