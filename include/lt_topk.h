@@ -123,6 +123,11 @@ lt_status lt_topk_blocked(const float* scores, const int32_t* lengths, int32_t r
  *   k            1 <= k <= LT_MAX_K
  * Errors as for lt_topk; cand_blocks NULL with n_cand > 0 and rows > 0, a
  * negative n_cand or block < 1 return LT_ERR_INVALID_ARG.
+ *
+ * A list of at most 16384 / block entries per row (2048 blocks of 8) is
+ * served by a kernel that reads only the listed blocks (one CTA per row);
+ * longer lists, and the _ex call with a forced cluster or thread count other
+ * than 1 / 512 or with force_exact, scan whole rows. Same results either way.
  */
 lt_status lt_topk_candidates(const float* scores, const int32_t* lengths, int32_t rows,
                              int64_t row_stride, int32_t block, const int32_t* cand_blocks,
@@ -161,7 +166,9 @@ lt_status lt_topk_candidates(const float* scores, const int32_t* lengths, int32_
  *                  that row's output is undefined -- never seen in practice).
  *                  For the two-level call, each row counts once per stage
  *                  (with k_blocks >= k and out_blocks NULL, only stage B
- *                  runs: once).
+ *                  runs: once); for the listed-candidate call, once (the
+ *                  kernel that reads only the listed blocks always counts
+ *                  [0]).
  *   trace          NULL, or device int64[grid CTAs * 16] receiving, from
  *                  thread 0 of each CTA, global-timer nanoseconds at phase
  *                  boundaries (entry, sample histogram, first cluster merge,
