@@ -275,6 +275,18 @@ def test_candidates_ignore_order_repeats_and_padding():
     assert np.all(i3 == -1) and np.all(np.isneginf(v3))
 
 
+def test_listed_workload_lists_are_valid_inputs():
+    """The c6 input generator: per row k_blocks distinct block ids of the row,
+    ascending, reproducible from the seed."""
+    w = workloads.CONFIGS["c6_listed_16"]
+    c = workloads.listed_blocks("c6_listed_16").numpy()
+    nb = (w.row_stride + w.block - 1) // w.block
+    assert c.shape == (w.rows, w.k_blocks) and c.dtype == np.int32
+    assert np.all(np.diff(c, axis=1) > 0) and c.min() >= 0 and c.max() < nb
+    assert np.array_equal(c, workloads.listed_blocks("c6_listed_16").numpy())
+    assert not np.array_equal(c, workloads.listed_blocks("c6_listed_16", seed=1).numpy())
+
+
 # ---------------------------------------------------------------- the pins have teeth
 
 def test_checkers_reject_planted_mistakes():
