@@ -37,7 +37,7 @@
 //     repeated ids count once, the list's order does not matter. Steps (3)
 //     and (4) above on the listed blocks.
 //
-// Float order (the pages are silent; reading stated here and in the design doc):
+// Float order (the pages are silent; the reading taken here):
 // IEEE order on numbers, so -0.0 == +0.0 and +-inf are ordinary extremes;
 // denormals compare as themselves; NaN ranks below every number (below -inf)
 // and NaNs tie with each other. The comparator below uses float compares,

@@ -16,7 +16,7 @@ from pathlib import Path
 
 import torch
 
-__all__ = ["topk", "topk_blocked", "plan", "load", "library_path", "LtError", "NUM_COUNTERS",
+__all__ = ["topk", "topk_blocked", "topk_candidates", "plan", "load", "library_path", "LtError", "NUM_COUNTERS",
            "status_string", "version", "PlanInfo", "KERNEL_AUTO", "KERNEL_RESIDENT", "KERNEL_STREAM"]
 
 _LIB_PATH = Path(__file__).resolve().parent / "liblt_topk.so"

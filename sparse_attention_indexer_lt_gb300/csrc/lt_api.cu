@@ -121,8 +121,13 @@ lt_status prepare_kernel(int dev, int slot, const void* func, uint32_t smem, int
     g_smem_set[dev][slot] = (int)smem;
   }
   if (cluster > 8 && !g_nonportable_set[dev][slot]) {
-    if (cudaFuncSetAttribute(func, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess)
+    // refused on devices without 16-CTA clusters: the plan then shrinks, so
+    // the error is cleared (only when no earlier error was pending)
+    const bool clean = cudaPeekAtLastError() == cudaSuccess;
+    if (cudaFuncSetAttribute(func, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess) {
+      if (clean) (void)cudaGetLastError();
       return LT_ERR_UNSUPPORTED;
+    }
     g_nonportable_set[dev][slot] = true;
   }
   return LT_OK;
@@ -149,8 +154,10 @@ int active_clusters_query(const void* func, int cluster, int threads, uint32_t s
   cfg.attrs = &attr;
   cfg.numAttrs = 1;
   int n = 0;
+  // a caller's pending error must survive: clear only an error this query set
+  const bool clean = cudaPeekAtLastError() == cudaSuccess;
   if (cudaOccupancyMaxActiveClusters(&n, func, &cfg) != cudaSuccess) {
-    (void)cudaGetLastError();  // clear the error this query may leave behind
+    if (clean) (void)cudaGetLastError();
     return 0;
   }
   return n;
@@ -316,8 +323,9 @@ lt_status make_stream_plan(int32_t rows, int64_t row_stride, int32_t k, int32_t 
     if (st == LT_OK) {
       if (c == 1) {
         int per_sm = 0;
+        const bool clean = cudaPeekAtLastError() == cudaSuccess;
         if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, plan->func, threads, smem) != cudaSuccess) {
-          (void)cudaGetLastError();
+          if (clean) (void)cudaGetLastError();
           per_sm = 0;
         }
         resident = per_sm * di->sms;
