@@ -4,6 +4,9 @@ Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
 ``bench.py`` may import this package. The CUDA library never imports, links or
 calls it, and it never imports the CUDA library.
 
+Scores may also be given as bf16 bit patterns (the ``*_bf16`` functions): they
+are widened to the fp32 numbers they denote (exact) and ranked as those.
+
 The arithmetic lives in ``lt_oracle.cpp`` (a per-row ``std::stable_sort`` by
 score descending, ties by index ascending; the two-level variant in the page's
 literal step order). This module only compiles it with the host compiler and
@@ -75,6 +78,33 @@ def _prep(scores, lengths):
 
 def _ptr(a):
     return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def widen_bf16(bits) -> np.ndarray:
+    """bf16 bit patterns (uint16) -> the fp32 numbers they denote.
+
+    A bf16 number is the upper half of an fp32 (sign, the same 8 exponent
+    bits, the leading 7 fraction bits), so the fp32 it denotes has those 16
+    bits on top and zeros below; the conversion is exact. Scores given as
+    bf16 are ranked as these fp32 numbers (the same selection rules apply).
+    """
+    b = np.ascontiguousarray(np.asarray(bits, dtype=np.uint16))
+    return (b.astype(np.uint32) << np.uint32(16)).view(np.float32)
+
+
+def topk_bf16(bits, lengths, k: int, nthreads: int | None = None):
+    """topk over bf16 scores (uint16 bit patterns): the fp32 numbers they denote."""
+    return topk(widen_bf16(bits), lengths, k, nthreads)
+
+
+def topk_blocked_bf16(bits, lengths, block: int, k_blocks: int, k: int, nthreads: int | None = None):
+    """topk_blocked over bf16 scores (uint16 bit patterns)."""
+    return topk_blocked(widen_bf16(bits), lengths, block, k_blocks, k, nthreads)
+
+
+def topk_candidates_bf16(bits, lengths, cand_blocks, block: int, k: int, nthreads: int | None = None):
+    """topk_candidates over bf16 scores (uint16 bit patterns)."""
+    return topk_candidates(widen_bf16(bits), lengths, cand_blocks, block, k, nthreads)
 
 
 def topk(scores, lengths, k: int, nthreads: int | None = None):

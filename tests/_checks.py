@@ -131,3 +131,16 @@ def equal_outputs(idx_a, val_a, idx_b, val_b) -> bool:
     """Bit-exact equality of two (idx, val) outputs."""
     return (np.array_equal(np.asarray(idx_a), np.asarray(idx_b))
             and np.array_equal(np.asarray(val_a).view(np.uint32), np.asarray(val_b).view(np.uint32)))
+
+
+def bf16_value(bits: int) -> float:
+    """The number a bf16 bit pattern denotes, from the format's fields (1 sign
+    bit, 8 exponent bits with bias 127, 7 fraction bits), not from a bit shift."""
+    s = -1.0 if (bits >> 15) & 1 else 1.0
+    e = (bits >> 7) & 0xFF
+    f = bits & 0x7F
+    if e == 0xFF:
+        return s * math.inf if f == 0 else math.nan
+    if e == 0:
+        return s * math.ldexp(f / 128.0, -126)
+    return s * math.ldexp(1.0 + f / 128.0, e - 127)

@@ -322,3 +322,87 @@ def test_checkers_reject_planted_mistakes():
     s = np.array([1.0, float("nan"), 2.0], dtype=np.float32)
     assert brute_topk_row(s, 3, 3) == [2, 0, 1]
     assert lexsort_topk_row(s, 3, 3) == [2, 0, 1]
+
+
+# ---------------------------------------------------------------- bf16 scores
+
+def _bf16_cases():
+    return _load("bf16_values.jsonl")
+
+
+@pytest.mark.parametrize("case", _bf16_cases(), ids=lambda c: c["bits"])
+def test_bf16_widening_hand_values(case):
+    """The oracle's bf16 widening gives the number worked out by hand from the
+    format's fields (sign of zero and NaN-ness included)."""
+    from _checks import bf16_value
+    bits = int(case["bits"], 16)
+    got = float(oracle.widen_bf16(np.array([bits], np.uint16))[0])
+    want = _f(case["value"])
+    assert bf16_value(bits) == want or (math.isnan(want) and math.isnan(bf16_value(bits)))
+    if math.isnan(want):
+        assert math.isnan(got)
+    else:
+        assert got == want and math.copysign(1.0, got) == math.copysign(1.0, want)
+
+
+def test_bf16_widening_matches_field_decoding_and_torch_everywhere():
+    """All 65536 patterns: the widened fp32 equals the field decoding and
+    torch's own bf16 -> float32 conversion (bitwise for numbers)."""
+    from _checks import bf16_value
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    got = oracle.widen_bf16(bits)
+    lib = torch.from_numpy(bits.view(np.int16).copy()).view(torch.bfloat16).float().numpy()
+    nan = np.isnan(got)
+    assert np.array_equal(nan, np.isnan(lib))
+    assert np.array_equal(got[~nan].view(np.uint32), lib[~nan].view(np.uint32))
+    ref = np.array([bf16_value(int(b)) for b in bits], dtype=np.float64)
+    assert np.array_equal(np.isnan(ref), nan)
+    assert np.array_equal(got[~nan].astype(np.float64), ref[~nan])
+    assert np.array_equal(np.signbit(got[~nan]), np.signbit(ref[~nan]))
+
+
+BF16_ALPHABET = [0x0000, 0x8000, 0x3F80, 0x3F81, 0xFF80, 0x7FC0, 0x0001]  # +0 -0 1 1+2^-7 -inf NaN 2^-133
+
+
+def test_bf16_topk_brute_force_small_rows():
+    """Every row of length <= 4 over a 7-pattern bf16 alphabet (ties, signed
+    zeros, NaN, -inf, a subnormal), every k: the oracle on bf16 bits equals
+    Python `sorted` over the field-decoded numbers, and its values are the
+    decoded numbers."""
+    from _checks import bf16_value
+    for n in range(1, 5):
+        for row in itertools.product(BF16_ALPHABET, repeat=n):
+            bits = np.array(row, np.uint16)
+            dec = [bf16_value(b) for b in row]
+            for k in range(1, n + 2):
+                idx, val = oracle.topk_bf16(bits[None, :], None, k, nthreads=1)
+                want = brute_topk_row(dec, n, k)
+                assert idx[0].tolist() == want, (row, k)
+                for j, i in enumerate(want):
+                    if i < 0:
+                        assert val[0, j] == -np.inf
+                    elif math.isnan(dec[i]):
+                        assert np.isnan(val[0, j])
+                    else:
+                        assert float(val[0, j]) == dec[i] and np.signbit(val[0, j]) == (math.copysign(1, dec[i]) < 0)
+
+
+def test_bf16_blocked_and_candidates_brute_force():
+    """Two-level and listed-candidate oracles on bf16 bits against their Python
+    restatements over the field-decoded numbers."""
+    from _checks import bf16_value
+    rng = np.random.default_rng(7)
+    pool = np.array(BF16_ALPHABET + [0x4049, 0xC0A0, 0x7F80], np.uint16)
+    for _ in range(200):
+        n = int(rng.integers(1, 40))
+        bits = pool[rng.integers(0, pool.size, n)]
+        dec = [bf16_value(int(b)) for b in bits]
+        B = int(rng.choice([4, 8]))
+        kb = int(rng.integers(1, 6))
+        k = int(rng.integers(1, 12))
+        idx, _, blk = oracle.topk_blocked_bf16(bits[None, :], None, B, kb, k, nthreads=1)
+        wi, wb = brute_blocked_row(dec, n, B, kb, k)
+        assert idx[0].tolist() == wi and blk[0].tolist() == wb
+        listed = rng.integers(-1, (n + B - 1) // B + 1, 5).astype(np.int32)
+        ci, _ = oracle.topk_candidates_bf16(bits[None, :], None, listed[None, :], B, k, nthreads=1)
+        assert ci[0].tolist() == brute_candidates_row(dec, n, B, listed.tolist(), k)
