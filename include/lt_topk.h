@@ -24,6 +24,7 @@
  * library allocates nothing, keeps no per-call state and never synchronises
  * the stream. Layouts are row-major:
  *   scores      float  [rows][row_stride]; row r is read on [0, L_r) only
+ *               (the _bf16 calls: uint16_t bf16 bit patterns, same layout)
  *   lengths     int32  [rows] or NULL; L_r = clamp(lengths[r], 0, row_stride),
  *                      NULL means L_r = row_stride for every row
  *   out_idx     int32  [rows][k]; row-relative, 0-based positions
@@ -31,8 +32,15 @@
  *   out_blocks  int32  [rows][k_blocks] or NULL (two-level only)
  * A row with L_r < k fills slots [L_r, k) with index -1 and value -inf.
  * Rows whose start is 16-byte aligned (scores 16-byte aligned and row_stride a
- * multiple of 4) use 128-bit loads (batches of such rows: bulk copies into
- * shared memory); any other alignment takes scalar loads.
+ * multiple of 4) use 128-bit loads; bf16 rows need 8-byte aligned starts for
+ * their 64-bit loads. Any other alignment takes scalar loads.
+ *
+ * bf16 scores. A low-precision indexer (the day-0 post on SGLang and Miles
+ * for DeepSeek-V4.1 credits fused kernels and an FP4 indexer in its summary)
+ * can hand its scores over in bf16, which halves the bytes this selection
+ * reads. A bf16 score is ranked as the fp32 number it denotes
+ * (its 16 bits as the upper half of an fp32, the rest zero: exact), under the
+ * same rules; out_val receives that fp32 number.
  *
  * Errors. Argument errors return LT_ERR_INVALID_ARG or LT_ERR_UNSUPPORTED
  * synchronously and launch nothing. A failed launch returns LT_ERR_CUDA
@@ -54,6 +62,10 @@ typedef enum lt_status {
   LT_ERR_UNSUPPORTED = 2,  /* valid but outside this build's limits */
   LT_ERR_CUDA = 3          /* a CUDA runtime call failed */
 } lt_status;
+
+/* Score element types of the _ex calls. */
+#define LT_DTYPE_F32 0
+#define LT_DTYPE_BF16 1
 
 /* Largest k and k_blocks accepted. */
 #define LT_MAX_K 2048
@@ -77,6 +89,10 @@ typedef enum lt_status {
  */
 lt_status lt_topk(const float* scores, const int32_t* lengths, int32_t rows, int64_t row_stride,
                   int32_t k, int32_t* out_idx, float* out_val, void* stream);
+
+/* lt_topk over bf16 scores (uint16_t bit patterns); otherwise identical. */
+lt_status lt_topk_bf16(const uint16_t* scores, const int32_t* lengths, int32_t rows, int64_t row_stride,
+                       int32_t k, int32_t* out_idx, float* out_val, void* stream);
 
 /*
  * lt_topk_blocked -- two-level, candidate-restricted top-k.
@@ -102,6 +118,11 @@ lt_status lt_topk(const float* scores, const int32_t* lengths, int32_t rows, int
 lt_status lt_topk_blocked(const float* scores, const int32_t* lengths, int32_t rows,
                           int64_t row_stride, int32_t block, int32_t k_blocks, int32_t k,
                           int32_t* out_idx, float* out_val, int32_t* out_blocks, void* stream);
+
+/* lt_topk_blocked over bf16 scores; otherwise identical. */
+lt_status lt_topk_blocked_bf16(const uint16_t* scores, const int32_t* lengths, int32_t rows,
+                               int64_t row_stride, int32_t block, int32_t k_blocks, int32_t k,
+                               int32_t* out_idx, float* out_val, int32_t* out_blocks, void* stream);
 
 /*
  * lt_topk_candidates -- top-k restricted to the positions of given blocks.
@@ -134,6 +155,12 @@ lt_status lt_topk_candidates(const float* scores, const int32_t* lengths, int32_
                              int32_t n_cand, int32_t k, int32_t* out_idx, float* out_val,
                              void* stream);
 
+/* lt_topk_candidates over bf16 scores; otherwise identical. */
+lt_status lt_topk_candidates_bf16(const uint16_t* scores, const int32_t* lengths, int32_t rows,
+                                  int64_t row_stride, int32_t block, const int32_t* cand_blocks,
+                                  int32_t n_cand, int32_t k, int32_t* out_idx, float* out_val,
+                                  void* stream);
+
 /* Kernels (force_kernel, lt_plan_info.kernel). */
 #define LT_KERNEL_AUTO 0
 /* Register-resident: each CTA holds its first rounds of the row in registers
@@ -146,6 +173,9 @@ lt_status lt_topk_candidates(const float* scores, const int32_t* lengths, int32_
 /*
  * Launch-plan control, for tests and measurement (not needed for normal use).
  *
+ *   scores, dtype  the scores as for the plain calls; dtype LT_DTYPE_F32
+ *                  (float) or LT_DTYPE_BF16 (uint16_t bf16 bits), anything
+ *                  else returns LT_ERR_INVALID_ARG
  *   force_cluster  0 lets the planner choose; 1, 2, 4, 8 or 16 forces the
  *                  number of CTAs that share one row (16 needs a device that
  *                  can schedule a 16-CTA cluster, else LT_ERR_UNSUPPORTED)
@@ -154,16 +184,16 @@ lt_status lt_topk_candidates(const float* scores, const int32_t* lengths, int32_
  *   force_exact    nonzero skips the sampled-threshold fast path and runs the
  *                  streaming radix select on every row (same results)
  *   force_kernel   LT_KERNEL_AUTO lets the planner choose (currently always
- *                  register-resident); LT_KERNEL_STREAM on unaligned rows
- *                  returns LT_ERR_UNSUPPORTED
+ *                  register-resident); LT_KERNEL_STREAM on unaligned or
+ *                  bf16 rows returns LT_ERR_UNSUPPORTED
  *   counters       NULL, or device int32[LT_NUM_COUNTERS] that the kernel
  *                  increments atomically, once per row: [0] rows finished on
  *                  the fast path, [1] rows finished on the streaming radix
  *                  select, [2] rows whose candidate set overflowed, [3] rows
  *                  whose sampled threshold kept fewer than k candidates,
  *                  [4] rows of the streamed kernel during which a wait for a
- *                  bulk copy gave up after its poll limit (a hardware fault;
- *                  that row's output is undefined -- never seen in practice).
+ *                  bulk copy gave up after its poll limit (a hardware fault,
+ *                  or lt_test_inject; that row's output is undefined).
  *                  For the two-level call, each row counts once per stage
  *                  (with k_blocks >= k and out_blocks NULL, only stage B
  *                  runs: once); for the listed-candidate call, once (the
@@ -187,16 +217,16 @@ lt_status lt_topk_candidates(const float* scores, const int32_t* lengths, int32_
  * slots other than the entry timestamp.
  */
 #define LT_NUM_COUNTERS 5
-lt_status lt_topk_ex(const float* scores, const int32_t* lengths, int32_t rows,
+lt_status lt_topk_ex(const void* scores, int32_t dtype, const int32_t* lengths, int32_t rows,
                      int64_t row_stride, int32_t k, int32_t* out_idx, float* out_val,
                      int32_t force_cluster, int32_t force_threads, int32_t force_exact,
                      int32_t force_kernel, int32_t* counters, int64_t* trace, void* stream);
-lt_status lt_topk_blocked_ex(const float* scores, const int32_t* lengths, int32_t rows,
+lt_status lt_topk_blocked_ex(const void* scores, int32_t dtype, const int32_t* lengths, int32_t rows,
                              int64_t row_stride, int32_t block, int32_t k_blocks, int32_t k,
                              int32_t* out_idx, float* out_val, int32_t* out_blocks,
                              int32_t force_cluster, int32_t force_threads, int32_t force_exact,
                              int32_t* counters, int64_t* trace, void* stream);
-lt_status lt_topk_candidates_ex(const float* scores, const int32_t* lengths, int32_t rows,
+lt_status lt_topk_candidates_ex(const void* scores, int32_t dtype, const int32_t* lengths, int32_t rows,
                                 int64_t row_stride, int32_t block, const int32_t* cand_blocks,
                                 int32_t n_cand, int32_t k, int32_t* out_idx, float* out_val,
                                 int32_t force_cluster, int32_t force_threads, int32_t force_exact,
@@ -228,6 +258,28 @@ const char* lt_status_string(lt_status status);
 
 /* Library version, major*10000 + minor*100 + patch. */
 int32_t lt_version(void);
+
+/*
+ * lt_test_inject -- failure injection for tests of the error paths (off unless
+ * called; host-side state of the library, shared by all threads).
+ *
+ *   LT_TEST_FAIL_LAUNCHES   the next `value` launches return LT_ERR_CUDA
+ *                           without launching anything and without setting a
+ *                           CUDA error (0 cancels)
+ *   LT_TEST_STALL_STREAMED  the next launch of the streamed kernel
+ *                           (LT_KERNEL_STREAM) never issues the final bulk
+ *                           copy of each CTA, and every one of its mbarrier
+ *                           waits gives up after `value` polls (0 cancels):
+ *                           the wait for that chunk runs out, counters[4]
+ *                           records it, the kernel still finishes (no copy is
+ *                           left in flight) and the affected rows' outputs are
+ *                           undefined
+ *
+ * Returns LT_ERR_INVALID_ARG for an unknown `what` or a negative value.
+ */
+#define LT_TEST_FAIL_LAUNCHES 1
+#define LT_TEST_STALL_STREAMED 2
+lt_status lt_test_inject(int32_t what, int32_t value);
 
 #ifdef __cplusplus
 }

@@ -8,6 +8,9 @@ the tensors are not on a CUDA device, the call raises.
 
     idx, val = topk(scores, lengths, k=512)
     idx, val, blocks = topk_blocked(scores, lengths, block=8, k_blocks=2048, k=512)
+
+Scores may be float32 or bfloat16 (the bf16 entry points); values come back
+as float32 either way (a bf16 score widens to fp32 exactly).
 """
 from __future__ import annotations
 
@@ -16,12 +19,13 @@ from pathlib import Path
 
 import torch
 
-__all__ = ["topk", "topk_blocked", "topk_candidates", "plan", "load", "library_path", "LtError", "NUM_COUNTERS",
+__all__ = ["topk", "topk_blocked", "topk_candidates", "plan", "DTYPE_F32", "DTYPE_BF16", "load", "library_path", "LtError", "NUM_COUNTERS",
            "status_string", "version", "PlanInfo", "KERNEL_AUTO", "KERNEL_RESIDENT", "KERNEL_STREAM"]
 
 _LIB_PATH = Path(__file__).resolve().parent / "liblt_topk.so"
 _lib = None
 NUM_COUNTERS = 5
+DTYPE_F32, DTYPE_BF16 = 0, 1
 KERNEL_AUTO, KERNEL_RESIDENT, KERNEL_STREAM = 0, 1, 2
 _KERNEL_NAMES = {KERNEL_RESIDENT: "resident", KERNEL_STREAM: "stream"}
 
@@ -59,22 +63,28 @@ def load() -> ctypes.CDLL:
     i32, i64, vp = ctypes.c_int32, ctypes.c_int64, ctypes.c_void_p
     lib.lt_topk.argtypes = [vp, vp, i32, i64, i32, vp, vp, vp]
     lib.lt_topk.restype = ctypes.c_int
-    lib.lt_topk_ex.argtypes = [vp, vp, i32, i64, i32, vp, vp, i32, i32, i32, i32, vp, vp, vp]
+    lib.lt_topk_ex.argtypes = [vp, i32, vp, i32, i64, i32, vp, vp, i32, i32, i32, i32, vp, vp, vp]
     lib.lt_topk_ex.restype = ctypes.c_int
     lib.lt_topk_blocked.argtypes = [vp, vp, i32, i64, i32, i32, i32, vp, vp, vp, vp]
     lib.lt_topk_blocked.restype = ctypes.c_int
-    lib.lt_topk_blocked_ex.argtypes = [vp, vp, i32, i64, i32, i32, i32, vp, vp, vp, i32, i32, i32, vp, vp,
-                                       vp]
+    lib.lt_topk_blocked_ex.argtypes = [vp, i32, vp, i32, i64, i32, i32, i32, vp, vp, vp, i32, i32, i32, vp,
+                                       vp, vp]
     lib.lt_topk_blocked_ex.restype = ctypes.c_int
     lib.lt_topk_candidates.argtypes = [vp, vp, i32, i64, i32, vp, i32, i32, vp, vp, vp]
     lib.lt_topk_candidates.restype = ctypes.c_int
-    lib.lt_topk_candidates_ex.argtypes = [vp, vp, i32, i64, i32, vp, i32, i32, vp, vp, i32, i32, i32, vp,
-                                          vp, vp]
+    lib.lt_topk_candidates_ex.argtypes = [vp, i32, vp, i32, i64, i32, vp, i32, i32, vp, vp, i32, i32, i32,
+                                          vp, vp, vp]
     lib.lt_topk_candidates_ex.restype = ctypes.c_int
+    for name in ("lt_topk_bf16", "lt_topk_blocked_bf16", "lt_topk_candidates_bf16"):
+        f = getattr(lib, name)
+        f.argtypes = getattr(lib, name[:-5]).argtypes
+        f.restype = ctypes.c_int
     lib.lt_topk_plan.argtypes = [i32, i64, i32, i32, i32, i32, i32, i32, i32, i32, vp]
     lib.lt_topk_plan.restype = ctypes.c_int
     lib.lt_status_string.argtypes = [ctypes.c_int]
     lib.lt_status_string.restype = ctypes.c_char_p
+    lib.lt_test_inject.argtypes = [i32, i32]
+    lib.lt_test_inject.restype = ctypes.c_int
     lib.lt_version.argtypes = []
     lib.lt_version.restype = i32
     _lib = lib
@@ -93,11 +103,14 @@ def _ptr(t):
     return None if t is None else ctypes.c_void_p(t.data_ptr())
 
 
+_DTYPES = {torch.float32: DTYPE_F32, torch.bfloat16: DTYPE_BF16}
+
+
 def _check_scores(scores: torch.Tensor):
     if not isinstance(scores, torch.Tensor) or not scores.is_cuda:
         raise TypeError("scores must be a CUDA tensor")
-    if scores.dtype != torch.float32:
-        raise TypeError("scores must be float32")
+    if scores.dtype not in _DTYPES:
+        raise TypeError("scores must be float32 or bfloat16")
     if scores.dim() != 2:
         raise ValueError("scores must be 2-D [rows, positions]")
     rows, n = scores.shape
@@ -142,7 +155,8 @@ def topk(scores: torch.Tensor, lengths: torch.Tensor | None = None, k: int = 512
          force_exact: bool = False, force_kernel: int = KERNEL_AUTO,
          counters: torch.Tensor | None = None, trace: torch.Tensor | None = None,
          stream: torch.cuda.Stream | None = None):
-    """Per-row top-k by (score desc, index asc); returns (idx int32 [rows, k], val float32 [rows, k] or None)."""
+    """Per-row top-k by (score desc, index asc) of float32 or bfloat16 scores; returns
+    (idx int32 [rows, k], val float32 [rows, k] or None)."""
     lib = load()
     rows, n = _check_scores(scores)
     dev = scores.device
@@ -155,7 +169,7 @@ def topk(scores: torch.Tensor, lengths: torch.Tensor | None = None, k: int = 512
     counters = _counters(counters, dev)
     with torch.cuda.device(dev):
         s = (stream or torch.cuda.current_stream(dev)).cuda_stream
-        st = lib.lt_topk_ex(_ptr(scores), _ptr(lengths), rows, max(n, 1), int(k), _ptr(out_idx),
+        st = lib.lt_topk_ex(_ptr(scores), _DTYPES[scores.dtype], _ptr(lengths), rows, max(n, 1), int(k), _ptr(out_idx),
                             _ptr(out_val), int(force_cluster), int(force_threads),
                             int(bool(force_exact)), int(force_kernel), _ptr(counters), _ptr(trace),
                             ctypes.c_void_p(s))
@@ -182,7 +196,7 @@ def topk_blocked(scores: torch.Tensor, lengths: torch.Tensor | None = None, bloc
     counters = _counters(counters, dev)
     with torch.cuda.device(dev):
         s = (stream or torch.cuda.current_stream(dev)).cuda_stream
-        st = lib.lt_topk_blocked_ex(_ptr(scores), _ptr(lengths), rows, max(n, 1), int(block),
+        st = lib.lt_topk_blocked_ex(_ptr(scores), _DTYPES[scores.dtype], _ptr(lengths), rows, max(n, 1), int(block),
                                     int(k_blocks), int(k), _ptr(out_idx), _ptr(out_val),
                                     _ptr(out_blocks), int(force_cluster), int(force_threads),
                                     int(bool(force_exact)), _ptr(counters), _ptr(trace), ctypes.c_void_p(s))
@@ -213,7 +227,7 @@ def topk_candidates(scores: torch.Tensor, cand_blocks: torch.Tensor, lengths: to
     counters = _counters(counters, dev)
     with torch.cuda.device(dev):
         s = (stream or torch.cuda.current_stream(dev)).cuda_stream
-        st = lib.lt_topk_candidates_ex(_ptr(scores), _ptr(lengths), rows, max(n, 1), int(block),
+        st = lib.lt_topk_candidates_ex(_ptr(scores), _DTYPES[scores.dtype], _ptr(lengths), rows, max(n, 1), int(block),
                                        _ptr(cand_blocks), int(cand_blocks.shape[1]), int(k), _ptr(out_idx),
                                        _ptr(out_val), int(force_cluster), int(force_threads),
                                        int(bool(force_exact)), _ptr(counters), _ptr(trace),

@@ -18,6 +18,7 @@
 
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cstdint>
 #include <cstdlib>
 #include <mutex>
@@ -33,7 +34,8 @@ constexpr int kMaxDevices = 64;
 constexpr int kWideThreads = 512;
 constexpr int kNarrowThreads = 256;
 constexpr int64_t kWideRound = 512 * 8 * 4;  // positions per CTA per round (wide)
-constexpr int kSlots = 18;                    // kernel variants
+constexpr int kTypeSlots = 18;                // kernel variants per score type
+constexpr int kSlots = 2 * kTypeSlots;        // fp32, then bf16
 // the streamed kernel's launch bounds: CTAs per SM for 256 / 512 threads
 constexpr int stream_ctas_per_sm(int threads) { return threads == 256 ? 3 : 2; }
 constexpr int kStreamMaxStages = 8;
@@ -47,6 +49,17 @@ struct DeviceInfo {
 };
 
 std::mutex g_mu;
+// test hooks (lt_test_inject): launches still to fail, polls of the next
+// streamed launch's stalled wait
+std::atomic<int32_t> g_fail_launches{0};
+std::atomic<int32_t> g_stall_polls{0};
+
+bool take_one(std::atomic<int32_t>& n) {
+  int32_t v = n.load(std::memory_order_relaxed);
+  while (v > 0 && !n.compare_exchange_weak(v, v - 1, std::memory_order_relaxed)) {
+  }
+  return v > 0;
+}
 DeviceInfo g_dev[kMaxDevices];
 int g_smem_set[kMaxDevices][kSlots];  // largest dynamic smem already granted per kernel
 bool g_nonportable_set[kMaxDevices][kSlots];
@@ -61,13 +74,16 @@ int block_index(int block) {
   }
 }
 
-// slots 14..17: the listed-candidate kernel, by block size
-int kernel_slot(bool blocked, int block, int threads, bool stream = false, bool one_round = false) {
+// slots 14..17: the listed-candidate kernel, by block size; bf16 kernels
+// follow the fp32 ones (kTypeSlots later)
+int kernel_slot(bool blocked, int block, int threads, bool stream = false, bool one_round = false,
+                bool bf16 = false) {
   const int wide = threads == kWideThreads ? 1 : 0;
+  const int base = bf16 ? kTypeSlots : 0;
   if (stream) return 10 + wide;
-  if (!blocked) return (one_round ? 12 : 0) + wide;
+  if (!blocked) return base + (one_round ? 12 : 0) + wide;
   const int b = block_index(block);
-  return b < 0 ? -1 : 2 + 2 * b + wide;
+  return b < 0 ? -1 : base + 2 + 2 * b + wide;
 }
 
 uint32_t next_pow2(uint32_t x) {
@@ -183,7 +199,7 @@ lt_status make_stream_plan(int32_t rows, int64_t row_stride, int32_t k, int32_t 
 
 lt_status make_plan(int32_t rows, int64_t row_stride, int32_t k, bool blocked, int32_t block,
                     int32_t k_blocks, int32_t force_cluster, int32_t force_threads, int32_t force_kernel,
-                    bool aligned, Plan* plan, int* dev_out) {
+                    bool aligned, bool bf16, Plan* plan, int* dev_out) {
   DeviceInfo* di = nullptr;
   int dev = 0;
   lt_status st = device_info(&di, &dev);
@@ -194,7 +210,7 @@ lt_status make_plan(int32_t rows, int64_t row_stride, int32_t k, bool blocked, i
   // their first instruction and which keeps three CTAs per SM.
   bool stream = false;
   if (force_kernel == LT_KERNEL_STREAM) {
-    if (blocked || !aligned) return LT_ERR_UNSUPPORTED;
+    if (blocked || !aligned || bf16) return LT_ERR_UNSUPPORTED;
     stream = true;
   }
   if (stream) {
@@ -205,19 +221,19 @@ lt_status make_plan(int32_t rows, int64_t row_stride, int32_t k, bool blocked, i
 
   int threads = force_threads;
   if (threads == 0) threads = (int64_t)rows >= di->sms ? kNarrowThreads : kWideThreads;
-  if (kernel_slot(blocked, block, threads) < 0) return LT_ERR_UNSUPPORTED;
+  if (kernel_slot(blocked, block, threads, false, false, bf16) < 0) return LT_ERR_UNSUPPORTED;
   plan->threads = threads;
   // the top-k kernel has a variant for slices of one register round
   auto pick = [&](int c, int* slot) -> const void* {
     if (blocked) {
-      *slot = kernel_slot(true, block, threads);
-      return lt::blocked_kernel_ptr(threads, block);
+      *slot = kernel_slot(true, block, threads, false, false, bf16);
+      return lt::blocked_kernel_ptr(threads, block, bf16);
     }
     int64_t per = (row_stride + c - 1) / c;
     per = (per + 3) & ~(int64_t)3;
     plan->one_round = per <= lt::topk_round_positions(threads);
-    *slot = kernel_slot(false, 4, threads, false, plan->one_round);
-    return lt::topk_kernel_ptr(threads, plan->one_round);
+    *slot = kernel_slot(false, 4, threads, false, plan->one_round, bf16);
+    return lt::topk_kernel_ptr(threads, plan->one_round, bf16);
   };
   int slot = 0;
   plan->func = pick(1, &slot);
@@ -347,7 +363,7 @@ lt_status make_stream_plan(int32_t rows, int64_t row_stride, int32_t k, int32_t 
   }
 }
 
-lt_status check_common(const float* scores, int32_t rows, int64_t row_stride, int32_t k,
+lt_status check_common(const void* scores, int32_t rows, int64_t row_stride, int32_t k,
                        const int32_t* out_idx, int32_t force_cluster, int32_t force_threads) {
   if (rows < 0 || row_stride < 1 || k < 1) return LT_ERR_INVALID_ARG;
   if (!(force_threads == 0 || force_threads == kNarrowThreads || force_threads == kWideThreads))
@@ -361,7 +377,9 @@ lt_status check_common(const float* scores, int32_t rows, int64_t row_stride, in
 }
 
 lt_status launch(const Plan& plan, const lt::Params& prm, void* stream) {
+  if (take_one(g_fail_launches)) return LT_ERR_CUDA;  // injected by a test
   lt::Params p = prm;
+  if (plan.kernel == LT_KERNEL_STREAM) p.stall_polls = g_stall_polls.exchange(0, std::memory_order_relaxed);
   p.cap = (int32_t)plan.cap;
   p.seg_shift = (int32_t)plan.seg_shift;
   p.wstage = (int32_t)plan.wstage;
@@ -389,26 +407,35 @@ lt_status launch(const Plan& plan, const lt::Params& prm, void* stream) {
   return cudaLaunchKernelExC(&cfg, plan.func, args) == cudaSuccess ? LT_OK : LT_ERR_CUDA;
 }
 
-bool aligned16(const void* p, int64_t row_stride) {
-  return (reinterpret_cast<uintptr_t>(p) % 16u) == 0 && (row_stride % 4) == 0;
+// Every row start allows the vector loads of four scores: 16 bytes of fp32,
+// 8 bytes of bf16.
+bool rows_aligned(const void* p, int64_t row_stride, bool bf16) {
+  return (reinterpret_cast<uintptr_t>(p) % (bf16 ? 8u : 16u)) == 0 && (row_stride % 4) == 0;
+}
+
+lt_status check_dtype(int32_t dtype) {
+  return (dtype == LT_DTYPE_F32 || dtype == LT_DTYPE_BF16) ? LT_OK : LT_ERR_INVALID_ARG;
 }
 
 }  // namespace
 
 extern "C" {
 
-lt_status lt_topk_ex(const float* scores, const int32_t* lengths, int32_t rows, int64_t row_stride,
-                     int32_t k, int32_t* out_idx, float* out_val, int32_t force_cluster,
+lt_status lt_topk_ex(const void* scores, int32_t dtype, const int32_t* lengths, int32_t rows,
+                     int64_t row_stride, int32_t k, int32_t* out_idx, float* out_val, int32_t force_cluster,
                      int32_t force_threads, int32_t force_exact, int32_t force_kernel, int32_t* counters,
                      int64_t* trace, void* stream) {
   lt_status st = check_common(scores, rows, row_stride, k, out_idx, force_cluster, force_threads);
   if (st != LT_OK) return st;
+  if (check_dtype(dtype) != LT_OK) return LT_ERR_INVALID_ARG;
   if (force_kernel < LT_KERNEL_AUTO || force_kernel > LT_KERNEL_STREAM) return LT_ERR_INVALID_ARG;
   if (rows == 0) return LT_OK;
+  const bool bf16 = dtype == LT_DTYPE_BF16;
+  const bool aligned = rows_aligned(scores, row_stride, bf16);
   Plan plan;
   int dev = 0;
-  st = make_plan(rows, row_stride, k, false, 4, 1, force_cluster, force_threads, force_kernel,
-                 aligned16(scores, row_stride), &plan, &dev);
+  st = make_plan(rows, row_stride, k, false, 4, 1, force_cluster, force_threads, force_kernel, aligned, bf16,
+                 &plan, &dev);
   if (st != LT_OK) return st;
   lt::Params p = {};
   p.scores = scores;
@@ -423,23 +450,32 @@ lt_status lt_topk_ex(const float* scores, const int32_t* lengths, int32_t rows, 
   p.k = k;
   p.k_blocks = 1;
   p.force_exact = force_exact ? 1 : 0;
-  p.vec_ok = aligned16(scores, row_stride) ? 1 : 0;
+  p.vec_ok = aligned ? 1 : 0;
   return launch(plan, p, stream);
 }
 
 lt_status lt_topk(const float* scores, const int32_t* lengths, int32_t rows, int64_t row_stride,
                   int32_t k, int32_t* out_idx, float* out_val, void* stream) {
-  return lt_topk_ex(scores, lengths, rows, row_stride, k, out_idx, out_val, 0, 0, 0, LT_KERNEL_AUTO, nullptr,
-                    nullptr, stream);
+  return lt_topk_ex(scores, LT_DTYPE_F32, lengths, rows, row_stride, k, out_idx, out_val, 0, 0, 0,
+                    LT_KERNEL_AUTO, nullptr, nullptr, stream);
 }
 
-lt_status lt_topk_blocked_ex(const float* scores, const int32_t* lengths, int32_t rows,
+lt_status lt_topk_bf16(const uint16_t* scores, const int32_t* lengths, int32_t rows, int64_t row_stride,
+                       int32_t k, int32_t* out_idx, float* out_val, void* stream) {
+  return lt_topk_ex(scores, LT_DTYPE_BF16, lengths, rows, row_stride, k, out_idx, out_val, 0, 0, 0,
+                    LT_KERNEL_AUTO, nullptr, nullptr, stream);
+}
+
+lt_status lt_topk_blocked_ex(const void* scores, int32_t dtype, const int32_t* lengths, int32_t rows,
                              int64_t row_stride, int32_t block, int32_t k_blocks, int32_t k,
                              int32_t* out_idx, float* out_val, int32_t* out_blocks,
                              int32_t force_cluster, int32_t force_threads, int32_t force_exact,
                              int32_t* counters, int64_t* trace, void* stream) {
   lt_status st = check_common(scores, rows, row_stride, k, out_idx, force_cluster, force_threads);
   if (st != LT_OK) return st;
+  if (check_dtype(dtype) != LT_OK) return LT_ERR_INVALID_ARG;
+  const bool bf16 = dtype == LT_DTYPE_BF16;
+  const bool aligned = rows_aligned(scores, row_stride, bf16);
   if (block < 1 || k_blocks < 1) return LT_ERR_INVALID_ARG;
   if (k_blocks > LT_MAX_K || block_index(block) < 0) return LT_ERR_UNSUPPORTED;
   if (rows == 0) return LT_OK;
@@ -452,7 +488,7 @@ lt_status lt_topk_blocked_ex(const float* scores, const int32_t* lengths, int32_
   Plan plan;
   int dev = 0;
   st = make_plan(rows * groups, row_stride, k, true, block, k_blocks, force_cluster, force_threads,
-                 LT_KERNEL_AUTO, aligned16(scores, row_stride), &plan, &dev);
+                 LT_KERNEL_AUTO, aligned, bf16, &plan, &dev);
   if (st != LT_OK) return st;
   lt::Params p = {};
   p.split = split ? 1 : 0;
@@ -468,24 +504,34 @@ lt_status lt_topk_blocked_ex(const float* scores, const int32_t* lengths, int32_
   p.k = k;
   p.k_blocks = k_blocks;
   p.force_exact = force_exact ? 1 : 0;
-  p.vec_ok = aligned16(scores, row_stride) ? 1 : 0;
+  p.vec_ok = aligned ? 1 : 0;
   return launch(plan, p, stream);
 }
 
 lt_status lt_topk_blocked(const float* scores, const int32_t* lengths, int32_t rows,
                           int64_t row_stride, int32_t block, int32_t k_blocks, int32_t k,
                           int32_t* out_idx, float* out_val, int32_t* out_blocks, void* stream) {
-  return lt_topk_blocked_ex(scores, lengths, rows, row_stride, block, k_blocks, k, out_idx, out_val,
-                            out_blocks, 0, 0, 0, nullptr, nullptr, stream);
+  return lt_topk_blocked_ex(scores, LT_DTYPE_F32, lengths, rows, row_stride, block, k_blocks, k, out_idx,
+                            out_val, out_blocks, 0, 0, 0, nullptr, nullptr, stream);
 }
 
-lt_status lt_topk_candidates_ex(const float* scores, const int32_t* lengths, int32_t rows,
+lt_status lt_topk_blocked_bf16(const uint16_t* scores, const int32_t* lengths, int32_t rows,
+                               int64_t row_stride, int32_t block, int32_t k_blocks, int32_t k,
+                               int32_t* out_idx, float* out_val, int32_t* out_blocks, void* stream) {
+  return lt_topk_blocked_ex(scores, LT_DTYPE_BF16, lengths, rows, row_stride, block, k_blocks, k, out_idx,
+                            out_val, out_blocks, 0, 0, 0, nullptr, nullptr, stream);
+}
+
+lt_status lt_topk_candidates_ex(const void* scores, int32_t dtype, const int32_t* lengths, int32_t rows,
                                 int64_t row_stride, int32_t block, const int32_t* cand_blocks,
                                 int32_t n_cand, int32_t k, int32_t* out_idx, float* out_val,
                                 int32_t force_cluster, int32_t force_threads, int32_t force_exact,
                                 int32_t* counters, int64_t* trace, void* stream) {
   lt_status st = check_common(scores, rows, row_stride, k, out_idx, force_cluster, force_threads);
   if (st != LT_OK) return st;
+  if (check_dtype(dtype) != LT_OK) return LT_ERR_INVALID_ARG;
+  const bool bf16 = dtype == LT_DTYPE_BF16;
+  const bool aligned = rows_aligned(scores, row_stride, bf16);
   if (block < 1 || n_cand < 0 || (n_cand > 0 && cand_blocks == nullptr && rows > 0))
     return LT_ERR_INVALID_ARG;
   if (block_index(block) < 0) return LT_ERR_UNSUPPORTED;
@@ -511,17 +557,17 @@ lt_status lt_topk_candidates_ex(const float* scores, const int32_t* lengths, int
     plan.seg_shift = 14;
     plan.wstage = (uint32_t)kWideThreads * 16u * (uint32_t)lt::kStageF4;
     plan.sel_cap = next_pow2(k < 32 ? 32u : (uint32_t)k);
-    plan.func = lt::listed_kernel_ptr(block);
+    plan.func = lt::listed_kernel_ptr(block, bf16);
     plan.smem = lt::make_layout(false, plan.cap, plan.sel_cap, plan.wstage).total;
     gathered = plan.func != nullptr && (int)plan.smem <= di->smem_optin;
     if (gathered) {
-      st = prepare_kernel(dev, 14 + block_index(block), plan.func, plan.smem, 1);
+      st = prepare_kernel(dev, (bf16 ? kTypeSlots : 0) + 14 + block_index(block), plan.func, plan.smem, 1);
       if (st != LT_OK) return st;
     }
   }
   if (!gathered) {
     st = make_plan(rows, row_stride, k, true, block, 1, force_cluster, force_threads, LT_KERNEL_AUTO,
-                   aligned16(scores, row_stride), &plan, &dev);
+                   aligned, bf16, &plan, &dev);
     if (st != LT_OK) return st;
   }
   lt::Params p = {};
@@ -540,7 +586,7 @@ lt_status lt_topk_candidates_ex(const float* scores, const int32_t* lengths, int
   p.k = k;
   p.k_blocks = 1;
   p.force_exact = force_exact ? 1 : 0;
-  p.vec_ok = aligned16(scores, row_stride) ? 1 : 0;
+  p.vec_ok = aligned ? 1 : 0;
   return launch(plan, p, stream);
 }
 
@@ -548,8 +594,16 @@ lt_status lt_topk_candidates(const float* scores, const int32_t* lengths, int32_
                              int64_t row_stride, int32_t block, const int32_t* cand_blocks,
                              int32_t n_cand, int32_t k, int32_t* out_idx, float* out_val,
                              void* stream) {
-  return lt_topk_candidates_ex(scores, lengths, rows, row_stride, block, cand_blocks, n_cand, k,
-                               out_idx, out_val, 0, 0, 0, nullptr, nullptr, stream);
+  return lt_topk_candidates_ex(scores, LT_DTYPE_F32, lengths, rows, row_stride, block, cand_blocks, n_cand,
+                               k, out_idx, out_val, 0, 0, 0, nullptr, nullptr, stream);
+}
+
+lt_status lt_topk_candidates_bf16(const uint16_t* scores, const int32_t* lengths, int32_t rows,
+                                  int64_t row_stride, int32_t block, const int32_t* cand_blocks,
+                                  int32_t n_cand, int32_t k, int32_t* out_idx, float* out_val,
+                                  void* stream) {
+  return lt_topk_candidates_ex(scores, LT_DTYPE_BF16, lengths, rows, row_stride, block, cand_blocks,
+                               n_cand, k, out_idx, out_val, 0, 0, 0, nullptr, nullptr, stream);
 }
 
 lt_status lt_topk_plan(int32_t rows, int64_t row_stride, int32_t k, int32_t blocked, int32_t block,
@@ -570,7 +624,7 @@ lt_status lt_topk_plan(int32_t rows, int64_t row_stride, int32_t k, int32_t bloc
   if ((int64_t)rows * groups > 0x7fffffffLL) return LT_ERR_UNSUPPORTED;
   lt_status st = make_plan(rows * groups, row_stride, k, blocked != 0, blocked ? block : 4, blocked ? k_blocks : 1,
                            force_cluster, force_threads, force_kernel, aligned != 0 && row_stride % 4 == 0,
-                           &plan, &dev);
+                           false, &plan, &dev);
   if (st != LT_OK) return st;
   info->kernel = plan.kernel;
   info->cluster_size = plan.cluster;
@@ -592,6 +646,15 @@ const char* lt_status_string(lt_status status) {
   }
 }
 
-int32_t lt_version(void) { return 320; }
+int32_t lt_version(void) { return 400; }
+
+lt_status lt_test_inject(int32_t what, int32_t value) {
+  if (value < 0) return LT_ERR_INVALID_ARG;
+  switch (what) {
+    case LT_TEST_FAIL_LAUNCHES: g_fail_launches.store(value, std::memory_order_relaxed); return LT_OK;
+    case LT_TEST_STALL_STREAMED: g_stall_polls.store(value, std::memory_order_relaxed); return LT_OK;
+    default: return LT_ERR_INVALID_ARG;
+  }
+}
 
 }  // extern "C"

@@ -18,13 +18,13 @@ namespace lt {
 // [0, rows)) computes the plain top-k of its row, group 2 (clusters
 // [rows, 2 rows), launched only when out_blocks is wanted) stage A alone. Both
 // read the row once, side by side, instead of one stage after the other.
-template <int T, int W>
+template <int T, int W, class S>
 __global__ void __launch_bounds__(T, (T <= 256 ? 3 : 1)) blocked_kernel(Params p) {
   constexpr int U0 = T <= 256 ? 4 : 8;  // float4 per thread per round
   constexpr int U = (W / 4 > U0) ? W / 4 : U0;
   using G = Geo<T, U, W>;
   extern __shared__ __align__(128) unsigned char smem[];
-  Row R;
+  RowT<S> R;
   stamp(p, kTrStart);
   grid_dependents_launch();
   const int64_t cid = (int64_t)(blockIdx.x / (p.clustered ? cluster_size() : 1u));
@@ -247,13 +247,13 @@ __global__ void __launch_bounds__(T, (T <= 256 ? 3 : 1)) blocked_kernel(Params p
   wait_init(R);
 }
 
-template <int T>
-inline const void* blocked_ptr(int block) {
+template <int T, class S>
+const void* blocked_kernel_ptr_of(int block) {
   switch (block) {
-    case 4: return reinterpret_cast<const void*>(&blocked_kernel<T, 4>);
-    case 8: return reinterpret_cast<const void*>(&blocked_kernel<T, 8>);
-    case 16: return reinterpret_cast<const void*>(&blocked_kernel<T, 16>);
-    case 32: return reinterpret_cast<const void*>(&blocked_kernel<T, 32>);
+    case 4: return reinterpret_cast<const void*>(&blocked_kernel<T, 4, S>);
+    case 8: return reinterpret_cast<const void*>(&blocked_kernel<T, 8, S>);
+    case 16: return reinterpret_cast<const void*>(&blocked_kernel<T, 16, S>);
+    case 32: return reinterpret_cast<const void*>(&blocked_kernel<T, 32, S>);
     default: return nullptr;
   }
 }

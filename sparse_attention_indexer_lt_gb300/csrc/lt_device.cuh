@@ -90,7 +90,7 @@ enum TracePoint {
 };
 
 struct Params {
-  const float* scores;
+  const void* scores;   // float, or uint16_t bf16 bits (the kernel's score type)
   const int32_t* lengths;
   int64_t row_stride;
   int32_t* out_idx;
@@ -113,6 +113,9 @@ struct Params {
   const int32_t* cand_blocks;  // listed-candidate call: n_cand block ids per row
   int32_t n_cand;
   int32_t external;     // two-level kernel: stage B over the listed blocks only
+  int32_t stall_polls;  // streamed kernel, tests only (0 normally): the final chunk of
+                        // each CTA is never issued and every wait gives up after
+                        // this many polls (see lt_test_inject)
 };
 
 // ------------------------------------------------------------------ smem layout
@@ -227,8 +230,23 @@ __device__ __forceinline__ void stamp(const Params& p, int slot) {
   }
 }
 
+// Scores are read as fp32 or as bf16. A bf16 value is the upper half of the
+// fp32 with the same sign, exponent and leading seven mantissa bits, so
+// widening it is exact: its 16 bits move to the top of a 32-bit word. Every
+// later step (keys, compares, copied values) sees the widened fp32.
+__device__ __forceinline__ float bf16_widen(uint32_t h) { return __uint_as_float(h << 16); }
+
+__device__ __forceinline__ float load1(const float* p) { return __ldg(p); }
+__device__ __forceinline__ float load1(const uint16_t* p) { return bf16_widen(__ldg(p)); }
+
+// Four consecutive scores; p 16-byte (fp32) or 8-byte (bf16) aligned.
 __device__ __forceinline__ float4 ldg4(const float* p) {
   return __ldg(reinterpret_cast<const float4*>(p));
+}
+__device__ __forceinline__ float4 ldg4(const uint16_t* p) {
+  const uint2 q = __ldg(reinterpret_cast<const uint2*>(p));  // element 2i in the low half of word i
+  return make_float4(__uint_as_float(q.x << 16), __uint_as_float(q.x & 0xffff0000u),
+                     __uint_as_float(q.y << 16), __uint_as_float(q.y & 0xffff0000u));
 }
 
 // ------------------------------------------------------------------ keys
@@ -267,8 +285,9 @@ __device__ __forceinline__ float threshold_float(uint32_t t) {
 
 // Score bits from a key. The key loses the sign of zero and the NaN payload,
 // so those two cases re-read the score itself.
-__device__ __forceinline__ float value_of(uint32_t key, const float* rowp, uint32_t idx) {
-  if (key == 0u || key == 0x80000000u) return rowp[idx];
+template <class S>
+__device__ __forceinline__ float value_of(uint32_t key, const S* rowp, uint32_t idx) {
+  if (key == 0u || key == 0x80000000u) return load1(rowp + idx);
   const uint32_t b = (key & 0x80000000u) ? (key & 0x7fffffffu) : ~key;
   return __uint_as_float(b);
 }

@@ -30,7 +30,9 @@ struct Geo {
   static_assert(W % 4 == 0 && U % kVS == 0 && kSlots >= 1, "bad geometry");
 };
 
-struct Row {
+// Per-row state of one CTA. RowCore holds everything but the score pointer;
+// RowT<S> adds it for the score type S (float, or uint16_t holding bf16 bits).
+struct RowCore {
   Misc* m;
   uint32_t* hist;
   uint32_t* aux;
@@ -39,7 +41,6 @@ struct Row {
   uint2* cand;           // nclus segments of (1 << seg_shift) slots
   uint64_t* stage;
   float4* wst;           // this warp's staging area: [kStageF4][32] float4
-  const float* rowp;
   int64_t row;
   int64_t L;             // valid positions of the row
   int64_t begin, end;    // this CTA's slice of positions
@@ -53,8 +54,14 @@ struct Row {
   int64_t* trace;        // phase timestamps of this row (nullable)
 };
 
+template <class S>
+struct RowT : RowCore {
+  const S* rowp;         // scores of this row
+};
+using Row = RowT<float>;
+
 // Phase timestamp of this row (thread 0 of each CTA), when traced.
-__device__ __forceinline__ void stamp(const Row& R, int slot) {
+__device__ __forceinline__ void stamp(const RowCore& R, int slot) {
   if (R.trace != nullptr && threadIdx.x == 0) {
     uint64_t t;
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
@@ -70,29 +77,30 @@ struct OwnSlice {
     return all || ((int64_t)idx >= b && (int64_t)idx < e);
   }
 };
-__device__ __forceinline__ OwnSlice own_slice(const Row& R) { return OwnSlice{R.begin, R.end, R.nclus == 1}; }
+__device__ __forceinline__ OwnSlice own_slice(const RowCore& R) { return OwnSlice{R.begin, R.end, R.nclus == 1}; }
 
 // Filler of positions past the slice end: a NaN (never passes x >= g) whose
 // raw key is 0 (lands in the lowest histogram bin).
 __device__ __forceinline__ float nan_f() { return __int_as_float((int)0xffffffffu); }
 
 template <int T, int U, int W>
-__device__ __forceinline__ int64_t slot_pos(const Row& R, int r, int s) {
+__device__ __forceinline__ int64_t slot_pos(const RowCore& R, int r, int s) {
   return R.tbase + (int64_t)(r + R.rounds * s) * Geo<T, U, W>::kTile;
 }
 
 // Scalar load of a ragged or unaligned group of four positions: [0, nv) are
 // read, the rest are NaN (no threshold compare accepts NaN).
-__device__ __forceinline__ float4 load4_scalar(const float* p, int nv) {
+template <class S>
+__device__ __forceinline__ float4 load4_scalar(const S* p, int nv) {
   float e[4];
 #pragma unroll
-  for (int q = 0; q < 4; ++q) e[q] = (q < nv) ? __ldg(p + q) : nan_f();
+  for (int q = 0; q < 4; ++q) e[q] = (q < nv) ? load1(p + q) : nan_f();
   return make_float4(e[0], e[1], e[2], e[3]);
 }
 
 // Load round r; n[s] = valid positions of slot s (a prefix of the slot).
-template <int T, int U, int W>
-__device__ __forceinline__ void load_round(const Row& R, bool vec, int r, float4 (&v)[U],
+template <int T, int U, int W, class S>
+__device__ __forceinline__ void load_round(const RowT<S>& R, bool vec, int r, float4 (&v)[U],
                                            int (&n)[Geo<T, U, W>::kSlots]) {
   using G = Geo<T, U, W>;
 #pragma unroll
@@ -116,17 +124,17 @@ __device__ __forceinline__ void load_round(const Row& R, bool vec, int r, float4
 
 // Four-position slots (W = 4): round r lies wholly inside the slice.
 template <int T, int U>
-__device__ __forceinline__ bool round_whole(const Row& R, int r) {
+__device__ __forceinline__ bool round_whole(const RowCore& R, int r) {
   return (int64_t)(r + R.rounds * (U - 1) + 1) * Geo<T, U, 4>::kTile <= R.end - R.begin;
 }
 
 // Load round r of four-position slots: a whole round takes U vector loads
 // from this thread's slot pointers, others go through load_round.
-template <int T, int U>
-__device__ __forceinline__ void load_round4(const Row& R, bool vec, int r, float4 (&v)[U], int (&n)[U]) {
+template <int T, int U, class S>
+__device__ __forceinline__ void load_round4(const RowT<S>& R, bool vec, int r, float4 (&v)[U], int (&n)[U]) {
   using G = Geo<T, U, 4>;
   if (vec && round_whole<T, U>(R, r)) {
-    const float* pr = R.rowp + R.tbase + (int64_t)r * G::kTile;
+    const S* pr = R.rowp + R.tbase + (int64_t)r * G::kTile;
     const int64_t sstride = (int64_t)R.rounds * G::kTile;
 #pragma unroll
     for (int s = 0; s < U; ++s) {
@@ -164,7 +172,7 @@ __device__ __forceinline__ uint32_t slot_block_key(const float4 (&v)[U], int s, 
 struct KeepAll {
   static constexpr bool kAll = true;
   template <class V>
-  __device__ __forceinline__ bool operator()(const Row&, int, const V&, int, int) const { return true; }
+  __device__ __forceinline__ bool operator()(const RowCore&, int, const V&, int, int) const { return true; }
 };
 
 // Stage B of the two-level kernel: keep a slot (one block) when its block
@@ -176,7 +184,7 @@ struct KeepListed {
   static constexpr bool kAll = false;
   const uint32_t* bits;
   uint32_t nbits;
-  __device__ __forceinline__ bool operator()(const Row& R, int r, const float4 (&)[U], int s, int) const {
+  __device__ __forceinline__ bool operator()(const RowCore& R, int r, const float4 (&)[U], int s, int) const {
     const int64_t bid = slot_pos<T, U, W>(R, r, s) / W;
     return bid < (int64_t)nbits && ((bits[bid >> 5] >> (bid & 31)) & 1u) != 0u;
   }
@@ -186,7 +194,7 @@ template <int T, int U, int W>
 struct KeepBlocks {
   static constexpr bool kAll = false;
   uint64_t Tc;
-  __device__ __forceinline__ bool operator()(const Row& R, int r, const float4 (&v)[U], int s, int nv) const {
+  __device__ __forceinline__ bool operator()(const RowCore& R, int r, const float4 (&v)[U], int s, int nv) const {
     const uint32_t bid = (uint32_t)(slot_pos<T, U, W>(R, r, s) / W);
     return composite(slot_block_key<T, U, W>(v, s, nv), bid) >= Tc;
   }
@@ -196,8 +204,8 @@ struct KeepBlocks {
 
 // row < 0: the row of this CTA's cluster (one row per cluster); otherwise the
 // given row (persistent kernels).
-template <int T, int U, int W>
-__device__ __forceinline__ void setup_row(Row& R, const Params& p, unsigned char* smem, int64_t row = -1) {
+template <int T, int U, int W, class S>
+__device__ __forceinline__ void setup_row(RowT<S>& R, const Params& p, unsigned char* smem, int64_t row = -1) {
   using G = Geo<T, U, W>;
   R.nclus = p.clustered ? cluster_size() : 1u;
   R.rank = p.clustered ? cluster_rank() : 0u;
@@ -244,7 +252,7 @@ __device__ __forceinline__ void setup_row(Row& R, const Params& p, unsigned char
     L = L < 0 ? 0 : (L > p.row_stride ? p.row_stride : L);
   }
   R.L = L;
-  R.rowp = p.scores + R.row * p.row_stride;
+  R.rowp = static_cast<const S*>(p.scores) + R.row * p.row_stride;
   // the cluster size, T, W and the slots per round are powers of two
   const int cl2 = 31 - __clz((int)R.nclus);
   int64_t per = (L + R.nclus - 1) >> cl2;
@@ -267,7 +275,7 @@ __device__ __forceinline__ void setup_row(Row& R, const Params& p, unsigned char
   }
 }
 
-__device__ __forceinline__ void wait_init(Row& R) {
+__device__ __forceinline__ void wait_init(RowCore& R) {
   if (R.init_pending) {
     cluster_wait();
     R.init_pending = false;
@@ -281,7 +289,7 @@ __device__ __forceinline__ void zero_bins(uint32_t* b) {
   __syncthreads();
 }
 
-__device__ __forceinline__ void bump(const Params& p, const Row& R, int which) {
+__device__ __forceinline__ void bump(const Params& p, const RowCore& R, int which) {
   if (p.counters && R.rank == 0 && threadIdx.x == 0) atomicAdd(&p.counters[which], 1);
 }
 
@@ -295,7 +303,7 @@ __device__ __forceinline__ void dsmem_st_u32(uint32_t addr, uint32_t v) {
 // segment q holding seg_cnt[q] entries. Warps are spread over the segments
 // (several warps per segment when there are fewer segments than warps).
 template <int T, class F>
-__device__ __forceinline__ void for_each_cand(const Row& R, F f) {
+__device__ __forceinline__ void for_each_cand(const RowCore& R, F f) {
   constexpr uint32_t NW = T / 32;
   const Misc* m = R.m;
   const uint32_t nseg = m->nseg, shift = m->shift;
@@ -333,7 +341,7 @@ __device__ __forceinline__ void reset_candidate_range(Misc* m) {
 // are pushed: the cluster-wide lo_rank-th key is at least that large, so every
 // bin at or above its digit still arrives complete (used with a full sample).
 template <int T>
-__device__ __forceinline__ const uint32_t* merge_hist(Row& R, int buf, uint32_t lo_rank = 0) {
+__device__ __forceinline__ const uint32_t* merge_hist(RowCore& R, int buf, uint32_t lo_rank = 0) {
   __syncthreads();
   if (R.nclus == 1) return R.hist;
   uint32_t dlo = 0;
@@ -358,7 +366,7 @@ __device__ __forceinline__ const uint32_t* merge_hist(Row& R, int buf, uint32_t 
 // After the digit search on merged buffer `buf`: clear it for its next use.
 // Peers only write it again after a later cluster barrier.
 template <int T>
-__device__ __forceinline__ void release_merged(Row& R, int buf) {
+__device__ __forceinline__ void release_merged(RowCore& R, int buf) {
   if (R.nclus == 1) return;
   uint4* p = reinterpret_cast<uint4*>(buf ? R.merged1 : R.merged0);
   for (int i = threadIdx.x; i < kBins / 4; i += T) p[i] = make_uint4(0, 0, 0, 0);
@@ -369,7 +377,7 @@ __device__ __forceinline__ void release_merged(Row& R, int buf) {
 // (which then orders and writes the whole row). One cluster barrier, no
 // remote atomics.
 template <int T>
-__device__ __forceinline__ void exchange_segments(Row& R, bool gather) {
+__device__ __forceinline__ void exchange_segments(RowCore& R, bool gather) {
   Misc* m = R.m;
   __syncthreads();
   const uint32_t n = m->local_count;
@@ -432,7 +440,7 @@ __device__ __forceinline__ void exchange_segments(Row& R, bool gather) {
 // Sample histogram of one round. level 1: top 11 bits of the raw key;
 // level 2: the next 11 bits of the items whose top 11 bits equal d1.
 template <int T, int U, int W, int kLevel, class Keep>
-__device__ __forceinline__ void hist_round(Row& R, int r, const float4 (&v)[U],
+__device__ __forceinline__ void hist_round(RowCore& R, int r, const float4 (&v)[U],
                                            const int (&n)[Geo<T, U, W>::kSlots], uint32_t d1, Keep keep) {
   using G = Geo<T, U, W>;
 #pragma unroll
@@ -456,7 +464,7 @@ __device__ __forceinline__ void hist_round(Row& R, int r, const float4 (&v)[U],
 // element e of float4 f (x >= g, or every valid position when `all`), for
 // kept slots only.
 template <int T, int U, int W, class Keep>
-__device__ __forceinline__ uint32_t round_mask(const Row& R, int r, const float4 (&v)[U],
+__device__ __forceinline__ uint32_t round_mask(const RowCore& R, int r, const float4 (&v)[U],
                                                const int (&n)[Geo<T, U, W>::kSlots], float g, bool all,
                                                Keep keep) {
   using G = Geo<T, U, W>;
@@ -493,7 +501,7 @@ __device__ __forceinline__ uint32_t round_mask(const Row& R, int r, const float4
 // busiest lane holds candidates. Bit 4*f + e is element e of float4 f, i.e.
 // slot f / kVS, float4 f % kVS. kmn/kmx collect the lane's key range.
 template <int T, int U, int W>
-__device__ __forceinline__ void extract_lane(const Row& R, int r, const float4 (&v)[U], uint32_t mask,
+__device__ __forceinline__ void extract_lane(const RowCore& R, int r, const float4 (&v)[U], uint32_t mask,
                                              uint32_t* counter, uint2* list, uint32_t cap, uint32_t& kmn,
                                              uint32_t& kmx) {
   using G = Geo<T, U, W>;
@@ -519,7 +527,7 @@ __device__ __forceinline__ void extract_lane(const Row& R, int r, const float4 (
 }
 
 // Fold the warp's key range into the CTA's (local_min / local_max).
-__device__ __forceinline__ void flush_key_range(const Row& R, uint32_t kmn, uint32_t kmx) {
+__device__ __forceinline__ void flush_key_range(const RowCore& R, uint32_t kmn, uint32_t kmx) {
   kmn = __reduce_min_sync(kFull, kmn);
   kmx = __reduce_max_sync(kFull, kmx);
   if (lane_id() == 0 && kmn <= kmx) {
@@ -531,7 +539,7 @@ __device__ __forceinline__ void flush_key_range(const Row& R, uint32_t kmn, uint
 // Append every kept position whose score passes the threshold (x >= g, or
 // every valid position when `all`) to the list.
 template <int T, int U, int W, class Keep>
-__device__ __forceinline__ void filter_round(Row& R, int r, const float4 (&v)[U],
+__device__ __forceinline__ void filter_round(RowCore& R, int r, const float4 (&v)[U],
                                              const int (&n)[Geo<T, U, W>::kSlots], float g, bool all,
                                              uint32_t* counter, uint2* list, uint32_t cap, Keep keep) {
   uint32_t kmn = 0xffffffffu, kmx = 0u;
@@ -545,7 +553,7 @@ __device__ __forceinline__ void filter_round(Row& R, int r, const float4 (&v)[U]
 // F >= U slot F - U of round r + 1. kPos: every flagged score is > 0 (the
 // threshold is positive), so its key is its bits with the sign bit set.
 template <int T, int U, bool kPos>
-__device__ __forceinline__ void walk_lane(const Row& R, uint32_t mask, uint32_t p0, uint32_t sstride,
+__device__ __forceinline__ void walk_lane(const RowCore& R, uint32_t mask, uint32_t p0, uint32_t sstride,
                                           uint32_t* counter, uint2* list, uint32_t cap, uint32_t& kmn,
                                           uint32_t& kmx) {
   constexpr uint32_t kTile = (uint32_t)Geo<T, U, 4>::kTile;
@@ -574,8 +582,8 @@ __device__ __forceinline__ void walk_lane(const Row& R, uint32_t mask, uint32_t 
 // lanes stage it in shared memory before its buffer reloads, so the next
 // loads leave before the candidates are written; with 16-position rounds
 // (U = 4) both rounds of a pair share one walk over a 32-bit mask.
-template <int T, int U, bool kPos>
-__device__ __forceinline__ void filter_rounds_all(Row& R, bool vec, float4 (&a)[U], int (&na)[U], float4 (&b)[U],
+template <int T, int U, bool kPos, class S>
+__device__ __forceinline__ void filter_rounds_all(RowT<S>& R, bool vec, float4 (&a)[U], int (&na)[U], float4 (&b)[U],
                                                   int (&nb)[U], float g, bool all, uint32_t* counter, uint2* list,
                                                   uint32_t cap) {
   using G = Geo<T, U, 4>;
@@ -626,7 +634,7 @@ __device__ __forceinline__ void filter_rounds_all(Row& R, bool vec, float4 (&a)[
 // ------------------------------------------------------------------ block items (stage A)
 
 template <int T, int U, int W, int kLevel>
-__device__ __forceinline__ void hist_round_blocks(Row& R, const float4 (&v)[U],
+__device__ __forceinline__ void hist_round_blocks(RowCore& R, const float4 (&v)[U],
                                                   const int (&n)[Geo<T, U, W>::kSlots], uint32_t d1) {
 #pragma unroll
   for (int s = 0; s < Geo<T, U, W>::kSlots; ++s) {
@@ -638,7 +646,7 @@ __device__ __forceinline__ void hist_round_blocks(Row& R, const float4 (&v)[U],
 }
 
 template <int T, int U, int W>
-__device__ __forceinline__ void filter_round_blocks(Row& R, int r, const float4 (&v)[U],
+__device__ __forceinline__ void filter_round_blocks(RowCore& R, int r, const float4 (&v)[U],
                                                     const int (&n)[Geo<T, U, W>::kSlots], uint32_t t,
                                                     uint32_t* counter, uint2* list, uint32_t cap) {
   uint32_t kmn = 0xffffffffu, kmx = 0u;
@@ -690,7 +698,7 @@ __device__ __forceinline__ uint32_t bins_total(const uint32_t* bins, Misc* m) {
 // exactly K of them >= Tc. Requires 1 <= K <= number of valid candidates and
 // all composites distinct.
 template <int T>
-__device__ __forceinline__ uint64_t select_local(Row& R, uint32_t K, int64_t idx_limit) {
+__device__ __forceinline__ uint64_t select_local(RowCore& R, uint32_t K, int64_t idx_limit) {
   Misc* m = R.m;
   uint64_t tval = 0, tmask = 0;
   uint32_t need = K;
@@ -721,7 +729,7 @@ __device__ __forceinline__ uint64_t select_local(Row& R, uint32_t K, int64_t idx
 
 // Compact every candidate with composite >= Tc into stage[] (as composites).
 template <int T>
-__device__ __forceinline__ uint32_t compact_selected(Row& R, uint64_t Tc) {
+__device__ __forceinline__ uint32_t compact_selected(RowCore& R, uint64_t Tc) {
   Misc* m = R.m;
   if (threadIdx.x == 0) m->aux[0] = 0;
   __syncthreads();
@@ -744,7 +752,7 @@ __device__ __forceinline__ uint32_t compact_selected(Row& R, uint64_t Tc) {
 // then the exact rank of the items of b* among themselves. Returns false,
 // deciding nothing, when b* holds more than kMaxBucket items.
 template <int T>
-__device__ __forceinline__ bool threshold_by_buckets(Row& R, uint32_t K, uint32_t lo, uint32_t hi, uint64_t* Tc) {
+__device__ __forceinline__ bool threshold_by_buckets(RowCore& R, uint32_t K, uint32_t lo, uint32_t hi, uint64_t* Tc) {
   constexpr int NB = kOutBuckets;
   constexpr int BPT = NB / T;
   Misc* m = R.m;
@@ -799,14 +807,15 @@ __device__ __forceinline__ bool threshold_by_buckets(Row& R, uint32_t K, uint32_
 
 // ------------------------------------------------------------------ ordered output
 
-__device__ __forceinline__ void write_slot(int32_t* oi, float* ov, uint32_t slot, uint64_t c, const float* rowp) {
+template <class S>
+__device__ __forceinline__ void write_slot(int32_t* oi, float* ov, uint32_t slot, uint64_t c, const S* rowp) {
   const uint32_t key = (uint32_t)(c >> 32), idx = ~(uint32_t)c;
   oi[slot] = (int32_t)idx;
   if (ov) ov[slot] = value_of(key, rowp, idx);
 }
 
 template <int T>
-__device__ __forceinline__ void write_padding(const Row& R, int32_t* oi, float* ov, uint32_t K, uint32_t kout) {
+__device__ __forceinline__ void write_padding(const RowCore& R, int32_t* oi, float* ov, uint32_t K, uint32_t kout) {
   if (R.rank != 0) return;
   for (uint32_t j = K + threadIdx.x; j < kout; j += T) {
     oi[j] = -1;
@@ -817,8 +826,8 @@ __device__ __forceinline__ void write_padding(const Row& R, int32_t* oi, float* 
 // Output fallback for candidate sets with heavily populated buckets: radix
 // select of the K-th composite, compaction, then a bitonic sort (one CTA or
 // large own slices) or a rank count per own item.
-template <int T>
-__device__ __noinline__ void sorted_fallback(Row R, bool exact, uint64_t Tc, uint32_t K, uint32_t kout,
+template <int T, class S>
+__device__ __noinline__ void sorted_fallback(RowT<S> R, bool exact, uint64_t Tc, uint32_t K, uint32_t kout,
                                              int32_t* oi, float* ov, int64_t idx_limit, OwnSlice owner) {
   Misc* m = R.m;
   const uint64_t T64 = exact ? Tc : select_local<T>(R, K, idx_limit);
@@ -871,8 +880,8 @@ __device__ __noinline__ void sorted_fallback(Row R, bool exact, uint64_t Tc, uin
 // histogram is already zero (the fast path clears it before the filter and
 // the exchange's barrier follows); otherwise one pass finds them. Expects
 // res_max reset.
-template <int T>
-__device__ __forceinline__ bool bucket_select_sort(Row& R, uint32_t K, uint32_t kout, int32_t* oi, float* ov,
+template <int T, class S>
+__device__ __forceinline__ bool bucket_select_sort(RowT<S>& R, uint32_t K, uint32_t kout, int32_t* oi, float* ov,
                                                    OwnSlice owner, bool have_range, uint32_t lo, uint32_t hi,
                                                    uint32_t N) {
   constexpr int NB = kOutBuckets;
@@ -969,8 +978,8 @@ __device__ __forceinline__ bool bucket_select_sort(Row& R, uint32_t K, uint32_t 
 // re-reading the slice and merging histograms over DSMEM, then one capture
 // pass of the K items >= the K-th composite into a flat candidate array.
 // Returns that composite. Requires R.init_pending == false.
-template <int T, int U, int W, bool kBlocks, class Keep>
-__device__ __noinline__ uint64_t exact_select(Row R, const Params p, uint32_t K, int64_t idx_limit, Keep keep) {
+template <int T, int U, int W, bool kBlocks, class Keep, class S>
+__device__ __noinline__ uint64_t exact_select(RowT<S> R, const Params p, uint32_t K, int64_t idx_limit, Keep keep) {
   using G = Geo<T, U, W>;
   Misc* m = R.m;
   const bool vec = p.vec_ok != 0;
@@ -1095,7 +1104,7 @@ __device__ __noinline__ uint64_t exact_select(Row R, const Params p, uint32_t K,
 // instead of 2048-bin ones. Returns the lower edge of the 16-bit bin holding
 // the r-th largest sample key.
 template <int T, int U, int W>
-__device__ __forceinline__ uint32_t estimate_small(Row& R, const float4 (&v)[U],
+__device__ __forceinline__ uint32_t estimate_small(RowCore& R, const float4 (&v)[U],
                                                    const int (&n)[Geo<T, U, W>::kSlots], uint32_t K,
                                                    int64_t items) {
   using G = Geo<T, U, W>;
@@ -1150,8 +1159,8 @@ __device__ __forceinline__ uint32_t estimate_small(Row& R, const float4 (&v)[U],
 // path (the candidates are every item >= a lower bound of the K-th item).
 // cur/nxt hold rounds 0 and 1 on entry when `loaded`; *regs_intact tells
 // whether they still do on return.
-template <int T, int U, int W, bool kBlocks, class Keep>
-__device__ __forceinline__ bool select_stage(Row& R, const Params& p, float4 (&cur)[U],
+template <int T, int U, int W, bool kBlocks, class Keep, class S>
+__device__ __forceinline__ bool select_stage(RowT<S>& R, const Params& p, float4 (&cur)[U],
                                              int (&nc)[Geo<T, U, W>::kSlots], float4 (&nxt)[U],
                                              int (&nn)[Geo<T, U, W>::kSlots], bool loaded, uint32_t K,
                                              int64_t items, int64_t idx_limit, Keep keep, bool first,
@@ -1345,7 +1354,7 @@ struct RoundRegs {
 // is the rank sought inside that bin. Rare (heavily populated first-level
 // bins), so it lives out of line and the common path stays compact.
 template <int T, int U, int W>
-__device__ __noinline__ uint32_t refine_level2(Row R, RoundRegs<U, Geo<T, U, W>::kSlots> rr, uint32_t d1,
+__device__ __noinline__ uint32_t refine_level2(RowCore R, RoundRegs<U, Geo<T, U, W>::kSlots> rr, uint32_t d1,
                                                uint32_t r2) {
   zero_bins<T>(R.hist);
   hist_round<T, U, W, 2>(R, 0, rr.v, rr.n, d1, KeepAll{});
@@ -1361,8 +1370,8 @@ __device__ __noinline__ uint32_t refine_level2(Row R, RoundRegs<U, Geo<T, U, W>:
 // select_stage (first stage, every position kept) without the second
 // register buffer, the streaming filter and the inline second estimate level:
 // the code a row executes once per CTA is what its latency pays to fetch.
-template <int T, int U, int W>
-__device__ __forceinline__ bool select_one(Row& R, const Params& p, float4 (&v)[U], int (&n)[Geo<T, U, W>::kSlots],
+template <int T, int U, int W, class S>
+__device__ __forceinline__ bool select_one(RowT<S>& R, const Params& p, float4 (&v)[U], int (&n)[Geo<T, U, W>::kSlots],
                                            uint32_t K, uint64_t* Tc) {
   using G = Geo<T, U, W>;
   Misc* m = R.m;
@@ -1449,10 +1458,10 @@ __device__ __forceinline__ bool select_one(Row& R, const Params& p, float4 (&v)[
 // Select and write the top K positions of this row after select_stage.
 // gather: the fast-path exchange gathered every candidate in rank 0, which
 // writes the whole row alone; the other CTAs are done.
-template <int T>
-__device__ __forceinline__ void output_positions(Row& R0, const Params& p, bool exact, uint64_t Tc, uint32_t K,
+template <int T, class S>
+__device__ __forceinline__ void output_positions(RowT<S>& R0, const Params& p, bool exact, uint64_t Tc, uint32_t K,
                                                  int64_t idx_limit, bool gather) {
-  Row R = R0;
+  RowT<S> R = R0;
   if (gather && !exact && R.nclus > 1) {
     if (R.rank != 0) {
       stamp(R, kTrOutput);

@@ -23,7 +23,7 @@ __device__ __forceinline__ uint32_t pick_id(const uint32_t (&a)[B], uint32_t i) 
 // output. The candidate area holds every gathered position, so no row can
 // overflow it. Should a filter ever keep fewer than K, it is redone keeping
 // every position.
-template <int T, int W>
+template <int T, int W, class S>
 __global__ void __launch_bounds__(T, 1) listed_kernel(Params p) {
   constexpr int U = 8;          // float4 per thread: the round
   constexpr int VS = W / 4;     // float4 per block
@@ -31,7 +31,7 @@ __global__ void __launch_bounds__(T, 1) listed_kernel(Params p) {
   using G = Geo<T, U, W>;
   static_assert(G::kSlots == BPT, "a slot is a block");
   extern __shared__ __align__(128) unsigned char smem[];
-  Row R;
+  RowT<S> R;
   stamp(p, kTrStart);
   grid_dependents_launch();
   setup_row<T, U, W>(R, p, smem);
@@ -185,14 +185,19 @@ __global__ void __launch_bounds__(T, 1) listed_kernel(Params p) {
   wait_init(R);
 }
 
-const void* listed_kernel_ptr(int block) {
+template <class S>
+const void* listed_ptr(int block) {
   switch (block) {
-    case 4: return reinterpret_cast<const void*>(&listed_kernel<512, 4>);
-    case 8: return reinterpret_cast<const void*>(&listed_kernel<512, 8>);
-    case 16: return reinterpret_cast<const void*>(&listed_kernel<512, 16>);
-    case 32: return reinterpret_cast<const void*>(&listed_kernel<512, 32>);
+    case 4: return reinterpret_cast<const void*>(&listed_kernel<512, 4, S>);
+    case 8: return reinterpret_cast<const void*>(&listed_kernel<512, 8, S>);
+    case 16: return reinterpret_cast<const void*>(&listed_kernel<512, 16, S>);
+    case 32: return reinterpret_cast<const void*>(&listed_kernel<512, 32, S>);
     default: return nullptr;
   }
+}
+
+const void* listed_kernel_ptr(int block, bool bf16) {
+  return bf16 ? listed_ptr<uint16_t>(block) : listed_ptr<float>(block);
 }
 
 // Blocks one listed-kernel CTA gathers in its single register round.

@@ -93,10 +93,10 @@ __device__ __forceinline__ void bulk_g2s(float* dst, const float* src, uint32_t 
                :: "r"(smem_addr(dst)), "l"(src), "r"(bytes), "r"(smem_addr(bar)) : "memory");
 }
 
-__device__ __forceinline__ bool ring_wait(uint64_t* bars, uint32_t ns, uint32_t seq) {
+__device__ __forceinline__ bool ring_wait(uint64_t* bars, uint32_t ns, uint32_t seq, uint32_t polls) {
   uint64_t* bar = bars + (seq % ns);
   const uint32_t parity = (seq / ns) & 1u;
-  for (uint32_t i = 0; i < kWaitPolls; ++i)
+  for (uint32_t i = 0; i < polls; ++i)
     if (mbar_try_wait(bar, parity)) return true;
   return false;
 }
@@ -181,6 +181,7 @@ struct Prod {
   int chunk, rounds;
   uint32_t seq;       // next chunk number to issue
   uint32_t released;  // chunks whose stage is free again
+  bool skip_last;     // tests only: never issue this CTA's final chunk
 };
 static_assert(sizeof(Prod) <= kProdBytes, "producer state does not fit its shared-memory slot");
 
@@ -219,6 +220,14 @@ __device__ __forceinline__ void produce(Prod& P, uint32_t limit) {
       continue;
     }
     const uint32_t st = P.seq % P.ns;
+    if (P.skip_last && P.chunk == P.rounds - 1 && P.row + P.step >= P.rows) {
+      // tests only: the CTA's final chunk is never issued, so its stage's
+      // barrier never completes and the consumers' bounded wait gives up;
+      // no copy is in flight for it
+      ++P.chunk;
+      ++P.seq;
+      continue;
+    }
     float* dst = P.ring + (size_t)st * SG::kChunk;
     uint32_t n[SG::kSlots];
     uint32_t bytes = 0;
@@ -330,8 +339,9 @@ __device__ __forceinline__ void stream_row(Row& R, const Params& p, uint64_t* ba
   const uint32_t cap = (uint32_t)p.cap;
   const bool full = rounds_max <= 2;
   auto stage = [&](int c) -> float* { return ring + (size_t)((g0 + (uint32_t)c) % ns) * SG::kChunk; };
+  const uint32_t polls = p.stall_polls > 0 ? (uint32_t)p.stall_polls : kWaitPolls;
   auto wait_chunk = [&](int c) {
-    if (!ring_wait(bars, ns, g0 + (uint32_t)c)) late = true;
+    if (!ring_wait(bars, ns, g0 + (uint32_t)c, polls)) late = true;
   };
   // block barrier (every thread is done with the chunk's stage), then refill
   auto release_chunk = [&](int c) {

@@ -30,7 +30,7 @@ __global__ void __launch_bounds__(T, kMinCtas) stream_kernel(Params p) {
   grid_dependency_wait();
   Prod& P = *reinterpret_cast<Prod*>(smem + sl.prod);  // thread 0 only
   if (threadIdx.x == 0) {
-    P.scores = p.scores;
+    P.scores = static_cast<const float*>(p.scores);
     P.lengths = p.lengths;
     P.row_stride = p.row_stride;
     P.rows = p.rows;
@@ -42,6 +42,7 @@ __global__ void __launch_bounds__(T, kMinCtas) stream_kernel(Params p) {
     P.nclus = nclus;
     P.seq = 0;
     P.released = 0;
+    P.skip_last = p.stall_polls > 0;
     prod_row<T, UC>(P, first);
     produce<T, UC>(P, ns);
   }
@@ -73,7 +74,7 @@ __global__ void __launch_bounds__(T, kMinCtas) stream_kernel(Params p) {
   if (threadIdx.x == 0) {
     for (uint32_t i = 0; i < ns && i < g0; ++i) {
       const uint32_t seq = g0 - 1u - i;
-      (void)ring_wait(bars, ns, seq);
+      (void)ring_wait(bars, ns, seq, p.stall_polls > 0 ? (uint32_t)p.stall_polls : kWaitPolls);
     }
   }
   __syncthreads();

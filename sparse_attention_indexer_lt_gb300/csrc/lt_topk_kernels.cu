@@ -7,11 +7,12 @@ namespace lt {
 // One CTA (or one cluster of CTAs) per row: select the top K = min(k, L)
 // positions and write them ordered by (score desc, index asc). kOne: every
 // CTA's slice is a single register round (the planner guarantees it).
-template <int T, int U, bool kOne>
+// S: the score type (float, or uint16_t holding bf16 bits).
+template <int T, int U, bool kOne, class S>
 __global__ void __launch_bounds__(T, (T <= 256 ? 3 : 1)) topk_kernel(Params p) {
   extern __shared__ __align__(128) unsigned char smem[];
   using G = Geo<T, U, 4>;
-  Row R;
+  RowT<S> R;
   stamp(p, kTrStart);
   grid_dependents_launch();
   setup_row<T, U, 4>(R, p, smem);
@@ -33,13 +34,24 @@ __global__ void __launch_bounds__(T, (T <= 256 ? 3 : 1)) topk_kernel(Params p) {
   wait_init(R);
 }
 
-const void* topk_kernel_ptr(int threads, bool one_round) {
+template <class S>
+const void* topk_ptr(int threads, bool one_round) {
   if (threads == 256)
-    return one_round ? reinterpret_cast<const void*>(&topk_kernel<256, 4, true>)
-                     : reinterpret_cast<const void*>(&topk_kernel<256, 4, false>);
+    return one_round ? reinterpret_cast<const void*>(&topk_kernel<256, 4, true, S>)
+                     : reinterpret_cast<const void*>(&topk_kernel<256, 4, false, S>);
   if (threads == 512)
-    return one_round ? reinterpret_cast<const void*>(&topk_kernel<512, 8, true>)
-                     : reinterpret_cast<const void*>(&topk_kernel<512, 8, false>);
+    return one_round ? reinterpret_cast<const void*>(&topk_kernel<512, 8, true, S>)
+                     : reinterpret_cast<const void*>(&topk_kernel<512, 8, false, S>);
+  return nullptr;
+}
+
+const void* topk_kernel_ptr(int threads, bool one_round, bool bf16) {
+  return bf16 ? topk_ptr<uint16_t>(threads, one_round) : topk_ptr<float>(threads, one_round);
+}
+
+const void* blocked_kernel_ptr(int threads, int block, bool bf16) {
+  if (threads == 256) return bf16 ? blocked_kernel_ptr_of<256, uint16_t>(block) : blocked_kernel_ptr_of<256, float>(block);
+  if (threads == 512) return bf16 ? blocked_kernel_ptr_of<512, uint16_t>(block) : blocked_kernel_ptr_of<512, float>(block);
   return nullptr;
 }
 

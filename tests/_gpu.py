@@ -77,5 +77,29 @@ def parity_candidates(S, L, cand, block, k, what="", **kw):
     return gi, gv
 
 
+def parity_bf16(T, L, k, what="", kind="topk", block=8, k_blocks=2048, cand=None, **kw):
+    """bf16 scores (a CPU torch.bfloat16 tensor) through the bf16 path and the
+    oracle on the same bit patterns: indices, value bits and kept blocks agree."""
+    import workloads
+    bits = workloads.bf16_bits(T)
+    Ln = None if L is None else np.asarray(L, dtype=np.int32)
+    s = T.cuda()
+    l = None if Ln is None else torch.as_tensor(Ln).cuda()
+    if kind == "topk":
+        gi, gv = lt.topk(s, l, k, **kw)
+        oi, ov = oracle.topk_bf16(bits, Ln, k)
+    elif kind == "blocked":
+        gi, gv, gb = lt.topk_blocked(s, l, block, k_blocks, k, **kw)
+        oi, ov, ob = oracle.topk_blocked_bf16(bits, Ln, block, k_blocks, k)
+    else:
+        C = np.ascontiguousarray(np.asarray(cand, dtype=np.int32))
+        gi, gv = lt.topk_candidates(s, torch.as_tensor(C).cuda(), l, block, k, **kw)
+        oi, ov = oracle.topk_candidates_bf16(bits, Ln, C, block, k)
+    torch.cuda.synchronize()
+    assert_same(gi.cpu().numpy(), None if gv is None else gv.cpu().numpy(), oi, ov, what)
+    if kind == "blocked" and gb is not None:
+        assert np.array_equal(gb.cpu().numpy(), ob), f"{what}: out_blocks differ"
+
+
 def counters():
     return torch.zeros(lt.NUM_COUNTERS, dtype=torch.int32, device="cuda")

@@ -45,8 +45,8 @@ def test_status_strings_and_version(lib):
 P = ctypes.c_void_p
 
 
-def _topk(lib, scores, lengths, rows, stride, k, oi, ov, fc=0, fk=0):
-    return lib.lt_topk_ex(scores, lengths, rows, stride, k, oi, ov, fc, 0, 0, fk, None, None, None)
+def _topk(lib, scores, lengths, rows, stride, k, oi, ov, fc=0, fk=0, dtype=0):
+    return lib.lt_topk_ex(scores, dtype, lengths, rows, stride, k, oi, ov, fc, 0, 0, fk, None, None, None)
 
 
 def test_invalid_arguments_rejected_without_launch(lib):
@@ -59,7 +59,9 @@ def test_invalid_arguments_rejected_without_launch(lib):
     assert _topk(lib, fake, None, 1, 16, 4, fake, None, fc=3) == 1  # cluster not a power of two
     assert _topk(lib, fake, None, 1, 16, 4096, fake, None) == 2  # k > LT_MAX_K
     assert _topk(lib, fake, None, 1, (1 << 30) + 1, 4, fake, None) == 2  # row too long
-    assert lib.lt_topk_ex(fake, None, 1, 16, 4, fake, None, 0, 1024, 0, 0, None, None, None) == 1  # bad threads
+    assert lib.lt_topk_ex(fake, 0, None, 1, 16, 4, fake, None, 0, 1024, 0, 0, None, None, None) == 1  # bad threads
+    assert _topk(lib, fake, None, 1, 16, 4, fake, None, dtype=2) == 1  # unknown score type
+    assert _topk(lib, fake, None, 1, 16, 4, fake, None, dtype=-1) == 1
     assert _topk(lib, fake, None, 1, 16, 4, fake, None, fk=3) == 1  # unknown kernel
     assert _topk(lib, fake, None, 1, 16, 4, fake, None, fk=-1) == 1
     # rows == 0 is a valid no-op
@@ -68,11 +70,16 @@ def test_invalid_arguments_rejected_without_launch(lib):
 
 def test_blocked_invalid_arguments(lib):
     fake = P(0x1000)
-    f = lib.lt_topk_blocked_ex
+    g = lib.lt_topk_blocked_ex
+
+    def f(*a, dtype=0):
+        return g(a[0], dtype, *a[1:])
+
     assert f(fake, None, 1, 64, 0, 4, 4, fake, None, None, 0, 0, 0, None, None, None) == 1   # block < 1
     assert f(fake, None, 1, 64, 8, 0, 4, fake, None, None, 0, 0, 0, None, None, None) == 1   # k_blocks < 1
     assert f(fake, None, 1, 64, 6, 4, 4, fake, None, None, 0, 0, 0, None, None, None) == 2   # block unsupported
     assert f(fake, None, 1, 64, 8, 5000, 4, fake, None, None, 0, 0, 0, None, None, None) == 2
+    assert f(fake, None, 1, 64, 8, 4, 4, fake, None, None, 0, 0, 0, None, None, None, dtype=5) == 1  # score type
     assert f(None, None, 0, 64, 8, 4, 4, None, None, None, 0, 0, 0, None, None, None) == 0
 
 
@@ -80,8 +87,8 @@ def test_candidates_invalid_arguments(lib):
     fake = P(0x1000)
     f = lib.lt_topk_candidates_ex
 
-    def call(scores, rows, stride, block, cand, n_cand, k, oi):
-        return f(scores, None, rows, stride, block, cand, n_cand, k, oi, None, 0, 0, 0, None, None, None)
+    def call(scores, rows, stride, block, cand, n_cand, k, oi, dtype=0):
+        return f(scores, dtype, None, rows, stride, block, cand, n_cand, k, oi, None, 0, 0, 0, None, None, None)
 
     assert call(fake, 1, 64, 0, fake, 4, 4, fake) == 1          # block < 1
     assert call(fake, 1, 64, 8, fake, -1, 4, fake) == 1         # n_cand < 0
@@ -91,6 +98,7 @@ def test_candidates_invalid_arguments(lib):
     assert call(fake, 1, 64, 6, fake, 4, 4, fake) == 2          # block unsupported
     assert call(fake, 1, 64, 8, fake, 4, 4096, fake) == 2       # k > LT_MAX_K
     assert call(fake, 1, 262148, 4, fake, 4, 4, fake) == 2      # more than 65536 blocks per row
+    assert call(fake, 1, 64, 8, fake, 4, 4, fake, dtype=3) == 1  # unknown score type
     assert call(None, 0, 64, 8, None, 4, 4, None) == 0          # rows == 0: nothing to do
 
 
@@ -102,6 +110,21 @@ def test_plan_rejects_bad_arguments(lib):
     assert f(1, 64, 4, 0, 4, 1, 0, 0, 0, 1, None) == 1                    # no output struct
     assert f(1, 64, 4, 0, 4, 1, 0, 0, 7, 1, ctypes.byref(info)) == 1      # unknown kernel
     assert f(1, 64, 4, 1, 6, 4, 0, 0, 0, 1, ctypes.byref(info)) == 2      # block unsupported
+
+
+def test_valid_calls_without_a_device_report_a_cuda_error(lib):
+    """With no usable GPU every valid call fails in the CUDA runtime: the plain
+    entry points (fp32 and bf16) return LT_ERR_CUDA (3), having launched nothing."""
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present: the CUDA runtime does not fail here")
+    fake = P(0x1000)
+    assert lib.lt_topk(fake, None, 1, 16, 4, fake, None, None) == 3
+    assert lib.lt_topk_bf16(fake, None, 1, 16, 4, fake, None, None) == 3
+    assert lib.lt_topk_blocked(fake, None, 1, 16, 8, 4, 4, fake, None, None, None) == 3
+    assert lib.lt_topk_blocked_bf16(fake, None, 1, 16, 8, 4, 4, fake, None, None, None) == 3
+    assert lib.lt_topk_candidates(fake, None, 1, 16, 8, fake, 2, 4, fake, None, None) == 3
+    assert lib.lt_topk_candidates_bf16(fake, None, 1, 16, 8, fake, 2, 4, fake, None, None) == 3
 
 
 def test_binding_refuses_cpu_tensors():

@@ -1,0 +1,104 @@
+"""The contract's own entry points on the GPU, called through ctypes with device
+pointers and a stream, and the failure paths reachable without faulting a GPU."""
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads
+
+pytestmark = pytest.mark.gpu
+
+LT_TEST_FAIL_LAUNCHES, LT_TEST_STALL_STREAMED = 1, 2
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from sparse_attention_indexer_lt_gb300 import build, load
+    build.build()
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    return load()
+
+
+def P(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def test_plain_entry_points_match_the_oracle(lib):
+    """lt_topk, lt_topk_blocked and lt_topk_candidates (fp32) on a side stream."""
+    rows, stride, k, kb = 3, 70000, 256, 512
+    S, L = workloads.random_rows(rows, stride, seed=41, dist="tail", lengths="ragged", min_len=1)
+    Sn, Ln = S.numpy(), L.numpy()
+    s, l = S.cuda(), L.cuda()
+    oi = torch.empty(rows, k, dtype=torch.int32, device="cuda")
+    ov = torch.empty(rows, k, dtype=torch.float32, device="cuda")
+    ob = torch.empty(rows, kb, dtype=torch.int32, device="cuda")
+    st = torch.cuda.Stream()
+    sp = ctypes.c_void_p(st.cuda_stream)
+
+    def same(ei, ev):
+        assert np.array_equal(oi.cpu().numpy(), ei)
+        assert np.array_equal(ov.cpu().numpy().view(np.uint32), ev.view(np.uint32))
+
+    assert lib.lt_topk(P(s), P(l), rows, stride, k, P(oi), P(ov), sp) == 0
+    st.synchronize()
+    same(*oracle.topk(Sn, Ln, k))
+    assert lib.lt_topk_blocked(P(s), P(l), rows, stride, 8, kb, k, P(oi), P(ov), P(ob), sp) == 0
+    st.synchronize()
+    ei, ev, eb = oracle.topk_blocked(Sn, Ln, 8, kb, k)
+    same(ei, ev)
+    assert np.array_equal(ob.cpu().numpy(), eb)
+    # the kept blocks as the published list of a later layer's call
+    assert lib.lt_topk_candidates(P(s), P(l), rows, stride, 8, P(ob), kb, k, P(oi), P(ov), sp) == 0
+    st.synchronize()
+    same(*oracle.topk_candidates(Sn, Ln, eb, 8, k))
+    # k_blocks < k: the stages run one after the other
+    assert lib.lt_topk_blocked(P(s), P(l), rows, stride, 8, 16, k, P(oi), P(ov), None, sp) == 0
+    st.synchronize()
+    ei, ev, _ = oracle.topk_blocked(Sn, Ln, 8, 16, k)
+    same(ei, ev)
+
+
+def test_injected_launch_failure_returns_cuda_error_and_launches_nothing(lib):
+    import sparse_attention_indexer_lt_gb300 as lt
+    S, _ = workloads.random_rows(2, 5000, seed=42, dist="normal")
+    s = S.cuda()
+    oi = torch.full((2, 64), 7, dtype=torch.int32, device="cuda")
+    assert lib.lt_test_inject(LT_TEST_FAIL_LAUNCHES, 3) == 0
+    for call in (lambda: lib.lt_topk(P(s), None, 2, 5000, 64, P(oi), None, None),
+                 lambda: lib.lt_topk_blocked(P(s), None, 2, 5000, 8, 128, 64, P(oi), None, None, None),
+                 lambda: lib.lt_topk_candidates(P(s), None, 2, 5000, 8, None, 0, 64, P(oi), None, None)):
+        assert call() == 3  # LT_ERR_CUDA
+    torch.cuda.synchronize()
+    assert bool((oi == 7).all()), "a failed launch wrote outputs"
+    assert lib.lt_test_inject(99, 1) == 1 and lib.lt_test_inject(LT_TEST_FAIL_LAUNCHES, -1) == 1
+    # the hook is spent: the next call works and the context is healthy
+    idx, _ = lt.topk(s, None, 64)
+    assert np.array_equal(idx.cpu().numpy(), oracle.topk(S.numpy(), None, 64)[0])
+
+
+def test_streamed_kernel_wait_gives_up_and_returns(lib):
+    """The streamed kernel's mbarrier waits are bounded: with the final copy of
+    each CTA never issued, the wait for it gives up after a few polls, the row
+    is counted in counters[4], and the kernel finishes; the next launch is
+    correct again."""
+    import sparse_attention_indexer_lt_gb300 as lt
+    rows, stride = 40, 12000
+    S, _ = workloads.random_rows(rows, stride, seed=43, dist="bf16")
+    s = S.cuda()
+    c = torch.zeros(lt.NUM_COUNTERS, dtype=torch.int32, device="cuda")
+    assert lib.lt_test_inject(LT_TEST_STALL_STREAMED, 4) == 0
+    lt.topk(s, None, 128, force_kernel=lt.KERNEL_STREAM, counters=c)
+    torch.cuda.synchronize()
+    pl = lt.plan(rows, stride, 128, force_kernel=lt.KERNEL_STREAM)
+    assert c.cpu().numpy()[4] >= 1
+    assert c.cpu().numpy()[4] <= pl["grid"] // pl["cluster"]
+    # the hook applied to that launch only
+    c.zero_()
+    idx, val = lt.topk(s, None, 128, force_kernel=lt.KERNEL_STREAM, counters=c)
+    torch.cuda.synchronize()
+    oi, ov = oracle.topk(S.numpy(), None, 128)
+    assert np.array_equal(idx.cpu().numpy(), oi)
+    assert c.cpu().numpy()[4] == 0

@@ -145,6 +145,28 @@ def random_rows(rows: int, stride: int, seed: int, *, dist: str = "normal",
     return x.contiguous(), ln
 
 
+def to_bf16(scores: torch.Tensor) -> torch.Tensor:
+    """The bf16 form of a workload's scores (round to nearest even; exact for the
+    bf16-rounded configs). A layout of the inputs, not part of the method."""
+    return scores.to(torch.bfloat16).contiguous()
+
+
+def bf16_bits(t: torch.Tensor):
+    """The uint16 bit patterns of a CPU bf16 tensor, as a numpy array."""
+    import numpy as np
+    return t.contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+def random_bf16_special(rows: int, stride: int, seed: int):
+    """bf16 bit patterns drawn from a pool of special values (+-0, +-inf,
+    subnormals, NaNs with payloads, the largest finite) and ordinary numbers."""
+    g = torch.Generator("cpu").manual_seed(seed)
+    pool = torch.tensor([0x0000, 0x8000, 0x7F80, 0xFF80, 0x0001, 0x8001, 0x007F, 0x7FC0, 0xFFC1, 0x7FA0,
+                         0x7F7F, 0xFF7F, 0x3F80, 0xBF80, 0x4049, 0xC0A0, 0x3F81, 0x3F80], dtype=torch.int32)
+    pick = torch.randint(0, pool.numel(), (rows, stride), generator=g)
+    return pool[pick].to(torch.int16).view(torch.bfloat16).contiguous()
+
+
 def read_bytes(lengths, rows: int, stride: int) -> int:
     """Bytes a read-once pass touches: 4 bytes per valid position."""
     if lengths is None:
