@@ -58,6 +58,7 @@ def parse():
     ap.add_argument("--force-cluster", type=int, default=0)
     ap.add_argument("--only", choices=sorted(workloads.CONFIGS), default=None,
                     help="time one workload's kernel alone (for profilers); prints a short JSON line")
+    ap.add_argument("--dtype", choices=["f32", "bf16"], default="f32", help="score type in --only / --trace runs")
     ap.add_argument("--kernel", choices=["auto", "resident", "stream"], default="auto",
                     help="force the top-k kernel in --only / --trace runs")
     return ap.parse_args()
@@ -274,6 +275,7 @@ def bench_ours(args, world, rank):
         warm_ms = timed_steps(lambda i: lt.topk(base, None, w.k, out_idx=oi, out_val=ov),
                               args.steps, args.warmup, world)
         batched = [] if args.no_batched else bench_batched(lt, dev, args, world, peak, L2)
+        compress = [] if args.no_batched else bench_compress(lt, dev, args, world, peak)
         ttk = bench_torch_topk(base, w.k, args, world)
     clocks = clk.summary()
     total_ms = max_over_ranks(total_ms, world)
@@ -314,6 +316,7 @@ def bench_ours(args, world, rank):
         "clocks": clocks,
         "torch_topk_us": ttk,
         "batched": batched,
+        "compress": compress,
         "published_context": {"lightning_topk_us": PUBLISHED_US, "plain_pytorch_us": 100.0,
                               "hardware": "not stated on the pages"},
     }
@@ -322,18 +325,26 @@ def bench_ours(args, world, rank):
     return line
 
 
+BATCHED = [("c3_ragged_64", "f32"), ("c4_prefill_4096", "f32"), ("c5_blocked_16", "f32"),
+           ("c6_listed_16", "f32"), ("c4_prefill_4096", "bf16"), ("c2_decode_262144", "bf16"),
+           ("c5_blocked_16", "bf16")]
+
+
 def bench_batched(lt, dev, args, world, peak, L2):
     out = []
     steps = max(3, min(args.steps, 50))
-    for name in ("c3_ragged_64", "c4_prefill_4096", "c5_blocked_16", "c6_listed_16"):
+    for name, dtype in BATCHED:
         S, L, w = workloads.make(name)
+        if dtype == "bf16":  # the same scores handed over as bf16: half the bytes per position
+            S = workloads.to_bf16(S)
+        esize = S.element_size()
         listed = name.startswith("c6")
-        nbytes = workloads.read_bytes(L, w.rows, w.row_stride)
+        nbytes = workloads.read_bytes(L, w.rows, w.row_stride) * esize // 4
         # copies rotate over what a step touches (whole rows, for every kernel here)
         ncopies = workloads.l2_rotation_copies(nbytes, L2) if nbytes < 4 * L2 else 1
         cand = workloads.listed_blocks(name).to(dev) if listed else None
         if listed:  # the method reads the listed blocks' scores and the list, not the whole row
-            nbytes = 4 * cand.numel() * w.block + 4 * cand.numel()
+            nbytes = esize * cand.numel() * w.block + 4 * cand.numel()
         base = S.to(dev)
         copies = [base] + [base.clone() for _ in range(ncopies - 1)]
         ld = None if L is None else L.to(dev)
@@ -355,7 +366,7 @@ def bench_batched(lt, dev, args, world, peak, L2):
         kern_ms = step_ms
         gbs = nbytes / (kern_ms * 1e-3) / 1e9
         out.append({
-            "workload": name, "rows": w.rows, "read_bytes": nbytes,
+            "workload": name, "dtype": dtype, "rows": w.rows, "read_bytes": nbytes,
             "rows_per_s": round(w.rows * world / (step_ms * 1e-3), 1),
             "us_per_row": round(step_ms * 1000.0 / w.rows, 4),
             "kernel_us": round(kern_ms * 1000.0, 2),
@@ -364,10 +375,44 @@ def bench_batched(lt, dev, args, world, peak, L2):
             "plan": lt.plan(w.rows, w.row_stride, w.k, blocked=w.blocked or listed,
                             k_blocks=1 if listed else w.k_blocks),
         })
+        if w.rows == 1:
+            out[-1]["us_per_row_note"] = "one row: latency per call, back to back"
         if listed:
             out[-1]["bytes"] = "listed blocks' scores + the list"
             out[-1]["plan"] = {"kernel": "listed", "cluster": 1, "threads": 512, "grid": w.rows}
         del copies, base
+        torch.cuda.empty_cache()
+    return out
+
+
+def compress_bytes(w, esize: int) -> int:
+    """Algorithmic bytes of one compressor launch: kv and score read once, one
+    entry per block written, the bias read once."""
+    nblk = w.tokens // w.ratio
+    return w.rows * (nblk * w.ratio * w.dim * 2 * esize + nblk * w.dim * esize) + w.ratio * w.dim * 4
+
+
+def bench_compress(lt, dev, args, world, peak):
+    """The fused KV compressor at a million-token context (bf16 kv and scores,
+    inputs larger than the L2, drawn on the device)."""
+    out = []
+    steps = max(3, min(args.steps, 20))
+    for name in sorted(workloads.COMPRESS_CONFIGS):
+        w = workloads.COMPRESS_CONFIGS[name]
+        kv, sc, bias = workloads.compress_inputs(w.rows, w.tokens, w.dim, w.ratio, seed=0, device=dev,
+                                                 dtype=torch.bfloat16)
+        y = torch.empty(w.rows, w.tokens // w.ratio, w.dim, dtype=torch.bfloat16, device=dev)
+        nbytes = compress_bytes(w, 2)
+        total_ms = timed_steps(lambda i: lt.compress(kv, sc, bias, w.ratio, out=y), steps, max(3, args.warmup),
+                               world)
+        step_ms = max_over_ranks(total_ms, world) / steps
+        gbs = nbytes / (step_ms * 1e-3) / 1e9
+        out.append({"workload": name, "dtype": "bf16", "tokens": w.tokens, "dim": w.dim, "ratio": w.ratio,
+                    "bytes": nbytes, "kernel_us": round(step_ms * 1000.0, 2), "hbm_gbs": round(gbs, 1),
+                    "frac_of_peak": round(gbs / peak, 4),
+                    "tokens_per_s": round(w.rows * w.tokens * world / (step_ms * 1e-3), 1),
+                    "l2": f"inputs {2 * kv.numel() * 2 >> 20} MiB, larger than the L2"})
+        del kv, sc, bias, y
         torch.cuda.empty_cache()
     return out
 
@@ -382,7 +427,9 @@ def bench_only(args, world):
     ltb.build()
     dev = torch.device("cuda", torch.cuda.current_device())
     S, L, w = workloads.make(args.only)
-    nbytes = workloads.read_bytes(L, w.rows, w.row_stride)
+    if args.dtype == "bf16":
+        S = workloads.to_bf16(S)
+    nbytes = workloads.read_bytes(L, w.rows, w.row_stride) * S.element_size() // 4
     L2 = l2_bytes()
     ncopies = workloads.l2_rotation_copies(nbytes, L2) if nbytes < 4 * L2 else 1
     base = S.to(dev)
@@ -394,7 +441,7 @@ def bench_only(args, world):
     listed = args.only.startswith("c6")
     cand = workloads.listed_blocks(args.only).to(dev) if listed else None
     if listed:
-        nbytes = 4 * cand.numel() * w.block + 4 * cand.numel()
+        nbytes = S.element_size() * cand.numel() * w.block + 4 * cand.numel()
 
     def step(i):
         c = copies[i % ncopies]
@@ -409,7 +456,7 @@ def bench_only(args, world):
 
     total_ms = timed_steps(step, args.steps, args.warmup, world)
     kern = total_ms / args.steps
-    return {"workload": args.only, "steps": args.steps, "step_us": round(kern * 1000, 3),
+    return {"workload": args.only, "dtype": args.dtype, "steps": args.steps, "step_us": round(kern * 1000, 3),
             "read_bytes": nbytes,
             "hbm_gbs": round(nbytes / (kern * 1e-3) / 1e9, 1), "copies": ncopies,
             "plan": ({"kernel": "listed", "cluster": 1, "threads": 512, "grid": w.rows} if listed else
@@ -431,6 +478,8 @@ def bench_trace(args):
     ltb.build()
     dev = torch.device("cuda", torch.cuda.current_device())
     S, L, w = workloads.make(args.trace)
+    if args.dtype == "bf16":
+        S = workloads.to_bf16(S)
     base = S.to(dev)
     # as many rotating copies as the timed bench uses, so the traced launch reads cold rows
     nbytes = workloads.read_bytes(L, w.rows, w.row_stride)

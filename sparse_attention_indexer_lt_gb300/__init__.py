@@ -19,7 +19,7 @@ from pathlib import Path
 
 import torch
 
-__all__ = ["topk", "topk_blocked", "topk_candidates", "plan", "DTYPE_F32", "DTYPE_BF16", "load", "library_path", "LtError", "NUM_COUNTERS",
+__all__ = ["topk", "topk_blocked", "topk_candidates", "compress", "compress_decode", "plan", "DTYPE_F32", "DTYPE_BF16", "load", "library_path", "LtError", "NUM_COUNTERS",
            "status_string", "version", "PlanInfo", "KERNEL_AUTO", "KERNEL_RESIDENT", "KERNEL_STREAM"]
 
 _LIB_PATH = Path(__file__).resolve().parent / "liblt_topk.so"
@@ -83,6 +83,10 @@ def load() -> ctypes.CDLL:
     lib.lt_topk_plan.restype = ctypes.c_int
     lib.lt_status_string.argtypes = [ctypes.c_int]
     lib.lt_status_string.restype = ctypes.c_char_p
+    lib.lt_compress.argtypes = [vp, vp, vp, vp, i32, i64, i32, i32, vp, i32, vp]
+    lib.lt_compress.restype = ctypes.c_int
+    lib.lt_compress_decode.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, i32, vp, i32, vp]
+    lib.lt_compress_decode.restype = ctypes.c_int
     lib.lt_test_inject.argtypes = [i32, i32]
     lib.lt_test_inject.restype = ctypes.c_int
     lib.lt_version.argtypes = []
@@ -235,6 +239,69 @@ def topk_candidates(scores: torch.Tensor, cand_blocks: torch.Tensor, lengths: to
     if st != 0:
         raise LtError("lt_topk_candidates", st)
     return out_idx, out_val
+
+
+def _check_kv(name, t, device, dtype=None):
+    if not isinstance(t, torch.Tensor) or not t.is_cuda or t.device != device or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous CUDA tensor on {device}")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}")
+
+
+def compress(kv: torch.Tensor, score: torch.Tensor, bias: torch.Tensor, ratio: int,
+             lengths: torch.Tensor | None = None, *, out: torch.Tensor | None = None,
+             stream: torch.cuda.Stream | None = None) -> torch.Tensor:
+    """Fused KV compressor: kv, score [rows, T, d] (float32 or bfloat16, the same), bias float32
+    [ratio, d]; returns out [rows, T // ratio, d] in kv's dtype, with block g of row r written when
+    g < L_r // ratio (see include/lt_compress.h)."""
+    lib = load()
+    if kv.dim() != 3 or score.shape != kv.shape or score.dtype != kv.dtype or kv.dtype not in _DTYPES:
+        raise ValueError("kv and score must be [rows, T, d] tensors of one dtype (float32 or bfloat16)")
+    dev = kv.device
+    _check_kv("kv", kv, dev)
+    _check_kv("score", score, dev)
+    _check_kv("bias", bias, dev, torch.float32)
+    rows, T, d = kv.shape
+    if tuple(bias.shape) != (ratio, d):
+        raise ValueError(f"bias must be [{ratio}, {d}]")
+    lengths = _check_lengths(lengths, rows, dev)
+    out = _out(out, (rows, T // ratio, d), kv.dtype, dev, "out")
+    with torch.cuda.device(dev):
+        s = (stream or torch.cuda.current_stream(dev)).cuda_stream
+        st = lib.lt_compress(_ptr(kv), _ptr(score), _ptr(bias), _ptr(lengths), rows, max(T, 1), d, int(ratio),
+                             _ptr(out), _DTYPES[kv.dtype], ctypes.c_void_p(s))
+    if st != 0:
+        raise LtError("lt_compress", st)
+    return out
+
+
+def compress_decode(kv_new: torch.Tensor, score_new: torch.Tensor, bias: torch.Tensor, ring_kv: torch.Tensor,
+                    ring_score: torch.Tensor, pos: torch.Tensor, out: torch.Tensor, *,
+                    stream: torch.cuda.Stream | None = None) -> torch.Tensor:
+    """One decode step of the compressor: kv_new, score_new [seqs, d]; rings [seqs, ratio, d]
+    (updated in place); pos int32 [seqs]; out [seqs, d] written for the sequences whose new token
+    completes a block."""
+    lib = load()
+    dev = kv_new.device
+    seqs, d = kv_new.shape
+    ratio = ring_kv.shape[1]
+    for n, t in (("kv_new", kv_new), ("score_new", score_new), ("ring_kv", ring_kv), ("ring_score", ring_score),
+                 ("out", out)):
+        _check_kv(n, t, dev, kv_new.dtype)
+    _check_kv("bias", bias, dev, torch.float32)
+    _check_kv("pos", pos, dev, torch.int32)
+    if (kv_new.dtype not in _DTYPES or score_new.shape != (seqs, d) or ring_kv.shape != (seqs, ratio, d)
+            or ring_score.shape != (seqs, ratio, d) or tuple(bias.shape) != (ratio, d) or out.shape != (seqs, d)
+            or pos.numel() != seqs):
+        raise ValueError("compress_decode: inconsistent shapes or dtype")
+    with torch.cuda.device(dev):
+        s = (stream or torch.cuda.current_stream(dev)).cuda_stream
+        st = lib.lt_compress_decode(_ptr(kv_new), _ptr(score_new), _ptr(bias), _ptr(ring_kv), _ptr(ring_score),
+                                    _ptr(pos), seqs, d, int(ratio), _ptr(out), _DTYPES[kv_new.dtype],
+                                    ctypes.c_void_p(s))
+    if st != 0:
+        raise LtError("lt_compress_decode", st)
+    return out
 
 
 def plan(rows: int, row_stride: int, k: int, *, blocked: bool = False, block: int = 8,

@@ -17,7 +17,7 @@ INCLUDE = PKG.parent / "include"
 BUILD = PKG / "_build"
 LIB = PKG / "liblt_topk.so"
 SOURCES = ["lt_api.cu", "lt_topk_kernels.cu", "lt_stream_kernels.cu", "lt_blocked_256_f32.cu",
-           "lt_blocked_256_bf16.cu", "lt_blocked_512_f32.cu", "lt_blocked_512_bf16.cu", "lt_listed_kernels.cu"]
+           "lt_blocked_256_bf16.cu", "lt_blocked_512_f32.cu", "lt_blocked_512_bf16.cu", "lt_listed_kernels.cu", "lt_compress.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", f"-I{INCLUDE}"]
 

@@ -7,7 +7,8 @@ import re
 import pytest
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-HEADER = os.path.join(ROOT, "include", "lt_topk.h")
+HEADERS = [os.path.join(ROOT, "include", h) for h in sorted(os.listdir(os.path.join(ROOT, "include")))
+           if h.endswith(".h")]
 
 
 @pytest.fixture(scope="module")
@@ -18,15 +19,17 @@ def lib():
 
 
 def declared_functions():
-    text = open(HEADER).read()
+    text = "".join(open(h).read() for h in HEADERS)
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(lt_[a-z_]+)\s*\(", text)))
+    return sorted(set(re.findall(r"\b(lt_[a-z0-9_]+)\s*\(", text)))
 
 
 def test_header_declares_the_entry_points():
     names = declared_functions()
     for n in ["lt_topk", "lt_topk_blocked", "lt_topk_ex", "lt_topk_blocked_ex", "lt_topk_candidates",
-              "lt_topk_candidates_ex", "lt_topk_plan", "lt_status_string", "lt_version"]:
+              "lt_topk_candidates_ex", "lt_topk_plan", "lt_status_string", "lt_version", "lt_topk_bf16",
+              "lt_topk_blocked_bf16", "lt_topk_candidates_bf16", "lt_test_inject", "lt_compress",
+              "lt_compress_decode"]:
         assert n in names
 
 
@@ -100,6 +103,26 @@ def test_candidates_invalid_arguments(lib):
     assert call(fake, 1, 262148, 4, fake, 4, 4, fake) == 2      # more than 65536 blocks per row
     assert call(fake, 1, 64, 8, fake, 4, 4, fake, dtype=3) == 1  # unknown score type
     assert call(None, 0, 64, 8, None, 4, 4, None) == 0          # rows == 0: nothing to do
+
+
+def test_compress_invalid_arguments(lib):
+    fake = P(0x1000)
+    f = lib.lt_compress
+    assert f(fake, fake, fake, None, 1, 16, 8, 0, fake, 0, None) == 1      # ratio < 1
+    assert f(fake, fake, fake, None, 1, 16, 0, 4, fake, 0, None) == 1      # dim < 1
+    assert f(fake, fake, fake, None, 1, 0, 8, 4, fake, 0, None) == 1       # no tokens
+    assert f(fake, fake, fake, None, -1, 16, 8, 4, fake, 0, None) == 1     # rows < 0
+    assert f(fake, fake, fake, None, 1, 16, 8, 4, fake, 7, None) == 1      # unknown dtype
+    assert f(None, fake, fake, None, 1, 16, 8, 4, fake, 0, None) == 1      # kv NULL
+    assert f(fake, fake, None, None, 1, 16, 8, 4, fake, 0, None) == 1      # bias NULL
+    assert f(fake, fake, fake, None, 1, 1 << 14, 8, 8192, fake, 0, None) == 2  # ratio > LT_MAX_RATIO
+    assert f(None, None, None, None, 0, 16, 8, 4, None, 0, None) == 0      # rows == 0
+    assert f(fake, fake, fake, None, 1, 3, 8, 4, fake, 0, None) == 0       # no complete block: no-op
+    d = lib.lt_compress_decode
+    assert d(fake, fake, fake, fake, fake, fake, 1, 8, 0, fake, 0, None) == 1   # ratio < 1
+    assert d(fake, fake, fake, fake, None, fake, 1, 8, 4, fake, 0, None) == 1   # ring NULL
+    assert d(fake, fake, fake, fake, fake, fake, 1, 8, 4, fake, 2, None) == 1   # dtype
+    assert d(None, None, None, None, None, None, 0, 8, 4, None, 0, None) == 0   # no sequences
 
 
 def test_plan_rejects_bad_arguments(lib):

@@ -167,6 +167,39 @@ def random_bf16_special(rows: int, stride: int, seed: int):
     return pool[pick].to(torch.int16).view(torch.bfloat16).contiguous()
 
 
+@dataclass(frozen=True)
+class CompressWorkload:
+    name: str
+    rows: int
+    tokens: int
+    dim: int
+    ratio: int
+    description: str = ""
+
+
+# The compressor at a million-token context, prefill: one row of 2^20 tokens,
+# 512 channels, bf16 KV and scores; 4:1 (CSA) and 128:1 (HCA).
+COMPRESS_CONFIGS = {
+    "compress_csa_1m": CompressWorkload("compress_csa_1m", 1, 1 << 20, 512, 4,
+                                        "1 row x 2^20 tokens x 512 channels, bf16, 4:1"),
+    "compress_hca_1m": CompressWorkload("compress_hca_1m", 1, 1 << 20, 512, 128,
+                                        "1 row x 2^20 tokens x 512 channels, bf16, 128:1"),
+}
+
+
+def compress_inputs(rows: int, tokens: int, dim: int, ratio: int, seed: int, device="cpu",
+                    dtype=torch.float32, score_scale: float = 1.0):
+    """Seeded compressor inputs: kv ~ N(0,1), score ~ N(0, score_scale^2) (gate
+    logits), bias ~ N(0, 0.25) float32 [ratio, dim]. On a CUDA device the
+    device's own generator draws them (large inputs); the values depend only
+    on the seed and the device type."""
+    g = torch.Generator(device).manual_seed(seed)
+    kv = torch.randn(rows, tokens, dim, generator=g, device=device)
+    sc = torch.randn(rows, tokens, dim, generator=g, device=device) * score_scale
+    bias = torch.randn(ratio, dim, generator=g, device=device) * 0.5
+    return kv.to(dtype).contiguous(), sc.to(dtype).contiguous(), bias.float().contiguous()
+
+
 def read_bytes(lengths, rows: int, stride: int) -> int:
     """Bytes a read-once pass touches: 4 bytes per valid position."""
     if lengths is None:
