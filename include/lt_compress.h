@@ -53,9 +53,11 @@ extern "C" {
  *               (tokens g*ratio .. g*ratio + ratio - 1) is written when
  *               g < L_r / ratio (integer division); the other entries are not
  *               touched (an incomplete trailing block waits for its tokens)
- * bf16 outputs are the fp32 result rounded to nearest even. Rows whose
- * pointers are 16-byte (fp32) or 8-byte (bf16) aligned with dim % 4 == 0
- * take vector loads; any other layout takes scalar loads.
+ * bf16 outputs are the fp32 result rounded to nearest even. When kv, score
+ * and bias are 16-byte aligned, dim * size is a multiple of 16 bytes and out
+ * allows vector stores, bulk copies stream the rows through shared memory
+ * (the fast path); other layouts take register loads (vector loads when
+ * aligned with dim % 4 == 0, else scalar). Same results up to rounding.
  */
 lt_status lt_compress(const void* kv, const void* score, const float* bias, const int32_t* lengths,
                       int32_t rows, int64_t row_tokens, int32_t dim, int32_t ratio, void* out,
@@ -74,8 +76,10 @@ lt_status lt_compress(const void* kv, const void* score, const float* bias, cons
  *   out                   [seqs][dim] of `dtype`: written for the sequences
  *                         whose new token completes a block
  *                         (pos[s] mod ratio == ratio - 1), from the ring's
- *                         ratio tokens, exactly as lt_compress does; the other
- *                         rows are not touched
+ *                         ratio tokens: the same function as lt_compress (the
+ *                         same bits whenever a block fits one stage of
+ *                         lt_compress's ring, ratio * dim * size <= 16 KB);
+ *                         the other rows are not touched
  * A sequence with a negative pos is skipped.
  */
 lt_status lt_compress_decode(const void* kv_new, const void* score_new, const float* bias,

@@ -27,8 +27,16 @@
 #include <mutex>
 
 #include "../../include/lt_compress.h"
+#include "lt_async.cuh"
 
 namespace {
+
+using lt::bulk_g2s;
+using lt::kWaitPolls;
+using lt::mbar_arrive_tx;
+using lt::mbar_fence_init;
+using lt::mbar_init;
+using lt::ring_wait;
 
 constexpr int kThreads = 256;
 constexpr int kChunk = 4;  // tokens loaded together
@@ -239,6 +247,267 @@ __global__ void __launch_bounds__(kThreads) compress_kernel(CParams p) {
   }
 }
 
+// ---- prefill through a ring of shared-memory stages (bulk copies)
+//
+// The register kernel above keeps only a few loads in flight per thread; on
+// GB300 that leaves HBM idle. Here thread 0 of each (persistent) CTA copies
+// whole token ranges of kv and score -- contiguous in memory -- into a ring of
+// shared-memory stages with cp.async.bulk, each stage completing on its own
+// mbarrier, so the bytes in flight no longer depend on registers. A unit of
+// work is either several whole blocks (small ratios: a block fits a stage;
+// the bias then lives in shared memory for the whole launch) or one block
+// streamed over several stages (large ratios: each stage also carries the
+// bias rows of its tokens, and the two threads of a channel group take
+// alternate tokens and merge their partial sums with a shuffle at the end).
+// Producer and consumers walk the same unit sequence (units of this CTA that
+// hold at least one complete block), so no descriptors are exchanged. Waits
+// are bounded (a copy that never lands leaves that unit's output undefined
+// rather than hanging).
+
+constexpr uint32_t kRingInSmall = 16384;  // kv bytes per stage when a block fits (score the same)
+constexpr uint32_t kRingInLarge = 8192;   // kv bytes per stage of a streamed block (+ bias rows)
+constexpr uint32_t kRingBudget = 112 * 1024;  // two CTAs per SM
+constexpr int kRingMaxStages = 4;
+
+struct RParams {
+  const void* kv;
+  const void* score;
+  const float* bias;
+  const int32_t* lengths;
+  void* out;
+  int64_t row_tokens;
+  int64_t nblk;           // blocks per row
+  int64_t units_per_row;
+  int64_t units;          // rows * units_per_row
+  int32_t dim, ratio, groups;
+  int32_t st;             // tokens per full stage
+  int32_t bpu;            // blocks per unit (1 when a block is streamed)
+  int32_t subtiles;       // stages per unit
+  int32_t tpg;            // streamed blocks: threads per channel group (power of two)
+  int32_t stages;
+  uint32_t in_bytes;      // kv bytes of a full stage
+  uint32_t stage_bytes;   // kv + score (+ bias rows)
+  uint32_t bias_off, ring_off;  // shared-memory offsets
+};
+
+// Unit u of the launch: row r, first block g0 and its complete blocks nb
+// (0 when the unit lies past the row's last complete block).
+__device__ __forceinline__ int unit_blocks(const RParams& p, int64_t u, int64_t* r, int64_t* g0) {
+  *r = u / p.units_per_row;
+  const int64_t ui = u - *r * p.units_per_row;
+  int64_t L = p.row_tokens;
+  if (p.lengths) {
+    L = (int64_t)__ldg(p.lengths + *r);
+    L = L < 0 ? 0 : (L > p.row_tokens ? p.row_tokens : L);
+  }
+  *g0 = ui * p.bpu;
+  const int64_t n = L / p.ratio - *g0;
+  return n <= 0 ? 0 : (n < p.bpu ? (int)n : p.bpu);
+}
+
+// The next unit at or after u (stepping by the grid) that has work.
+__device__ __forceinline__ bool next_unit(const RParams& p, int64_t& u, int64_t* r, int64_t* g0, int* nb) {
+  for (; u < p.units; u += gridDim.x) {
+    *nb = unit_blocks(p, u, r, g0);
+    if (*nb > 0) return true;
+  }
+  return false;
+}
+
+// Tokens of stage `sub` of a unit: first token (row-relative) and count.
+__device__ __forceinline__ void stage_tokens(const RParams& p, int64_t g0, int nb, int sub, int64_t* t0, int* n) {
+  if (p.subtiles == 1) {
+    *t0 = g0 * p.ratio;
+    *n = nb * p.ratio;
+  } else {
+    *t0 = g0 * p.ratio + (int64_t)sub * p.st;
+    const int left = p.ratio - sub * p.st;
+    *n = left < p.st ? left : p.st;
+  }
+}
+
+template <int V>
+__device__ __forceinline__ void lds_v(const float* p, float (&x)[V]) {
+  const float4 q = *reinterpret_cast<const float4*>(p);
+  x[0] = q.x; x[1] = q.y; x[2] = q.z; x[3] = q.w;
+}
+template <int V>
+__device__ __forceinline__ void lds_v(const uint16_t* p, float (&x)[V]) {
+  const uint2 q = *reinterpret_cast<const uint2*>(p);
+  x[0] = widen(q.x & 0xffffu); x[1] = __uint_as_float(q.x & 0xffff0000u);
+  x[2] = widen(q.y & 0xffffu); x[3] = __uint_as_float(q.y & 0xffff0000u);
+}
+
+template <class S>
+__global__ void __launch_bounds__(kThreads, 2) compress_ring_kernel(RParams p) {
+  constexpr int V = 4;
+  extern __shared__ __align__(128) unsigned char smem[];
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem);
+  float* bias_s = reinterpret_cast<float*>(smem + p.bias_off);
+  unsigned char* ring = smem + p.ring_off;
+  const int tid = threadIdx.x;
+  const uint32_t ns = (uint32_t)p.stages;
+  if (tid == 0) {
+    for (uint32_t i = 0; i < ns; ++i) mbar_init(&bars[i], 1);
+    mbar_fence_init();
+  }
+  grid_dependents_launch();
+  grid_dependency_wait();  // inputs and lengths may come from the previous kernel
+  if (p.subtiles == 1) {
+    for (int i = tid; i < p.ratio * p.dim; i += kThreads) bias_s[i] = __ldg(p.bias + i);
+  }
+  __syncthreads();
+
+  const S* kv = static_cast<const S*>(p.kv);
+  const S* sc = static_cast<const S*>(p.score);
+  // ---- producer state (thread 0)
+  int64_t pu = blockIdx.x, pr = 0, pg0 = 0;
+  int pnb = 0, psub = 0;
+  bool pvalid = false;
+  uint32_t pseq = 0;
+  auto produce = [&](uint32_t limit) {
+    while (pvalid && (int32_t)(limit - pseq) > 0) {
+      int64_t t0;
+      int n;
+      stage_tokens(p, pg0, pnb, psub, &t0, &n);
+      unsigned char* dst = ring + (size_t)(pseq % ns) * p.stage_bytes;
+      const uint32_t bytes = (uint32_t)n * (uint32_t)p.dim * (uint32_t)sizeof(S);
+      const uint32_t bbytes = p.subtiles > 1 ? (uint32_t)n * (uint32_t)p.dim * 4u : 0u;
+      uint64_t* bar = &bars[pseq % ns];
+      mbar_arrive_tx(bar, 2u * bytes + bbytes);
+      const int64_t e0 = (pr * p.row_tokens + t0) * p.dim;
+      bulk_g2s(dst, kv + e0, bytes, bar);
+      bulk_g2s(dst + p.in_bytes, sc + e0, bytes, bar);
+      if (bbytes) bulk_g2s(dst + 2u * p.in_bytes, p.bias + (int64_t)psub * p.st * p.dim, bbytes, bar);
+      ++pseq;
+      if (++psub == p.subtiles) {
+        psub = 0;
+        pu += gridDim.x;
+        pvalid = next_unit(p, pu, &pr, &pg0, &pnb);
+      }
+    }
+  };
+  if (tid == 0) {
+    pvalid = next_unit(p, pu, &pr, &pg0, &pnb);
+    produce(ns);
+  }
+
+  // ---- consumers (every thread)
+  S* out = static_cast<S*>(p.out);
+  int64_t cu = blockIdx.x, cr = 0, cg0 = 0;
+  int cnb = 0;
+  bool cvalid = next_unit(p, cu, &cr, &cg0, &cnb);
+  uint32_t seq = 0;
+  bool late = false;
+  // streamed blocks: this thread's channel group and token phase
+  const int cgB = tid / p.tpg, hB = tid - cgB * p.tpg;
+  Acc<V> acc;
+  while (cvalid) {
+    for (int sub = 0; sub < p.subtiles; ++sub) {
+      if (!ring_wait(bars, ns, seq, kWaitPolls)) late = true;
+      const unsigned char* stg = ring + (size_t)(seq % ns) * p.stage_bytes;
+      const S* xs = reinterpret_cast<const S*>(stg);
+      const S* zs = reinterpret_cast<const S*>(stg + p.in_bytes);
+      int64_t t0;
+      int n;
+      stage_tokens(p, cg0, cnb, sub, &t0, &n);
+      if (p.subtiles == 1) {
+        // whole blocks: one item per (block, channel group)
+        const int items = cnb * p.groups;
+        for (int it = tid; it < items; it += kThreads) {
+          const int q = it / p.groups;
+          const int cg = it - q * p.groups;
+          const int64_t o = (int64_t)q * p.ratio * p.dim + (int64_t)cg * V;
+          Acc<V> a;
+          a.init();
+          for (int j = 0; j < p.ratio; j += kChunk) {
+            const int m = p.ratio - j < kChunk ? p.ratio - j : kChunk;
+            float x[kChunk][V], v[kChunk][V];
+#pragma unroll
+            for (int u = 0; u < kChunk; ++u) {
+              if (u < m) {
+                float z[V], bb[V];
+                const int64_t ot = o + (int64_t)(j + u) * p.dim;
+                lds_v<V>(xs + ot, x[u]);
+                lds_v<V>(zs + ot, z);
+                lds_v<V>(bias_s + (int64_t)(j + u) * p.dim + (int64_t)cg * V, bb);
+#pragma unroll
+                for (int c = 0; c < V; ++c) v[u][c] = z[c] + bb[c];
+              }
+            }
+            a.add<kChunk>(v, x, m);
+          }
+          float y[V];
+          a.result(y);
+          store_v<V>(out + (cr * p.nblk + cg0 + q) * p.dim + (int64_t)cg * V, y);
+        }
+      } else {
+        // one block over several stages: tokens t with t mod tpg == hB
+        if (sub == 0) acc.init();
+        const float* bs = reinterpret_cast<const float*>(stg + 2u * p.in_bytes);
+        if (cgB < p.groups) {
+          const int base = sub * p.st;
+          int i = (hB - base) % p.tpg;
+          if (i < 0) i += p.tpg;
+          const int64_t oc = (int64_t)cgB * V;
+          while (i < n) {
+            float x[kChunk][V], v[kChunk][V];
+            int m = 0;
+#pragma unroll
+            for (int u = 0; u < kChunk; ++u) {
+              const int ii = i + u * p.tpg;
+              if (ii < n) {
+                float z[V], bb[V];
+                lds_v<V>(xs + (int64_t)ii * p.dim + oc, x[u]);
+                lds_v<V>(zs + (int64_t)ii * p.dim + oc, z);
+                lds_v<V>(bs + (int64_t)ii * p.dim + oc, bb);
+#pragma unroll
+                for (int c = 0; c < V; ++c) v[u][c] = z[c] + bb[c];
+                m = u + 1;
+              }
+            }
+            acc.add<kChunk>(v, x, m);
+            i += kChunk * p.tpg;
+          }
+        }
+        if (sub == p.subtiles - 1) {
+          // merge the tpg partial sums of each channel group (adjacent lanes)
+          for (int off = 1; off < p.tpg; off <<= 1) {
+#pragma unroll
+            for (int c = 0; c < V; ++c) {
+              const float m2 = __shfl_xor_sync(0xffffffffu, acc.m[c], off);
+              const float s2 = __shfl_xor_sync(0xffffffffu, acc.s[c], off);
+              const float a2 = __shfl_xor_sync(0xffffffffu, acc.a[c], off);
+              const float mn = fmaxf(acc.m[c], m2);
+              const float r1 = acc.m[c] == mn ? 1.0f : __expf(acc.m[c] - mn);
+              const float r2 = m2 == mn ? 1.0f : __expf(m2 - mn);
+              acc.s[c] = acc.s[c] * r1 + s2 * r2;
+              acc.a[c] = acc.a[c] * r1 + a2 * r2;
+              acc.m[c] = mn;
+            }
+          }
+          if (cgB < p.groups && hB == 0) {
+            float y[V];
+            acc.result(y);
+            store_v<V>(out + (cr * p.nblk + cg0) * p.dim + (int64_t)cgB * V, y);
+          }
+        }
+      }
+      __syncthreads();  // every thread is done with this stage
+      if (tid == 0) produce(seq + 1 + ns);
+      ++seq;
+    }
+    cu += gridDim.x;
+    cvalid = next_unit(p, cu, &cr, &cg0, &cnb);
+  }
+  // A wait that gave up may leave its copy in flight: give the last stages a
+  // bounded chance to land before the CTA's shared memory goes away.
+  if (__syncthreads_or(late ? 1 : 0) && tid == 0) {
+    for (uint32_t i = 0; i < ns && i < seq; ++i) (void)ring_wait(bars, ns, seq - 1u - i, kWaitPolls);
+  }
+  __syncthreads();
+}
+
 // ---- decode: one new token per sequence, state in the two rings
 
 template <class S, int V>
@@ -298,8 +567,58 @@ std::mutex g_mu;
 int g_ctas_per_sm[kMaxDevices][4];  // prefill kernels: resident CTAs per SM (0: not asked yet)
 int g_sms[kMaxDevices];
 
+int g_ring_smem_set[kMaxDevices][2];  // dynamic shared memory granted to the ring kernels
+int g_ring_ctas[kMaxDevices][2];      // their resident CTAs per SM
+
 template <class S, int V>
 const void* prefill_ptr() { return reinterpret_cast<const void*>(&compress_kernel<S, V>); }
+
+bool aligned_to(const void* p, unsigned a);
+
+// Ring geometry for this launch; false when the layout does not allow bulk
+// copies (then the register kernel runs).
+bool ring_plan(const void* kv, const void* score, const float* bias, const void* out, int64_t row_tokens,
+               int32_t dim, int32_t ratio, bool bf16, RParams* r, uint32_t* smem) {
+  const uint32_t es = bf16 ? 2u : 4u;
+  const uint64_t row_bytes = (uint64_t)dim * es;
+  if (dim % 4 != 0 || row_bytes % 16 != 0) return false;
+  if (!aligned_to(kv, 16) || !aligned_to(score, 16) || !aligned_to(bias, 16) || !aligned_to(out, bf16 ? 8 : 16))
+    return false;
+  const uint32_t groups = (uint32_t)dim / 4;
+  uint32_t bias_bytes = 0;
+  if ((uint64_t)ratio * row_bytes <= kRingInSmall) {
+    r->bpu = (int32_t)(kRingInSmall / ((uint64_t)ratio * row_bytes));
+    r->st = r->bpu * ratio;
+    r->subtiles = 1;
+    r->tpg = 1;
+    r->in_bytes = (uint32_t)(r->st * row_bytes);
+    r->stage_bytes = 2u * r->in_bytes;
+    bias_bytes = (uint32_t)ratio * (uint32_t)dim * 4u;
+  } else {
+    if (groups > (uint32_t)kThreads || row_bytes > kRingInLarge) return false;
+    r->bpu = 1;
+    r->st = (int32_t)(kRingInLarge / row_bytes);
+    r->subtiles = (ratio + r->st - 1) / r->st;
+    int tpg = 1;
+    while (tpg * 2 <= 32 && (uint32_t)(tpg * 2) * groups <= (uint32_t)kThreads) tpg *= 2;
+    r->tpg = tpg;
+    r->in_bytes = (uint32_t)(r->st * row_bytes);
+    r->stage_bytes = 2u * r->in_bytes + (uint32_t)r->st * (uint32_t)dim * 4u;
+  }
+  r->bias_off = 128;
+  r->ring_off = (r->bias_off + bias_bytes + 127u) / 128u * 128u;
+  if (r->ring_off + 2u * r->stage_bytes > kRingBudget) return false;
+  r->stages = (int32_t)((kRingBudget - r->ring_off) / r->stage_bytes);
+  if (r->stages > kRingMaxStages) r->stages = kRingMaxStages;
+  *smem = r->ring_off + (uint32_t)r->stages * r->stage_bytes;
+  r->groups = (int32_t)groups;
+  r->dim = dim;
+  r->ratio = ratio;
+  r->row_tokens = row_tokens;
+  r->nblk = row_tokens / ratio;
+  r->units_per_row = (r->nblk + r->bpu - 1) / r->bpu;
+  return true;
+}
 
 lt_status launch(const void* func, dim3 grid, dim3 block, void* args, void* stream) {
   cudaLaunchConfig_t cfg = {};
@@ -317,6 +636,17 @@ lt_status launch(const void* func, dim3 grid, dim3 block, void* args, void* stre
 
 bool aligned_to(const void* p, unsigned a) { return p == nullptr || reinterpret_cast<uintptr_t>(p) % a == 0; }
 
+lt_status device_sms(int* dev, int* sms) {
+  if (cudaGetDevice(dev) != cudaSuccess) return LT_ERR_CUDA;
+  if (*dev < 0 || *dev >= kMaxDevices) return LT_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (g_sms[*dev] == 0 &&
+      cudaDeviceGetAttribute(&g_sms[*dev], cudaDevAttrMultiProcessorCount, *dev) != cudaSuccess)
+    return LT_ERR_CUDA;
+  *sms = g_sms[*dev];
+  return LT_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -332,6 +662,54 @@ lt_status lt_compress(const void* kv, const void* score, const float* bias, cons
   const int64_t nblk = row_tokens / ratio;
   if (rows == 0 || nblk == 0) return LT_OK;
   const bool bf16 = dtype == LT_DTYPE_BF16;
+  {
+    // the ring kernel whenever the layout allows bulk copies
+    RParams rp = {};
+    uint32_t smem = 0;
+    if (ring_plan(kv, score, bias, out, row_tokens, dim, ratio, bf16, &rp, &smem)) {
+      rp.kv = kv;
+      rp.score = score;
+      rp.bias = bias;
+      rp.lengths = lengths;
+      rp.out = out;
+      rp.units = (int64_t)rows * rp.units_per_row;
+      const void* func = bf16 ? reinterpret_cast<const void*>(&compress_ring_kernel<uint16_t>)
+                              : reinterpret_cast<const void*>(&compress_ring_kernel<float>);
+      int dev = 0, sms = 0;
+      lt_status st = device_sms(&dev, &sms);
+      if (st != LT_OK) return st;
+      int per_sm = 0;
+      {
+        std::lock_guard<std::mutex> lk(g_mu);
+        const int k = bf16 ? 1 : 0;
+        if ((int)smem > g_ring_smem_set[dev][k]) {
+          if (cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+            return LT_ERR_CUDA;
+          g_ring_smem_set[dev][k] = (int)smem;
+          g_ring_ctas[dev][k] = 0;
+        }
+        if (g_ring_ctas[dev][k] == 0 &&
+            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&g_ring_ctas[dev][k], func, kThreads, smem) != cudaSuccess)
+          return LT_ERR_CUDA;
+        per_sm = g_ring_ctas[dev][k];
+      }
+      if (per_sm < 1) return LT_ERR_UNSUPPORTED;
+      int64_t ctas = (int64_t)sms * per_sm;
+      if (ctas > rp.units) ctas = rp.units;
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3((unsigned)ctas);
+      cfg.blockDim = dim3(kThreads);
+      cfg.dynamicSmemBytes = smem;
+      cfg.stream = static_cast<cudaStream_t>(stream);
+      cudaLaunchAttribute attr;
+      attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+      attr.val.programmaticStreamSerializationAllowed = 1;
+      cfg.attrs = &attr;
+      cfg.numAttrs = 1;
+      void* a[] = {&rp};
+      return cudaLaunchKernelExC(&cfg, func, a) == cudaSuccess ? LT_OK : LT_ERR_CUDA;
+    }
+  }
   const unsigned va = bf16 ? 8u : 16u;
   const bool vec = dim % 4 == 0 && aligned_to(kv, va) && aligned_to(score, va) && aligned_to(out, va) &&
                    aligned_to(bias, 16u);

@@ -31,13 +31,12 @@
 
 #pragma once
 
+#include "lt_async.cuh"
 #include "lt_kernels.cuh"
 
 namespace lt {
 
 constexpr int kTilePos = 1024;            // positions per bulk copy (4 KB)
-constexpr uint32_t kWaitPolls = 1u << 16;  // try_wait calls before a wait gives up
-constexpr uint32_t kSuspendNs = 20000;     // longest suspension per try_wait call
 
 template <int T, int UC>
 struct SGeo {
@@ -62,43 +61,6 @@ __host__ __device__ inline StreamLayout make_stream_layout(bool clustered, uint3
   s.ring = align_up_u32(s.bars + 8 * stages, 128);
   s.total = s.ring + stages * chunk_bytes;
   return s;
-}
-
-// ------------------------------------------------------------------ mbarrier + bulk copy
-
-__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" :: "r"(smem_addr(bar)), "r"(count) : "memory");
-}
-__device__ __forceinline__ void mbar_fence_init() {
-  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-}
-// One arrival that also announces `bytes` of asynchronous transfers.
-__device__ __forceinline__ void mbar_arrive_tx(uint64_t* bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" :: "r"(smem_addr(bar)), "r"(bytes)
-               : "memory");
-}
-// Waits for the phase with the given parity to complete; the thread may be
-// suspended for up to kSuspendNs per call instead of spinning.
-__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n selp.u32 %0, 1, 0, p;\n}"
-      : "=r"(ok) : "r"(smem_addr(bar)), "r"(parity), "r"(kSuspendNs) : "memory");
-  return ok != 0;
-}
-// Global -> this CTA's shared memory; completes `bytes` on the mbarrier.
-// Both addresses 16-byte aligned, bytes a multiple of 16.
-__device__ __forceinline__ void bulk_g2s(float* dst, const float* src, uint32_t bytes, uint64_t* bar) {
-  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
-               :: "r"(smem_addr(dst)), "l"(src), "r"(bytes), "r"(smem_addr(bar)) : "memory");
-}
-
-__device__ __forceinline__ bool ring_wait(uint64_t* bars, uint32_t ns, uint32_t seq, uint32_t polls) {
-  uint64_t* bar = bars + (seq % ns);
-  const uint32_t parity = (seq / ns) & 1u;
-  for (uint32_t i = 0; i < polls; ++i)
-    if (mbar_try_wait(bar, parity)) return true;
-  return false;
 }
 
 // ------------------------------------------------------------------ geometry

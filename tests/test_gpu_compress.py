@@ -59,7 +59,7 @@ def check(y_gpu, kv, sc, bias, ratio, lengths, what):
             bad = err > tol
             assert not bad.any(), (f"{what}: row {r}: {int(bad.sum())} entries off; worst err "
                                    f"{float(err.max()):.3g} at tol {float(tol.flat[int(np.argmax(err - tol))]):.3g}")
-        assert np.all(got[r, n:nb] == 12345.0), f"{what}: row {r}: blocks past L/ratio were written"
+        assert np.all(got[r, n:nb] == 12288.0), f"{what}: row {r}: blocks past L/ratio were written"
 
 
 @pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
@@ -73,7 +73,7 @@ def test_small_shapes_ragged(dtype, ratio, dim):
     kv, sc, bias = workloads.compress_inputs(rows, T, dim, ratio, seed=ratio * 1000 + dim, dtype=dtype,
                                              score_scale=2.0)
     L = np.array([T, 0, min(ratio - 1, T), T - 5], np.int32)
-    out = torch.full((rows, T // ratio, dim), 12345.0, dtype=dtype, device="cuda")
+    out = torch.full((rows, T // ratio, dim), 12288.0, dtype=dtype, device="cuda")
     lt.compress(kv.cuda(), sc.cuda(), bias.cuda(), ratio, torch.as_tensor(L).cuda(), out=out)
     torch.cuda.synchronize()
     check(out, kv, sc, bias, ratio, L, f"{dtype} ratio={ratio} dim={dim}")
@@ -89,7 +89,7 @@ def test_unaligned_views_take_scalar_loads(dtype):
     s2 = big_sc[1:].view(2, 65, 16)
     k2.copy_(kv.cuda())
     s2.copy_(sc.cuda())
-    out = torch.full((2, 16, 16), 12345.0, dtype=dtype, device="cuda")
+    out = torch.full((2, 16, 16), 12288.0, dtype=dtype, device="cuda")
     lt.compress(k2, s2, bias.cuda(), 4, out=out)
     torch.cuda.synchronize()
     check(out, kv, sc, bias, 4, None, f"{dtype} unaligned")
@@ -99,7 +99,7 @@ def test_large_scores_stay_finite():
     """Scores far from zero: the running maximum keeps every exponent <= 0."""
     import sparse_attention_indexer_lt_gb300 as lt
     kv, sc, bias = workloads.compress_inputs(1, 512, 8, 128, seed=6, score_scale=40.0)
-    out = torch.full((1, 4, 8), 12345.0, device="cuda")
+    out = torch.full((1, 4, 8), 12288.0, device="cuda")
     lt.compress(kv.cuda(), sc.cuda(), bias.cuda(), 128, out=out)
     torch.cuda.synchronize()
     assert torch.isfinite(out).all()
@@ -122,7 +122,7 @@ def test_full_size_workloads_sampled(name):
     tok = (pick[:, None] * w.ratio + torch.arange(w.ratio)[None]).reshape(-1).cuda()
     kv_s = kv[0, tok].view(1, -1, w.dim)
     sc_s = sc[0, tok].view(1, -1, w.dim)
-    sub = torch.full((1, pick.numel(), w.dim), 12345.0, dtype=torch.bfloat16)
+    sub = torch.full((1, pick.numel(), w.dim), 12288.0, dtype=torch.bfloat16)
     sub[0] = out[0, pick.cuda()].cpu()
     check(sub, kv_s, sc_s, bias, w.ratio, None, name)
     del kv, sc, out
@@ -143,19 +143,19 @@ def test_decode_steps_match_prefill(dtype, ratio):
     ref = lt.compress(kvd, scd, bd, ratio)
     ring_k = torch.zeros(seqs, ratio, d, dtype=dtype, device="cuda")
     ring_s = torch.zeros_like(ring_k)
-    out = torch.full((seqs, d), 12345.0, dtype=dtype, device="cuda")
+    out = torch.full((seqs, d), 12288.0, dtype=dtype, device="cuda")
     for t in range(T):
         pos = torch.full((seqs,), t, dtype=torch.int32)
         pos[4] = -1
-        out.fill_(12345.0)
+        out.fill_(12288.0)
         lt.compress_decode(kvd[:, t].contiguous(), scd[:, t].contiguous(), bd, ring_k, ring_s, pos.cuda(), out)
         torch.cuda.synchronize()
         o = out.cpu()
         if t % ratio == ratio - 1:
             assert torch.equal(o[:4], ref[:4, t // ratio].cpu()), f"step {t}"
         else:
-            assert bool((o[:4] == 12345.0).all())
-        assert bool((o[4] == 12345.0).all())
+            assert bool((o[:4] == 12288.0).all())
+        assert bool((o[4] == 12288.0).all())
     # and the oracle's ring form agrees on the last completed block
     check_blocks = ref[:, (T // ratio) - 1].cpu()
     want = oc.compress(_num(kv[:, :(T // ratio) * ratio]), _num(sc[:, :(T // ratio) * ratio]), _num(bias), ratio)
