@@ -56,7 +56,7 @@ def parse():
                     help="print per-phase kernel timestamps (thread 0 of each CTA) for one workload")
     ap.add_argument("--force-threads", type=int, default=0)
     ap.add_argument("--force-cluster", type=int, default=0)
-    ap.add_argument("--only", choices=sorted(workloads.CONFIGS), default=None,
+    ap.add_argument("--only", choices=sorted(workloads.CONFIGS) + sorted(workloads.COMPRESS_CONFIGS), default=None,
                     help="time one workload's kernel alone (for profilers); prints a short JSON line")
     ap.add_argument("--dtype", choices=["f32", "bf16"], default="f32", help="score type in --only / --trace runs")
     ap.add_argument("--kernel", choices=["auto", "resident", "stream"], default="auto",
@@ -380,6 +380,8 @@ def bench_batched(lt, dev, args, world, peak, L2):
         if listed:
             out[-1]["bytes"] = "listed blocks' scores + the list"
             out[-1]["plan"] = {"kernel": "listed", "cluster": 1, "threads": 512, "grid": w.rows}
+        if not args.no_cpu and world == 1 and dtype == "f32":
+            out[-1]["cpu_baseline"] = cpu_batched(name, S, L, w, None if cand is None else cand.cpu())
         del copies, base
         torch.cuda.empty_cache()
     return out
@@ -426,6 +428,16 @@ def bench_only(args, world):
     from sparse_attention_indexer_lt_gb300 import build as ltb
     ltb.build()
     dev = torch.device("cuda", torch.cuda.current_device())
+    if args.only in workloads.COMPRESS_CONFIGS:
+        w = workloads.COMPRESS_CONFIGS[args.only]
+        kv, sc, bias = workloads.compress_inputs(w.rows, w.tokens, w.dim, w.ratio, seed=0, device=dev,
+                                                 dtype=torch.bfloat16)
+        y = torch.empty(w.rows, w.tokens // w.ratio, w.dim, dtype=torch.bfloat16, device=dev)
+        total_ms = timed_steps(lambda i: lt.compress(kv, sc, bias, w.ratio, out=y), args.steps, args.warmup, world)
+        kern = total_ms / args.steps
+        nbytes = compress_bytes(w, 2)
+        return {"workload": args.only, "dtype": "bf16", "steps": args.steps, "step_us": round(kern * 1000, 3),
+                "bytes": nbytes, "hbm_gbs": round(nbytes / (kern * 1e-3) / 1e9, 1)}
     S, L, w = workloads.make(args.only)
     if args.dtype == "bf16":
         S = workloads.to_bf16(S)
@@ -599,6 +611,33 @@ def cpu_baseline(S, w, seconds):
     dt = time.perf_counter() - t0
     return {"value": round(dt / (n * w.rows) * 1e6, 1), "unit": "µs/row", "cores": 1, "kind": "oracle",
             "sample": f"{n} repetitions of the {HEADLINE} row (std::stable_sort, one thread: batch size 1)",
+            "cpu": cpu_name()}
+
+
+def cpu_batched(name, S, L, w, cand, seconds: float = 2.0):
+    """The oracle on a batched workload, rows spread over every host core this
+    process may use; whole batches repeated for about `seconds`."""
+    import oracle
+    oracle.build()
+    nt = oracle.default_threads()
+    x = S.numpy()
+    ln = None if L is None else L.numpy()
+
+    def run():
+        if w.blocked:
+            oracle.topk_blocked(x, ln, w.block, w.k_blocks, w.k, nthreads=nt)
+        elif cand is not None:
+            oracle.topk_candidates(x, ln, cand.numpy(), w.block, w.k, nthreads=nt)
+        else:
+            oracle.topk(x, ln, w.k, nthreads=nt)
+
+    n, t0 = 0, time.perf_counter()
+    while n == 0 or time.perf_counter() - t0 < seconds:
+        run()
+        n += 1
+    dt = time.perf_counter() - t0
+    return {"value": round(dt / (n * w.rows) * 1e6, 2), "unit": "µs/row", "cores": nt, "kind": "oracle",
+            "sample": f"{n} whole batches of {name} ({w.rows} rows), rows spread over {nt} threads",
             "cpu": cpu_name()}
 
 

@@ -183,9 +183,13 @@ lt_status lt_topk_candidates_bf16(const uint16_t* scores, const int32_t* lengths
  *                  large batches) or 512 (one CTA per SM, for few rows)
  *   force_exact    nonzero skips the sampled-threshold fast path and runs the
  *                  streaming radix select on every row (same results)
- *   force_kernel   LT_KERNEL_AUTO lets the planner choose (currently always
- *                  register-resident); LT_KERNEL_STREAM on unaligned or
- *                  bf16 rows returns LT_ERR_UNSUPPORTED
+ *   force_kernel   LT_KERNEL_AUTO lets the planner choose (register-resident;
+ *                  in batches of more rows than one wave of single-CTA rows,
+ *                  a row may start from the threshold implied by the output
+ *                  of the row one wave earlier -- see below); forcing
+ *                  LT_KERNEL_RESIDENT makes every row estimate its own;
+ *                  LT_KERNEL_STREAM on unaligned or bf16 rows returns
+ *                  LT_ERR_UNSUPPORTED
  *   counters       NULL, or device int32[LT_NUM_COUNTERS] that the kernel
  *                  increments atomically, once per row: [0] rows finished on
  *                  the fast path, [1] rows finished on the streaming radix
@@ -193,7 +197,10 @@ lt_status lt_topk_candidates_bf16(const uint16_t* scores, const int32_t* lengths
  *                  whose sampled threshold kept fewer than k candidates,
  *                  [4] rows of the streamed kernel during which a wait for a
  *                  bulk copy gave up after its poll limit (a hardware fault,
- *                  or lt_test_inject; that row's output is undefined).
+ *                  or lt_test_inject; that row's output is undefined),
+ *                  [5] rows that started from an earlier row's threshold and
+ *                  found it did not fit (they then count in [1] and [2] or
+ *                  [3]), [6] rows that finished from such a threshold.
  *                  For the two-level call, each row counts once per stage
  *                  (with k_blocks >= k and out_blocks NULL, only stage B
  *                  runs: once); for the listed-candidate call, once (the
@@ -211,12 +218,24 @@ lt_status lt_topk_candidates_bf16(const uint16_t* scores, const int32_t* lengths
  *                  of the stream: give traced launches their own buffer or
  *                  synchronise between them.
  *
+ * Thresholds from earlier rows. In a batch of single-CTA rows (256 threads,
+ * several register rounds, more rows than two waves of resident CTAs) row r
+ * reads the (k/2)-th and k-th values that row r - G wrote to out_val (G =
+ * the CTAs of two waves; that row has almost surely finished) and, instead of
+ * estimating, keeps the positions at or above k-th - ((k/2)-th - k-th):
+ * about 1.5k to 1.7k of a row like that one. The filter's count check accepts it
+ * only if at least k and at most the candidate area pass; otherwise the row
+ * takes the exact streaming select, as any miss does. Row r - G may still be being written (the
+ * values are then stale, e.g. from a previous call into the same buffer):
+ * a wrong guess costs time, never correctness. Needs out_val; results are
+ * identical with or without it.
+ *
  * Every launch uses programmatic dependent launch: a kernel may start while
  * the previous kernel of the stream finishes, and waits for it (device-side)
  * before it reads lengths or scores or writes outputs, counters or trace
  * slots other than the entry timestamp.
  */
-#define LT_NUM_COUNTERS 5
+#define LT_NUM_COUNTERS 7
 lt_status lt_topk_ex(const void* scores, int32_t dtype, const int32_t* lengths, int32_t rows,
                      int64_t row_stride, int32_t k, int32_t* out_idx, float* out_val,
                      int32_t force_cluster, int32_t force_threads, int32_t force_exact,

@@ -24,7 +24,7 @@ __all__ = ["topk", "topk_blocked", "topk_candidates", "compress", "compress_deco
 
 _LIB_PATH = Path(__file__).resolve().parent / "liblt_topk.so"
 _lib = None
-NUM_COUNTERS = 5
+NUM_COUNTERS = 7
 DTYPE_F32, DTYPE_BF16 = 0, 1
 KERNEL_AUTO, KERNEL_RESIDENT, KERNEL_STREAM = 0, 1, 2
 _KERNEL_NAMES = {KERNEL_RESIDENT: "resident", KERNEL_STREAM: "stream"}

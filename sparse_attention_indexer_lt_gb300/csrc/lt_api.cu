@@ -34,7 +34,7 @@ constexpr int kMaxDevices = 64;
 constexpr int kWideThreads = 512;
 constexpr int kNarrowThreads = 256;
 constexpr int64_t kWideRound = 512 * 8 * 4;  // positions per CTA per round (wide)
-constexpr int kTypeSlots = 18;                // kernel variants per score type
+constexpr int kTypeSlots = 19;                // kernel variants per score type
 constexpr int kSlots = 2 * kTypeSlots;        // fp32, then bf16
 // the streamed kernel's launch bounds: CTAs per SM for 256 / 512 threads
 constexpr int stream_ctas_per_sm(int threads) { return threads == 256 ? 3 : 2; }
@@ -74,8 +74,9 @@ int block_index(int block) {
   }
 }
 
-// slots 14..17: the listed-candidate kernel, by block size; bf16 kernels
-// follow the fp32 ones (kTypeSlots later)
+// slots 14..17: the listed-candidate kernel, by block size; 18: the top-k
+// whose rows start from an earlier row's output; bf16 kernels follow the
+// fp32 ones (kTypeSlots later)
 int kernel_slot(bool blocked, int block, int threads, bool stream = false, bool one_round = false,
                 bool bf16 = false) {
   const int wide = threads == kWideThreads ? 1 : 0;
@@ -104,6 +105,7 @@ struct Plan {
   uint32_t wstage = 0;     // candidate staging bytes (threads * 16 * kStageF4)
   uint32_t sel_cap = 0;
   uint32_t smem = 0;
+  int hint_rows = 0;       // > 0: rows start from the output of the row this many earlier
   const void* func = nullptr;
 };
 
@@ -283,6 +285,20 @@ lt_status make_plan(int32_t rows, int64_t row_stride, int32_t k, bool blocked, i
   }
   if ((int64_t)rows * plan->cluster > 0x7fffffffLL) return LT_ERR_UNSUPPORTED;
   plan->grid = rows * plan->cluster;
+  // Batches of single-CTA rows of several rounds: a row may start from the
+  // output of the row two waves of CTAs earlier, which has almost surely
+  // finished (the automatic plan only).
+  if (!blocked && force_kernel == LT_KERNEL_AUTO && threads == kNarrowThreads && plan->cluster == 1 &&
+      !plan->one_round) {
+    const int two_waves = 2 * di->sms * lt::kNarrowCtasPerSm;
+    if (rows > two_waves) {
+      const void* f = lt::topk_hint_kernel_ptr(bf16);
+      st = prepare_kernel(dev, (bf16 ? kTypeSlots : 0) + 18, f, plan->smem, 1);
+      if (st != LT_OK) return st;
+      plan->func = f;
+      plan->hint_rows = two_waves;
+    }
+  }
   *dev_out = dev;
   return LT_OK;
 }
@@ -386,6 +402,7 @@ lt_status launch(const Plan& plan, const lt::Params& prm, void* stream) {
   p.sel_cap = (int32_t)plan.sel_cap;
   p.clustered = plan.cluster > 1 ? 1 : 0;
   p.ring_stages = (int32_t)plan.stages;
+  p.hint_rows = plan.hint_rows;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)plan.grid);
   cfg.blockDim = dim3((unsigned)plan.threads);

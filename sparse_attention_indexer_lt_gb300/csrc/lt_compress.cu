@@ -132,7 +132,23 @@ __device__ __forceinline__ void copy_v(S* dst, const S* src) {
   for (int c = 0; c < V; ++c) dst[c] = src[c];
 }
 
-// ---- the online softmax-weighted sum
+// ---- the online softmax-weighted sum, in base 2
+//
+// exp(v) = 2^(v log2 e): the biased score is formed directly in base-2 units,
+// l = score * log2(e) + bias * log2(e) (one fused multiply-add), and every
+// weight is one hardware base-2 exponential (ex2.approx, relative error of a
+// few ulps; results below 2^-126 flush to zero, a weight far below what can
+// change the sum). The running maximum is kept in the same units.
+
+constexpr float kLog2e = 1.4426950408889634f;
+
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+// the biased score of one channel in base-2 units
+__device__ __forceinline__ float logit2(float z, float b) { return fmaf(z, kLog2e, b * kLog2e); }
 
 template <int V>
 struct Acc {
@@ -145,7 +161,7 @@ struct Acc {
       a[c] = 0.0f;
     }
   }
-  // add the n <= U tokens of a chunk: biased scores v, values x
+  // add the n <= U tokens of a chunk: base-2 biased scores v, values x
   template <int U>
   __device__ __forceinline__ void add(const float (&v)[U][V], const float (&x)[U][V], int n) {
 #pragma unroll
@@ -155,12 +171,12 @@ struct Acc {
       for (int u = 1; u < U; ++u)
         if (u < n) cm = fmaxf(cm, v[u][c]);
       const float mn = fmaxf(m[c], cm);
-      const float r = __expf(m[c] - mn);  // 0 for the first chunk (m = -inf)
+      const float r = ex2(m[c] - mn);  // 0 for the first chunk (m = -inf)
       float sc = s[c] * r, ac = a[c] * r;
 #pragma unroll
       for (int u = 0; u < U; ++u) {
         if (u < n) {
-          const float e = __expf(v[u][c] - mn);
+          const float e = ex2(v[u][c] - mn);
           sc += e;
           ac = fmaf(e, x[u][c], ac);
         }
@@ -228,7 +244,7 @@ __global__ void __launch_bounds__(kThreads) compress_kernel(CParams p) {
               load_v<V>(zk + o, z);
               load_v<V>(bk + (int64_t)(j + u) * p.dim, bb);
 #pragma unroll
-              for (int c = 0; c < V; ++c) v[u][c] = z[c] + bb[c];  // add
+              for (int c = 0; c < V; ++c) v[u][c] = logit2(z[c], bb[c]);  // add
             }
           }
           acc.add<kChunk>(v, x, n);  // softmax terms and weighted sum
@@ -338,7 +354,73 @@ __device__ __forceinline__ void lds_v(const uint16_t* p, float (&x)[V]) {
   x[2] = widen(q.y & 0xffffu); x[3] = __uint_as_float(q.y & 0xffff0000u);
 }
 
+// Whole blocks of one stage, any ratio: one item per (block, channel group).
+// Offsets inside a stage fit 32 bits.
 template <class S>
+__device__ __forceinline__ void ring_blocks(const RParams& p, const S* xs, const S* zs, const float* bias_s, int nb,
+                                            S* ob, int tid) {
+  constexpr int V = 4;
+  const int items = nb * p.groups;
+  for (int it = tid; it < items; it += kThreads) {
+    const int q = it / p.groups;
+    const int cg = it - q * p.groups;
+    const uint32_t o = (uint32_t)(q * p.ratio) * (uint32_t)p.dim + (uint32_t)cg * V;
+    Acc<V> a;
+    a.init();
+    for (int j = 0; j < p.ratio; j += kChunk) {
+      const int m = p.ratio - j < kChunk ? p.ratio - j : kChunk;
+      float x[kChunk][V], v[kChunk][V];
+#pragma unroll
+      for (int u = 0; u < kChunk; ++u) {
+        if (u < m) {
+          float z[V], bb[V];
+          const uint32_t tok = (uint32_t)(j + u) * (uint32_t)p.dim;
+          lds_v<V>(xs + o + tok, x[u]);
+          lds_v<V>(zs + o + tok, z);
+          lds_v<V>(bias_s + tok + (uint32_t)cg * V, bb);
+#pragma unroll
+          for (int c = 0; c < V; ++c) v[u][c] = logit2(z[c], bb[c]);
+        }
+      }
+      a.add<kChunk>(v, x, m);
+    }
+    float y[V];
+    a.result(y);
+    store_v<V>(ob + (uint32_t)q * (uint32_t)p.dim + (uint32_t)cg * V, y);
+  }
+}
+
+// The same for a compile-time ratio R <= kChunk when the threads divide into
+// whole channel-group columns: each thread keeps one channel group for the
+// whole launch, with its R bias rows (already in base-2 units) in registers.
+template <class S, int R>
+__device__ __forceinline__ void ring_blocks_fixed(const S* xs, const S* zs, const float (&b2)[R > 0 ? R : 1][4],
+                                                  int nb, int dim, int cg, int q0, int qs, S* ob) {
+  constexpr int V = 4;
+  static_assert(R >= 1 && R <= kChunk, "one chunk per block");
+  for (int q = q0; q < nb; q += qs) {
+    const uint32_t o = (uint32_t)(q * R) * (uint32_t)dim + (uint32_t)cg * V;
+    float x[kChunk][V], v[kChunk][V];
+#pragma unroll
+    for (int u = 0; u < R; ++u) {
+      float z[V];
+      lds_v<V>(xs + o + (uint32_t)u * (uint32_t)dim, x[u]);
+      lds_v<V>(zs + o + (uint32_t)u * (uint32_t)dim, z);
+#pragma unroll
+      for (int c = 0; c < V; ++c) v[u][c] = fmaf(z[c], kLog2e, b2[u][c]);
+    }
+    Acc<V> a;
+    a.init();
+    a.add<kChunk>(v, x, R);
+    float y[V];
+    a.result(y);
+    store_v<V>(ob + (uint32_t)q * (uint32_t)dim + (uint32_t)cg * V, y);
+  }
+}
+
+// R: a compile-time ratio for the fixed-column path (blocks of R <= kChunk
+// tokens, threads a multiple of the channel groups), else 0.
+template <class S, int R>
 __global__ void __launch_bounds__(kThreads, 2) compress_ring_kernel(RParams p) {
   constexpr int V = 4;
   extern __shared__ __align__(128) unsigned char smem[];
@@ -357,6 +439,16 @@ __global__ void __launch_bounds__(kThreads, 2) compress_ring_kernel(RParams p) {
     for (int i = tid; i < p.ratio * p.dim; i += kThreads) bias_s[i] = __ldg(p.bias + i);
   }
   __syncthreads();
+  // fixed-column path: this thread's channel group, first block, block step
+  // and bias rows (base-2 units)
+  const int fixed_cg = R > 0 ? tid % p.groups : 0;
+  const int fixed_q0 = R > 0 ? tid / p.groups : 0;
+  const int fixed_qs = R > 0 ? kThreads / p.groups : 1;
+  float bfix[R > 0 ? R : 1][4];
+#pragma unroll
+  for (int u = 0; u < (R > 0 ? R : 1); ++u)
+#pragma unroll
+    for (int c = 0; c < 4; ++c) bfix[u][c] = R > 0 ? bias_s[u * p.dim + fixed_cg * 4 + c] * kLog2e : 0.0f;
 
   const S* kv = static_cast<const S*>(p.kv);
   const S* sc = static_cast<const S*>(p.score);
@@ -412,34 +504,11 @@ __global__ void __launch_bounds__(kThreads, 2) compress_ring_kernel(RParams p) {
       int n;
       stage_tokens(p, cg0, cnb, sub, &t0, &n);
       if (p.subtiles == 1) {
-        // whole blocks: one item per (block, channel group)
-        const int items = cnb * p.groups;
-        for (int it = tid; it < items; it += kThreads) {
-          const int q = it / p.groups;
-          const int cg = it - q * p.groups;
-          const int64_t o = (int64_t)q * p.ratio * p.dim + (int64_t)cg * V;
-          Acc<V> a;
-          a.init();
-          for (int j = 0; j < p.ratio; j += kChunk) {
-            const int m = p.ratio - j < kChunk ? p.ratio - j : kChunk;
-            float x[kChunk][V], v[kChunk][V];
-#pragma unroll
-            for (int u = 0; u < kChunk; ++u) {
-              if (u < m) {
-                float z[V], bb[V];
-                const int64_t ot = o + (int64_t)(j + u) * p.dim;
-                lds_v<V>(xs + ot, x[u]);
-                lds_v<V>(zs + ot, z);
-                lds_v<V>(bias_s + (int64_t)(j + u) * p.dim + (int64_t)cg * V, bb);
-#pragma unroll
-                for (int c = 0; c < V; ++c) v[u][c] = z[c] + bb[c];
-              }
-            }
-            a.add<kChunk>(v, x, m);
-          }
-          float y[V];
-          a.result(y);
-          store_v<V>(out + (cr * p.nblk + cg0 + q) * p.dim + (int64_t)cg * V, y);
+        S* ob = out + (cr * p.nblk + cg0) * p.dim;
+        if constexpr (R > 0) {
+          ring_blocks_fixed<S, R>(xs, zs, bfix, cnb, p.dim, fixed_cg, fixed_q0, fixed_qs, ob);
+        } else {
+          ring_blocks<S>(p, xs, zs, bias_s, cnb, ob, tid);
         }
       } else {
         // one block over several stages: tokens t with t mod tpg == hB
@@ -449,7 +518,7 @@ __global__ void __launch_bounds__(kThreads, 2) compress_ring_kernel(RParams p) {
           const int base = sub * p.st;
           int i = (hB - base) % p.tpg;
           if (i < 0) i += p.tpg;
-          const int64_t oc = (int64_t)cgB * V;
+          const uint32_t oc = (uint32_t)cgB * V;
           while (i < n) {
             float x[kChunk][V], v[kChunk][V];
             int m = 0;
@@ -458,11 +527,12 @@ __global__ void __launch_bounds__(kThreads, 2) compress_ring_kernel(RParams p) {
               const int ii = i + u * p.tpg;
               if (ii < n) {
                 float z[V], bb[V];
-                lds_v<V>(xs + (int64_t)ii * p.dim + oc, x[u]);
-                lds_v<V>(zs + (int64_t)ii * p.dim + oc, z);
-                lds_v<V>(bs + (int64_t)ii * p.dim + oc, bb);
+                const uint32_t ot = (uint32_t)ii * (uint32_t)p.dim + oc;
+                lds_v<V>(xs + ot, x[u]);
+                lds_v<V>(zs + ot, z);
+                lds_v<V>(bs + ot, bb);
 #pragma unroll
-                for (int c = 0; c < V; ++c) v[u][c] = z[c] + bb[c];
+                for (int c = 0; c < V; ++c) v[u][c] = logit2(z[c], bb[c]);
                 m = u + 1;
               }
             }
@@ -479,8 +549,8 @@ __global__ void __launch_bounds__(kThreads, 2) compress_ring_kernel(RParams p) {
               const float s2 = __shfl_xor_sync(0xffffffffu, acc.s[c], off);
               const float a2 = __shfl_xor_sync(0xffffffffu, acc.a[c], off);
               const float mn = fmaxf(acc.m[c], m2);
-              const float r1 = acc.m[c] == mn ? 1.0f : __expf(acc.m[c] - mn);
-              const float r2 = m2 == mn ? 1.0f : __expf(m2 - mn);
+              const float r1 = acc.m[c] == mn ? 1.0f : ex2(acc.m[c] - mn);
+              const float r2 = m2 == mn ? 1.0f : ex2(m2 - mn);
               acc.s[c] = acc.s[c] * r1 + s2 * r2;
               acc.a[c] = acc.a[c] * r1 + a2 * r2;
               acc.m[c] = mn;
@@ -550,7 +620,7 @@ __global__ void __launch_bounds__(kThreads) compress_decode_kernel(DParams p) {
         }
         load_v<V>(p.bias + (int64_t)(j + u) * p.dim + c0, bb);
 #pragma unroll
-        for (int c = 0; c < V; ++c) v[u][c] = z[c] + bb[c];
+        for (int c = 0; c < V; ++c) v[u][c] = logit2(z[c], bb[c]);
       }
     }
     acc.add<kChunk>(v, x, n);
@@ -567,8 +637,8 @@ std::mutex g_mu;
 int g_ctas_per_sm[kMaxDevices][4];  // prefill kernels: resident CTAs per SM (0: not asked yet)
 int g_sms[kMaxDevices];
 
-int g_ring_smem_set[kMaxDevices][2];  // dynamic shared memory granted to the ring kernels
-int g_ring_ctas[kMaxDevices][2];      // their resident CTAs per SM
+int g_ring_smem_set[kMaxDevices][4];  // dynamic shared memory granted to the ring kernels
+int g_ring_ctas[kMaxDevices][4];      // their resident CTAs per SM
 
 template <class S, int V>
 const void* prefill_ptr() { return reinterpret_cast<const void*>(&compress_kernel<S, V>); }
@@ -673,15 +743,21 @@ lt_status lt_compress(const void* kv, const void* score, const float* bias, cons
       rp.lengths = lengths;
       rp.out = out;
       rp.units = (int64_t)rows * rp.units_per_row;
-      const void* func = bf16 ? reinterpret_cast<const void*>(&compress_ring_kernel<uint16_t>)
-                              : reinterpret_cast<const void*>(&compress_ring_kernel<float>);
+      // CSA's 4:1 blocks take the fixed-column variant
+      const bool fixed = rp.subtiles == 1 && ratio == 4 && kThreads % rp.groups == 0;
+      const void* func =
+          bf16 ? (fixed ? reinterpret_cast<const void*>(&compress_ring_kernel<uint16_t, 4>)
+                        : reinterpret_cast<const void*>(&compress_ring_kernel<uint16_t, 0>))
+               : (fixed ? reinterpret_cast<const void*>(&compress_ring_kernel<float, 4>)
+                        : reinterpret_cast<const void*>(&compress_ring_kernel<float, 0>));
+      const int kslot = (bf16 ? 2 : 0) + (fixed ? 1 : 0);
       int dev = 0, sms = 0;
       lt_status st = device_sms(&dev, &sms);
       if (st != LT_OK) return st;
       int per_sm = 0;
       {
         std::lock_guard<std::mutex> lk(g_mu);
-        const int k = bf16 ? 1 : 0;
+        const int k = kslot;
         if ((int)smem > g_ring_smem_set[dev][k]) {
           if (cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
             return LT_ERR_CUDA;

@@ -72,7 +72,11 @@ constexpr unsigned kFull = 0xffffffffu;
 // predicts more candidates than this fraction of the candidate capacity.
 constexpr float kLevel2Frac = 0.75f;
 
-enum Counter { kCntFast = 0, kCntExact = 1, kCntOverflow = 2, kCntShort = 3, kCntTimeout = 4 };
+enum Counter {
+  kCntFast = 0, kCntExact = 1, kCntOverflow = 2, kCntShort = 3, kCntTimeout = 4,
+  kCntHintMiss = 5,  // rows whose threshold from an earlier row did not fit (then redone)
+  kCntHintUsed = 6   // rows that finished from a threshold taken from an earlier row
+};
 
 // Phase timestamps (nanoseconds of the global timer) written by thread 0 of
 // each CTA when a trace buffer is given: slot i of CTA b at trace[b * 16 + i].
@@ -113,6 +117,8 @@ struct Params {
   const int32_t* cand_blocks;  // listed-candidate call: n_cand block ids per row
   int32_t n_cand;
   int32_t external;     // two-level kernel: stage B over the listed blocks only
+  int32_t hint_rows;    // > 0: row r starts from the output of row r - hint_rows (batches
+                        // of single-CTA rows; see Hint in lt_kernels.cuh), else 0
   int32_t stall_polls;  // streamed kernel, tests only (0 normally): the final chunk of
                         // each CTA is never issued and every wait gives up after
                         // this many polls (see lt_test_inject)
@@ -240,13 +246,47 @@ __device__ __forceinline__ float load1(const float* p) { return __ldg(p); }
 __device__ __forceinline__ float load1(const uint16_t* p) { return bf16_widen(__ldg(p)); }
 
 // Four consecutive scores; p 16-byte (fp32) or 8-byte (bf16) aligned.
+// A load that may race with another CTA's store to the same word (the value
+// is only used as a guess that is checked afterwards).
+__device__ __forceinline__ float ld_relaxed(const float* p) {
+  float v;
+  asm volatile("ld.relaxed.gpu.global.f32 %0, [%1];" : "=f"(v) : "l"(p) : "memory");
+  return v;
+}
+
 __device__ __forceinline__ float4 ldg4(const float* p) {
   return __ldg(reinterpret_cast<const float4*>(p));
 }
-__device__ __forceinline__ float4 ldg4(const uint16_t* p) {
-  const uint2 q = __ldg(reinterpret_cast<const uint2*>(p));  // element 2i in the low half of word i
+// four bf16 scores as loaded (element 2i in the low half of word i), widened
+__device__ __forceinline__ float4 widen4(uint2 q) {
   return make_float4(__uint_as_float(q.x << 16), __uint_as_float(q.x & 0xffff0000u),
                      __uint_as_float(q.y << 16), __uint_as_float(q.y & 0xffff0000u));
+}
+__device__ __forceinline__ float4 ldg4(const uint16_t* p) {
+  return widen4(__ldg(reinterpret_cast<const uint2*>(p)));
+}
+
+// A whole round of vector loads: slot s of this thread starts at
+// p0 + s * sstride and holds VS consecutive float4. Every load is issued
+// before any of its results is used; bf16 rows keep the raw 64-bit words
+// until the last load has left and widen them afterwards (widening each word
+// as it arrives would make the next load wait for it).
+template <int U, int VS>
+__device__ __forceinline__ void gather_round(const float* p0, int64_t sstride, float4 (&v)[U]) {
+#pragma unroll
+  for (int s = 0; s < U / VS; ++s)
+#pragma unroll
+    for (int j = 0; j < VS; ++j) v[s * VS + j] = ldg4(p0 + s * sstride + 4 * j);
+}
+template <int U, int VS>
+__device__ __forceinline__ void gather_round(const uint16_t* p0, int64_t sstride, float4 (&v)[U]) {
+  uint2 raw[U];
+#pragma unroll
+  for (int s = 0; s < U / VS; ++s)
+#pragma unroll
+    for (int j = 0; j < VS; ++j) raw[s * VS + j] = __ldg(reinterpret_cast<const uint2*>(p0 + s * sstride + 4 * j));
+#pragma unroll
+  for (int i = 0; i < U; ++i) v[i] = widen4(raw[i]);
 }
 
 // ------------------------------------------------------------------ keys

@@ -103,6 +103,13 @@ template <int T, int U, int W, class S>
 __device__ __forceinline__ void load_round(const RowT<S>& R, bool vec, int r, float4 (&v)[U],
                                            int (&n)[Geo<T, U, W>::kSlots]) {
   using G = Geo<T, U, W>;
+  // every slot full (the last one is the furthest): one straight run of loads
+  if (vec && slot_pos<T, U, W>(R, r, G::kSlots - 1) + W <= R.end) {
+    gather_round<U, G::kVS>(R.rowp + slot_pos<T, U, W>(R, r, 0), (int64_t)R.rounds * G::kTile, v);
+#pragma unroll
+    for (int s = 0; s < G::kSlots; ++s) n[s] = W;
+    return;
+  }
 #pragma unroll
   for (int s = 0; s < G::kSlots; ++s) {
     const int64_t pos = slot_pos<T, U, W>(R, r, s);
@@ -134,13 +141,9 @@ template <int T, int U, class S>
 __device__ __forceinline__ void load_round4(const RowT<S>& R, bool vec, int r, float4 (&v)[U], int (&n)[U]) {
   using G = Geo<T, U, 4>;
   if (vec && round_whole<T, U>(R, r)) {
-    const S* pr = R.rowp + R.tbase + (int64_t)r * G::kTile;
-    const int64_t sstride = (int64_t)R.rounds * G::kTile;
+    gather_round<U, 1>(R.rowp + R.tbase + (int64_t)r * G::kTile, (int64_t)R.rounds * G::kTile, v);
 #pragma unroll
-    for (int s = 0; s < U; ++s) {
-      v[s] = ldg4(pr + s * sstride);
-      n[s] = 4;
-    }
+    for (int s = 0; s < U; ++s) n[s] = 4;
   } else {
     load_round<T, U, 4>(R, vec, r, v, n);
   }
@@ -1096,6 +1099,21 @@ __device__ __noinline__ uint64_t exact_select(RowT<S> R, const Params p, uint32_
   return tval;
 }
 
+// Positions in round 0 of this CTA's slice, from the geometry: round 0 holds
+// tiles 0, rounds, 2 rounds, ... (each clipped to the slice).
+template <int T, int U, int W>
+__device__ __forceinline__ uint32_t round0_size(const RowCore& R) {
+  using G = Geo<T, U, W>;
+  const int64_t len = R.end - R.begin;
+  uint32_t n = 0;
+#pragma unroll
+  for (int s = 0; s < G::kSlots; ++s) {
+    const int64_t t0 = (int64_t)R.rounds * s * G::kTile;
+    if (t0 < len) n += (uint32_t)(len - t0 < G::kTile ? len - t0 : G::kTile);
+  }
+  return n;
+}
+
 // Threshold estimate of a single-CTA, 256-thread row from its spread round-0
 // sample (not the whole slice) with two 8-bit digit levels of 256 bins, one
 // bin per thread: the top 8 bits of the raw key, then the next 8 bits of the
@@ -1123,14 +1141,7 @@ __device__ __forceinline__ uint32_t estimate_small(RowCore& R, const float4 (&v)
 #pragma unroll
     for (int e = 0; e < 4; ++e) atomicAdd(&h1[raw_key(__float_as_uint(lane4(v[s], e))) >> 24], 1u);
   }
-  // sample size from the geometry: round 0 holds tiles 0, rounds, 2 rounds, ...
-  const int64_t len = R.end - R.begin;
-  uint32_t nsamp = 0;
-#pragma unroll
-  for (int s = 0; s < G::kSlots; ++s) {
-    const int64_t t0 = (int64_t)R.rounds * s * G::kTile;
-    if (t0 < len) nsamp += (uint32_t)(len - t0 < G::kTile ? len - t0 : G::kTile);
-  }
+  const uint32_t nsamp = round0_size<T, U, W>(R);
   const uint32_t r = sample_target(K, nsamp, items, false);
   __syncthreads();
   const uint32_t v1[1] = {h1[threadIdx.x]};
@@ -1159,12 +1170,34 @@ __device__ __forceinline__ uint32_t estimate_small(RowCore& R, const float4 (&v)
 // path (the candidates are every item >= a lower bound of the K-th item).
 // cur/nxt hold rounds 0 and 1 on entry when `loaded`; *regs_intact tells
 // whether they still do on return.
+//
+// hint (nullable): the (k/2)-th and k-th values an earlier row of the batch
+// wrote to its output. Rows of one batch score the same context, so from
+// those two values, lo = k-th and hi = (k/2)-th, the filter can start at
+// lo - (hi - lo): about 1.5k to 1.7k of a similar row pass it (the scores
+// thin out above the k-th), far more than the row-to-row spread of the k-th
+// value needs. The estimate is then skipped.
+// Whether it fits is decided by the filter's own count check: fewer than K
+// kept or more than the candidate area holds, and the row takes the exact
+// path, as any miss does. Values that give no usable threshold (NaN,
+// infinities, hi < lo) leave the estimate in place.
+struct Hint {
+  float hi, lo;
+};
+
+__device__ __forceinline__ uint32_t hint_threshold(const Hint& h) {
+  const float t = h.lo - (h.hi - h.lo);
+  // finite and ordered (NaN fails every compare); key 0 would mean "keep all"
+  if (!(h.hi > h.lo) || !(fabsf(h.hi) <= 3.4e38f) || !(fabsf(t) <= 3.4e38f)) return 0u;
+  return key_of(t);
+}
+
 template <int T, int U, int W, bool kBlocks, class Keep, class S>
 __device__ __forceinline__ bool select_stage(RowT<S>& R, const Params& p, float4 (&cur)[U],
                                              int (&nc)[Geo<T, U, W>::kSlots], float4 (&nxt)[U],
                                              int (&nn)[Geo<T, U, W>::kSlots], bool loaded, uint32_t K,
                                              int64_t items, int64_t idx_limit, Keep keep, bool first,
-                                             bool* regs_intact, uint64_t* Tc, int tr) {
+                                             bool* regs_intact, uint64_t* Tc, int tr, Hint* hint = nullptr) {
   using G = Geo<T, U, W>;
   Misc* m = R.m;
   const bool vec = p.vec_ok != 0;
@@ -1224,8 +1257,18 @@ __device__ __forceinline__ bool select_stage(RowT<S>& R, const Params& p, float4
     // ---- threshold estimate from the digit histogram of the sample
     uint32_t t = 0;
     bool estimated = false;
+    bool hinted = false;
+    if constexpr (!kBlocks && W == 4 && Keep::kAll) {
+      if (hint != nullptr && R.nclus == 1) {
+        // from an earlier row's output (0: none usable); taken without a
+        // block barrier, so the warps go on filtering at their own pace
+        t = hint_threshold(*hint);
+        hinted = t != 0u;
+        estimated = hinted;
+      }
+    }
     if constexpr (!kBlocks && T == 256 && W == 4 && Keep::kAll) {
-      if (items > (int64_t)(cap / 2) && !full && R.nclus == 1 && first) {
+      if (!estimated && items > (int64_t)(cap / 2) && !full && R.nclus == 1) {
         t = estimate_small<T, U, W>(R, cur, nc, K, items);
         estimated = true;
       }
@@ -1322,8 +1365,11 @@ __device__ __forceinline__ bool select_stage(RowT<S>& R, const Params& p, float4
     const uint32_t total = __reduce_add_sync(kFull, cq);
     const bool overflow = __any_sync(kFull, cq > seg);
     if (overflow || total < K) {
+      if (hinted) bump(p, R, kCntHintMiss);  // the earlier row's threshold does not fit this one
       exact = true;
       stat = overflow ? kCntOverflow : kCntShort;
+    } else if (hinted) {
+      bump(p, R, kCntHintUsed);
     }
   }
 

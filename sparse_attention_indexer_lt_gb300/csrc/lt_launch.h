@@ -9,6 +9,10 @@ namespace lt {
 // one_round: the variant for slices of at most topk_round_positions(threads) positions.
 const void* topk_kernel_ptr(int threads, bool one_round, bool bf16);
 int64_t topk_round_positions(int threads);
+// the 256-thread multi-round top-k whose rows start from an earlier row's output
+const void* topk_hint_kernel_ptr(bool bf16);
+// resident CTAs per SM of the 256-thread kernels (their launch bounds)
+constexpr int kNarrowCtasPerSm = 3;
 // nullptr for an unsupported block size or thread count.
 const void* blocked_kernel_ptr(int threads, int block, bool bf16);
 // one instantiation per (threads, score type), each in its own translation unit

@@ -5,6 +5,23 @@
 
 namespace lt {
 
+// The U float4 at block bid[f] * W + off of a row, every one full and aligned.
+template <int U>
+__device__ __forceinline__ void gather_listed(const float* row, const uint32_t (&bid)[U], int W, int off,
+                                              float4 (&v)[U]) {
+#pragma unroll
+  for (int f = 0; f < U; ++f) v[f] = ldg4(row + (int64_t)bid[f] * W + off);
+}
+template <int U>
+__device__ __forceinline__ void gather_listed(const uint16_t* row, const uint32_t (&bid)[U], int W, int off,
+                                              float4 (&v)[U]) {
+  uint2 raw[U];
+#pragma unroll
+  for (int f = 0; f < U; ++f) raw[f] = __ldg(reinterpret_cast<const uint2*>(row + (int64_t)bid[f] * W + off));
+#pragma unroll
+  for (int f = 0; f < U; ++f) v[f] = widen4(raw[f]);
+}
+
 // The i-th of a thread's block ids (i < B).
 template <int B>
 __device__ __forceinline__ uint32_t pick_id(const uint32_t (&a)[B], uint32_t i) {
@@ -94,14 +111,25 @@ __global__ void __launch_bounds__(T, 1) listed_kernel(Params p) {
   float4 v[U];
   int nf[U];
   const bool vec = p.vec_ok != 0;
+  bool whole = vec;
 #pragma unroll
   for (int f = 0; f < U; ++f) {
     const int64_t p0 = (int64_t)bidf[f] * W + 4 * q;
     int64_t nv = ubase + f * LPB < n_u ? R.L - p0 : 0;
     nv = nv < 0 ? 0 : (nv > 4 ? 4 : nv);
     nf[f] = (int)nv;
-    if (vec && nv == 4) v[f] = ldg4(R.rowp + p0);
-    else v[f] = load4_scalar(R.rowp + p0, (int)nv);
+    whole = whole && nv == 4;
+  }
+  if (whole) {
+    // every float4 full: all loads in flight before any is used
+    gather_listed(R.rowp, bidf, W, 4 * q, v);
+  } else {
+#pragma unroll
+    for (int f = 0; f < U; ++f) {
+      const int64_t p0 = (int64_t)bidf[f] * W + 4 * q;
+      if (vec && nf[f] == 4) v[f] = ldg4(R.rowp + p0);
+      else v[f] = load4_scalar(R.rowp + p0, nf[f]);
+    }
   }
   const int64_t ncand = (int64_t)n_u * W - (last ? nblocks * W - R.L : 0);
   const uint32_t K = (uint32_t)(ncand < (int64_t)p.k ? ncand : (int64_t)p.k);

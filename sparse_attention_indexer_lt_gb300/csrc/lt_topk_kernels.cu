@@ -7,8 +7,9 @@ namespace lt {
 // One CTA (or one cluster of CTAs) per row: select the top K = min(k, L)
 // positions and write them ordered by (score desc, index asc). kOne: every
 // CTA's slice is a single register round (the planner guarantees it).
-// S: the score type (float, or uint16_t holding bf16 bits).
-template <int T, int U, bool kOne, class S>
+// S: the score type (float, or uint16_t holding bf16 bits). kHint: rows
+// start from the output of an earlier row (batches of single-CTA rows).
+template <int T, int U, bool kOne, class S, bool kHint = false>
 __global__ void __launch_bounds__(T, (T <= 256 ? 3 : 1)) topk_kernel(Params p) {
   extern __shared__ __align__(128) unsigned char smem[];
   using G = Geo<T, U, 4>;
@@ -27,8 +28,25 @@ __global__ void __launch_bounds__(T, (T <= 256 ? 3 : 1)) topk_kernel(Params p) {
     float4 vb[U];
     int nb[G::kSlots];
     bool intact;
-    exact = select_stage<T, U, 4, false>(R, p, va, na, vb, nb, false, K, R.L, p.row_stride, KeepAll{}, true,
-                                         &intact, &Tc, 0);
+    // Batches of single-CTA rows (256 threads): start from the (k/2)-th and
+    // k-th values of the row hint_rows earlier (two waves of CTAs, so almost
+    // surely finished; see Hint). Another CTA may still be writing them: they
+    // are a guess the filter checks; a miss takes the exact path.
+    if constexpr (kHint) {
+      Hint hint = {};
+      const bool hinted = p.out_val != nullptr && K == (uint32_t)p.k && p.k >= 2 && R.row >= p.hint_rows &&
+                          R.L > (int64_t)(p.cap / 2);
+      if (hinted) {
+        const float* prev = p.out_val + (R.row - p.hint_rows) * (int64_t)p.k;
+        hint.hi = ld_relaxed(prev + p.k / 2 - 1);
+        hint.lo = ld_relaxed(prev + p.k - 1);
+      }
+      exact = select_stage<T, U, 4, false>(R, p, va, na, vb, nb, false, K, R.L, p.row_stride, KeepAll{}, true,
+                                           &intact, &Tc, 0, hinted ? &hint : nullptr);
+    } else {
+      exact = select_stage<T, U, 4, false>(R, p, va, na, vb, nb, false, K, R.L, p.row_stride, KeepAll{}, true,
+                                           &intact, &Tc, 0);
+    }
   }
   output_positions<T>(R, p, exact, Tc, K, p.row_stride, true);
   wait_init(R);
@@ -47,6 +65,11 @@ const void* topk_ptr(int threads, bool one_round) {
 
 const void* topk_kernel_ptr(int threads, bool one_round, bool bf16) {
   return bf16 ? topk_ptr<uint16_t>(threads, one_round) : topk_ptr<float>(threads, one_round);
+}
+
+const void* topk_hint_kernel_ptr(bool bf16) {
+  return bf16 ? reinterpret_cast<const void*>(&topk_kernel<256, 4, false, uint16_t, true>)
+              : reinterpret_cast<const void*>(&topk_kernel<256, 4, false, float, true>);
 }
 
 const void* blocked_kernel_ptr(int threads, int block, bool bf16) {
