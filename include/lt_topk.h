@@ -222,8 +222,8 @@ lt_status lt_topk_candidates_bf16(const uint16_t* scores, const int32_t* lengths
  * several register rounds, more rows than two waves of resident CTAs) row r
  * reads the (k/2)-th and k-th values that row r - G wrote to out_val (G =
  * the CTAs of two waves; that row has almost surely finished) and, instead of
- * estimating, keeps the positions at or above k-th - ((k/2)-th - k-th):
- * about 1.5k to 1.7k of a row like that one. The filter's count check accepts it
+ * estimating, keeps the positions at or above k-th - 0.75 ((k/2)-th - k-th):
+ * about 1.4k to 1.5k of a row like that one. The filter's count check accepts it
  * only if at least k and at most the candidate area pass; otherwise the row
  * takes the exact streaming select, as any miss does. Row r - G may still be being written (the
  * values are then stale, e.g. from a previous call into the same buffer):

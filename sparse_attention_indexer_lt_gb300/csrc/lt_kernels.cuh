@@ -1174,9 +1174,9 @@ __device__ __forceinline__ uint32_t estimate_small(RowCore& R, const float4 (&v)
 // hint (nullable): the (k/2)-th and k-th values an earlier row of the batch
 // wrote to its output. Rows of one batch score the same context, so from
 // those two values, lo = k-th and hi = (k/2)-th, the filter can start at
-// lo - (hi - lo): about 1.5k to 1.7k of a similar row pass it (the scores
-// thin out above the k-th), far more than the row-to-row spread of the k-th
-// value needs. The estimate is then skipped.
+// lo - 0.75 (hi - lo): about 1.4k to 1.5k of a similar row pass it (the
+// scores thin out above the k-th), a margin of many times the row-to-row
+// spread of the k-th value. The estimate is then skipped.
 // Whether it fits is decided by the filter's own count check: fewer than K
 // kept or more than the candidate area holds, and the row takes the exact
 // path, as any miss does. Values that give no usable threshold (NaN,
@@ -1186,7 +1186,7 @@ struct Hint {
 };
 
 __device__ __forceinline__ uint32_t hint_threshold(const Hint& h) {
-  const float t = h.lo - (h.hi - h.lo);
+  const float t = h.lo - 0.75f * (h.hi - h.lo);
   // finite and ordered (NaN fails every compare); key 0 would mean "keep all"
   if (!(h.hi > h.lo) || !(fabsf(h.hi) <= 3.4e38f) || !(fabsf(t) <= 3.4e38f)) return 0u;
   return key_of(t);
