@@ -129,6 +129,21 @@ __device__ __forceinline__ void load_round(const RowT<S>& R, bool vec, int r, fl
   }
 }
 
+// Bulk prefetch of this CTA's slice [begin, end) into L2, in 32 pieces (one
+// per lane of the calling warp); pieces that do not start on a 16-byte
+// boundary are skipped (a prefetch only changes timing).
+template <class S>
+__device__ __forceinline__ void prefetch_slice_l2(const RowT<S>& R) {
+  const char* b = reinterpret_cast<const char*>(R.rowp + R.begin);
+  const int64_t bytes = (R.end - R.begin) * (int64_t)sizeof(S);
+  const int64_t piece = ((bytes + 31) / 32 + 15) & ~(int64_t)15;
+  const int64_t off = (int64_t)lane_id() * piece;
+  int64_t n = bytes - off;
+  n = (n < piece ? n : piece) & ~(int64_t)15;
+  if (n > 0 && (reinterpret_cast<uintptr_t>(b + off) & 15u) == 0)
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" :: "l"(b + off), "r"((uint32_t)n) : "memory");
+}
+
 // Four-position slots (W = 4): round r lies wholly inside the slice.
 template <int T, int U>
 __device__ __forceinline__ bool round_whole(const RowCore& R, int r) {
@@ -1233,6 +1248,12 @@ __device__ __forceinline__ bool select_stage(RowT<S>& R, const Params& p, float4
       if (R.rounds > 1) load_round4<T, U>(R, vec, 1, nxt, nn);
       else clear_round(nn);
       loaded = true;
+      if constexpr (T == 256) {
+        // Single-CTA rows of many rounds (the batched rows, three CTAs per
+        // SM): the whole slice is asked into L2 at once, so the rounds the
+        // registers load later come from L2 while HBM keeps streaming.
+        if (R.rounds > 2 && threadIdx.x < 32) prefetch_slice_l2(R);
+      }
     }
   }
   if (!loaded) {
