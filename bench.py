@@ -458,7 +458,8 @@ def bench_only(args, world):
     def step(i):
         c = copies[i % ncopies]
         if w.blocked:
-            lt.topk_blocked(c, ld, w.block, w.k_blocks, w.k, out_idx=oi, out_val=ov, out_blocks=ob)
+            lt.topk_blocked(c, ld, w.block, w.k_blocks, w.k, out_idx=oi, out_val=ov, out_blocks=ob,
+                            force_cluster=args.force_cluster, force_threads=args.force_threads)
         elif listed:
             lt.topk_candidates(c, cand, ld, w.block, w.k, out_idx=oi, out_val=ov,
                                force_cluster=args.force_cluster, force_threads=args.force_threads)
@@ -474,8 +475,7 @@ def bench_only(args, world):
             "plan": ({"kernel": "listed", "cluster": 1, "threads": 512, "grid": w.rows} if listed else
                      lt.plan(w.rows, w.row_stride, w.k, blocked=w.blocked, k_blocks=w.k_blocks,
                              force_kernel=0 if w.blocked else KERNEL_IDS[args.kernel],
-                             force_cluster=0 if w.blocked else args.force_cluster,
-                             force_threads=0 if w.blocked else args.force_threads))}
+                             force_cluster=args.force_cluster, force_threads=args.force_threads))}
 
 
 TRACE_NAMES = ["start", "hist", "merge", "estimate", "filter", "exchange", "exact", "output",

@@ -135,8 +135,7 @@ lt_status lt_topk_blocked_bf16(const uint16_t* scores, const int32_t* lengths, i
  * the valid positions i < L of the listed blocks; keep the first
  * min(k, ncand) by (score desc, position asc), written as for lt_topk.
  *
- *   block        4, 8, 16 or 32; ceil(row_stride / block) <= 65536, else
- *                LT_ERR_UNSUPPORTED
+ *   block        4, 8, 16 or 32
  *   cand_blocks  device int32[rows][n_cand], owned by the caller, read only:
  *                block ids in any order; ids outside [0, nblocks) are
  *                ignored (-1 pads a short list), a repeated id counts once
@@ -146,9 +145,12 @@ lt_status lt_topk_blocked_bf16(const uint16_t* scores, const int32_t* lengths, i
  * negative n_cand or block < 1 return LT_ERR_INVALID_ARG.
  *
  * A list of at most 16384 / block entries per row (2048 blocks of 8) is
- * served by a kernel that reads only the listed blocks (one CTA per row);
- * longer lists, and the _ex call with a forced cluster or thread count other
- * than 1 / 512 or with force_exact, scan whole rows. Same results either way.
+ * served by a kernel that reads only the listed blocks (one CTA per row, any
+ * row length); longer lists, and the _ex call with a forced cluster or
+ * thread count other than 1 / 512 or with force_exact, scan whole rows, each
+ * CTA of a row's cluster holding a bitmap of its own slice: those rows may
+ * have at most 65536 blocks per CTA (for example 8,388,608 positions of
+ * 8-blocks on 16 CTAs), else LT_ERR_UNSUPPORTED. Same results either way.
  */
 lt_status lt_topk_candidates(const float* scores, const int32_t* lengths, int32_t rows,
                              int64_t row_stride, int32_t block, const int32_t* cand_blocks,

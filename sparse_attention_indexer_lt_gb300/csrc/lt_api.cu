@@ -552,8 +552,6 @@ lt_status lt_topk_candidates_ex(const void* scores, int32_t dtype, const int32_t
   if (block < 1 || n_cand < 0 || (n_cand > 0 && cand_blocks == nullptr && rows > 0))
     return LT_ERR_INVALID_ARG;
   if (block_index(block) < 0) return LT_ERR_UNSUPPORTED;
-  // every CTA holds a bitmap of the row's blocks in kBins words
-  if ((row_stride + block - 1) / block > (int64_t)32 * lt::kBins) return LT_ERR_UNSUPPORTED;
   if (rows == 0) return LT_OK;
   Plan plan;
   int dev = 0;
@@ -586,6 +584,10 @@ lt_status lt_topk_candidates_ex(const void* scores, int32_t dtype, const int32_t
     st = make_plan(rows, row_stride, k, true, block, 1, force_cluster, force_threads, LT_KERNEL_AUTO,
                    aligned, bf16, &plan, &dev);
     if (st != LT_OK) return st;
+    // every CTA holds a bitmap of its slice's blocks in kBins words
+    int64_t per = (row_stride + plan.cluster - 1) / plan.cluster;
+    per = (per + block - 1) / block;
+    if (per > (int64_t)32 * lt::kBins) return LT_ERR_UNSUPPORTED;
   }
   lt::Params p = {};
   p.external = 1;

@@ -36,31 +36,40 @@ __global__ void __launch_bounds__(T, (T <= 256 ? 3 : 1)) blocked_kernel(Params p
   float4 va[U], vb[U];
   int na[G::kSlots], nb[G::kSlots];
   if (role == 3) {
-    // a bitmap of the row's listed blocks in the output's bucket-start area
-    // (unused until the ordered output); every CTA holds the whole row's, so
-    // it counts the candidate positions itself
+    // a bitmap of this CTA's slice of blocks (slices hold whole blocks) in the
+    // output's bucket-start area (unused until the ordered output); the
+    // listed positions of the row are summed over the cluster
     const int64_t nblocks = (R.L + W - 1) / W;
-    const uint32_t words = (uint32_t)((nblocks + 31) >> 5);  // <= kBins: checked by the host
+    const int64_t b0 = R.begin / W, b1 = (R.end + W - 1) / W;
+    const uint32_t words = (uint32_t)((b1 - b0 + 31) >> 5);  // <= kBins: checked by the host
     uint32_t* bits = R.aux;
     for (uint32_t i = threadIdx.x; i < words; i += T) bits[i] = 0u;
     __syncthreads();
     const int32_t* listed = p.cand_blocks + R.row * (int64_t)p.n_cand;
     for (int32_t j = (int32_t)threadIdx.x; j < p.n_cand; j += T) {
-      const int32_t b = listed[j];
-      if (b >= 0 && (int64_t)b < nblocks) atomicOr(&bits[b >> 5], 1u << (b & 31));
+      const int64_t b = listed[j];
+      if (b >= b0 && b < b1) atomicOr(&bits[(b - b0) >> 5], 1u << ((b - b0) & 31));
     }
     __syncthreads();
     uint32_t cnt = 0;
     for (uint32_t i = threadIdx.x; i < words; i += T) cnt += (uint32_t)__popc(bits[i]);
     const uint32_t nlisted = block_sum<T>(cnt, m);
-    const int64_t lastb = nblocks - 1;
-    const bool last = nblocks > 0 && ((bits[lastb >> 5] >> (lastb & 31)) & 1u) != 0u;
-    const int64_t ncand = (int64_t)nlisted * W - (last ? nblocks * W - R.L : 0);
+    const int64_t lastb = nblocks - 1;  // may be partial: its positions past L do not count
+    const bool last = lastb >= b0 && lastb < b1 && ((bits[(lastb - b0) >> 5] >> ((lastb - b0) & 31)) & 1u) != 0u;
+    int64_t ncand = (int64_t)nlisted * W - (last ? nblocks * W - R.L : 0);
+    if (R.nclus > 1) {
+      // every CTA adds its count into every peer (zeroed before the start-up barrier)
+      wait_init(R);
+      if (threadIdx.x < R.nclus)
+        dsmem_red_add(peer_addr(smem_addr(&m->aux[7]), threadIdx.x), (uint32_t)ncand);
+      cluster_sync();
+      ncand = (int64_t)m->aux[7];
+    }
     const uint32_t K = (uint32_t)(ncand < (int64_t)p.k ? ncand : (int64_t)p.k);
     bool intact;
     uint64_t Tc;
     const bool exact = select_stage<T, U, W, false>(R, p, va, na, vb, nb, false, K, ncand, p.row_stride,
-                                                    KeepListed<T, U, W>{bits, words * 32u}, true, &intact,
+                                                    KeepListed<T, U, W>{bits, b0, words * 32u}, true, &intact,
                                                     &Tc, 0);
     output_positions<T>(R, p, exact, Tc, K, p.row_stride, true);
     wait_init(R);

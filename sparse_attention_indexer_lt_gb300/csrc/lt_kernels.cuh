@@ -198,13 +198,15 @@ struct KeepAll {
 // Keep the positions of listed blocks: bit b of bits[b >> 5] marks block b of
 // the row; blocks at or past nbits are not listed.
 template <int T, int U, int W>
+// bits covers blocks [b0, b0 + nbits) of the row (this CTA's slice).
 struct KeepListed {
   static constexpr bool kAll = false;
   const uint32_t* bits;
+  int64_t b0;
   uint32_t nbits;
   __device__ __forceinline__ bool operator()(const RowCore& R, int r, const float4 (&)[U], int s, int) const {
-    const int64_t bid = slot_pos<T, U, W>(R, r, s) / W;
-    return bid < (int64_t)nbits && ((bits[bid >> 5] >> (bid & 31)) & 1u) != 0u;
+    const int64_t bid = slot_pos<T, U, W>(R, r, s) / W - b0;
+    return bid >= 0 && bid < (int64_t)nbits && ((bits[bid >> 5] >> (bid & 31)) & 1u) != 0u;
   }
 };
 
@@ -252,6 +254,7 @@ __device__ __forceinline__ void setup_row(RowT<S>& R, const Params& p, unsigned 
     m->local_max = 0u;
     m->flags = 0;
     m->own_count = 0;
+    m->aux[7] = 0;  // cluster-wide sums pushed by peers (listed positions)
   }
   if (p.clustered) {
     uint4* z0 = reinterpret_cast<uint4*>(R.merged0);

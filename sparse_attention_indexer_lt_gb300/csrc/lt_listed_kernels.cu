@@ -22,6 +22,55 @@ __device__ __forceinline__ void gather_listed(const uint16_t* row, const uint32_
   for (int f = 0; f < U; ++f) v[f] = widen4(raw[f]);
 }
 
+// The unique valid ids of the row's list (at most T * BPT entries: host) in
+// ids[0, *n_u) -- in no particular order -- through an open-addressing hash
+// set of 2 * T * BPT slots placed after them in the candidate area; *last:
+// whether the row's last block is listed. For rows too long for a bitmap of
+// their blocks. Probing is bounded: the set is never more than half full.
+template <int T, int BPT>
+__device__ __noinline__ void listed_ids_hashed(const Params p, const RowCore R, int64_t nblocks, uint32_t* ids,
+                                               uint32_t* n_u, bool* last) {
+  constexpr uint32_t kSlotsH = 2u * T * BPT;  // a power of two
+  constexpr uint32_t kEmpty = 0xffffffffu;
+  Misc* m = R.m;
+  uint32_t* tab = ids + T * BPT;
+  for (uint32_t i = threadIdx.x; i < kSlotsH; i += T) tab[i] = kEmpty;
+  if (threadIdx.x == 0) m->aux[1] = 0u;  // the last block seen
+  __syncthreads();
+  const int32_t* listed = p.cand_blocks + R.row * (int64_t)p.n_cand;
+  uint32_t mine[BPT];
+  uint32_t cnt = 0;
+#pragma unroll
+  for (int i = 0; i < BPT; ++i) {
+    const int32_t j = (int32_t)threadIdx.x + i * T;
+    const int32_t b = j < p.n_cand ? __ldg(listed + j) : -1;
+    mine[i] = kEmpty;
+    if (b >= 0 && (int64_t)b < nblocks) {
+      uint32_t h = ((uint32_t)b * 2654435761u) & (kSlotsH - 1u);
+      for (uint32_t probe = 0; probe < kSlotsH; ++probe) {
+        const uint32_t old = atomicCAS(&tab[h], kEmpty, (uint32_t)b);
+        if (old == kEmpty) {  // first occurrence of b
+          mine[i] = (uint32_t)b;
+          ++cnt;
+          if ((int64_t)b == nblocks - 1) m->aux[1] = 1u;
+          break;
+        }
+        if (old == (uint32_t)b) break;  // a repeat
+        h = (h + 1u) & (kSlotsH - 1u);
+      }
+    }
+  }
+  uint32_t o = block_prefix_excl<T>(cnt, m);
+#pragma unroll
+  for (int i = 0; i < BPT; ++i)
+    if (mine[i] != kEmpty) ids[o++] = mine[i];
+  if (threadIdx.x == T - 1) m->aux[0] = o;
+  __syncthreads();
+  *n_u = m->aux[0];
+  *last = m->aux[1] != 0u;
+  __syncthreads();
+}
+
 // The i-th of a thread's block ids (i < B).
 template <int B>
 __device__ __forceinline__ uint32_t pick_id(const uint32_t (&a)[B], uint32_t i) {
@@ -54,8 +103,15 @@ __global__ void __launch_bounds__(T, 1) listed_kernel(Params p) {
   setup_row<T, U, W>(R, p, smem);
   Misc* m = R.m;
   const int64_t nblocks = (R.L + W - 1) / W;
-  const uint32_t words = (uint32_t)((nblocks + 31) >> 5);  // <= kBins: checked by the host
-
+  const uint32_t words = (uint32_t)((nblocks + 31) >> 5);
+  uint32_t* ids = reinterpret_cast<uint32_t*>(R.cand);
+  uint32_t n_u;
+  bool last;
+  if (words > (uint32_t)kBins) {
+    // rows of more than 32 * kBins blocks: the unique listed ids through a
+    // hash set in the candidate area instead of a bitmap of the row
+    listed_ids_hashed<T, BPT>(p, R, nblocks, ids, &n_u, &last);
+  } else {
   // (1) bitmap of the listed blocks, then their ids ascending in the
   // candidate area (free until the filter)
   uint32_t* bits = R.aux;
@@ -82,15 +138,15 @@ __global__ void __launch_bounds__(T, 1) listed_kernel(Params p) {
   const uint32_t w1 = min(w0 + wpt, words);
   uint32_t cnt = 0;
   for (uint32_t w = w0; w < w1; ++w) cnt += (uint32_t)__popc(bits[w]);
-  uint32_t* ids = reinterpret_cast<uint32_t*>(R.cand);
   uint32_t o = block_prefix_excl<T>(cnt, m);
   for (uint32_t w = w0; w < w1; ++w)
     for (uint32_t x = bits[w]; x; x &= x - 1u) ids[o++] = 32u * w + (uint32_t)(__ffs(x) - 1);
   if (threadIdx.x == T - 1) m->aux[0] = o;  // the number of unique listed blocks (<= T * BPT: host)
   const int64_t lastb = nblocks - 1;
-  const bool last = nblocks > 0 && ((bits[lastb >> 5] >> (lastb & 31)) & 1u) != 0u;
+  last = nblocks > 0 && ((bits[lastb >> 5] >> (lastb & 31)) & 1u) != 0u;
   __syncthreads();
-  const uint32_t n_u = m->aux[0];
+  n_u = m->aux[0];
+  }
 
   // (2) the gathered round: warp w takes blocks [w * U * LPB, (w + 1) * U * LPB)
   // of the list; its float4 f of lane l is float4 l % VS of block

@@ -94,3 +94,39 @@ def test_unaligned_rows():
     S, L = workloads.random_rows(3, 40001, seed=45, dist="bf16", lengths="ragged")
     cand = _random_lists(rng, 3, (40001 + 7) // 8, 700)
     parity_candidates(S.numpy(), L.numpy(), cand, 8, 512, what="stride 40001")
+
+
+@pytest.mark.parametrize("block", [4, 8])
+def test_short_lists_on_rows_longer_than_a_bitmap(block):
+    """A short list (the kernel that reads only the listed blocks) on rows of
+    2^20 positions, more blocks than a bitmap of the row can hold: the unique
+    ids come from a hash set; repeats, pads and ids past the row included."""
+    rng = np.random.default_rng(51 + block)
+    rows, stride = 3, 1 << 20
+    S, L = workloads.random_rows(rows, stride, seed=52, dist="bf16", lengths="ragged", min_len=stride // 2)
+    nb = stride // block
+    n = (512 * 8 * 4 // block) // 2
+    lists = _random_lists(rng, rows, nb, n, pads=7, repeats=n // 3, beyond=5)[:, : 512 * 8 * 4 // block]
+    c = counters()
+    parity_candidates(S.numpy(), L.numpy(), lists, block, 512, what=f"long rows, short list, block {block}",
+                      counters=c)
+    parity_candidates(S.numpy(), L.numpy(), lists, block, 2048, what=f"long rows, short list, k=2048, block {block}")
+
+
+def test_long_lists_on_rows_longer_than_a_bitmap():
+    """A long list (whole-row scan) on rows of 2^20 positions: every CTA of the
+    row's cluster holds a bitmap of its own slice and the listed positions
+    are summed over the cluster."""
+    import sparse_attention_indexer_lt_gb300 as lt
+    rng = np.random.default_rng(53)
+    rows, stride, block = 2, 1 << 20, 8
+    S, L = workloads.random_rows(rows, stride, seed=54, dist="tail", lengths="ragged", min_len=stride // 2)
+    nb = stride // block
+    lists = _random_lists(rng, rows, nb, 20000, pads=3, repeats=100, beyond=4)
+    parity_candidates(S.numpy(), L.numpy(), lists, block, 512, what="long rows, long list")
+    for fc in (4, 8, 16):
+        parity_candidates(S.numpy(), L.numpy(), lists, block, 512, what=f"long rows, long list, cluster {fc}",
+                          force_cluster=fc)
+    # one CTA would need a bitmap of 131072 blocks: refused
+    with pytest.raises(lt.LtError):
+        lt.topk_candidates(S.cuda(), torch.as_tensor(lists).cuda(), L.cuda(), block, 512, force_cluster=1)
