@@ -145,9 +145,12 @@ lt_status lt_topk_blocked_bf16(const uint16_t* scores, const int32_t* lengths, i
  * negative n_cand or block < 1 return LT_ERR_INVALID_ARG.
  *
  * A list of at most 16384 / block entries per row (2048 blocks of 8) is
- * served by a kernel that reads only the listed blocks (one CTA per row, any
- * row length); longer lists, and the _ex call with a forced cluster or
- * thread count other than 1 / 512 or with force_exact, scan whole rows, each
+ * served by a kernel that reads only the listed blocks (any row length):
+ * with few rows each row's unique blocks are shared out over a cluster of up
+ * to 8 CTAs (rows of at most 65536 blocks), with enough rows to fill the SMs,
+ * or a forced cluster of 1 or 512 threads, one CTA per row; longer lists,
+ * and the _ex call with any other forced cluster or thread count or with
+ * force_exact, scan whole rows, each
  * CTA of a row's cluster holding a bitmap of its own slice: those rows may
  * have at most 65536 blocks per CTA (for example 8,388,608 positions of
  * 8-blocks on 16 CTAs), else LT_ERR_UNSUPPORTED. Same results either way.

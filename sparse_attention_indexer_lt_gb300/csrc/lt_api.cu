@@ -34,7 +34,7 @@ constexpr int kMaxDevices = 64;
 constexpr int kWideThreads = 512;
 constexpr int kNarrowThreads = 256;
 constexpr int64_t kWideRound = 512 * 8 * 4;  // positions per CTA per round (wide)
-constexpr int kTypeSlots = 19;                // kernel variants per score type
+constexpr int kTypeSlots = 23;                // kernel variants per score type
 constexpr int kSlots = 2 * kTypeSlots;        // fp32, then bf16
 // the streamed kernel's launch bounds: CTAs per SM for 256 / 512 threads
 constexpr int stream_ctas_per_sm(int threads) { return threads == 256 ? 3 : 2; }
@@ -74,9 +74,10 @@ int block_index(int block) {
   }
 }
 
-// slots 14..17: the listed-candidate kernel, by block size; 18: the top-k
-// whose rows start from an earlier row's output; bf16 kernels follow the
-// fp32 ones (kTypeSlots later)
+// slots 14..17: the listed-candidate kernel, by block size (512 threads, one
+// CTA per row); 18: the top-k whose rows start from an earlier row's output;
+// 19..22: the listed-candidate kernel with 256 threads (a cluster per row);
+// bf16 kernels follow the fp32 ones (kTypeSlots later)
 int kernel_slot(bool blocked, int block, int threads, bool stream = false, bool one_round = false,
                 bool bf16 = false) {
   const int wide = threads == kWideThreads ? 1 : 0;
@@ -565,19 +566,39 @@ lt_status lt_topk_candidates_ex(const void* scores, int32_t dtype, const int32_t
     DeviceInfo* di = nullptr;
     st = device_info(&di, &dev);
     if (st != LT_OK) return st;
-    plan.threads = kWideThreads;
-    plan.cluster = 1;
-    plan.grid = rows;
-    plan.cap = 512u * 8u * 4u;  // a slot for every gathered position: no overflow
-    plan.seg_shift = 14;
-    plan.wstage = (uint32_t)kWideThreads * 16u * (uint32_t)lt::kStageF4;
-    plan.sel_cap = next_pow2(k < 32 ? 32u : (uint32_t)k);
-    plan.func = lt::listed_kernel_ptr(block, bf16);
-    plan.smem = lt::make_layout(false, plan.cap, plan.sel_cap, plan.wstage).total;
-    gathered = plan.func != nullptr && (int)plan.smem <= di->smem_optin;
-    if (gathered) {
-      st = prepare_kernel(dev, (bf16 ? kTypeSlots : 0) + 14 + block_index(block), plan.func, plan.smem, 1);
+    // a row's scattered block reads spread over a cluster of up to 8 CTAs
+    // (256 threads each) while the rows' clusters still fit the SMs once;
+    // rows enough to fill the SMs take one 512-thread CTA each
+    // (rows too long for a bitmap of their blocks build the id list in a
+    // hash set, in an order the CTAs of a cluster would not agree on: one CTA)
+    int c = 1;
+    const bool bitmap = (row_stride + block - 1) / block <= (int64_t)32 * lt::kBins;
+    if (force_cluster == 0 && force_threads == 0 && bitmap)
+      while (c < 8 && (int64_t)rows * c * 2 <= di->sms) c *= 2;
+    const uint32_t sel_cap = next_pow2(k < 32 ? 32u : (uint32_t)k);
+    for (;; c /= 2) {
+      const int threads = c > 1 ? kNarrowThreads : kWideThreads;
+      plan.threads = threads;
+      plan.cluster = c;
+      plan.grid = rows * c;
+      // every CTA's segment holds every position of its share of the list
+      plan.cap = (uint32_t)lt::kListedPositions;
+      plan.seg_shift = 0;
+      while ((1u << plan.seg_shift) < plan.cap / (uint32_t)c) ++plan.seg_shift;
+      plan.wstage = (uint32_t)threads * 16u * (uint32_t)lt::kStageF4;
+      plan.sel_cap = sel_cap;
+      plan.func = lt::listed_kernel_ptr(threads, block, bf16);
+      plan.smem = lt::make_layout(c > 1, plan.cap, plan.sel_cap, plan.wstage).total;
+      gathered = plan.func != nullptr && (int)plan.smem <= di->smem_optin;
+      if (!gathered) {
+        if (c == 1) break;
+        gathered = true;  // try a smaller cluster
+        continue;
+      }
+      const int slot = (bf16 ? kTypeSlots : 0) + (c > 1 ? 19 : 14) + block_index(block);
+      st = prepare_kernel(dev, slot, plan.func, plan.smem, c);
       if (st != LT_OK) return st;
+      if (c == 1 || active_clusters(dev, slot, plan.func, c, threads, plan.smem) >= rows) break;
     }
   }
   if (!gathered) {

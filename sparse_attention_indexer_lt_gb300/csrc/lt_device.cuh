@@ -63,6 +63,9 @@ namespace lt {
 
 constexpr int kBins = 2048;       // 11-bit digits / linear buckets
 constexpr int kMaxCluster = 16;
+// Positions a row's block list may cover on the listed kernel: one register
+// round of a 512-thread CTA (512 threads x 8 float4).
+constexpr int64_t kListedPositions = 512 * 8 * 4;
 constexpr int kMaxWarps = 32;
 constexpr int kMaxBucket = 256;   // largest bucket ranked by counting
 constexpr int kOutBuckets = 1024; // linear key buckets of the ordered output

@@ -24,8 +24,9 @@ extern template const void* blocked_kernel_ptr_of<512, float>(int);
 extern template const void* blocked_kernel_ptr_of<512, uint16_t>(int);
 // the streamed top-k kernel (fp32 scores): 256 threads (three CTAs per SM) or 512 (two)
 const void* stream_kernel_ptr(int threads);
-// listed-candidate kernel (512 threads, one CTA per row, only the listed
-// blocks read): nullptr for an unsupported block size
-const void* listed_kernel_ptr(int block, bool bf16);
+// listed-candidate kernel (only the listed blocks read): 512 threads with one
+// CTA per row, 256 threads with a cluster per row; nullptr for an unsupported
+// block size or thread count
+const void* listed_kernel_ptr(int threads, int block, bool bf16);
 int64_t listed_round_blocks(int block);
 }  // namespace lt

@@ -80,22 +80,30 @@ __device__ __forceinline__ uint32_t pick_id(const uint32_t (&a)[B], uint32_t i) 
   return r;
 }
 
-// One CTA per row. The row's listed blocks (ids outside the row ignored,
-// repeats once) fit one register round of T threads x U float4, gathered from
-// the ascending unique list, so the CTA reads only those blocks' scores. Then the single-round selection:
-// exact 11-bit histogram of the keys of every gathered score (key_of: NaN
-// lowest, like the fillers past the list), so the threshold -- the lower
-// edge of the bin holding the K-th key -- keeps at least K; filter; ordered
-// output. The candidate area holds every gathered position, so no row can
-// overflow it. Should a filter ever keep fewer than K, it is redone keeping
-// every position.
+// One CTA, or one cluster of C CTAs, per row. The row's listed blocks (ids
+// outside the row ignored, repeats once) -- at most kListedPositions / W of
+// them (host) -- form the ascending unique list, which every CTA of the row
+// builds (ascending, from a bitmap of the row's blocks; rows too long for
+// one build it unordered in a hash set and run on one CTA); CTA q gathers the
+// q-th of C equal shares of it in one register
+// round, so the row's scattered reads are spread over C SMs and only the
+// listed blocks' scores are read. Then the single-round selection: exact
+// 11-bit histogram of the keys of every gathered score (key_of: NaN lowest,
+// like the fillers past the list), merged over the cluster, so the threshold
+// -- the lower edge of the bin holding the K-th key -- keeps at least K;
+// filter; rank 0 gathers the candidates and writes the ordered row. Each
+// CTA's segment of the candidate area holds every position of its share, so
+// no row can overflow it. Should a filter ever keep fewer than K, it is redone
+// keeping every position.
 template <int T, int W, class S>
 __global__ void __launch_bounds__(T, 1) listed_kernel(Params p) {
   constexpr int U = 8;          // float4 per thread: the round
   constexpr int VS = W / 4;     // float4 per block
-  constexpr int BPT = U / VS;   // blocks per thread
+  constexpr int BPT = (int)(kListedPositions / W) / T;  // list entries per thread
+  constexpr int NW = T / 32;
   using G = Geo<T, U, W>;
-  static_assert(G::kSlots == BPT, "a slot is a block");
+  static_assert(BPT >= 1 && BPT * T * W == (int)kListedPositions, "the list divides over the threads");
+  (void)sizeof(G);
   extern __shared__ __align__(128) unsigned char smem[];
   RowT<S> R;
   stamp(p, kTrStart);
@@ -148,20 +156,23 @@ __global__ void __launch_bounds__(T, 1) listed_kernel(Params p) {
   n_u = m->aux[0];
   }
 
-  // (2) the gathered round: warp w takes blocks [w * U * LPB, (w + 1) * U * LPB)
-  // of the list; its float4 f of lane l is float4 l % VS of block
-  // w * U * LPB + f * LPB + l / VS, so the lanes of one load share whole
-  // blocks (each 32-byte sector of a block is requested once). Positions past
-  // the list or the row hold NaN; nf[f] counts a float4's valid positions.
+  // (2) the gathered round over this CTA's share [s0, s1) of the list: its
+  // float4 f of lane l of warp w is float4 l % VS of share block
+  // f * NW * LPB + w * LPB + l / VS, so the lanes of one load share whole
+  // blocks (each 32-byte sector of a block is requested once) and a small
+  // share still spreads over every warp. Positions past the share or the row
+  // hold NaN; nf[f] counts a float4's valid positions.
   constexpr int LPB = 32 / VS;  // blocks per warp load
   const uint32_t lane = lane_id();
   const uint32_t q = lane % VS;
-  const uint32_t ubase = (threadIdx.x >> 5) * (U * LPB) + lane / VS;
+  const uint32_t per = (n_u + R.nclus - 1) / R.nclus;
+  const uint32_t s0 = min(R.rank * per, n_u), s1 = min(s0 + per, n_u);
+  const uint32_t ubase = s0 + (threadIdx.x >> 5) * LPB + lane / VS;
   uint32_t bidf[U];
 #pragma unroll
   for (int f = 0; f < U; ++f) {
-    const uint32_t u = ubase + f * LPB;
-    bidf[f] = u < n_u ? ids[u] : 0u;
+    const uint32_t u = ubase + (uint32_t)f * (uint32_t)(NW * LPB);
+    bidf[f] = u < s1 ? ids[u] : 0u;
   }
   __syncthreads();  // the id list is in registers: the candidate area is free
   float4 v[U];
@@ -171,7 +182,7 @@ __global__ void __launch_bounds__(T, 1) listed_kernel(Params p) {
 #pragma unroll
   for (int f = 0; f < U; ++f) {
     const int64_t p0 = (int64_t)bidf[f] * W + 4 * q;
-    int64_t nv = ubase + f * LPB < n_u ? R.L - p0 : 0;
+    int64_t nv = ubase + (uint32_t)f * (uint32_t)(NW * LPB) < s1 ? R.L - p0 : 0;
     nv = nv < 0 ? 0 : (nv > 4 ? 4 : nv);
     nf[f] = (int)nv;
     whole = whole && nv == 4;
@@ -190,6 +201,13 @@ __global__ void __launch_bounds__(T, 1) listed_kernel(Params p) {
   const int64_t ncand = (int64_t)n_u * W - (last ? nblocks * W - R.L : 0);
   const uint32_t K = (uint32_t)(ncand < (int64_t)p.k ? ncand : (int64_t)p.k);
   const uint32_t cap = (uint32_t)p.cap;
+  const uint32_t seg = 1u << R.seg_shift;  // this CTA's segment: every position of its share fits
+  if (R.nclus > 1 && K > 0 && ncand <= (int64_t)(cap / 2)) {
+    // no histogram merge (whose barrier would do it) before the first push
+    // into rank 0's candidate area, which held rank 0's id list until now
+    wait_init(R);
+    cluster_sync();
+  }
 
   if (K > 0) {
     // (3) threshold from the exact histogram of the gathered keys (the NaN
@@ -198,17 +216,23 @@ __global__ void __launch_bounds__(T, 1) listed_kernel(Params p) {
     uint32_t t = 0;
     if (ncand > (int64_t)(cap / 2)) {
       zero_bins<T>(R.hist);
+      // the gathered positions only (fillers past a small share would pile
+      // up on bin 0)
 #pragma unroll
       for (int u = 0; u < U; ++u) {
-        atomicAdd(&R.hist[key_of(v[u].x) >> 21], 1u);
-        atomicAdd(&R.hist[key_of(v[u].y) >> 21], 1u);
-        atomicAdd(&R.hist[key_of(v[u].z) >> 21], 1u);
-        atomicAdd(&R.hist[key_of(v[u].w) >> 21], 1u);
+        if (nf[u] > 0) atomicAdd(&R.hist[key_of(v[u].x) >> 21], 1u);
+        if (nf[u] > 1) atomicAdd(&R.hist[key_of(v[u].y) >> 21], 1u);
+        if (nf[u] > 2) atomicAdd(&R.hist[key_of(v[u].z) >> 21], 1u);
+        if (nf[u] > 3) atomicAdd(&R.hist[key_of(v[u].w) >> 21], 1u);
       }
       stamp(R, kTrHist);
-      __syncthreads();
-      find_digit<T>(R.hist, K, m);
+      // the cluster's histogram; a CTA holding K keys pushes only the bins at
+      // or above its own K-th key's (the row's K-th key is no lower)
+      const uint32_t* bins = merge_hist<T>(R, 0, R.nclus > 1 ? K : 0u);
+      stamp(R, kTrMerge);
+      find_digit<T>(bins, K, m);
       t = m->res_digit << 21;
+      release_merged<T>(R, 0);
     }
     stamp(R, kTrEstimate);
     {
@@ -230,7 +254,7 @@ __global__ void __launch_bounds__(T, 1) listed_kernel(Params p) {
       }
       uint32_t kmn = 0xffffffffu, kmx = 0u;
       if (mask) {
-        uint2* list = R.cand;
+        uint2* list = R.cand + (R.rank << R.seg_shift);
         uint32_t oc = atomicAdd(&m->local_count, (uint32_t)__popc(mask));
 #pragma unroll
         for (int f = 0; f < U; ++f) R.wst[f * 32 + lane] = v[f];
@@ -243,15 +267,17 @@ __global__ void __launch_bounds__(T, 1) listed_kernel(Params p) {
           kmn = min(kmn, kk);
           kmx = max(kmx, kk);
           const uint32_t pos = pick_id<U>(bidf, F) * W + 4u * q + e;
-          if (oc < cap) list[oc] = make_uint2(kk, pos);
+          if (oc < seg) list[oc] = make_uint2(kk, pos);
           ++oc;
         } while (mask);
       }
       flush_key_range(R, kmn, kmx);
       stamp(R, kTrFilter);
-      exchange_segments<T>(R, false);  // one CTA: segment 0 is the whole list
+      // one CTA: segment 0 is the whole list; a cluster gathers to rank 0
+      exchange_segments<T>(R, R.nclus > 1);
       stamp(R, kTrExchange);
-      if (m->seg_cnt[0] >= K) break;
+      const uint32_t cq = lane < R.nclus ? m->seg_cnt[lane] : 0u;
+      if (__reduce_add_sync(kFull, cq) >= K) break;
       // fewer than K kept (the threshold above guarantees at least K): start
       // over keeping every position
       __syncthreads();
@@ -265,26 +291,28 @@ __global__ void __launch_bounds__(T, 1) listed_kernel(Params p) {
     stamp(R, kTrExact);
     bump(p, R, kCntFast);
   }
-  output_positions<T>(R, p, false, 0, K, p.row_stride, false);
+  output_positions<T>(R, p, false, 0, K, p.row_stride, R.nclus > 1);
   wait_init(R);
 }
 
-template <class S>
+template <int T, class S>
 const void* listed_ptr(int block) {
   switch (block) {
-    case 4: return reinterpret_cast<const void*>(&listed_kernel<512, 4, S>);
-    case 8: return reinterpret_cast<const void*>(&listed_kernel<512, 8, S>);
-    case 16: return reinterpret_cast<const void*>(&listed_kernel<512, 16, S>);
-    case 32: return reinterpret_cast<const void*>(&listed_kernel<512, 32, S>);
+    case 4: return reinterpret_cast<const void*>(&listed_kernel<T, 4, S>);
+    case 8: return reinterpret_cast<const void*>(&listed_kernel<T, 8, S>);
+    case 16: return reinterpret_cast<const void*>(&listed_kernel<T, 16, S>);
+    case 32: return reinterpret_cast<const void*>(&listed_kernel<T, 32, S>);
     default: return nullptr;
   }
 }
 
-const void* listed_kernel_ptr(int block, bool bf16) {
-  return bf16 ? listed_ptr<uint16_t>(block) : listed_ptr<float>(block);
+const void* listed_kernel_ptr(int threads, int block, bool bf16) {
+  if (threads == 512) return bf16 ? listed_ptr<512, uint16_t>(block) : listed_ptr<512, float>(block);
+  if (threads == 256) return bf16 ? listed_ptr<256, uint16_t>(block) : listed_ptr<256, float>(block);
+  return nullptr;
 }
 
-// Blocks one listed-kernel CTA gathers in its single register round.
-int64_t listed_round_blocks(int block) { return 512 * 8 * 4 / block; }
+// Listed blocks a row may have on the listed kernel.
+int64_t listed_round_blocks(int block) { return kListedPositions / block; }
 
 }  // namespace lt

@@ -51,10 +51,12 @@ def test_own_kept_blocks_reproduce_the_two_level_result():
         assert np.array_equal(gi, i2) and np.array_equal(gv.view(np.uint32), v2.view(np.uint32))
 
 
-@pytest.mark.parametrize("ft", [256, 512])
+@pytest.mark.parametrize("ft", [0, 256, 512])
 @pytest.mark.parametrize("block", [4, 8, 16, 32])
 @pytest.mark.parametrize("dist", ["normal", "bf16", "coarse", "special", "equal"])
 def test_small_lists(block, dist, ft):
+    """ft 0: a cluster of CTAs per row shares each list; 512: one CTA per
+    row; 256: the whole-row scan of the two-level kernel."""
     rng = np.random.default_rng(block * 31 + len(dist))
     stride = 30000
     S, L = workloads.random_rows(3, stride, seed=block + len(dist), dist=dist, lengths="ragged", min_len=0)
@@ -75,6 +77,21 @@ def test_forced_plans_and_exact_path(fc, ft):
     kw = dict(force_cluster=fc, force_threads=ft)
     parity_candidates(S.numpy(), L.numpy(), cand, 8, 512, what=f"cluster {fc}x{ft}", **kw)
     parity_candidates(S.numpy(), L.numpy(), cand, 8, 512, what=f"cluster {fc}x{ft} exact", force_exact=True, **kw)
+
+
+@pytest.mark.parametrize("rows", [1, 5, 20, 40, 80])
+def test_listed_rows_by_cluster_size(rows):
+    """The automatic plan shares a row's list over clusters of 8, 4, 2 or 1
+    CTAs as the row count grows (every cluster size once)."""
+    rng = np.random.default_rng(rows)
+    stride = 65536
+    S, L = workloads.random_rows(rows, stride, seed=rows + 60, dist="bf16", lengths="ragged", min_len=stride // 4)
+    cand = _random_lists(rng, rows, stride // 8, 2048, pads=9, repeats=40, beyond=2)
+    c = counters()
+    parity_candidates(S.numpy(), L.numpy(), cand, 8, 512, what=f"{rows} rows", counters=c)
+    cnt = c.cpu().numpy()
+    assert cnt[0] == rows and cnt[1] == 0, cnt
+    parity_candidates(S.numpy(), L.numpy(), cand[:, :300], 8, 2048, what=f"{rows} rows, k > listed positions")
 
 
 def test_empty_and_short_lists():
