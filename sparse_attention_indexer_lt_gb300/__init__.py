@@ -110,9 +110,15 @@ def _ptr(t):
 _DTYPES = {torch.float32: DTYPE_F32, torch.bfloat16: DTYPE_BF16}
 
 
+def _device_of(scores: torch.Tensor) -> torch.device:
+    """The device that runs the call: the scores' own, or for pinned host
+    scores (read by the kernel over the host link) the current one."""
+    return scores.device if scores.is_cuda else torch.device("cuda", torch.cuda.current_device())
+
+
 def _check_scores(scores: torch.Tensor):
-    if not isinstance(scores, torch.Tensor) or not scores.is_cuda:
-        raise TypeError("scores must be a CUDA tensor")
+    if not isinstance(scores, torch.Tensor) or not (scores.is_cuda or scores.is_pinned()):
+        raise TypeError("scores must be a CUDA tensor or a pinned host tensor")
     if scores.dtype not in _DTYPES:
         raise TypeError("scores must be float32 or bfloat16")
     if scores.dim() != 2:
@@ -163,7 +169,7 @@ def topk(scores: torch.Tensor, lengths: torch.Tensor | None = None, k: int = 512
     (idx int32 [rows, k], val float32 [rows, k] or None)."""
     lib = load()
     rows, n = _check_scores(scores)
-    dev = scores.device
+    dev = _device_of(scores)
     lengths = _check_lengths(lengths, rows, dev)
     out_idx = _out(out_idx, (rows, k), torch.int32, dev, "out_idx")
     if with_values:
@@ -192,7 +198,7 @@ def topk_blocked(scores: torch.Tensor, lengths: torch.Tensor | None = None, bloc
     """Two-level top-k; returns (idx [rows, k], val [rows, k] or None, blocks [rows, k_blocks] or None)."""
     lib = load()
     rows, n = _check_scores(scores)
-    dev = scores.device
+    dev = _device_of(scores)
     lengths = _check_lengths(lengths, rows, dev)
     out_idx = _out(out_idx, (rows, k), torch.int32, dev, "out_idx")
     out_val = _out(out_val, (rows, k), torch.float32, dev, "out_val") if with_values else None
@@ -220,7 +226,7 @@ def topk_candidates(scores: torch.Tensor, cand_blocks: torch.Tensor, lengths: to
     (idx [rows, k], val [rows, k] or None)."""
     lib = load()
     rows, n = _check_scores(scores)
-    dev = scores.device
+    dev = _device_of(scores)
     lengths = _check_lengths(lengths, rows, dev)
     if (not isinstance(cand_blocks, torch.Tensor) or cand_blocks.device != dev
             or cand_blocks.dtype != torch.int32 or cand_blocks.dim() != 2 or cand_blocks.shape[0] != rows

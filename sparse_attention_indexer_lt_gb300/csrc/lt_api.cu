@@ -431,6 +431,24 @@ bool rows_aligned(const void* p, int64_t row_stride, bool bf16) {
   return (reinterpret_cast<uintptr_t>(p) % (bf16 ? 8u : 16u)) == 0 && (row_stride % 4) == 0;
 }
 
+// Scores may be device memory or page-locked host memory mapped into the
+// device's address space (the kernels then read the rows over the host link,
+// which on a Grace host is NVLink-C2C). Replaces *scores with the address the
+// device uses; unregistered host memory is refused.
+lt_status resolve_scores(const void** scores, bool* host) {
+  cudaPointerAttributes a;
+  if (cudaPointerGetAttributes(&a, *scores) != cudaSuccess) return LT_ERR_CUDA;
+  *host = false;
+  if (a.type == cudaMemoryTypeHost) {
+    if (a.devicePointer == nullptr) return LT_ERR_INVALID_ARG;
+    *scores = a.devicePointer;
+    *host = true;
+  } else if (a.type == cudaMemoryTypeUnregistered) {
+    return LT_ERR_INVALID_ARG;
+  }
+  return LT_OK;
+}
+
 lt_status check_dtype(int32_t dtype) {
   return (dtype == LT_DTYPE_F32 || dtype == LT_DTYPE_BF16) ? LT_OK : LT_ERR_INVALID_ARG;
 }
@@ -448,6 +466,10 @@ lt_status lt_topk_ex(const void* scores, int32_t dtype, const int32_t* lengths, 
   if (check_dtype(dtype) != LT_OK) return LT_ERR_INVALID_ARG;
   if (force_kernel < LT_KERNEL_AUTO || force_kernel > LT_KERNEL_STREAM) return LT_ERR_INVALID_ARG;
   if (rows == 0) return LT_OK;
+  bool host = false;
+  st = resolve_scores(&scores, &host);
+  if (st != LT_OK) return st;
+  if (host && force_kernel == LT_KERNEL_STREAM) return LT_ERR_UNSUPPORTED;  // bulk copies read device memory
   const bool bf16 = dtype == LT_DTYPE_BF16;
   const bool aligned = rows_aligned(scores, row_stride, bf16);
   Plan plan;
@@ -456,6 +478,7 @@ lt_status lt_topk_ex(const void* scores, int32_t dtype, const int32_t* lengths, 
                  &plan, &dev);
   if (st != LT_OK) return st;
   lt::Params p = {};
+  p.host_scores = host ? 1 : 0;
   p.scores = scores;
   p.lengths = lengths;
   p.row_stride = row_stride;
@@ -493,10 +516,13 @@ lt_status lt_topk_blocked_ex(const void* scores, int32_t dtype, const int32_t* l
   if (st != LT_OK) return st;
   if (check_dtype(dtype) != LT_OK) return LT_ERR_INVALID_ARG;
   const bool bf16 = dtype == LT_DTYPE_BF16;
-  const bool aligned = rows_aligned(scores, row_stride, bf16);
   if (block < 1 || k_blocks < 1) return LT_ERR_INVALID_ARG;
   if (k_blocks > LT_MAX_K || block_index(block) < 0) return LT_ERR_UNSUPPORTED;
   if (rows == 0) return LT_OK;
+  bool host = false;
+  st = resolve_scores(&scores, &host);
+  if (st != LT_OK) return st;
+  const bool aligned = rows_aligned(scores, row_stride, bf16);
   // k_blocks >= k: stage B equals the plain top-k, so the stages run as two
   // independent groups of clusters (see lt_blocked.cuh); the stage-A group
   // exists only when the kept blocks are wanted.
@@ -509,6 +535,7 @@ lt_status lt_topk_blocked_ex(const void* scores, int32_t dtype, const int32_t* l
                  LT_KERNEL_AUTO, aligned, bf16, &plan, &dev);
   if (st != LT_OK) return st;
   lt::Params p = {};
+  p.host_scores = host ? 1 : 0;
   p.split = split ? 1 : 0;
   p.scores = scores;
   p.lengths = lengths;
@@ -549,11 +576,14 @@ lt_status lt_topk_candidates_ex(const void* scores, int32_t dtype, const int32_t
   if (st != LT_OK) return st;
   if (check_dtype(dtype) != LT_OK) return LT_ERR_INVALID_ARG;
   const bool bf16 = dtype == LT_DTYPE_BF16;
-  const bool aligned = rows_aligned(scores, row_stride, bf16);
   if (block < 1 || n_cand < 0 || (n_cand > 0 && cand_blocks == nullptr && rows > 0))
     return LT_ERR_INVALID_ARG;
   if (block_index(block) < 0) return LT_ERR_UNSUPPORTED;
   if (rows == 0) return LT_OK;
+  bool host = false;
+  st = resolve_scores(&scores, &host);
+  if (st != LT_OK) return st;
+  const bool aligned = rows_aligned(scores, row_stride, bf16);
   Plan plan;
   int dev = 0;
   // A list of at most one register round of blocks goes to the listed
@@ -611,6 +641,7 @@ lt_status lt_topk_candidates_ex(const void* scores, int32_t dtype, const int32_t
     if (per > (int64_t)32 * lt::kBins) return LT_ERR_UNSUPPORTED;
   }
   lt::Params p = {};
+  p.host_scores = host ? 1 : 0;
   p.external = 1;
   p.cand_blocks = cand_blocks;
   p.n_cand = n_cand;

@@ -125,6 +125,7 @@ struct Params {
   int32_t stall_polls;  // streamed kernel, tests only (0 normally): the final chunk of
                         // each CTA is never issued and every wait gives up after
                         // this many polls (see lt_test_inject)
+  int32_t host_scores;  // the scores are host memory read over the host link (no L2 bulk prefetch)
 };
 
 // ------------------------------------------------------------------ smem layout

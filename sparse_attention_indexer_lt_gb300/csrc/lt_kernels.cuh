@@ -1255,7 +1255,7 @@ __device__ __forceinline__ bool select_stage(RowT<S>& R, const Params& p, float4
         // Single-CTA rows of many rounds (the batched rows, three CTAs per
         // SM): the whole slice is asked into L2 at once, so the rounds the
         // registers load later come from L2 while HBM keeps streaming.
-        if (R.rounds > 2 && threadIdx.x < 32) prefetch_slice_l2(R);
+        if (R.rounds > 2 && threadIdx.x < 32 && p.host_scores == 0) prefetch_slice_l2(R);
       }
     }
   }

@@ -102,3 +102,50 @@ def test_streamed_kernel_wait_gives_up_and_returns(lib):
     oi, ov = oracle.topk(S.numpy(), None, 128)
     assert np.array_equal(idx.cpu().numpy(), oi)
     assert c.cpu().numpy()[4] == 0
+
+
+def test_pinned_host_scores_read_in_place(lib):
+    """Scores in page-locked host memory are read by the kernels in place (over
+    the host link): every entry point and both score types give the oracle's
+    answer; unregistered host memory is refused; the streamed kernel refuses
+    host scores."""
+    import sparse_attention_indexer_lt_gb300 as lt
+    from _gpu import assert_same
+    rows, stride, k = 5, 70000, 300
+    S, L = workloads.random_rows(rows, stride, seed=47, dist="tail", lengths="ragged", min_len=1)
+    Sn, Ln = S.numpy(), L.numpy()
+    host = S.pin_memory()
+    l = L.cuda()
+    gi, gv = lt.topk(host, l, k)
+    oi, ov = oracle.topk(Sn, Ln, k)
+    assert_same(gi.cpu().numpy(), gv.cpu().numpy(), oi, ov, "pinned host, top-k")
+    gi, gv = lt.topk(host, l, k, force_exact=True)
+    assert_same(gi.cpu().numpy(), gv.cpu().numpy(), oi, ov, "pinned host, top-k exact")
+    # many rows of several rounds (the batched 256-thread path, whose L2 prefetch host rows skip)
+    S4, L4 = workloads.random_rows(400, 20000, seed=48, dist="normal", lengths="ragged", min_len=1)
+    gi, gv = lt.topk(S4.pin_memory(), L4.cuda(), 512)
+    oi4, ov4 = oracle.topk(S4.numpy(), L4.numpy(), 512)
+    assert_same(gi.cpu().numpy(), gv.cpu().numpy(), oi4, ov4, "pinned host, batched rows")
+    gi, gv, gb = lt.topk_blocked(host, l, 8, 512, k)
+    oi, ov, ob = oracle.topk_blocked(Sn, Ln, 8, 512, k)
+    assert_same(gi.cpu().numpy(), gv.cpu().numpy(), oi, ov, "pinned host, two-level")
+    assert np.array_equal(gb.cpu().numpy(), ob)
+    cand = np.sort(np.random.default_rng(49).choice(stride // 8, (rows, 900), replace=True), axis=1).astype(np.int32)
+    gi, gv = lt.topk_candidates(host, torch.as_tensor(cand).cuda(), l, 8, k)
+    oi, ov = oracle.topk_candidates(Sn, Ln, cand, 8, k)
+    assert_same(gi.cpu().numpy(), gv.cpu().numpy(), oi, ov, "pinned host, listed candidates")
+    T = workloads.to_bf16(S)
+    gi, gv = lt.topk(T.pin_memory(), l, k)
+    oi, ov = oracle.topk_bf16(workloads.bf16_bits(T), Ln, k)
+    assert_same(gi.cpu().numpy(), gv.cpu().numpy(), oi, ov, "pinned host, bf16")
+    # unregistered host memory (a numpy buffer) and the streamed kernel
+    out = torch.empty(rows, k, dtype=torch.int32, device="cuda")
+    arr = np.ascontiguousarray(Sn)
+    st = lib.lt_topk_ex(ctypes.c_void_p(arr.ctypes.data), 0, P(l), rows, stride, k, P(out), None, 0, 0, 0, 0,
+                        None, None, None)
+    assert st == 1
+    st = lib.lt_topk_ex(P(host), 0, P(l), rows, stride, k, P(out), None, 0, 0, 0, 2, None, None, None)
+    assert st == 2
+    torch.cuda.synchronize()
+    with pytest.raises(TypeError):
+        lt.topk(S, l, k)  # a pageable CPU tensor
