@@ -164,17 +164,6 @@ class Clocks:
 
 # ------------------------------------------------------------------ timing helpers
 
-def listed_plan(rows: int) -> dict:
-    """The listed-candidate launch (display only; the library's planner decides): a
-    cluster of up to 8 CTAs of 256 threads per row while rows x 2 x cluster fit the
-    SMs, one 512-thread CTA per row otherwise."""
-    sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
-    c = 1
-    while c < 8 and rows * c * 2 <= sms:
-        c *= 2
-    return {"kernel": "listed", "cluster": c, "threads": 256 if c > 1 else 512, "grid": rows * c}
-
-
 def timed_steps(launch, steps: int, warmup: int, world: int) -> float:
     """The timed region: `warmup` untimed steps, then exactly `steps` steps
     launched back to back between two CUDA events on the launching stream,
@@ -390,7 +379,7 @@ def bench_batched(lt, dev, args, world, peak, L2):
             out[-1]["us_per_row_note"] = "one row: latency per call, back to back"
         if listed:
             out[-1]["bytes"] = "listed blocks' scores + the list"
-            out[-1]["plan"] = listed_plan(w.rows)
+            out[-1]["plan"] = lt.plan_candidates(w.rows, w.row_stride, w.block, cand.shape[1], w.k, dtype=S.dtype)
         if not args.no_cpu and world == 1 and dtype == "f32":
             out[-1]["cpu_baseline"] = cpu_batched(name, S, L, w, None if cand is None else cand.cpu())
         del copies, base
@@ -483,7 +472,7 @@ def bench_only(args, world):
     return {"workload": args.only, "dtype": args.dtype, "steps": args.steps, "step_us": round(kern * 1000, 3),
             "read_bytes": nbytes,
             "hbm_gbs": round(nbytes / (kern * 1e-3) / 1e9, 1), "copies": ncopies,
-            "plan": (listed_plan(w.rows) if listed else
+            "plan": (lt.plan_candidates(w.rows, w.row_stride, w.block, cand.shape[1], w.k, dtype=S.dtype) if listed else
                      lt.plan(w.rows, w.row_stride, w.k, blocked=w.blocked, k_blocks=w.k_blocks,
                              force_kernel=0 if w.blocked else KERNEL_IDS[args.kernel],
                              force_cluster=args.force_cluster, force_threads=args.force_threads))}
@@ -513,15 +502,13 @@ def bench_trace(args):
     listed = args.trace.startswith("c6")
     cand = workloads.listed_blocks(args.trace).to(dev) if listed else None
     kid = 0 if (w.blocked or listed) else KERNEL_IDS[args.kernel]
-    if listed and args.force_cluster in (0, 1) and args.force_threads in (0, 512):
-        # a list of at most one register round of blocks takes the listed kernel: one CTA per row
-        pl = listed_plan(w.rows)
+    if listed:
+        pl = lt.plan_candidates(w.rows, w.row_stride, w.block, cand.shape[1], w.k, dtype=S.dtype,
+                                force_cluster=args.force_cluster, force_threads=args.force_threads)
     else:
         pl = lt.plan(w.rows, w.row_stride, w.k, blocked=w.blocked or listed, k_blocks=1 if listed else w.k_blocks,
                      force_cluster=args.force_cluster, force_threads=args.force_threads, force_kernel=kid)
-    # persistent kernels: the first row of each CTA is traced; a listed launch
-    # gets room for its largest cluster (8 CTAs per row)
-    ctas = max(w.rows * 8, pl["grid"]) if listed else pl["grid"]
+    ctas = pl["grid"]  # persistent kernels: the first row of each CTA is traced
     tr = torch.full((ctas, 16), -1, dtype=torch.int64, device=dev)
     kw = dict(force_cluster=args.force_cluster, force_threads=args.force_threads)
     for i in range(max(3, args.warmup) + 1):

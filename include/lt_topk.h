@@ -180,6 +180,9 @@ lt_status lt_topk_candidates_bf16(const uint16_t* scores, const int32_t* lengths
 /* Streamed: 16-byte aligned rows move into a shared-memory ring by bulk
  * copies; persistent CTAs walk the rows and prefetch the next one. */
 #define LT_KERNEL_STREAM 2
+/* Listed: the listed-candidate kernel, which reads only the listed blocks
+ * (reported by lt_topk_candidates_plan; not a force_kernel value). */
+#define LT_KERNEL_LISTED 3
 
 /*
  * Launch-plan control, for tests and measurement (not needed for normal use).
@@ -269,7 +272,7 @@ lt_status lt_topk_candidates_ex(const void* scores, int32_t dtype, const int32_t
  * *info (host memory, owned by the caller).
  */
 typedef struct lt_plan_info {
-  int32_t kernel;           /* LT_KERNEL_RESIDENT or LT_KERNEL_STREAM */
+  int32_t kernel;           /* LT_KERNEL_RESIDENT, LT_KERNEL_STREAM or LT_KERNEL_LISTED */
   int32_t cluster_size;     /* CTAs that share one row */
   int32_t threads_per_cta;
   int32_t smem_bytes;       /* dynamic shared memory per CTA */
@@ -282,6 +285,13 @@ lt_status lt_topk_plan(int32_t rows, int64_t row_stride, int32_t k, int32_t bloc
                        int32_t block, int32_t k_blocks, int32_t force_cluster,
                        int32_t force_threads, int32_t force_kernel, int32_t aligned,
                        lt_plan_info* info);
+/* The launch lt_topk_candidates_ex would make for n_cand listed blocks per
+ * row (dtype LT_DTYPE_F32 or LT_DTYPE_BF16): kernel LT_KERNEL_LISTED with its
+ * cluster and grid, or the whole-row scan's plan (LT_KERNEL_RESIDENT). */
+lt_status lt_topk_candidates_plan(int32_t rows, int64_t row_stride, int32_t block, int32_t n_cand,
+                                  int32_t k, int32_t dtype, int32_t force_cluster,
+                                  int32_t force_threads, int32_t force_exact, int32_t aligned,
+                                  lt_plan_info* info);
 
 /* Static description of a status code. */
 const char* lt_status_string(lt_status status);

@@ -20,14 +20,15 @@ from pathlib import Path
 import torch
 
 __all__ = ["topk", "topk_blocked", "topk_candidates", "compress", "compress_decode", "plan", "DTYPE_F32", "DTYPE_BF16", "load", "library_path", "LtError", "NUM_COUNTERS",
-           "status_string", "version", "PlanInfo", "KERNEL_AUTO", "KERNEL_RESIDENT", "KERNEL_STREAM"]
+           "status_string", "version", "PlanInfo", "KERNEL_AUTO", "KERNEL_RESIDENT", "KERNEL_STREAM",
+           "KERNEL_LISTED", "plan_candidates"]
 
 _LIB_PATH = Path(__file__).resolve().parent / "liblt_topk.so"
 _lib = None
 NUM_COUNTERS = 7
 DTYPE_F32, DTYPE_BF16 = 0, 1
-KERNEL_AUTO, KERNEL_RESIDENT, KERNEL_STREAM = 0, 1, 2
-_KERNEL_NAMES = {KERNEL_RESIDENT: "resident", KERNEL_STREAM: "stream"}
+KERNEL_AUTO, KERNEL_RESIDENT, KERNEL_STREAM, KERNEL_LISTED = 0, 1, 2, 3
+_KERNEL_NAMES = {KERNEL_RESIDENT: "resident", KERNEL_STREAM: "stream", KERNEL_LISTED: "listed"}
 
 
 class PlanInfo(ctypes.Structure):
@@ -81,6 +82,8 @@ def load() -> ctypes.CDLL:
         f.restype = ctypes.c_int
     lib.lt_topk_plan.argtypes = [i32, i64, i32, i32, i32, i32, i32, i32, i32, i32, vp]
     lib.lt_topk_plan.restype = ctypes.c_int
+    lib.lt_topk_candidates_plan.argtypes = [i32, i64, i32, i32, i32, i32, i32, i32, i32, i32, vp]
+    lib.lt_topk_candidates_plan.restype = ctypes.c_int
     lib.lt_status_string.argtypes = [ctypes.c_int]
     lib.lt_status_string.restype = ctypes.c_char_p
     lib.lt_compress.argtypes = [vp, vp, vp, vp, i32, i64, i32, i32, vp, i32, vp]
@@ -323,6 +326,26 @@ def plan(rows: int, row_stride: int, k: int, *, blocked: bool = False, block: in
                               int(bool(aligned)), ctypes.byref(info))
     if st != 0:
         raise LtError("lt_topk_plan", st)
+    return {"kernel": _KERNEL_NAMES.get(info.kernel, str(info.kernel)), "cluster": info.cluster_size,
+            "threads": info.threads_per_cta, "smem": info.smem_bytes, "grid": info.grid_ctas,
+            "stages": info.ring_stages, "one_round": bool(info.one_round)}
+
+
+def plan_candidates(rows: int, row_stride: int, block: int, n_cand: int, k: int, *,
+                    dtype: torch.dtype = torch.float32, force_cluster: int = 0, force_threads: int = 0,
+                    force_exact: bool = False, aligned: bool = True, device: int | None = None) -> dict:
+    """The launch topk_candidates would make ('kernel' is 'listed' for the kernel
+    that reads only the listed blocks); keys as for plan()."""
+    lib = load()
+    info = PlanInfo()
+    if dtype not in _DTYPES:
+        raise ValueError(f"scores must be float32 or bfloat16, got {dtype}")
+    with torch.cuda.device(device if device is not None else torch.cuda.current_device()):
+        st = lib.lt_topk_candidates_plan(int(rows), int(row_stride), int(block), int(n_cand), int(k),
+                                         _DTYPES[dtype], int(force_cluster), int(force_threads),
+                                         int(bool(force_exact)), int(bool(aligned)), ctypes.byref(info))
+    if st != 0:
+        raise LtError("lt_topk_candidates_plan", st)
     return {"kernel": _KERNEL_NAMES.get(info.kernel, str(info.kernel)), "cluster": info.cluster_size,
             "threads": info.threads_per_cta, "smem": info.smem_bytes, "grid": info.grid_ctas,
             "stages": info.ring_stages, "one_round": bool(info.one_round)}

@@ -380,6 +380,71 @@ lt_status make_stream_plan(int32_t rows, int64_t row_stride, int32_t k, int32_t 
   }
 }
 
+// The listed-candidate call's launch: the listed kernel (reads only the
+// listed blocks) or role 3 of the two-level kernel (whole-row scan). Sets
+// *listed accordingly.
+lt_status make_candidates_plan(int32_t rows, int64_t row_stride, int32_t block, int32_t n_cand, int32_t k,
+                               bool bf16, bool aligned, int32_t force_cluster, int32_t force_threads,
+                               int32_t force_exact, Plan* plan, int* dev, bool* listed) {
+  lt_status st = LT_OK;
+  // A list of at most one register round of blocks goes to the listed
+  // kernel, which reads only those blocks; longer lists, forced cluster
+  // shapes and force_exact scan whole rows with the two-level kernel.
+  bool gathered = force_exact == 0 && (force_cluster == 0 || force_cluster == 1) &&
+                  (force_threads == 0 || force_threads == kWideThreads) &&
+                  (int64_t)n_cand <= lt::listed_round_blocks(block);
+  if (gathered) {
+    DeviceInfo* di = nullptr;
+    st = device_info(&di, dev);
+    if (st != LT_OK) return st;
+    // a row's scattered block reads spread over a cluster of up to 8 CTAs
+    // (256 threads each) while the rows' clusters still fit the SMs once;
+    // rows enough to fill the SMs take one 512-thread CTA each
+    // (rows too long for a bitmap of their blocks build the id list in a
+    // hash set, in an order the CTAs of a cluster would not agree on: one CTA)
+    int c = 1;
+    const bool bitmap = (row_stride + block - 1) / block <= (int64_t)32 * lt::kBins;
+    if (force_cluster == 0 && force_threads == 0 && bitmap)
+      while (c < 8 && (int64_t)rows * c * 2 <= di->sms) c *= 2;
+    const uint32_t sel_cap = next_pow2(k < 32 ? 32u : (uint32_t)k);
+    for (;; c /= 2) {
+      const int threads = c > 1 ? kNarrowThreads : kWideThreads;
+      plan->threads = threads;
+      plan->cluster = c;
+      plan->grid = rows * c;
+      // every CTA's segment holds every position of its share of the list
+      plan->cap = (uint32_t)lt::kListedPositions;
+      plan->seg_shift = 0;
+      while ((1u << plan->seg_shift) < plan->cap / (uint32_t)c) ++plan->seg_shift;
+      plan->wstage = (uint32_t)threads * 16u * (uint32_t)lt::kStageF4;
+      plan->sel_cap = sel_cap;
+      plan->func = lt::listed_kernel_ptr(threads, block, bf16);
+      plan->smem = lt::make_layout(c > 1, plan->cap, plan->sel_cap, plan->wstage).total;
+      gathered = plan->func != nullptr && (int)plan->smem <= di->smem_optin;
+      if (!gathered) {
+        if (c == 1) break;
+        gathered = true;  // try a smaller cluster
+        continue;
+      }
+      const int slot = (bf16 ? kTypeSlots : 0) + (c > 1 ? 19 : 14) + block_index(block);
+      st = prepare_kernel(*dev, slot, plan->func, plan->smem, c);
+      if (st != LT_OK) return st;
+      if (c == 1 || active_clusters(*dev, slot, plan->func, c, threads, plan->smem) >= rows) break;
+    }
+  }
+  if (!gathered) {
+    st = make_plan(rows, row_stride, k, true, block, 1, force_cluster, force_threads, LT_KERNEL_AUTO,
+                   aligned, bf16, plan, dev);
+    if (st != LT_OK) return st;
+    // every CTA holds a bitmap of its slice's blocks in kBins words
+    int64_t per = (row_stride + plan->cluster - 1) / plan->cluster;
+    per = (per + block - 1) / block;
+    if (per > (int64_t)32 * lt::kBins) return LT_ERR_UNSUPPORTED;
+  }
+  *listed = gathered;
+  return LT_OK;
+}
+
 lt_status check_common(const void* scores, int32_t rows, int64_t row_stride, int32_t k,
                        const int32_t* out_idx, int32_t force_cluster, int32_t force_threads) {
   if (rows < 0 || row_stride < 1 || k < 1) return LT_ERR_INVALID_ARG;
@@ -586,60 +651,10 @@ lt_status lt_topk_candidates_ex(const void* scores, int32_t dtype, const int32_t
   const bool aligned = rows_aligned(scores, row_stride, bf16);
   Plan plan;
   int dev = 0;
-  // A list of at most one register round of blocks goes to the listed
-  // kernel, which reads only those blocks; longer lists, forced cluster
-  // shapes and force_exact scan whole rows with the two-level kernel.
-  bool gathered = force_exact == 0 && (force_cluster == 0 || force_cluster == 1) &&
-                  (force_threads == 0 || force_threads == kWideThreads) &&
-                  (int64_t)n_cand <= lt::listed_round_blocks(block);
-  if (gathered) {
-    DeviceInfo* di = nullptr;
-    st = device_info(&di, &dev);
-    if (st != LT_OK) return st;
-    // a row's scattered block reads spread over a cluster of up to 8 CTAs
-    // (256 threads each) while the rows' clusters still fit the SMs once;
-    // rows enough to fill the SMs take one 512-thread CTA each
-    // (rows too long for a bitmap of their blocks build the id list in a
-    // hash set, in an order the CTAs of a cluster would not agree on: one CTA)
-    int c = 1;
-    const bool bitmap = (row_stride + block - 1) / block <= (int64_t)32 * lt::kBins;
-    if (force_cluster == 0 && force_threads == 0 && bitmap)
-      while (c < 8 && (int64_t)rows * c * 2 <= di->sms) c *= 2;
-    const uint32_t sel_cap = next_pow2(k < 32 ? 32u : (uint32_t)k);
-    for (;; c /= 2) {
-      const int threads = c > 1 ? kNarrowThreads : kWideThreads;
-      plan.threads = threads;
-      plan.cluster = c;
-      plan.grid = rows * c;
-      // every CTA's segment holds every position of its share of the list
-      plan.cap = (uint32_t)lt::kListedPositions;
-      plan.seg_shift = 0;
-      while ((1u << plan.seg_shift) < plan.cap / (uint32_t)c) ++plan.seg_shift;
-      plan.wstage = (uint32_t)threads * 16u * (uint32_t)lt::kStageF4;
-      plan.sel_cap = sel_cap;
-      plan.func = lt::listed_kernel_ptr(threads, block, bf16);
-      plan.smem = lt::make_layout(c > 1, plan.cap, plan.sel_cap, plan.wstage).total;
-      gathered = plan.func != nullptr && (int)plan.smem <= di->smem_optin;
-      if (!gathered) {
-        if (c == 1) break;
-        gathered = true;  // try a smaller cluster
-        continue;
-      }
-      const int slot = (bf16 ? kTypeSlots : 0) + (c > 1 ? 19 : 14) + block_index(block);
-      st = prepare_kernel(dev, slot, plan.func, plan.smem, c);
-      if (st != LT_OK) return st;
-      if (c == 1 || active_clusters(dev, slot, plan.func, c, threads, plan.smem) >= rows) break;
-    }
-  }
-  if (!gathered) {
-    st = make_plan(rows, row_stride, k, true, block, 1, force_cluster, force_threads, LT_KERNEL_AUTO,
-                   aligned, bf16, &plan, &dev);
-    if (st != LT_OK) return st;
-    // every CTA holds a bitmap of its slice's blocks in kBins words
-    int64_t per = (row_stride + plan.cluster - 1) / plan.cluster;
-    per = (per + block - 1) / block;
-    if (per > (int64_t)32 * lt::kBins) return LT_ERR_UNSUPPORTED;
-  }
+  bool listed = false;
+  st = make_candidates_plan(rows, row_stride, block, n_cand, k, bf16, aligned, force_cluster, force_threads,
+                            force_exact, &plan, &dev, &listed);
+  if (st != LT_OK) return st;
   lt::Params p = {};
   p.host_scores = host ? 1 : 0;
   p.external = 1;
@@ -698,6 +713,34 @@ lt_status lt_topk_plan(int32_t rows, int64_t row_stride, int32_t k, int32_t bloc
                            false, &plan, &dev);
   if (st != LT_OK) return st;
   info->kernel = plan.kernel;
+  info->cluster_size = plan.cluster;
+  info->threads_per_cta = plan.threads;
+  info->smem_bytes = (int32_t)plan.smem;
+  info->grid_ctas = plan.grid;
+  info->ring_stages = (int32_t)plan.stages;
+  info->one_round = plan.one_round ? 1 : 0;
+  return LT_OK;
+}
+
+lt_status lt_topk_candidates_plan(int32_t rows, int64_t row_stride, int32_t block, int32_t n_cand, int32_t k,
+                                  int32_t dtype, int32_t force_cluster, int32_t force_threads,
+                                  int32_t force_exact, int32_t aligned, lt_plan_info* info) {
+  if (rows < 1 || row_stride < 1 || k < 1 || n_cand < 0 || block < 1 || info == nullptr) return LT_ERR_INVALID_ARG;
+  if (check_dtype(dtype) != LT_OK) return LT_ERR_INVALID_ARG;
+  if (!(force_threads == 0 || force_threads == kNarrowThreads || force_threads == kWideThreads))
+    return LT_ERR_INVALID_ARG;
+  if (!(force_cluster == 0 || force_cluster == 1 || force_cluster == 2 || force_cluster == 4 ||
+        force_cluster == 8 || force_cluster == 16))
+    return LT_ERR_INVALID_ARG;
+  if (block_index(block) < 0 || k > LT_MAX_K || row_stride > LT_MAX_ROW_STRIDE) return LT_ERR_UNSUPPORTED;
+  Plan plan;
+  int dev = 0;
+  bool listed = false;
+  const lt_status st = make_candidates_plan(rows, row_stride, block, n_cand, k, dtype == LT_DTYPE_BF16,
+                                            aligned != 0 && row_stride % 4 == 0, force_cluster, force_threads,
+                                            force_exact, &plan, &dev, &listed);
+  if (st != LT_OK) return st;
+  info->kernel = listed ? LT_KERNEL_LISTED : plan.kernel;
   info->cluster_size = plan.cluster;
   info->threads_per_cta = plan.threads;
   info->smem_bytes = (int32_t)plan.smem;

@@ -195,10 +195,10 @@ struct KeepAll {
 
 // Stage B of the two-level kernel: keep a slot (one block) when its block
 // composite is >= the stage-A threshold composite Tc.
-// Keep the positions of listed blocks: bit b of bits[b >> 5] marks block b of
-// the row; blocks at or past nbits are not listed.
+// Keep the positions of listed blocks: bits covers blocks [b0, b0 + nbits) of
+// the row (this CTA's slice), bit i of bits[i >> 5] marking block b0 + i;
+// blocks outside it are not listed.
 template <int T, int U, int W>
-// bits covers blocks [b0, b0 + nbits) of the row (this CTA's slice).
 struct KeepListed {
   static constexpr bool kAll = false;
   const uint32_t* bits;

@@ -29,7 +29,7 @@ def test_header_declares_the_entry_points():
     for n in ["lt_topk", "lt_topk_blocked", "lt_topk_ex", "lt_topk_blocked_ex", "lt_topk_candidates",
               "lt_topk_candidates_ex", "lt_topk_plan", "lt_status_string", "lt_version", "lt_topk_bf16",
               "lt_topk_blocked_bf16", "lt_topk_candidates_bf16", "lt_test_inject", "lt_compress",
-              "lt_compress_decode"]:
+              "lt_compress_decode", "lt_topk_candidates_plan"]:
         assert n in names
 
 
@@ -133,6 +133,13 @@ def test_plan_rejects_bad_arguments(lib):
     assert f(1, 64, 4, 0, 4, 1, 0, 0, 0, 1, None) == 1                    # no output struct
     assert f(1, 64, 4, 0, 4, 1, 0, 0, 7, 1, ctypes.byref(info)) == 1      # unknown kernel
     assert f(1, 64, 4, 1, 6, 4, 0, 0, 0, 1, ctypes.byref(info)) == 2      # block unsupported
+    g = lib.lt_topk_candidates_plan
+    assert g(0, 64, 8, 4, 4, 0, 0, 0, 0, 1, ctypes.byref(info)) == 1      # rows < 1
+    assert g(1, 64, 8, -1, 4, 0, 0, 0, 0, 1, ctypes.byref(info)) == 1     # negative list length
+    assert g(1, 64, 8, 4, 4, 5, 0, 0, 0, 1, ctypes.byref(info)) == 1      # unknown dtype
+    assert g(1, 64, 8, 4, 4, 0, 3, 0, 0, 1, ctypes.byref(info)) == 1      # cluster size 3
+    assert g(1, 64, 6, 4, 4, 0, 0, 0, 0, 1, ctypes.byref(info)) == 2      # block unsupported
+    assert g(1, 64, 8, 4, 4, 0, 0, 0, 0, 1, None) == 1                    # no output struct
 
 
 def test_valid_calls_without_a_device_report_a_cuda_error(lib):

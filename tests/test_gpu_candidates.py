@@ -147,3 +147,19 @@ def test_long_lists_on_rows_longer_than_a_bitmap():
     # one CTA would need a bitmap of 131072 blocks: refused
     with pytest.raises(lt.LtError):
         lt.topk_candidates(S.cuda(), torch.as_tensor(lists).cuda(), L.cuda(), block, 512, force_cluster=1)
+
+
+def test_listed_plan_query():
+    """lt_topk_candidates_plan reports the launch the call makes."""
+    import sparse_attention_indexer_lt_gb300 as lt
+    pl = lt.plan_candidates(16, 262144, 8, 2048, 512)
+    assert pl["kernel"] == "listed" and pl["cluster"] in (2, 4, 8) and pl["threads"] == 256, pl
+    assert pl["grid"] == 16 * pl["cluster"], pl
+    pl = lt.plan_candidates(200, 262144, 8, 2048, 512)
+    assert pl["kernel"] == "listed" and pl["cluster"] == 1 and pl["threads"] == 512, pl
+    pl = lt.plan_candidates(16, 262144, 8, 2048, 512, force_cluster=2)
+    assert pl["kernel"] == "resident" and pl["cluster"] == 2, pl  # the whole-row scan
+    pl = lt.plan_candidates(16, 262144, 8, 5000, 512)
+    assert pl["kernel"] == "resident", pl  # longer than one register round of blocks
+    pl = lt.plan_candidates(3, 1 << 20, 4, 100, 512)
+    assert pl["kernel"] == "listed" and pl["cluster"] == 1, pl  # hash-set rows: one CTA each
