@@ -547,11 +547,12 @@ def bench_torch_topk(x, k, args, world):
 
 def bench_e2e(lt, S, w, dev, args, world):
     """The headline step through the public API with host buffers: the row from
-    pinned host memory, the selection, and indices and values back to pinned
-    host memory in one copy (both outputs share one device buffer). The kernel
-    reads the pinned row in place over the host link (NVLink-C2C on this Grace
-    host); the same step with the row first staged into device memory by a
-    copy is timed too and reported beside it. Each step is captured once in a
+    pinned host memory, the selection, and indices and values in pinned host
+    memory. The kernel reads the pinned row and writes the pinned outputs in
+    place over the host link (NVLink-C2C on this Grace host); the same step
+    with the row first copied into device memory and the outputs copied back
+    (one copy: both share one device buffer) is timed too and reported beside
+    it. Each step is captured once in a
     CUDA graph and replayed, as a decode loop would run it; if capture fails,
     the same calls run eagerly."""
     host = S.pin_memory()
@@ -560,9 +561,11 @@ def bench_e2e(lt, S, w, dev, args, world):
     oi, ov = out[0], out[1].view(torch.float32)
     hout = torch.empty(2, w.rows, w.k, dtype=torch.int32).pin_memory()
 
+    hoi, hov = hout[0], hout[1].view(torch.float32)
+
     def in_place(_):
-        lt.topk(host, None, w.k, out_idx=oi, out_val=ov)
-        hout.copy_(out, non_blocking=True)
+        # the kernel reads the pinned row and writes the pinned outputs in place
+        lt.topk(host, None, w.k, out_idx=hoi, out_val=hov)
 
     def staged(_):
         dev_in.copy_(host, non_blocking=True)
@@ -611,9 +614,10 @@ def bench_e2e(lt, S, w, dev, args, world):
     return {"value": us, "unit": "µs/row",
             "h2d_bytes_per_step": host.numel() * 4, "d2h_bytes_per_step": 8 * w.rows * w.k,
             "staged_copy_value": us_staged,
-            "note": f"pinned host row read in place by the kernel over the host link, lt.topk, indices and "
-                    f"values -> pinned host (one copy); {mode}; host launch overhead included. "
-                    f"staged_copy_value: the row first copied to device memory ({mode_staged})"}
+            "note": f"lt.topk reading the pinned host row and writing indices and values to pinned host "
+                    f"memory in place over the host link; {mode}; host launch overhead included. "
+                    f"staged_copy_value: the row copied to device memory and the results copied back "
+                    f"({mode_staged})"}
 
 
 def cpu_baseline(S, w, seconds):

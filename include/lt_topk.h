@@ -21,14 +21,15 @@
  *   - the k outputs of a row are written in that rank order.
  *
  * Memory. Every pointer argument is DEVICE memory owned by the caller, with
- * one exception: scores may also be page-locked host memory mapped into the
- * device's address space (cudaHostAlloc, or cudaHostRegister with mapping;
- * mapped by default under unified addressing), which the kernels then read
- * over the host link -- NVLink-C2C on a Grace host -- instead of from a
- * staged device copy. Other host memory returns LT_ERR_INVALID_ARG, and the
- * streamed kernel (LT_KERNEL_STREAM) returns LT_ERR_UNSUPPORTED for host
- * scores. The library allocates nothing, keeps no per-call state and never
- * synchronises the stream. Layouts are row-major:
+ * one exception: scores, lengths, cand_blocks and the outputs may also be
+ * page-locked host memory mapped into the device's address space
+ * (cudaHostAlloc, or cudaHostRegister with mapping; mapped by default under
+ * unified addressing), which the kernels then read or write over the host
+ * link -- NVLink-C2C on a Grace host -- without staging copies (counters and
+ * trace stay device memory). Other host memory returns LT_ERR_INVALID_ARG,
+ * and the streamed kernel (LT_KERNEL_STREAM) returns LT_ERR_UNSUPPORTED for
+ * host scores. The library allocates nothing, keeps no per-call state and
+ * never synchronises the stream. Layouts are row-major:
  *   scores      float  [rows][row_stride]; row r is read on [0, L_r) only
  *               (the _bf16 calls: uint16_t bf16 bit patterns, same layout)
  *   lengths     int32  [rows] or NULL; L_r = clamp(lengths[r], 0, row_stride),

@@ -136,11 +136,16 @@ def _check_scores(scores: torch.Tensor):
     return rows, n
 
 
+def _usable(t: torch.Tensor, device: torch.device) -> bool:
+    """On the call's device, or page-locked host memory the kernels reach over the host link."""
+    return t.device == device or (t.device.type == "cpu" and t.is_pinned())
+
+
 def _check_lengths(lengths, rows, device):
     if lengths is None:
         return None
-    if not isinstance(lengths, torch.Tensor) or lengths.device != device:
-        raise TypeError("lengths must be a tensor on the same device as scores")
+    if not isinstance(lengths, torch.Tensor) or not _usable(lengths, device):
+        raise TypeError("lengths must be a tensor on the scores' device or in pinned host memory")
     if lengths.dtype != torch.int32 or lengths.numel() != rows or not lengths.is_contiguous():
         raise ValueError("lengths must be a contiguous int32 tensor with one entry per row")
     return lengths
@@ -149,8 +154,9 @@ def _check_lengths(lengths, rows, device):
 def _out(t, shape, dtype, device, name):
     if t is None:
         return torch.empty(shape, dtype=dtype, device=device)
-    if t.dtype != dtype or tuple(t.shape) != tuple(shape) or t.device != device or not t.is_contiguous():
-        raise ValueError(f"{name} must be a contiguous {dtype} tensor of shape {tuple(shape)} on {device}")
+    if t.dtype != dtype or tuple(t.shape) != tuple(shape) or not _usable(t, device) or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous {dtype} tensor of shape {tuple(shape)} on {device} "
+                         "or in pinned host memory")
     return t
 
 
@@ -231,10 +237,11 @@ def topk_candidates(scores: torch.Tensor, cand_blocks: torch.Tensor, lengths: to
     rows, n = _check_scores(scores)
     dev = _device_of(scores)
     lengths = _check_lengths(lengths, rows, dev)
-    if (not isinstance(cand_blocks, torch.Tensor) or cand_blocks.device != dev
+    if (not isinstance(cand_blocks, torch.Tensor) or not _usable(cand_blocks, dev)
             or cand_blocks.dtype != torch.int32 or cand_blocks.dim() != 2 or cand_blocks.shape[0] != rows
             or not cand_blocks.is_contiguous()):
-        raise ValueError("cand_blocks must be a contiguous int32 tensor [rows, n_cand] on the scores' device")
+        raise ValueError("cand_blocks must be a contiguous int32 tensor [rows, n_cand] on the scores' device "
+                         "or in pinned host memory")
     out_idx = _out(out_idx, (rows, k), torch.int32, dev, "out_idx")
     out_val = _out(out_val, (rows, k), torch.float32, dev, "out_val") if with_values else None
     counters = _counters(counters, dev)

@@ -496,22 +496,38 @@ bool rows_aligned(const void* p, int64_t row_stride, bool bf16) {
   return (reinterpret_cast<uintptr_t>(p) % (bf16 ? 8u : 16u)) == 0 && (row_stride % 4) == 0;
 }
 
-// Scores may be device memory or page-locked host memory mapped into the
-// device's address space (the kernels then read the rows over the host link,
-// which on a Grace host is NVLink-C2C). Replaces *scores with the address the
-// device uses; unregistered host memory is refused.
-lt_status resolve_scores(const void** scores, bool* host) {
-  cudaPointerAttributes a;
-  if (cudaPointerGetAttributes(&a, *scores) != cudaSuccess) return LT_ERR_CUDA;
+// A data pointer may be device memory or page-locked host memory mapped into
+// the device's address space (the kernels then reach it over the host link,
+// which on a Grace host is NVLink-C2C). Replaces *ptr with the address the
+// device uses; unregistered host memory is refused. nullptr stays nullptr.
+template <class P>
+lt_status resolve_ptr(P** ptr, bool* host) {
   *host = false;
+  if (*ptr == nullptr) return LT_OK;
+  cudaPointerAttributes a;
+  if (cudaPointerGetAttributes(&a, static_cast<const void*>(*ptr)) != cudaSuccess) return LT_ERR_CUDA;
   if (a.type == cudaMemoryTypeHost) {
     if (a.devicePointer == nullptr) return LT_ERR_INVALID_ARG;
-    *scores = a.devicePointer;
+    *ptr = static_cast<P*>(a.devicePointer);
     *host = true;
   } else if (a.type == cudaMemoryTypeUnregistered) {
     return LT_ERR_INVALID_ARG;
   }
   return LT_OK;
+}
+
+// The scores, lengths, lists and outputs of a call (counters and trace stay
+// device memory).
+lt_status resolve_data(const void** scores, bool* host_scores, const int32_t** lengths,
+                       const int32_t** cand_blocks, int32_t** out_idx, float** out_val, int32_t** out_blocks) {
+  bool h = false;
+  lt_status st = resolve_ptr(scores, host_scores);
+  if (st == LT_OK) st = resolve_ptr(lengths, &h);
+  if (st == LT_OK && cand_blocks != nullptr) st = resolve_ptr(cand_blocks, &h);
+  if (st == LT_OK) st = resolve_ptr(out_idx, &h);
+  if (st == LT_OK && out_val != nullptr) st = resolve_ptr(out_val, &h);
+  if (st == LT_OK && out_blocks != nullptr) st = resolve_ptr(out_blocks, &h);
+  return st;
 }
 
 lt_status check_dtype(int32_t dtype) {
@@ -532,7 +548,7 @@ lt_status lt_topk_ex(const void* scores, int32_t dtype, const int32_t* lengths, 
   if (force_kernel < LT_KERNEL_AUTO || force_kernel > LT_KERNEL_STREAM) return LT_ERR_INVALID_ARG;
   if (rows == 0) return LT_OK;
   bool host = false;
-  st = resolve_scores(&scores, &host);
+  st = resolve_data(&scores, &host, &lengths, nullptr, &out_idx, &out_val, nullptr);
   if (st != LT_OK) return st;
   if (host && force_kernel == LT_KERNEL_STREAM) return LT_ERR_UNSUPPORTED;  // bulk copies read device memory
   const bool bf16 = dtype == LT_DTYPE_BF16;
@@ -585,7 +601,7 @@ lt_status lt_topk_blocked_ex(const void* scores, int32_t dtype, const int32_t* l
   if (k_blocks > LT_MAX_K || block_index(block) < 0) return LT_ERR_UNSUPPORTED;
   if (rows == 0) return LT_OK;
   bool host = false;
-  st = resolve_scores(&scores, &host);
+  st = resolve_data(&scores, &host, &lengths, nullptr, &out_idx, &out_val, &out_blocks);
   if (st != LT_OK) return st;
   const bool aligned = rows_aligned(scores, row_stride, bf16);
   // k_blocks >= k: stage B equals the plain top-k, so the stages run as two
@@ -646,7 +662,7 @@ lt_status lt_topk_candidates_ex(const void* scores, int32_t dtype, const int32_t
   if (block_index(block) < 0) return LT_ERR_UNSUPPORTED;
   if (rows == 0) return LT_OK;
   bool host = false;
-  st = resolve_scores(&scores, &host);
+  st = resolve_data(&scores, &host, &lengths, &cand_blocks, &out_idx, &out_val, nullptr);
   if (st != LT_OK) return st;
   const bool aligned = rows_aligned(scores, row_stride, bf16);
   Plan plan;

@@ -134,6 +134,24 @@ def test_pinned_host_scores_read_in_place(lib):
     gi, gv = lt.topk_candidates(host, torch.as_tensor(cand).cuda(), l, 8, k)
     oi, ov = oracle.topk_candidates(Sn, Ln, cand, 8, k)
     assert_same(gi.cpu().numpy(), gv.cpu().numpy(), oi, ov, "pinned host, listed candidates")
+    # lengths and outputs in pinned host memory too (written in place by the kernel)
+    hi = torch.empty(rows, k, dtype=torch.int32).pin_memory()
+    hv = torch.empty(rows, k, dtype=torch.float32).pin_memory()
+    hb = torch.empty(rows, 512, dtype=torch.int32).pin_memory()
+    lt.topk(host, L.pin_memory(), k, out_idx=hi, out_val=hv)
+    torch.cuda.synchronize()
+    oi, ov = oracle.topk(Sn, Ln, k)
+    assert_same(hi.numpy(), hv.numpy(), oi, ov, "pinned host scores, lengths and outputs")
+    hv2 = torch.empty(rows, k, dtype=torch.float32).pin_memory()
+    lt.topk_blocked(host, L.pin_memory(), 8, 512, k, out_idx=hi, out_val=hv2, out_blocks=hb)
+    torch.cuda.synchronize()
+    oi, ov, ob = oracle.topk_blocked(Sn, Ln, 8, 512, k)
+    assert_same(hi.numpy(), hv2.numpy(), oi, ov, "pinned host, two-level outputs")
+    assert np.array_equal(hb.numpy(), ob)
+    lt.topk_candidates(host, torch.as_tensor(cand).pin_memory(), L.pin_memory(), 8, k, out_idx=hi, out_val=hv)
+    torch.cuda.synchronize()
+    oi, ov = oracle.topk_candidates(Sn, Ln, cand, 8, k)
+    assert_same(hi.numpy(), hv.numpy(), oi, ov, "pinned host list and outputs")
     T = workloads.to_bf16(S)
     gi, gv = lt.topk(T.pin_memory(), l, k)
     oi, ov = oracle.topk_bf16(workloads.bf16_bits(T), Ln, k)
