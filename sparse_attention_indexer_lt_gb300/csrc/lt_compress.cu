@@ -297,7 +297,7 @@ struct RParams {
   int64_t units;          // rows * units_per_row
   int32_t dim, ratio, groups;
   int32_t st;             // tokens per full stage
-  int32_t bpu;            // blocks per unit (1 when a block is streamed)
+  int32_t bpu;            // blocks per unit (streamed: blocks that stream side by side)
   int32_t subtiles;       // stages per unit
   int32_t tpg;            // streamed blocks: threads per channel group (power of two)
   int32_t stages;
@@ -464,13 +464,26 @@ __global__ void __launch_bounds__(kThreads, 2) compress_ring_kernel(RParams p) {
       stage_tokens(p, pg0, pnb, psub, &t0, &n);
       unsigned char* dst = ring + (size_t)(pseq % ns) * p.stage_bytes;
       const uint32_t bytes = (uint32_t)n * (uint32_t)p.dim * (uint32_t)sizeof(S);
-      const uint32_t bbytes = p.subtiles > 1 ? (uint32_t)n * (uint32_t)p.dim * 4u : 0u;
       uint64_t* bar = &bars[pseq % ns];
-      mbar_arrive_tx(bar, 2u * bytes + bbytes);
-      const int64_t e0 = (pr * p.row_tokens + t0) * p.dim;
-      bulk_g2s(dst, kv + e0, bytes, bar);
-      bulk_g2s(dst + p.in_bytes, sc + e0, bytes, bar);
-      if (bbytes) bulk_g2s(dst + 2u * p.in_bytes, p.bias + (int64_t)psub * p.st * p.dim, bbytes, bar);
+      if (p.subtiles == 1) {
+        // whole blocks, contiguous: kv, then score
+        mbar_arrive_tx(bar, 2u * bytes);
+        const int64_t e0 = (pr * p.row_tokens + t0) * p.dim;
+        bulk_g2s(dst, kv + e0, bytes, bar);
+        bulk_g2s(dst + p.in_bytes, sc + e0, bytes, bar);
+      } else {
+        // the same tokens of each of the unit's pnb streamed blocks (kv of
+        // block b at b * in_bytes, its score at (bpu + b) * in_bytes), then
+        // those tokens' bias rows once for all of them
+        const uint32_t bbytes = (uint32_t)n * (uint32_t)p.dim * 4u;
+        mbar_arrive_tx(bar, 2u * bytes * (uint32_t)pnb + bbytes);
+        for (int b = 0; b < pnb; ++b) {
+          const int64_t e0 = (pr * p.row_tokens + t0 + (int64_t)b * p.ratio) * p.dim;
+          bulk_g2s(dst + (uint32_t)b * p.in_bytes, kv + e0, bytes, bar);
+          bulk_g2s(dst + (uint32_t)(p.bpu + b) * p.in_bytes, sc + e0, bytes, bar);
+        }
+        bulk_g2s(dst + 2u * (uint32_t)p.bpu * p.in_bytes, p.bias + (int64_t)psub * p.st * p.dim, bbytes, bar);
+      }
       ++pseq;
       if (++psub == p.subtiles) {
         psub = 0;
@@ -491,8 +504,10 @@ __global__ void __launch_bounds__(kThreads, 2) compress_ring_kernel(RParams p) {
   bool cvalid = next_unit(p, cu, &cr, &cg0, &cnb);
   uint32_t seq = 0;
   bool late = false;
-  // streamed blocks: this thread's channel group and token phase
-  const int cgB = tid / p.tpg, hB = tid - cgB * p.tpg;
+  // streamed blocks: this thread's block of the unit, channel group and token phase
+  const int laneB = tid / (p.groups * p.tpg);
+  const int jB = tid - laneB * (p.groups * p.tpg);
+  const int cgB = jB / p.tpg, hB = jB - cgB * p.tpg;
   Acc<V> acc;
   while (cvalid) {
     for (int sub = 0; sub < p.subtiles; ++sub) {
@@ -511,10 +526,13 @@ __global__ void __launch_bounds__(kThreads, 2) compress_ring_kernel(RParams p) {
           ring_blocks<S>(p, xs, zs, bias_s, cnb, ob, tid);
         }
       } else {
-        // one block over several stages: tokens t with t mod tpg == hB
+        // a unit's blocks over several stages: this thread's block laneB,
+        // tokens t with t mod tpg == hB
         if (sub == 0) acc.init();
-        const float* bs = reinterpret_cast<const float*>(stg + 2u * p.in_bytes);
-        if (cgB < p.groups) {
+        const float* bs = reinterpret_cast<const float*>(stg + 2u * (uint32_t)p.bpu * p.in_bytes);
+        xs = reinterpret_cast<const S*>(stg + (uint32_t)laneB * p.in_bytes);
+        zs = reinterpret_cast<const S*>(stg + (uint32_t)(p.bpu + laneB) * p.in_bytes);
+        if (laneB < cnb && cgB < p.groups) {
           const int base = sub * p.st;
           int i = (hB - base) % p.tpg;
           if (i < 0) i += p.tpg;
@@ -556,10 +574,10 @@ __global__ void __launch_bounds__(kThreads, 2) compress_ring_kernel(RParams p) {
               acc.m[c] = mn;
             }
           }
-          if (cgB < p.groups && hB == 0) {
+          if (laneB < cnb && cgB < p.groups && hB == 0) {
             float y[V];
             acc.result(y);
-            store_v<V>(out + (cr * p.nblk + cg0) * p.dim + (int64_t)cgB * V, y);
+            store_v<V>(out + (cr * p.nblk + cg0 + laneB) * p.dim + (int64_t)cgB * V, y);
           }
         }
       }
@@ -666,14 +684,22 @@ bool ring_plan(const void* kv, const void* score, const float* bias, const void*
     bias_bytes = (uint32_t)ratio * (uint32_t)dim * 4u;
   } else {
     if (groups > (uint32_t)kThreads || row_bytes > kRingInLarge) return false;
-    r->bpu = 1;
     r->st = (int32_t)(kRingInLarge / row_bytes);
     r->subtiles = (ratio + r->st - 1) / r->st;
-    int tpg = 1;
-    while (tpg * 2 <= 32 && (uint32_t)(tpg * 2) * groups <= (uint32_t)kThreads) tpg *= 2;
-    r->tpg = tpg;
+    // two blocks stream side by side when both fit the threads (one thread
+    // per channel group of each): a stage's bias rows then serve both;
+    // otherwise one block, its channel groups split over tpg threads
+    if (2u * groups <= (uint32_t)kThreads) {
+      r->bpu = 2;
+      r->tpg = 1;
+    } else {
+      r->bpu = 1;
+      int tpg = 1;
+      while (tpg * 2 <= 32 && (uint32_t)(tpg * 2) * groups <= (uint32_t)kThreads) tpg *= 2;
+      r->tpg = tpg;
+    }
     r->in_bytes = (uint32_t)(r->st * row_bytes);
-    r->stage_bytes = 2u * r->in_bytes + (uint32_t)r->st * (uint32_t)dim * 4u;
+    r->stage_bytes = 2u * (uint32_t)r->bpu * r->in_bytes + (uint32_t)r->st * (uint32_t)dim * 4u;
   }
   r->bias_off = 128;
   r->ring_off = (r->bias_off + bias_bytes + 127u) / 128u * 128u;

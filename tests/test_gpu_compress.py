@@ -80,6 +80,23 @@ def test_small_shapes_ragged(dtype, ratio, dim):
 
 
 @pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+@pytest.mark.parametrize("ratio", [64, 128])
+@pytest.mark.parametrize("dim", [512, 1024])
+def test_streamed_blocks(dtype, ratio, dim):
+    """Blocks too large for one ring stage: two streamed side by side sharing
+    each stage's bias rows (512 channels), or one at a time with its channel
+    groups split over threads (1024); odd block counts leave a unit with one."""
+    import sparse_attention_indexer_lt_gb300 as lt
+    rows, T = 3, 700
+    kv, sc, bias = workloads.compress_inputs(rows, T, dim, ratio, seed=ratio + dim, dtype=dtype, score_scale=2.0)
+    L = np.array([T, T - ratio - 3, 2 * ratio + 1], np.int32)
+    out = torch.full((rows, T // ratio, dim), 12288.0, dtype=dtype, device="cuda")
+    lt.compress(kv.cuda(), sc.cuda(), bias.cuda(), ratio, torch.as_tensor(L).cuda(), out=out)
+    torch.cuda.synchronize()
+    check(out, kv, sc, bias, ratio, L, f"streamed {dtype} ratio={ratio} dim={dim}")
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
 def test_unaligned_views_take_scalar_loads(dtype):
     import sparse_attention_indexer_lt_gb300 as lt
     kv, sc, bias = workloads.compress_inputs(2, 65, 16, 4, seed=5, dtype=dtype)
