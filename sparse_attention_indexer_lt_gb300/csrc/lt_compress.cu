@@ -465,8 +465,9 @@ __global__ void __launch_bounds__(kThreads, 2) compress_ring_kernel(RParams p) {
       unsigned char* dst = ring + (size_t)(pseq % ns) * p.stage_bytes;
       const uint32_t bytes = (uint32_t)n * (uint32_t)p.dim * (uint32_t)sizeof(S);
       uint64_t* bar = &bars[pseq % ns];
-      if (p.subtiles == 1) {
-        // whole blocks, contiguous: kv, then score
+      if (R > 0 || p.subtiles == 1) {
+        // whole blocks, contiguous: kv, then score (the fixed-column kernel
+        // only ever sees these)
         mbar_arrive_tx(bar, 2u * bytes);
         const int64_t e0 = (pr * p.row_tokens + t0) * p.dim;
         bulk_g2s(dst, kv + e0, bytes, bar);
@@ -518,7 +519,7 @@ __global__ void __launch_bounds__(kThreads, 2) compress_ring_kernel(RParams p) {
       int64_t t0;
       int n;
       stage_tokens(p, cg0, cnb, sub, &t0, &n);
-      if (p.subtiles == 1) {
+      if (R > 0 || p.subtiles == 1) {
         S* ob = out + (cr * p.nblk + cg0) * p.dim;
         if constexpr (R > 0) {
           ring_blocks_fixed<S, R>(xs, zs, bfix, cnb, p.dim, fixed_cg, fixed_q0, fixed_qs, ob);
