@@ -275,3 +275,26 @@ def test_hinted_rows_redo_when_the_guess_misses(dist):
     idx, val = gpu_topk(S, L, 512, with_values=False, counters=c)
     assert val is None and c.cpu().numpy()[6] == 0
     assert np.array_equal(idx, __import__("oracle").topk(S, L, 512)[0])
+
+
+@pytest.mark.parametrize("stride", [1, 2, 3, 5])
+def test_tiny_rows(stride):
+    """Rows of a handful of positions (unaligned, scalar loads), k above and
+    below the row length, every plan the automatic planner picks for them."""
+    for rows in (1, 7, 300):
+        S, L = workloads.random_rows(rows, stride, seed=stable_seed("tiny", stride, rows), dist="coarse",
+                                     lengths="ragged", min_len=0)
+        for k in (1, 2, 4, 9):
+            parity_topk(S.numpy(), L.numpy(), k, what=f"stride {stride} rows {rows} k {k}")
+            parity_topk(S.numpy(), None, k, what=f"stride {stride} rows {rows} k {k} full")
+
+
+def test_many_short_rows():
+    """100,000 rows of 96 positions (one single-round CTA each, many waves),
+    ragged, ties and special values mixed in."""
+    rows, stride, k = 100000, 96, 16
+    S, L = workloads.random_rows(rows, stride, seed=61, dist="special", lengths="ragged", min_len=0)
+    c = counters()
+    parity_topk(S.numpy(), L.numpy(), k, what="100K rows", counters=c)
+    cnt = c.cpu().numpy()
+    assert cnt[0] + cnt[1] == int((L.numpy() > 0).sum()), cnt
