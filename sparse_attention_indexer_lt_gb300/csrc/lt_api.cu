@@ -246,10 +246,15 @@ lt_status make_plan(int32_t rows, int64_t row_stride, int32_t k, bool blocked, i
 
   // Candidate capacity: about 4k slots per row (the sampled threshold keeps
   // roughly k to 1.5k items), split into one segment per CTA of the cluster,
-  // each segment at least 256 slots so uneven slices still fit.
+  // each segment at least 256 slots so uneven slices still fit. Plans of one
+  // 512-thread CTA per SM have shared memory to spare and take at least 4096
+  // slots: the second estimate level (a histogram pass, a merge and a search,
+  // about 3 us on a 262144-position row) then only runs when the first level
+  // predicts more than 3072 candidates, instead of 1536.
   const uint32_t kmax = (uint32_t)(blocked ? (k > k_blocks ? k : k_blocks) : k);
   uint32_t base_cap = next_pow2(4 * kmax);
   base_cap = base_cap < 2048u ? 2048u : (base_cap > 4096u ? 4096u : base_cap);
+  if (threads == kWideThreads && !blocked && base_cap < 4096u) base_cap = 4096u;
   plan->sel_cap = next_pow2(kmax < 32u ? 32u : kmax);
 
   int c = 1;

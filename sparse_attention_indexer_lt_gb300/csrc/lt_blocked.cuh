@@ -18,9 +18,13 @@ namespace lt {
 // [0, rows)) computes the plain top-k of its row, group 2 (clusters
 // [rows, 2 rows), launched only when out_blocks is wanted) stage A alone. Both
 // read the row once, side by side, instead of one stage after the other.
+//
+// Rounds are four float4 per thread (eight only for 32-position blocks): with
+// eight, the 512-thread kernel (128 registers a thread) spilled, and the
+// side-by-side 16-row launch took 22.8 us against 21.5 with four.
 template <int T, int W, class S>
 __global__ void __launch_bounds__(T, (T <= 256 ? 3 : 1)) blocked_kernel(Params p) {
-  constexpr int U0 = T <= 256 ? 4 : 8;  // float4 per thread per round
+  constexpr int U0 = 4;  // float4 per thread per round
   constexpr int U = (W / 4 > U0) ? W / 4 : U0;
   using G = Geo<T, U, W>;
   extern __shared__ __align__(128) unsigned char smem[];
@@ -31,9 +35,24 @@ __global__ void __launch_bounds__(T, (T <= 256 ? 3 : 1)) blocked_kernel(Params p
   // 0: both stages in turn; 1 / 2: plain top-k / stage A side by side;
   // 3: stage B over a given block list
   const int role = p.external ? 3 : (p.split ? (cid < p.rows ? 1 : 2) : 0);
+  float4 va[U], vb[U];
+  if (role == 1) {
+    // the plain top-k of the row: items are single positions, so it runs on
+    // four-position slots (the top-k kernel's streaming filter: paired
+    // register rounds, compare masks without per-slot bookkeeping)
+    setup_row<T, U, 4>(R, p, smem, cid % p.rows);
+    int na4[U], nb4[U];
+    const uint32_t K = (uint32_t)(R.L < (int64_t)p.k ? R.L : (int64_t)p.k);
+    bool intact;
+    uint64_t Tc;
+    const bool exact = select_stage<T, U, 4, false>(R, p, va, na4, vb, nb4, false, K, R.L, p.row_stride, KeepAll{},
+                                                    true, &intact, &Tc, kTrStageB);
+    output_positions<T>(R, p, exact, Tc, K, p.row_stride, true);
+    wait_init(R);
+    return;
+  }
   setup_row<T, U, W>(R, p, smem, p.split ? cid % p.rows : cid);
   Misc* m = R.m;
-  float4 va[U], vb[U];
   int na[G::kSlots], nb[G::kSlots];
   if (role == 3) {
     // a bitmap of this CTA's slice of blocks (slices hold whole blocks) in the
@@ -71,16 +90,6 @@ __global__ void __launch_bounds__(T, (T <= 256 ? 3 : 1)) blocked_kernel(Params p
     const bool exact = select_stage<T, U, W, false>(R, p, va, na, vb, nb, false, K, ncand, p.row_stride,
                                                     KeepListed<T, U, W>{bits, b0, words * 32u}, true, &intact,
                                                     &Tc, 0);
-    output_positions<T>(R, p, exact, Tc, K, p.row_stride, true);
-    wait_init(R);
-    return;
-  }
-  if (role == 1) {
-    const uint32_t K = (uint32_t)(R.L < (int64_t)p.k ? R.L : (int64_t)p.k);
-    bool intact;
-    uint64_t Tc;
-    const bool exact = select_stage<T, U, W, false>(R, p, va, na, vb, nb, false, K, R.L, p.row_stride, KeepAll{},
-                                                    true, &intact, &Tc, kTrStageB);
     output_positions<T>(R, p, exact, Tc, K, p.row_stride, true);
     wait_init(R);
     return;
@@ -156,6 +165,7 @@ __global__ void __launch_bounds__(T, (T <= 256 ? 3 : 1)) blocked_kernel(Params p
       }
     }
     __syncthreads();
+    stamp(R, kTrOutput);
     wait_init(R);
     return;
   }
@@ -241,6 +251,7 @@ __global__ void __launch_bounds__(T, (T <= 256 ? 3 : 1)) blocked_kernel(Params p
   }
   __syncthreads();
   if (role == 2) {
+    stamp(R, kTrOutput);
     wait_init(R);
     return;
   }
