@@ -5,6 +5,94 @@
 
 namespace lt {
 
+// Stage A's kept blocks straight from the candidate segments, which the
+// exchange replicated in every CTA of the cluster. 1024 linear buckets over
+// the candidates' key range [lo, hi] locate the bucket b* holding the KA-th
+// composite; one more pass keeps every item above b* and stages the items of
+// b*, whose exact rank among themselves decides the rest. On the way each CTA
+// marks its own kept blocks in a bitmap and counts the kept blocks of the
+// lower-ranked slices (a block belongs to the slice holding its id: slices
+// hold whole blocks), then writes its own kept ids in ascending order after
+// them. Expects the bucket counts (R.hist) zeroed and a barrier passed since,
+// and this CTA's slice to hold at most 32 * kBins blocks. Returns false, having
+// written nothing, when b* holds more than kMaxBucket items.
+template <int T, int W>
+__device__ __forceinline__ bool kept_from_segments(RowCore& R, const Params& p, uint32_t KA, uint32_t lo,
+                                                   uint32_t hi) {
+  constexpr int NB = kOutBuckets;
+  constexpr int BPT = NB / T;
+  Misc* m = R.m;
+  const uint32_t b0s = (uint32_t)(R.begin / W), b1s = (uint32_t)((R.end + W - 1) / W);
+  const uint32_t words = (b1s - b0s + 31u) >> 5;
+  uint32_t* bits = R.aux;
+  for (uint32_t i = threadIdx.x; i < words; i += T) bits[i] = 0u;
+  if (threadIdx.x == 0) {
+    m->aux[2] = 0u;  // items staged from b*
+    m->aux[6] = 0u;  // kept blocks of the lower-ranked slices
+  }
+  const float scale = (float)NB / ((float)(hi - lo) + 1.0f);
+  auto bucket = [lo, scale](uint32_t key) -> uint32_t { return out_bucket(key, lo, scale); };
+  for_each_cand<T>(R, [&](uint2 e) { atomicAdd(&R.hist[bucket(e.x)], 1u); });
+  __syncthreads();
+  uint32_t v[BPT];
+#pragma unroll
+  for (int j = 0; j < BPT; ++j) v[j] = R.hist[threadIdx.x * BPT + j];
+  uint32_t tot = 0;
+#pragma unroll
+  for (int j = 0; j < BPT; ++j) tot += v[j];
+  uint32_t a = block_suffix_excl<T>(tot, m);
+#pragma unroll
+  for (int j = BPT - 1; j >= 0; --j) {
+    if (a < KA && KA <= a + v[j]) {
+      m->res_digit = threadIdx.x * BPT + j;
+      m->res_above = a;
+      m->res_cnt = v[j];
+    }
+    a += v[j];
+  }
+  __syncthreads();
+  const uint32_t bstar = m->res_digit, above = m->res_above, cstar = m->res_cnt;
+  if (cstar > (uint32_t)kMaxBucket) return false;
+  uint32_t before = 0;
+  auto keep = [&](uint32_t id) {
+    if (id < b0s) ++before;
+    else if (id < b1s) atomicOr(&bits[(id - b0s) >> 5], 1u << ((id - b0s) & 31u));
+  };
+  for_each_cand<T>(R, [&](uint2 e) {
+    const uint32_t b = bucket(e.x);
+    if (b > bstar) {
+      keep(e.y);
+    } else if (b == bstar) {
+      const uint32_t pos = atomicAdd(&m->aux[2], 1u);
+      if (pos < R.stage_cap) R.stage[pos] = composite(e.x, e.y);
+    }
+  });
+  __syncthreads();
+  const uint32_t need = KA - above;  // 1 <= need <= cstar
+  for (uint32_t i = threadIdx.x; i < cstar; i += T) {
+    const uint64_t c = R.stage[i];
+    uint32_t r = 0;
+    for (uint32_t j = 0; j < cstar; ++j) r += (R.stage[j] > c) ? 1u : 0u;
+    if (r < need) keep(~(uint32_t)c);
+  }
+  before = __reduce_add_sync(kFull, before);
+  if (lane_id() == 0 && before != 0u) atomicAdd(&m->aux[6], before);
+  __syncthreads();
+  int32_t* ob = p.out_blocks + R.row * (int64_t)p.k_blocks;
+  const uint32_t wpt = (words + T - 1) / T;
+  const uint32_t w0 = threadIdx.x * wpt;
+  const uint32_t w1 = min(w0 + wpt, words);
+  uint32_t cnt = 0;
+  for (uint32_t w = w0; w < w1; ++w) cnt += (uint32_t)__popc(bits[w]);
+  uint32_t out = m->aux[6] + block_prefix_excl<T>(cnt, m);
+  for (uint32_t w = w0; w < w1; ++w)
+    for (uint32_t x = bits[w]; x; x &= x - 1u) ob[out++] = (int32_t)(b0s + 32u * w + (uint32_t)(__ffs(x) - 1));
+  if (R.rank == 0) {
+    for (uint32_t j = KA + threadIdx.x; j < (uint32_t)p.k_blocks; j += T) ob[j] = -1;
+  }
+  return true;
+}
+
 // Stage A selects the top k_blocks blocks of W positions by block key (the
 // key of the block's best score), ties by lowest block id; stage B selects the
 // top k positions inside the kept blocks, ties by lowest position. The kept
@@ -103,71 +191,24 @@ __global__ void __launch_bounds__(T, (T <= 256 ? 3 : 1)) blocked_kernel(Params p
   const bool exactA = select_stage<T, U, W, true>(R, p, va, na, vb, nb, false, KA, nblocks, nblocks,
                                                   KeepAll{}, true, &intact, &TcA, 0);
   uint64_t TA = 0;
-  bool from_segments = false;  // stage-A-only clusters on the fast path
   if (KA > 0) {
-    // (the bitmap of this CTA's blocks lives in the histogram area)
-    if (role == 2 && !exactA && (R.end - R.begin + W - 1) / W <= 32 * (int64_t)kBins) {
-      const uint32_t seg = 1u << m->shift;
+    if (role == 2 && !exactA && (R.end - R.begin + W - 1) / W <= 32 * (int64_t)kBins && p.out_blocks) {
+      // stage-A-only clusters on the fast path: every CTA holds every segment
       uint32_t lo = 0xffffffffu, hi = 0u;
       for (uint32_t q = 0; q < m->nseg; ++q) {
         if (m->seg_cnt[q] == 0) continue;
         lo = min(lo, m->seg_min[q]);
         hi = max(hi, m->seg_max[q]);
       }
-      (void)seg;
-      from_segments = threshold_by_buckets<T>(R, KA, lo, hi, &TA);
-    }
-    if (!from_segments) {
-      TA = exactA ? TcA : select_local<T>(R, KA, nblocks);
-      compact_selected<T>(R, TA);  // stage[0, KA) = kept block composites
-    }
-  }
-  if (from_segments) {
-    // kept blocks straight from the candidate segments: this CTA's own kept
-    // blocks are the entries of its own segment >= TA, the lower-ranked
-    // slices' kept blocks precede them
-    const int64_t b0s = R.begin / W, b1s = (R.end + W - 1) / W;
-    const uint32_t seg = 1u << m->shift;
-    uint32_t before = 0;
-    for (uint32_t q = 0; q < R.rank; ++q) {
-      const uint32_t n = min(m->seg_cnt[q], seg);
-      const uint2* c = R.cand + (q << m->shift);
-      for (uint32_t j = threadIdx.x; j < n; j += T) before += composite(c[j].x, c[j].y) >= TA ? 1u : 0u;
-    }
-    const uint32_t n_before = block_sum<T>(before, m);
-    if (p.out_blocks) {
-      int32_t* ob = p.out_blocks + R.row * (int64_t)p.k_blocks;
-      const int64_t nbo = b1s - b0s;
-      uint32_t* bits = R.hist;
-      const uint32_t words = (uint32_t)((nbo + 31) >> 5);
-      for (uint32_t i = threadIdx.x; i < words; i += T) bits[i] = 0u;
-      __syncthreads();
-      const uint32_t n_own = min(m->seg_cnt[R.rank], seg);
-      const uint2* own = R.cand + (R.rank << m->shift);
-      for (uint32_t j = threadIdx.x; j < n_own; j += T) {
-        if (composite(own[j].x, own[j].y) >= TA) {
-          const uint32_t o = (uint32_t)((int64_t)own[j].y - b0s);
-          atomicOr(&bits[o >> 5], 1u << (o & 31u));
-        }
-      }
-      __syncthreads();
-      const uint32_t wpt = (words + T - 1) / T;
-      const uint32_t w0 = threadIdx.x * wpt;
-      const uint32_t w1 = min(w0 + wpt, words);
-      uint32_t cnt = 0;
-      for (uint32_t w = w0; w < w1; ++w) cnt += (uint32_t)__popc(bits[w]);
-      uint32_t out = n_before + block_prefix_excl<T>(cnt, m);
-      for (uint32_t w = w0; w < w1; ++w)
-        for (uint32_t x = bits[w]; x; x &= x - 1u)
-          ob[out++] = (int32_t)(b0s + 32 * (int64_t)w + (__ffs(x) - 1));
-      if (R.rank == 0) {
-        for (uint32_t j = KA + threadIdx.x; j < (uint32_t)p.k_blocks; j += T) ob[j] = -1;
+      if (kept_from_segments<T, W>(R, p, KA, lo, hi)) {
+        __syncthreads();
+        stamp(R, kTrOutput);
+        wait_init(R);
+        return;
       }
     }
-    __syncthreads();
-    stamp(R, kTrOutput);
-    wait_init(R);
-    return;
+    TA = exactA ? TcA : select_local<T>(R, KA, nblocks);
+    compact_selected<T>(R, TA);  // stage[0, KA) = kept block composites
   }
 
   // ---- kept block ids in ascending order: this CTA's own kept blocks,

@@ -146,11 +146,20 @@ struct Misc {
   uint32_t warp_a[kMaxWarps];
   uint32_t warp_b[kMaxWarps];
   uint32_t aux[8];
+  uint32_t hint_min[2], hint_max[2];  // bits of the warps' hint readings (hi, lo)
 };
 
 struct Layout {
   uint32_t misc, hist, aux, merged0, merged1, cand, stage, wstage, total;
 };
+
+// Output bucket of a candidate key: kOutBuckets buckets linear in the key
+// from lo (every candidate's key is >= lo), clamped at the top. Monotone in
+// the key, so a higher bucket never holds a smaller key.
+__device__ __forceinline__ uint32_t out_bucket(uint32_t key, uint32_t lo, float scale) {
+  const uint32_t b = (uint32_t)((float)(key - lo) * scale);
+  return b > (uint32_t)(kOutBuckets - 1) ? (uint32_t)(kOutBuckets - 1) : b;
+}
 
 __host__ __device__ inline uint32_t align_up_u32(uint32_t x, uint32_t a) { return (x + a - 1) / a * a; }
 

@@ -255,6 +255,10 @@ __device__ __forceinline__ void setup_row(RowT<S>& R, const Params& p, unsigned 
     m->flags = 0;
     m->own_count = 0;
     m->aux[7] = 0;  // cluster-wide sums pushed by peers (listed positions)
+    for (int i = 0; i < 2; ++i) {
+      m->hint_min[i] = 0xffffffffu;
+      m->hint_max[i] = 0u;
+    }
   }
   if (p.clustered) {
     uint4* z0 = reinterpret_cast<uint4*>(R.merged0);
@@ -767,65 +771,6 @@ __device__ __forceinline__ uint32_t compact_selected(RowCore& R, uint64_t Tc) {
   return cnt;
 }
 
-// Composite of the K-th largest fast-path candidate (segmented candidates,
-// key range [lo, hi], histogram zeroed and a barrier passed since): 1024
-// linear key buckets, a suffix scan for the bucket b* holding the K-th item,
-// then the exact rank of the items of b* among themselves. Returns false,
-// deciding nothing, when b* holds more than kMaxBucket items.
-template <int T>
-__device__ __forceinline__ bool threshold_by_buckets(RowCore& R, uint32_t K, uint32_t lo, uint32_t hi, uint64_t* Tc) {
-  constexpr int NB = kOutBuckets;
-  constexpr int BPT = NB / T;
-  Misc* m = R.m;
-  const float scale = (float)NB / ((float)(hi - lo) + 1.0f);
-  auto bucket = [lo, scale](uint32_t key) -> uint32_t {
-    const uint32_t b = (uint32_t)((float)(key - lo) * scale);
-    return b > (uint32_t)(NB - 1) ? (uint32_t)(NB - 1) : b;
-  };
-  if (threadIdx.x == 0) m->aux[2] = 0u;
-  for_each_cand<T>(R, [&](uint2 e) { atomicAdd(&R.hist[bucket(e.x)], 1u); });
-  __syncthreads();
-  uint32_t v[BPT];
-#pragma unroll
-  for (int j = 0; j < BPT; ++j) v[j] = R.hist[threadIdx.x * BPT + j];
-  uint32_t tot = 0;
-#pragma unroll
-  for (int j = 0; j < BPT; ++j) tot += v[j];
-  uint32_t a = block_suffix_excl<T>(tot, m);
-#pragma unroll
-  for (int j = BPT - 1; j >= 0; --j) {
-    if (a < K && K <= a + v[j]) {
-      m->res_digit = threadIdx.x * BPT + j;
-      m->res_above = a;
-      m->res_cnt = v[j];
-    }
-    a += v[j];
-  }
-  __syncthreads();
-  const uint32_t bstar = m->res_digit, above = m->res_above, cstar = m->res_cnt;
-  if (cstar > (uint32_t)kMaxBucket) return false;
-  for_each_cand<T>(R, [&](uint2 e) {
-    if (bucket(e.x) == bstar) {
-      const uint32_t pos = atomicAdd(&m->aux[2], 1u);
-      if (pos < R.stage_cap) R.stage[pos] = composite(e.x, e.y);
-    }
-  });
-  __syncthreads();
-  const uint32_t need = K - above;  // 1 <= need <= cstar
-  for (uint32_t i = threadIdx.x; i < cstar; i += T) {
-    const uint64_t c = R.stage[i];
-    uint32_t r = 0;
-    for (uint32_t j = 0; j < cstar; ++j) r += (R.stage[j] > c) ? 1u : 0u;
-    if (r == need - 1) {
-      m->aux[4] = (uint32_t)c;
-      m->aux[5] = (uint32_t)(c >> 32);
-    }
-  }
-  __syncthreads();
-  *Tc = ((uint64_t)m->aux[5] << 32) | m->aux[4];
-  return true;
-}
-
 // ------------------------------------------------------------------ ordered output
 
 template <class S>
@@ -935,10 +880,7 @@ __device__ __forceinline__ bool bucket_select_sort(RowT<S>& R, uint32_t K, uint3
   }
   if (hi == lo && N > (uint32_t)kMaxBucket) return false;
   const float scale = (float)NB / ((float)(hi - lo) + 1.0f);
-  auto bucket = [lo, scale](uint32_t key) -> uint32_t {
-    const uint32_t b = (uint32_t)((float)(key - lo) * scale);
-    return b > (uint32_t)(NB - 1) ? (uint32_t)(NB - 1) : b;
-  };
+  auto bucket = [lo, scale](uint32_t key) -> uint32_t { return out_bucket(key, lo, scale); };
   for_each_cand<T>(R, [&](uint2 e) { atomicAdd(&R.hist[bucket(e.x)], 1u); });
   __syncthreads();
   // exclusive suffix starts -> aux; the bucket b* holding the K-th item; the
@@ -1191,16 +1133,16 @@ __device__ __forceinline__ uint32_t estimate_small(RowCore& R, const float4 (&v)
 //
 // hint (nullable): the (k/2)-th and k-th values an earlier row of the batch
 // wrote to its output. Rows of one batch score the same context, so from
-// those two values, lo = k-th and hi = (k/2)-th, the filter can start at
-// lo - 0.75 (hi - lo): about 1.4k to 1.5k of a similar row pass it (the
-// scores thin out above the k-th), a margin of many times the row-to-row
-// spread of the k-th value. The estimate is then skipped.
-// Whether it fits is decided by the filter's own count check: fewer than K
-// kept or more than the candidate area holds, and the row takes the exact
-// path, as any miss does. Values that give no usable threshold (NaN,
-// infinities, hi < lo) leave the estimate in place.
+// lo = k-th and hi = (k/2)-th the filter can start at lo - 0.75 (hi - lo):
+// about 1.4k to 1.5k of a similar row pass it (the scores thin out above the
+// k-th), a margin of many times the row-to-row spread of the k-th value. The
+// estimate is then skipped. Whether it fits is decided by the filter's own
+// count check: fewer than K kept or more than the candidate area holds, and
+// the row takes the exact path, as any miss does. Values that give no usable
+// threshold (NaN, infinities, hi <= lo) keep every position, which the same
+// check settles.
 struct Hint {
-  float hi, lo;
+  float hi, lo;  // the earlier row's (k/2)-th and k-th values
 };
 
 __device__ __forceinline__ uint32_t hint_threshold(const Hint& h) {
@@ -1284,11 +1226,27 @@ __device__ __forceinline__ bool select_stage(RowT<S>& R, const Params& p, float4
     bool hinted = false;
     if constexpr (!kBlocks && W == 4 && Keep::kAll) {
       if (hint != nullptr && R.nclus == 1) {
-        // from an earlier row's output (0: none usable); taken without a
-        // block barrier, so the warps go on filtering at their own pace
-        t = hint_threshold(*hint);
-        hinted = t != 0u;
-        estimated = hinted;
+        // from an earlier row's output, taken without a block barrier, so
+        // the warps go on filtering at their own pace. Each warp takes its
+        // lane 0's reading; that row's CTA may still have been writing it, so
+        // the warps' readings are compared after the filter and any
+        // difference counts as a miss. An unusable reading gives t = 0
+        // (keep everything), which the count check also settles.
+        Hint h;
+        h.hi = __shfl_sync(kFull, hint->hi, 0);
+        h.lo = __shfl_sync(kFull, hint->lo, 0);
+        *hint = h;
+        if (lane_id() == 0) {
+          const uint32_t w[2] = {__float_as_uint(h.hi), __float_as_uint(h.lo)};
+#pragma unroll
+          for (int i = 0; i < 2; ++i) {
+            atomicMin(&m->hint_min[i], w[i]);
+            atomicMax(&m->hint_max[i], w[i]);
+          }
+        }
+        t = hint_threshold(h);
+        hinted = true;
+        estimated = true;
       }
     }
     if constexpr (!kBlocks && T == 256 && W == 4 && Keep::kAll) {
@@ -1370,16 +1328,20 @@ __device__ __forceinline__ bool select_stage(RowT<S>& R, const Params& p, float4
       if (!all && g > 0.0f) filter_rounds_all<T, U, true>(R, vec, cur, nc, nxt, nn, g, all, counter, list, seg);
       else filter_rounds_all<T, U, false>(R, vec, cur, nc, nxt, nn, g, all, counter, list, seg);
     } else {
+      // the two register buffers alternate: round r + 2 loads into the buffer
+      // round r just left, so two rounds are in flight while one is filtered
 #pragma unroll 1
-      for (int r = 0; r < R.rounds; ++r) {
+      for (int r = 0; r < R.rounds; r += 2) {
         if (kBlocks) filter_round_blocks<T, U, W>(R, r, cur, nc, t, counter, list, seg);
         else filter_round<T, U, W>(R, r, cur, nc, g, all, counter, list, seg, keep);
-#pragma unroll
-        for (int i = 0; i < U; ++i) cur[i] = nxt[i];
-#pragma unroll
-        for (int s = 0; s < G::kSlots; ++s) nc[s] = nn[s];
-        if (r + 2 < R.rounds) load_round<T, U, W>(R, vec, r + 2, nxt, nn);
-        else clear_round(nn);
+        if (r + 2 < R.rounds) load_round<T, U, W>(R, vec, r + 2, cur, nc);
+        else clear_round(nc);
+        if (r + 1 < R.rounds) {
+          if (kBlocks) filter_round_blocks<T, U, W>(R, r + 1, nxt, nn, t, counter, list, seg);
+          else filter_round<T, U, W>(R, r + 1, nxt, nn, g, all, counter, list, seg, keep);
+          if (r + 3 < R.rounds) load_round<T, U, W>(R, vec, r + 3, nxt, nn);
+          else clear_round(nn);
+        }
       }
     }
     stamp(R, tr + kTrFilter);
@@ -1388,7 +1350,8 @@ __device__ __forceinline__ bool select_stage(RowT<S>& R, const Params& p, float4
     const uint32_t cq = lane_id() < R.nclus ? m->seg_cnt[lane_id()] : 0u;
     const uint32_t total = __reduce_add_sync(kFull, cq);
     const bool overflow = __any_sync(kFull, cq > seg);
-    if (overflow || total < K) {
+    const bool split_hint = hinted && (m->hint_min[0] != m->hint_max[0] || m->hint_min[1] != m->hint_max[1]);
+    if (overflow || total < K || split_hint) {
       if (hinted) bump(p, R, kCntHintMiss);  // the earlier row's threshold does not fit this one
       exact = true;
       stat = overflow ? kCntOverflow : kCntShort;

@@ -31,7 +31,9 @@ __global__ void __launch_bounds__(T, (T <= 256 ? 3 : 1)) topk_kernel(Params p) {
     // Batches of single-CTA rows (256 threads): start from the (k/2)-th and
     // k-th values of the row hint_rows earlier (two waves of CTAs, so almost
     // surely finished; see Hint). Another CTA may still be writing them: they
-    // are a guess the filter checks; a miss takes the exact path.
+    // are a guess the filter checks; a miss takes the exact path. Whether a
+    // row is hinted depends only on values every thread reads alike (the
+    // row's length, the launch), so all warps take the same branch.
     if constexpr (kHint) {
       Hint hint = {};
       const bool hinted = p.out_val != nullptr && K == (uint32_t)p.k && p.k >= 2 && R.row >= p.hint_rows &&

@@ -277,6 +277,39 @@ def test_hinted_rows_redo_when_the_guess_misses(dist):
     assert np.array_equal(idx, __import__("oracle").topk(S, L, 512)[0])
 
 
+def test_hints_read_while_another_stream_rewrites_them():
+    """Later rows of a batch take their threshold from an earlier row's output
+    values. Here another stream keeps overwriting the values of the first rows
+    while the launch runs, so the readings change under the rows that take
+    them (and may differ between a CTA's warps): every index still matches the
+    oracle, and so does every value the other stream does not touch."""
+    import oracle
+    import sparse_attention_indexer_lt_gb300 as lt
+    rows, stride, k = 2400, 9000, 512
+    S, L = workloads.random_rows(rows, stride, seed=stable_seed("rewrite"), dist="normal", lengths="ragged")
+    S, L = S.numpy(), L.numpy()
+    oi, ov = oracle.topk(S, L, k)
+    dev = torch.device("cuda")
+    s = torch.from_numpy(S).to(dev)
+    l = torch.from_numpy(L).to(torch.int32).to(dev)
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    n_rw = rows - 2 * sms * 3  # rows whose values later rows read
+    assert n_rw > 0
+    side = torch.cuda.Stream()
+    for _ in range(3):
+        out_idx = torch.empty(rows, k, dtype=torch.int32, device=dev)
+        out_val = torch.empty(rows, k, dtype=torch.float32, device=dev)
+        torch.cuda.synchronize()
+        with torch.cuda.stream(side):
+            for i in range(200):
+                out_val[:n_rw].normal_()
+        lt.topk(s, l, k, out_idx=out_idx, out_val=out_val)
+        torch.cuda.synchronize()
+        gi, gv = out_idx.cpu().numpy(), out_val.cpu().numpy()
+        assert np.array_equal(gi, oi), np.nonzero((gi != oi).any(axis=1))[0][:8]
+        assert np.array_equal(gv[n_rw:].view(np.uint32), ov[n_rw:].view(np.uint32))
+
+
 @pytest.mark.parametrize("stride", [1, 2, 3, 5])
 def test_tiny_rows(stride):
     """Rows of a handful of positions (unaligned, scalar loads), k above and
