@@ -93,124 +93,91 @@ __device__ __forceinline__ bool kept_from_segments(RowCore& R, const Params& p, 
   return true;
 }
 
-// Stage A selects the top k_blocks blocks of W positions by block key (the
-// key of the block's best score), ties by lowest block id; stage B selects the
-// top k positions inside the kept blocks, ties by lowest position. The kept
-// block ids are also written in ascending order.
+// The roles other than stage A run out of line: a CTA runs its row's code
+// once, fetching it as it goes, and with these bodies inlined ahead of stage
+// A the side-by-side launch stalled longer on instruction fetch (cold
+// launch 30.9 against 25.9 us; back to back 20.3 against 20.2 us, and 19.8
+// with the general tail below out of line as well).
 //
-// With k_blocks >= k the stages are independent: every block holding one of
-// the row's plain top-k positions is kept (each block ranked above it has its
-// own maximum, a distinct position ranked above that position, so fewer than
-// k blocks rank above it), hence stage B returns exactly the plain top-k. The
-// launch then holds two groups of clusters (split): group 1 (clusters
-// [0, rows)) computes the plain top-k of its row, group 2 (clusters
-// [rows, 2 rows), launched only when out_blocks is wanted) stage A alone. Both
-// read the row once, side by side, instead of one stage after the other.
-//
-// Rounds are four float4 per thread (eight only for 32-position blocks): with
-// eight, the 512-thread kernel (128 registers a thread) spilled, and the
-// side-by-side 16-row launch took 22.8 us against 21.5 with four.
-template <int T, int W, class S>
-__global__ void __launch_bounds__(T, (T <= 256 ? 3 : 1)) blocked_kernel(Params p) {
-  constexpr int U0 = 4;  // float4 per thread per round
-  constexpr int U = (W / 4 > U0) ? W / 4 : U0;
-  using G = Geo<T, U, W>;
-  extern __shared__ __align__(128) unsigned char smem[];
+// The plain top-k of a row (group 1 of the side-by-side launch): items are
+// single positions, so it runs on four-position slots (the top-k kernel's
+// streaming filter: paired register rounds, compare masks without per-slot
+// bookkeeping).
+template <int T, int U, class S>
+__device__ __noinline__ void blocked_plain_row(const Params p, unsigned char* smem, int64_t row) {
   RowT<S> R;
-  stamp(p, kTrStart);
-  grid_dependents_launch();
-  const int64_t cid = (int64_t)(blockIdx.x / (p.clustered ? cluster_size() : 1u));
-  // 0: both stages in turn; 1 / 2: plain top-k / stage A side by side;
-  // 3: stage B over a given block list
-  const int role = p.external ? 3 : (p.split ? (cid < p.rows ? 1 : 2) : 0);
   float4 va[U], vb[U];
-  if (role == 1) {
-    // the plain top-k of the row: items are single positions, so it runs on
-    // four-position slots (the top-k kernel's streaming filter: paired
-    // register rounds, compare masks without per-slot bookkeeping)
-    setup_row<T, U, 4>(R, p, smem, cid % p.rows);
-    int na4[U], nb4[U];
-    const uint32_t K = (uint32_t)(R.L < (int64_t)p.k ? R.L : (int64_t)p.k);
-    bool intact;
-    uint64_t Tc;
-    const bool exact = select_stage<T, U, 4, false>(R, p, va, na4, vb, nb4, false, K, R.L, p.row_stride, KeepAll{},
-                                                    true, &intact, &Tc, kTrStageB);
-    output_positions<T>(R, p, exact, Tc, K, p.row_stride, true);
-    wait_init(R);
-    return;
-  }
-  setup_row<T, U, W>(R, p, smem, p.split ? cid % p.rows : cid);
-  Misc* m = R.m;
-  int na[G::kSlots], nb[G::kSlots];
-  if (role == 3) {
-    // a bitmap of this CTA's slice of blocks (slices hold whole blocks) in the
-    // output's bucket-start area (unused until the ordered output); the
-    // listed positions of the row are summed over the cluster
-    const int64_t nblocks = (R.L + W - 1) / W;
-    const int64_t b0 = R.begin / W, b1 = (R.end + W - 1) / W;
-    const uint32_t words = (uint32_t)((b1 - b0 + 31) >> 5);  // <= kBins: checked by the host
-    uint32_t* bits = R.aux;
-    for (uint32_t i = threadIdx.x; i < words; i += T) bits[i] = 0u;
-    __syncthreads();
-    const int32_t* listed = p.cand_blocks + R.row * (int64_t)p.n_cand;
-    for (int32_t j = (int32_t)threadIdx.x; j < p.n_cand; j += T) {
-      const int64_t b = listed[j];
-      if (b >= b0 && b < b1) atomicOr(&bits[(b - b0) >> 5], 1u << ((b - b0) & 31));
-    }
-    __syncthreads();
-    uint32_t cnt = 0;
-    for (uint32_t i = threadIdx.x; i < words; i += T) cnt += (uint32_t)__popc(bits[i]);
-    const uint32_t nlisted = block_sum<T>(cnt, m);
-    const int64_t lastb = nblocks - 1;  // may be partial: its positions past L do not count
-    const bool last = lastb >= b0 && lastb < b1 && ((bits[(lastb - b0) >> 5] >> ((lastb - b0) & 31)) & 1u) != 0u;
-    int64_t ncand = (int64_t)nlisted * W - (last ? nblocks * W - R.L : 0);
-    if (R.nclus > 1) {
-      // every CTA adds its count into every peer (zeroed before the start-up barrier)
-      wait_init(R);
-      if (threadIdx.x < R.nclus)
-        dsmem_red_add(peer_addr(smem_addr(&m->aux[7]), threadIdx.x), (uint32_t)ncand);
-      cluster_sync();
-      ncand = (int64_t)m->aux[7];
-    }
-    const uint32_t K = (uint32_t)(ncand < (int64_t)p.k ? ncand : (int64_t)p.k);
-    bool intact;
-    uint64_t Tc;
-    const bool exact = select_stage<T, U, W, false>(R, p, va, na, vb, nb, false, K, ncand, p.row_stride,
-                                                    KeepListed<T, U, W>{bits, b0, words * 32u}, true, &intact,
-                                                    &Tc, 0);
-    output_positions<T>(R, p, exact, Tc, K, p.row_stride, true);
-    wait_init(R);
-    return;
-  }
-  const int64_t nblocks = (R.L + W - 1) / W;
-  const uint32_t KA = (uint32_t)(nblocks < (int64_t)p.k_blocks ? nblocks : (int64_t)p.k_blocks);
-
-  // ---- stage A: the top k_blocks blocks by (block key desc, block id asc)
+  setup_row<T, U, 4>(R, p, smem, row);
+  int na4[U], nb4[U];
+  const uint32_t K = (uint32_t)(R.L < (int64_t)p.k ? R.L : (int64_t)p.k);
   bool intact;
-  uint64_t TcA;
-  const bool exactA = select_stage<T, U, W, true>(R, p, va, na, vb, nb, false, KA, nblocks, nblocks,
-                                                  KeepAll{}, true, &intact, &TcA, 0);
-  uint64_t TA = 0;
-  if (KA > 0) {
-    if (role == 2 && !exactA && (R.end - R.begin + W - 1) / W <= 32 * (int64_t)kBins && p.out_blocks) {
-      // stage-A-only clusters on the fast path: every CTA holds every segment
-      uint32_t lo = 0xffffffffu, hi = 0u;
-      for (uint32_t q = 0; q < m->nseg; ++q) {
-        if (m->seg_cnt[q] == 0) continue;
-        lo = min(lo, m->seg_min[q]);
-        hi = max(hi, m->seg_max[q]);
-      }
-      if (kept_from_segments<T, W>(R, p, KA, lo, hi)) {
-        __syncthreads();
-        stamp(R, kTrOutput);
-        wait_init(R);
-        return;
-      }
-    }
-    TA = exactA ? TcA : select_local<T>(R, KA, nblocks);
-    compact_selected<T>(R, TA);  // stage[0, KA) = kept block composites
-  }
+  uint64_t Tc;
+  const bool exact = select_stage<T, U, 4, false>(R, p, va, na4, vb, nb4, false, K, R.L, p.row_stride, KeepAll{},
+                                                  true, &intact, &Tc, kTrStageB);
+  output_positions<T>(R, p, exact, Tc, K, p.row_stride, true);
+  wait_init(R);
+}
 
+// Stage B over a given block list (role 3: the listed candidates of a later
+// layer when the listed kernel does not apply).
+template <int T, int U, int W, class S>
+__device__ __noinline__ void blocked_listed_row(RowT<S> R, const Params p) {
+  using G = Geo<T, U, W>;
+  Misc* m = R.m;
+  float4 va[U], vb[U];
+  int na[G::kSlots], nb[G::kSlots];
+  // a bitmap of this CTA's slice of blocks (slices hold whole blocks) in the
+  // output's bucket-start area (unused until the ordered output); the
+  // listed positions of the row are summed over the cluster
+  const int64_t nblocks = (R.L + W - 1) / W;
+  const int64_t b0 = R.begin / W, b1 = (R.end + W - 1) / W;
+  const uint32_t words = (uint32_t)((b1 - b0 + 31) >> 5);  // <= kBins: checked by the host
+  uint32_t* bits = R.aux;
+  for (uint32_t i = threadIdx.x; i < words; i += T) bits[i] = 0u;
+  __syncthreads();
+  const int32_t* listed = p.cand_blocks + R.row * (int64_t)p.n_cand;
+  for (int32_t j = (int32_t)threadIdx.x; j < p.n_cand; j += T) {
+    const int64_t b = listed[j];
+    if (b >= b0 && b < b1) atomicOr(&bits[(b - b0) >> 5], 1u << ((b - b0) & 31));
+  }
+  __syncthreads();
+  uint32_t cnt = 0;
+  for (uint32_t i = threadIdx.x; i < words; i += T) cnt += (uint32_t)__popc(bits[i]);
+  const uint32_t nlisted = block_sum<T>(cnt, m);
+  const int64_t lastb = nblocks - 1;  // may be partial: its positions past L do not count
+  const bool last = lastb >= b0 && lastb < b1 && ((bits[(lastb - b0) >> 5] >> ((lastb - b0) & 31)) & 1u) != 0u;
+  int64_t ncand = (int64_t)nlisted * W - (last ? nblocks * W - R.L : 0);
+  if (R.nclus > 1) {
+    // every CTA adds its count into every peer (zeroed before the start-up barrier)
+    wait_init(R);
+    if (threadIdx.x < R.nclus)
+      dsmem_red_add(peer_addr(smem_addr(&m->aux[7]), threadIdx.x), (uint32_t)ncand);
+    cluster_sync();
+    ncand = (int64_t)m->aux[7];
+  }
+  const uint32_t K = (uint32_t)(ncand < (int64_t)p.k ? ncand : (int64_t)p.k);
+  bool intact;
+  uint64_t Tc;
+  const bool exact = select_stage<T, U, W, false>(R, p, va, na, vb, nb, false, K, ncand, p.row_stride,
+                                                  KeepListed<T, U, W>{bits, b0, words * 32u}, true, &intact,
+                                                  &Tc, 0);
+  output_positions<T>(R, p, exact, Tc, K, p.row_stride, true);
+  wait_init(R);
+}
+
+// Kept blocks off the fast path (the exact stage A, a bucket past kMaxBucket
+// items, or stage A and B in turn), then stage B when both stages run in
+// turn. Out of line like the other rare paths; the two register rounds come
+// along for a stage B that reuses them.
+template <int T, int U, int W, class S>
+__device__ __noinline__ void blocked_general_tail(RowT<S> R, const Params p, int role, uint64_t TA, uint32_t KA,
+                                                  bool intact, RoundRegs<U, Geo<T, U, W>::kSlots> ra,
+                                                  RoundRegs<U, Geo<T, U, W>::kSlots> rb) {
+  Misc* m = R.m;
+  float4 (&va)[U] = ra.v;
+  float4 (&vb)[U] = rb.v;
+  int (&na)[Geo<T, U, W>::kSlots] = ra.n;
+  int (&nb)[Geo<T, U, W>::kSlots] = rb.n;
   // ---- kept block ids in ascending order: this CTA's own kept blocks,
   // sorted, placed after the kept blocks of the lower-ranked slices.
   const int64_t b0 = R.begin / W, b1 = (R.end + W - 1) / W;
@@ -306,6 +273,92 @@ __global__ void __launch_bounds__(T, (T <= 256 ? 3 : 1)) blocked_kernel(Params p
                                                    &intact_b, &TcB, kTrStageB);
   output_positions<T>(R, p, exactB, TcB, KB, p.row_stride, true);
   wait_init(R);
+}
+
+// Stage A selects the top k_blocks blocks of W positions by block key (the
+// key of the block's best score), ties by lowest block id; stage B selects the
+// top k positions inside the kept blocks, ties by lowest position. The kept
+// block ids are also written in ascending order.
+//
+// With k_blocks >= k the stages are independent: every block holding one of
+// the row's plain top-k positions is kept (each block ranked above it has its
+// own maximum, a distinct position ranked above that position, so fewer than
+// k blocks rank above it), hence stage B returns exactly the plain top-k. The
+// launch then holds two groups of clusters (split): group 1 (clusters
+// [0, rows)) computes the plain top-k of its row, group 2 (clusters
+// [rows, 2 rows), launched only when out_blocks is wanted) stage A alone. Both
+// read the row once, side by side, instead of one stage after the other.
+//
+// Rounds are four float4 per thread (eight only for 32-position blocks): with
+// eight, the 512-thread kernel (128 registers a thread) spilled, and the
+// side-by-side 16-row launch took 22.8 us against 21.5 with four.
+template <int T, int W, class S>
+__global__ void __launch_bounds__(T, (T <= 256 ? 3 : 1)) blocked_kernel(Params p) {
+  constexpr int U0 = 4;  // float4 per thread per round
+  constexpr int U = (W / 4 > U0) ? W / 4 : U0;
+  using G = Geo<T, U, W>;
+  extern __shared__ __align__(128) unsigned char smem[];
+  RowT<S> R;
+  stamp(p, kTrStart);
+  grid_dependents_launch();
+  const int64_t cid = (int64_t)(blockIdx.x / (p.clustered ? cluster_size() : 1u));
+  // 0: both stages in turn; 1 / 2: plain top-k / stage A side by side;
+  // 3: stage B over a given block list
+  const int role = p.external ? 3 : (p.split ? (cid < p.rows ? 1 : 2) : 0);
+  float4 va[U], vb[U];
+  if (role == 1) {
+    blocked_plain_row<T, U, S>(p, smem, cid % p.rows);
+    return;
+  }
+  setup_row<T, U, W>(R, p, smem, p.split ? cid % p.rows : cid);
+  Misc* m = R.m;
+  int na[G::kSlots], nb[G::kSlots];
+  if (role == 3) {
+    blocked_listed_row<T, U, W, S>(R, p);
+    return;
+  }
+  const int64_t nblocks = (R.L + W - 1) / W;
+  const uint32_t KA = (uint32_t)(nblocks < (int64_t)p.k_blocks ? nblocks : (int64_t)p.k_blocks);
+
+  // ---- stage A: the top k_blocks blocks by (block key desc, block id asc)
+  bool intact;
+  uint64_t TcA;
+  const bool exactA = select_stage<T, U, W, true>(R, p, va, na, vb, nb, false, KA, nblocks, nblocks,
+                                                  KeepAll{}, true, &intact, &TcA, 0);
+  uint64_t TA = 0;
+  if (KA > 0) {
+    if (role == 2 && !exactA && (R.end - R.begin + W - 1) / W <= 32 * (int64_t)kBins && p.out_blocks) {
+      // stage-A-only clusters on the fast path: every CTA holds every segment
+      uint32_t lo = 0xffffffffu, hi = 0u;
+      for (uint32_t q = 0; q < m->nseg; ++q) {
+        if (m->seg_cnt[q] == 0) continue;
+        lo = min(lo, m->seg_min[q]);
+        hi = max(hi, m->seg_max[q]);
+      }
+      if (kept_from_segments<T, W>(R, p, KA, lo, hi)) {
+        __syncthreads();
+        stamp(R, kTrOutput);
+        wait_init(R);
+        return;
+      }
+    }
+    TA = exactA ? TcA : select_local<T>(R, KA, nblocks);
+    compact_selected<T>(R, TA);  // stage[0, KA) = kept block composites
+  }
+  {
+    RoundRegs<U, G::kSlots> ra, rb;
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      ra.v[u] = va[u];
+      rb.v[u] = vb[u];
+    }
+#pragma unroll
+    for (int q = 0; q < G::kSlots; ++q) {
+      ra.n[q] = na[q];
+      rb.n[q] = nb[q];
+    }
+    blocked_general_tail<T, U, W, S>(R, p, role, TA, KA, intact, ra, rb);
+  }
 }
 
 template <int T, class S>
