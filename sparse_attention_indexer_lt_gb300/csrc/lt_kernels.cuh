@@ -1138,17 +1138,21 @@ __device__ __forceinline__ uint32_t estimate_small(RowCore& R, const float4 (&v)
 // k-th), a margin of many times the row-to-row spread of the k-th value. The
 // estimate is then skipped. Whether it fits is decided by the filter's own
 // count check: fewer than K kept or more than the candidate area holds, and
-// the row takes the exact path, as any miss does. Values that give no usable
-// threshold (NaN, infinities, hi <= lo) keep every position, which the same
-// check settles.
+// the row takes the exact path, as any miss does. With hi == lo (ties) the
+// margin is a sixteenth of lo; values that give no usable threshold (NaN,
+// infinities) keep every position, which the same check settles.
 struct Hint {
   float hi, lo;  // the earlier row's (k/2)-th and k-th values
 };
 
 __device__ __forceinline__ uint32_t hint_threshold(const Hint& h) {
-  const float t = h.lo - 0.75f * (h.hi - h.lo);
-  // finite and ordered (NaN fails every compare); key 0 would mean "keep all"
-  if (!(h.hi > h.lo) || !(fabsf(h.hi) <= 3.4e38f) || !(fabsf(t) <= 3.4e38f)) return 0u;
+  // finite (NaN fails every compare); key 0 would mean "keep all"
+  if (!(fabsf(h.lo) <= 3.4e38f)) return 0u;
+  // with the (k/2)-th value tied to the k-th (scores with few distinct
+  // values) the spread gives no margin: one sixteenth of the value instead
+  const float t = (h.hi > h.lo && fabsf(h.hi) <= 3.4e38f) ? h.lo - 0.75f * (h.hi - h.lo)
+                                                          : h.lo - 0.0625f * fabsf(h.lo);
+  if (!(fabsf(t) <= 3.4e38f)) return 0u;
   return key_of(t);
 }
 
