@@ -380,6 +380,11 @@ def bench_batched(lt, dev, args, world, peak, L2):
         if listed:
             out[-1]["bytes"] = "listed blocks' scores + the list"
             out[-1]["plan"] = lt.plan_candidates(w.rows, w.row_stride, w.block, cand.shape[1], w.k, dtype=S.dtype)
+        kname = "listed_kernel" if listed else ("blocked_kernel" if w.blocked else "topk_kernel")
+        key = name if dtype == "f32" else f"{name}:{dtype}"
+        # DRAM bytes per launch from the committed ncu capture (null when none
+        # matches the built sources)
+        out[-1]["traffic"] = profile_traffic(kname, key)
         if not args.no_cpu and world == 1 and dtype == "f32":
             out[-1]["cpu_baseline"] = cpu_batched(name, S, L, w, None if cand is None else cand.cpu())
         del copies, base
@@ -413,7 +418,8 @@ def bench_compress(lt, dev, args, world, peak):
                     "bytes": nbytes, "kernel_us": round(step_ms * 1000.0, 2), "hbm_gbs": round(gbs, 1),
                     "frac_of_peak": round(gbs / peak, 4),
                     "tokens_per_s": round(w.rows * w.tokens * world / (step_ms * 1e-3), 1),
-                    "l2": f"inputs {2 * kv.numel() * 2 >> 20} MiB, larger than the L2"})
+                    "l2": f"inputs {2 * kv.numel() * 2 >> 20} MiB, larger than the L2",
+                    "traffic": profile_traffic("compress_ring_kernel", name)})
         del kv, sc, bias, y
         torch.cuda.empty_cache()
     return out
